@@ -1,0 +1,321 @@
+"""Pins for the CPU oracle: each test checks it against something other than itself.
+
+Sources: "Hexagon backend developer details", section "Tiled Weight Formats" ("Tile Dimensions and
+Grid Layout", "Block-32 Quantized Formats").  Fixtures under tests/golden/ were worked out by hand
+from those sections.
+"""
+import os
+
+import numpy as np
+import pytest
+
+from block_quantized_matmul_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+TYPES = ["q4_0", "q8_0", "iq4_nl"]
+
+
+# ---------------------------------------------------------------------------------------------
+# binary16 conversion: against numpy's IEEE float16 (an independent library routine)
+# ---------------------------------------------------------------------------------------------
+def test_f16_conversion_matches_numpy(orc):
+    rng = np.random.default_rng(123)
+    vals = np.concatenate([
+        rng.standard_normal(3000).astype(np.float32) * np.float32(10.0) ** rng.integers(-9, 6, 3000),
+        np.array([0.0, -0.0, 1.0, -1.0, 65504.0, 65519.0, 65520.0, 1e9, -1e9, 6.1035156e-05, 6.0e-08,
+                  5.9604645e-08, 2.9802322e-08, 2.98023259e-08, 1e-40, 0.5 + 2.0 ** -12,
+                  1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 2048.0 + 1.0, 2048.0 + 3.0], dtype=np.float32),
+    ])
+    for v in vals:
+        with np.errstate(over="ignore"):
+            want = int(np.array([v], dtype=np.float32).astype(np.float16).view(np.uint16)[0])
+        got = orc.f32_to_f16(float(v))
+        assert got == want, (float(v), hex(got), hex(want))
+    for h in list(range(0, 0x7C00, 7)) + [0x0001, 0x03FF, 0x0400, 0x7BFF, 0x7C00, 0x8001, 0xFBFF, 0xFC00]:
+        want = float(np.array([h], dtype=np.uint16).view(np.float16).astype(np.float32)[0])
+        assert orc.f16_to_f32(h) == want, hex(h)
+
+
+# ---------------------------------------------------------------------------------------------
+# sizes and the tile grid
+# ---------------------------------------------------------------------------------------------
+def test_tile_and_block_sizes(orc):
+    # Tile sizes are printed on the pages; the flat blocks are 18 / 34 bytes, so tiling is lossless.
+    assert orc.tile_bytes("q4_0") == 576 and orc.tile_bytes("iq4_nl") == 576
+    assert orc.tile_bytes("q8_0") == 1088
+    assert 32 * orc.block_bytes("q4_0") == 576 and 32 * orc.block_bytes("iq4_nl") == 576
+    assert 32 * orc.block_bytes("q8_0") == 1088
+
+
+@pytest.mark.parametrize("K,N,type_,tiles", [
+    (4096, 4096, "q4_0", 128 * 128),
+    (4096, 14336, "q8_0", 448 * 128),
+    (4096, 128256, "q8_0", 4008 * 128),
+    (64, 33, "q4_0", 2 * 2),        # 33 rows -> 2 column tiles (ceil), 2 K tiles
+    (32, 1, "iq4_nl", 1),
+])
+def test_tiled_size_grid(orc, K, N, type_, tiles):
+    assert orc.tiled_bytes(type_, K, N) == tiles * orc.tile_bytes(type_)
+
+
+def test_tile_index_order(orc):
+    # tile_idx = ct * n_k_tiles + kt: the K-tiles of one column tile are consecutive.
+    assert orc.tile_index(0, 0, 128) == 0
+    assert orc.tile_index(0, 127, 128) == 127
+    assert orc.tile_index(1, 0, 128) == 128
+    assert orc.tile_index(3, 5, 7) == 26
+
+
+# ---------------------------------------------------------------------------------------------
+# repack: hand-placed quants land where the pages say
+# ---------------------------------------------------------------------------------------------
+def _read_positions():
+    rows = []
+    with open(os.path.join(GOLDEN, "tile_positions.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            a, b, c = [p.split() for p in line.split("|")]
+            rows.append((a[0], int(a[1]), int(a[2]), int(a[3]), int(b[0]), int(b[1]), int(c[0]),
+                         int(c[1]), int(c[2])))
+    return rows
+
+
+@pytest.mark.parametrize("case", _read_positions())
+def test_one_hot_tile_position(orc, case):
+    type_, row, col, code, fbyte, fshift, tbyte, tshift, sbyte = case
+    bb, ts = orc.block_bytes(type_), orc.tile_bytes(type_)
+    N, K = 32, 32
+    flat = np.zeros((N, bb), np.uint8)
+    raw = code & 0xFF if type_ == "q8_0" else code << fshift
+    flat[row, fbyte] = raw
+    flat[row, 0:2] = (0x34, 0x12)              # fp16 scale bits 0x1234 on that row
+    tiled = orc.repack(type_, flat, K, N)
+    assert tiled.size == ts
+    expect = np.zeros(ts, np.uint8)
+    expect[tbyte] = (code & 0xFF) if type_ == "q8_0" else (code << tshift)
+    expect[sbyte], expect[sbyte + 1] = 0x34, 0x12
+    assert np.array_equal(tiled, expect), np.nonzero(tiled != expect)
+
+
+@pytest.mark.parametrize("type_", TYPES)
+@pytest.mark.parametrize("K,N", [(32, 1), (64, 33), (96, 64), (128, 100)])
+def test_repack_unpack_roundtrip_and_padding(orc, type_, K, N):
+    rng = np.random.default_rng(K * 1000 + N)
+    flat = rng.integers(0, 256, size=(N, K // 32 * orc.block_bytes(type_)), dtype=np.uint8)
+    tiled = orc.repack(type_, flat, K, N)
+    assert np.array_equal(orc.unpack(type_, tiled, K, N), flat)
+    # rows past N in the last column tile are zero bytes
+    ts, nkt = orc.tile_bytes(type_), K // 32
+    last_ct = (N + 31) // 32 - 1
+    pad_rows = [r for r in range(32) if last_ct * 32 + r >= N]
+    if pad_rows:
+        for kt in range(nkt):
+            t = tiled[(last_ct * nkt + kt) * ts:(last_ct * nkt + kt + 1) * ts]
+            for r in pad_rows:
+                if type_ == "q8_0":
+                    assert all(t[cp * 64 + 2 * r + h] == 0 for cp in range(16) for h in range(2))
+                    assert t[1024 + 2 * r] == 0 and t[1025 + 2 * r] == 0
+                else:
+                    assert all(t[cp * 32 + r] == 0 for cp in range(16))
+                    assert t[512 + 2 * r] == 0 and t[513 + 2 * r] == 0
+
+
+def test_repack_keeps_k_tiles_of_a_column_tile_contiguous(orc):
+    # Block kt of row n must land in tile ct*n_k_tiles + kt: mark each block by its scale.
+    K, N = 32 * 5, 64
+    bb, ts = orc.block_bytes("q8_0"), orc.tile_bytes("q8_0")
+    flat = np.zeros((N, 5 * bb), np.uint8)
+    for n in range(N):
+        for kt in range(5):
+            flat[n, kt * bb] = n
+            flat[n, kt * bb + 1] = kt
+    tiled = orc.repack("q8_0", flat, K, N)
+    for ct in range(2):
+        for kt in range(5):
+            t = tiled[(ct * 5 + kt) * ts:(ct * 5 + kt + 1) * ts]
+            for r in range(32):
+                assert t[1024 + 2 * r] == ct * 32 + r and t[1025 + 2 * r] == kt
+
+
+# ---------------------------------------------------------------------------------------------
+# activation quantization
+# ---------------------------------------------------------------------------------------------
+def _read_act_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "act_quant_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, xs, qs, d = [p.strip() for p in line.split("|")]
+            x = np.zeros(32, np.float32)
+            q = np.zeros(32, np.int8)
+            for tok in xs.split():
+                i, v = tok.split(":")
+                x[int(i)] = np.float32(float(v))
+            for tok in qs.split():
+                i, v = tok.split(":")
+                q[int(i)] = int(v)
+            cases.append((name, x, q, int(d, 16)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _read_act_cases(), ids=lambda c: c[0])
+def test_act_quant_hand_cases(orc, case):
+    _, x, q, d16 = case
+    got_q, got_d = orc.quantize_block_q8_0(x)
+    assert np.array_equal(got_q, q)
+    assert got_d == d16
+
+
+def test_act_quant_invariants(orc):
+    x = synth.activations(16, 4096, outliers=True)
+    a_q, a_d = orc.quantize_act(x)
+    assert np.abs(a_q.astype(np.int32)).max() <= 127
+    blocks = x.reshape(16, 128, 32)
+    amax_idx = np.abs(blocks).argmax(axis=2)
+    qb = a_q.reshape(16, 128, 32)
+    picked = np.take_along_axis(qb, amax_idx[..., None], axis=2)[..., 0]
+    assert np.all(np.abs(picked.astype(np.int32)) == 127)          # the largest element maps to +-127
+    # dequantized activations stay within half a step (plus the fp16 scale rounding) of x
+    d = a_d.view(np.float16).astype(np.float64)[..., None]
+    err = np.abs(qb * d - blocks)
+    assert np.all(err <= d * (0.5 + 127 * 2.0 ** -11) + 1e-30)
+
+
+# ---------------------------------------------------------------------------------------------
+# weight quantizers (test-data generators)
+# ---------------------------------------------------------------------------------------------
+def test_q4_0_hand_case(orc):
+    x = np.zeros((1, 32), np.float32)
+    x[0, :4] = [-1.6, 0.2, 0.0, 1.0]
+    flat = orc.quantize_rows("q4_0", x)
+    d = np.array([int(flat[0, 0]) | (int(flat[0, 1]) << 8)], np.uint16).view(np.float16)[0]
+    assert d == np.float16(0.2)
+    codes = [(flat[0, 2 + j] & 15) if j < 16 else (flat[0, 2 + j - 16] >> 4) for j in range(32)]
+    assert codes[:4] == [0, 9, 8, 13]
+    assert all(c == 8 for c in codes[4:])
+
+
+@pytest.mark.parametrize("type_", TYPES)
+def test_weight_quantizer_error_bound(orc, type_):
+    w = synth.weights(64, 256)
+    flat = orc.quantize_rows(type_, w)
+    deq = orc.dequantize_flat(type_, flat, 64, 256)
+    blocks = w.reshape(64, 8, 32).astype(np.float64)
+    dq = deq.reshape(64, 8, 32)
+    amax = np.abs(blocks).max(axis=2, keepdims=True)
+    if type_ == "q8_0":
+        step = amax / 127
+        assert np.all(np.abs(dq - blocks) <= step * (0.5 + 127 * 2.0 ** -11) + 1e-12)
+    elif type_ == "q4_0":
+        step = amax / 8
+        assert np.all(np.abs(dq - blocks) <= step * (1.0 + 8 * 2.0 ** -11) + 1e-12)
+    else:
+        lut = orc.iq4nl_table().astype(np.float64)
+        gaps = np.diff(lut).max()
+        step = amax / 127
+        assert np.all(np.abs(dq - blocks) <= step * (gaps / 2 + 127 * 2.0 ** -11) + 1e-12)
+
+
+def test_iq4_nl_picks_nearest_entry(orc):
+    # Brute force in the precision the rule is stated in (fp32): no other entry is strictly closer.
+    w = synth.weights(8, 128)
+    lut = orc.iq4nl_table()
+    flat = orc.quantize_rows("iq4_nl", w)
+    for n in range(8):
+        for b in range(4):
+            blk = flat[n, b * 18:(b + 1) * 18]
+            d = np.float32(np.array([int(blk[0]) | (int(blk[1]) << 8)], np.uint16).view(np.float16)[0])
+            levels = (d * lut.astype(np.float32)).astype(np.float32)
+            for j in range(32):
+                c = (blk[2 + j] & 15) if j < 16 else (blk[2 + j - 16] >> 4)
+                x = w[n, b * 32 + j]
+                errs = np.abs(np.float32(x) - levels)
+                assert errs[c] <= errs.min()
+                assert c == int(np.argmax(errs == errs.min()))     # lowest index among ties
+
+
+def test_iq4_nl_table_is_the_lloyd_max_stand_in(orc):
+    # The pages print no table values; the stand-in is the 16-level Lloyd-Max quantizer of N(0,1),
+    # scaled to +-127 and rounded.  Recompute it from the centroid conditions.
+    scipy_stats = pytest.importorskip("scipy.stats")
+    norm = scipy_stats.norm
+    levels = np.linspace(-2.5, 2.5, 16)
+    for _ in range(5000):
+        edges = np.concatenate([[-np.inf], (levels[1:] + levels[:-1]) / 2, [np.inf]])
+        new = (norm.pdf(edges[:-1]) - norm.pdf(edges[1:])) / (norm.cdf(edges[1:]) - norm.cdf(edges[:-1]))
+        if np.max(np.abs(new - levels)) < 1e-14:
+            break
+        levels = new
+    table = np.round(levels * 127 / levels[-1]).astype(np.int8)
+    assert np.array_equal(orc.iq4nl_table(), table)
+
+
+# ---------------------------------------------------------------------------------------------
+# matmul: fp64 brute force on the FLAT blocks (never touches the tile layout) vs the tiled oracle
+# ---------------------------------------------------------------------------------------------
+def _brute(orc, type_, flat, a_q, a_d, N, K, lut=None):
+    W = orc.dequantize_flat(type_, flat, N, K, lut)                        # [N, K] fp64
+    A = a_q.astype(np.float64) * np.repeat(a_d.view(np.float16).astype(np.float64), 32, axis=1)
+    return A @ W.T
+
+
+@pytest.mark.parametrize("type_", TYPES)
+@pytest.mark.parametrize("K,N,M", [(32, 1, 1), (64, 31, 3), (96, 32, 1), (96, 33, 3), (160, 65, 2)])
+def test_matmul_matches_fp64_brute_force(orc, type_, K, N, M):
+    w = synth.weights(N, K, seed=K + N)
+    x = synth.activations(M, K, seed=M + 7, outliers=True)
+    flat = orc.quantize_rows(type_, w)
+    tiled = orc.repack(type_, flat, K, N)
+    a_q, a_d = orc.quantize_act(x)
+    y, bound = orc.matmul(type_, tiled, K, N, a_q, a_d)
+    ref = _brute(orc, type_, flat, a_q, a_d, N, K)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-15)
+    assert np.all(bound >= np.abs(y) - 1e-15)
+    ms, ns = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    ys, bs = orc.matmul_at(type_, tiled, K, a_q, a_d, ms.ravel(), ns.ravel())
+    assert np.array_equal(ys, y.ravel()) and np.array_equal(bs, bound.ravel())
+
+
+def test_matmul_one_hot_activation_reads_weight_column(orc):
+    K, N = 64, 40
+    w = synth.weights(N, K, seed=5)
+    flat = orc.quantize_rows("q4_0", w)
+    tiled = orc.repack("q4_0", flat, K, N)
+    W = orc.dequantize_flat("q4_0", flat, N, K)
+    for k in (0, 13, 33, 63):
+        a_q = np.zeros((1, K), np.int8)
+        a_q[0, k] = 1
+        a_d = np.full((1, K // 32), np.float16(1.0).view(np.uint16), np.uint16)
+        y, _ = orc.matmul("q4_0", tiled, K, N, a_q, a_d)
+        assert np.array_equal(y[0], W[:, k])
+
+
+def test_matmul_zero_and_linearity(orc):
+    K, N, M = 96, 48, 2
+    rng = np.random.default_rng(9)
+    flat = orc.quantize_rows("q8_0", synth.weights(N, K, seed=3))
+    tiled = orc.repack("q8_0", flat, K, N)
+    a_d = synth.activations(M, K // 32, seed=4).astype(np.float16).view(np.uint16)
+    q1 = rng.integers(-60, 60, size=(M, K), dtype=np.int8)
+    q2 = rng.integers(-60, 60, size=(M, K), dtype=np.int8)
+    y1, _ = orc.matmul("q8_0", tiled, K, N, q1, a_d)
+    y2, _ = orc.matmul("q8_0", tiled, K, N, q2, a_d)
+    y12, _ = orc.matmul("q8_0", tiled, K, N, (q1 + q2).astype(np.int8), a_d)
+    assert np.allclose(y12, y1 + y2, rtol=1e-13, atol=1e-15)
+    y0, b0 = orc.matmul("q8_0", tiled, K, N, np.zeros((M, K), np.int8), a_d)
+    assert not y0.any() and not b0.any()
+
+
+def test_iq4_nl_with_offset_table_equals_q4_0(orc):
+    # With lut[i] = i - 8 the IQ4_NL dequantization is the Q4_0 one on the same bytes.
+    K, N, M = 128, 64, 3
+    flat = orc.quantize_rows("q4_0", synth.weights(N, K, seed=11))
+    tiled = orc.repack("q4_0", flat, K, N)
+    a_q, a_d = orc.quantize_act(synth.activations(M, K, seed=12))
+    y4, b4 = orc.matmul("q4_0", tiled, K, N, a_q, a_d)
+    yi, bi = orc.matmul("iq4_nl", tiled, K, N, a_q, a_d, lut=np.arange(16) - 8)
+    assert np.array_equal(y4, yi) and np.array_equal(b4, bi)
