@@ -1,0 +1,133 @@
+// qmm_api.cu -- the extern "C" entry points of libqmm: host-side validation, then one or more
+// kernel launches on the caller's stream.  Nothing here allocates device memory.
+//
+// Following the pages' guidance on host-side precomputation ("Op and Kernel Development
+// Guidelines": shapes, strides, tiling and validation are settled on the host before the kernel
+// runs), every check below happens before anything is enqueued, and the kernels trust their
+// parameters.
+#include <mutex>
+
+#include "qmm_internal.cuh"
+
+using namespace qmm;
+
+namespace {
+
+bool valid_type(qmm_type t) { return t == QMM_Q4_0 || t == QMM_Q8_0 || t == QMM_IQ4_NL; }
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool valid_kn(int64_t K, int64_t N) { return K > 0 && (K % 32) == 0 && N > 0; }
+cudaStream_t cs(qmm_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
+
+// Sizes are capped so every byte offset fits comfortably in int64 arithmetic on both sides.
+constexpr int64_t kMaxDim = (int64_t)1 << 31;
+
+qmm_status check_matmul(qmm_type t, const void *w, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
+                        int64_t M, float *y, int64_t ldy) {
+    if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
+    if (!valid_kn(K, N) || M <= 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim || ldy < N) return QMM_ERR_INVALID_ARG;
+    if (!w || !a_q || !a_d || !y) return QMM_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || !aligned(a_q, 16) || !aligned(a_d, 4) || !aligned(y, 4)) return QMM_ERR_MISALIGNED;
+    return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qmm_status_str(qmm_status st) {
+    switch (st) {
+        case QMM_OK: return "ok";
+        case QMM_ERR_INVALID_ARG: return "invalid argument";
+        case QMM_ERR_UNSUPPORTED: return "unsupported type or path";
+        case QMM_ERR_MISALIGNED: return "misaligned pointer or stride";
+        case QMM_ERR_CUDA: return "CUDA error";
+        case QMM_ERR_TIMEOUT: return "device pipeline wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t qmm_block_size(qmm_type t) { return valid_type(t) ? (size_t)block_bytes(t) : 0; }
+
+size_t qmm_tile_size(qmm_type t) { return valid_type(t) ? (size_t)tile_bytes(t) : 0; }
+
+size_t qmm_tiled_size(qmm_type t, int64_t K, int64_t N) {
+    if (!valid_type(t) || !valid_kn(K, N) || K > kMaxDim || N > kMaxDim) return 0;
+    return (size_t)((N + 31) / 32) * (size_t)(K / 32) * (size_t)tile_bytes(t);
+}
+
+size_t qmm_flat_size(qmm_type t, int64_t K, int64_t N) {
+    if (!valid_type(t) || !valid_kn(K, N) || K > kMaxDim || N > kMaxDim) return 0;
+    return (size_t)N * (size_t)(K / 32) * (size_t)block_bytes(t);
+}
+
+void qmm_iq4nl_table(int8_t out[16]) {
+    if (!out) return;
+    for (int i = 0; i < 16; ++i) out[i] = kIq4nlTable[i];
+}
+
+int64_t qmm_decode_max_m(void) { return kDecodeMaxM; }
+
+qmm_status qmm_quantize_weight(qmm_type t, const float *w, int64_t N, int64_t K, int64_t ldw, void *w_flat,
+                               qmm_stream_t stream) {
+    if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
+    if (!valid_kn(K, N) || K > kMaxDim || N > kMaxDim || ldw < K || !w || !w_flat) return QMM_ERR_INVALID_ARG;
+    if (!aligned(w, 16) || (ldw % 4) != 0 || !aligned(w_flat, 2)) return QMM_ERR_MISALIGNED;
+    return from_cuda(launch_quantize_weight(t, w, N, K, ldw, static_cast<uint8_t *>(w_flat), cs(stream)));
+}
+
+qmm_status qmm_repack(qmm_type t, const void *w_flat, int64_t K, int64_t N, void *w_tiled, qmm_stream_t stream) {
+    if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
+    if (!valid_kn(K, N) || K > kMaxDim || N > kMaxDim || !w_flat || !w_tiled) return QMM_ERR_INVALID_ARG;
+    if (!aligned(w_flat, 2) || !aligned(w_tiled, 16)) return QMM_ERR_MISALIGNED;
+    return from_cuda(launch_repack(t, static_cast<const uint8_t *>(w_flat), K, N, static_cast<uint8_t *>(w_tiled),
+                                   cs(stream)));
+}
+
+qmm_status qmm_unpack(qmm_type t, const void *w_tiled, int64_t K, int64_t N, void *w_flat, qmm_stream_t stream) {
+    if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
+    if (!valid_kn(K, N) || K > kMaxDim || N > kMaxDim || !w_flat || !w_tiled) return QMM_ERR_INVALID_ARG;
+    if (!aligned(w_flat, 2) || !aligned(w_tiled, 16)) return QMM_ERR_MISALIGNED;
+    return from_cuda(launch_unpack(t, static_cast<const uint8_t *>(w_tiled), K, N, static_cast<uint8_t *>(w_flat),
+                                   cs(stream)));
+}
+
+qmm_status qmm_quantize_act(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *a_q, uint16_t *a_d,
+                            qmm_stream_t stream) {
+    if (M <= 0 || K <= 0 || (K % 32) != 0 || ldx < K || M > kMaxDim || K > kMaxDim || !x || !a_q || !a_d)
+        return QMM_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(a_q, 16) || !aligned(a_d, 4)) return QMM_ERR_MISALIGNED;
+    return from_cuda(launch_quantize_act(x, M, K, ldx, a_q, a_d, cs(stream)));
+}
+
+qmm_status qmm_matmul_path(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const int8_t *a_q,
+                           const uint16_t *a_d, int64_t M, float *y, int64_t ldy, qmm_path path,
+                           qmm_stream_t stream) {
+    qmm_status st = check_matmul(t, w_tiled, K, N, a_q, a_d, M, y, ldy);
+    if (st != QMM_OK) return st;
+    if (path != QMM_PATH_AUTO && path != QMM_PATH_MATVEC && path != QMM_PATH_GEMM) return QMM_ERR_UNSUPPORTED;
+    const uint8_t *w = static_cast<const uint8_t *>(w_tiled);
+    if (path == QMM_PATH_AUTO) path = (M <= kDecodeMaxM) ? QMM_PATH_MATVEC : QMM_PATH_GEMM;
+    cudaError_t e;
+    if (path == QMM_PATH_MATVEC) {
+        e = launch_matvec(t, w, K, N, a_q, a_d, M, y, ldy, cs(stream));
+    } else {
+        e = launch_gemm(t, w, K, N, a_q, a_d, M, y, ldy, cs(stream));
+        if (e == cudaErrorNotSupported) return QMM_ERR_UNSUPPORTED;
+    }
+    return from_cuda(e);
+}
+
+qmm_status qmm_matmul(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
+                      int64_t M, float *y, int64_t ldy, qmm_stream_t stream) {
+    return qmm_matmul_path(t, w_tiled, K, N, a_q, a_d, M, y, ldy, QMM_PATH_AUTO, stream);
+}
+
+qmm_status qmm_device_status(qmm_stream_t stream) {
+    unsigned v = 0;
+    cudaError_t e = read_and_clear_device_status(&v, cs(stream));
+    if (e != cudaSuccess) return QMM_ERR_CUDA;
+    return v ? QMM_ERR_TIMEOUT : QMM_OK;
+}
+
+}  // extern "C"

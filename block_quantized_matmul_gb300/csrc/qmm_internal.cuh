@@ -1,0 +1,56 @@
+// qmm_internal.cuh -- declarations shared by the libqmm translation units (product code only).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qmm.h"
+
+namespace qmm {
+
+constexpr int kTileRows = 32;         // rows (N) per tile
+constexpr int kTileCols = 32;         // columns (K) per tile = elements per GGML block
+constexpr int kTile4Bytes = 576;      // Q4_0 / IQ4_NL tile
+constexpr int kTile8Bytes = 1088;     // Q8_0 tile
+constexpr int kScale4Off = 512;       // FP16 row scales inside a 4-bit tile
+constexpr int kScale8Off = 1024;      // FP16 row scales inside a Q8_0 tile
+constexpr int kBlock4Bytes = 18;      // flat GGML block: fp16 d + 16 nibble bytes
+constexpr int kBlock8Bytes = 34;      // flat GGML block: fp16 d + 32 int8
+
+inline int tile_bytes(qmm_type t) { return t == QMM_Q8_0 ? kTile8Bytes : kTile4Bytes; }
+inline int block_bytes(qmm_type t) { return t == QMM_Q8_0 ? kBlock8Bytes : kBlock4Bytes; }
+
+// The built-in IQ4_NL table (16 int8 levels, ascending): 16-level Lloyd-Max quantizer of a unit
+// normal, scaled so the outer levels are -127 and +127, rounded to integers.
+constexpr int8_t kIq4nlTable[16] = {-127, -96, -75, -58, -44, -31, -18, -6, 6, 18, 31, 44, 58, 75, 96, 127};
+
+// Table passed by value to kernels (host-side precomputed parameters, no device-global state).
+struct Lut16 {
+    int8_t v[16];
+};
+inline Lut16 iq4nl_lut() {
+    Lut16 l;
+    for (int i = 0; i < 16; ++i) l.v[i] = kIq4nlTable[i];
+    return l;
+}
+
+// Launchers (each returns cudaGetLastError() after enqueueing).
+cudaError_t launch_quantize_act(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *a_q,
+                                uint16_t *a_d, cudaStream_t s);
+cudaError_t launch_quantize_weight(qmm_type t, const float *w, int64_t N, int64_t K, int64_t ldw,
+                                   uint8_t *flat, cudaStream_t s);
+cudaError_t launch_repack(qmm_type t, const uint8_t *flat, int64_t K, int64_t N, uint8_t *tiled,
+                          cudaStream_t s);
+cudaError_t launch_unpack(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, uint8_t *flat,
+                          cudaStream_t s);
+cudaError_t launch_matvec(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
+                          const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
+cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
+                        const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
+cudaError_t read_and_clear_device_status(unsigned *out, cudaStream_t s);
+
+// Largest M handled by one decode-matvec launch (two 8-token mma fragments).
+constexpr int kDecodeMaxM = 16;
+
+}  // namespace qmm

@@ -1,0 +1,171 @@
+// quant.cu -- activation quantization (hot path) and weight quantization (model-load helper).
+//
+// Activation rule (dynamic Q8_0, per 32 elements): amax = max|x|, d = amax/127, id = d ? 1/d : 0,
+// q = round-half-away(x*id) clamped to [-127,127] (NaN product -> 0), stored scale fp16(d).
+// Every operation is an IEEE-rounded fp32 intrinsic (__fdiv_rn, __frcp_rn-free 1/d via __fdiv_rn,
+// __fmul_rn, __fadd_rn), so nvcc cannot contract or reassociate them.
+#include "qmm_internal.cuh"
+
+namespace qmm {
+namespace {
+
+__device__ __forceinline__ int q8_code(float x, float id) {
+    float v = __fmul_rn(x, id);
+    if (isnan(v)) return 0;                    // 0 * inf when 1/d overflowed
+    float r = roundf(v);                       // halfway cases away from zero
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return (int)r;
+}
+
+__device__ __forceinline__ float q8_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
+__device__ __forceinline__ float inv_or_zero(float d) { return d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f; }
+
+// 8 threads per 32-element block, 4 consecutive elements per thread.  Grid-stride over all
+// M*K/4 element quads.  `vec` selects float4 loads (x 16-byte aligned, ldx % 4 == 0).
+template <bool vec>
+__global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x, int64_t M, int64_t K,
+                                                           int64_t ldx, int8_t *__restrict__ a_q,
+                                                           uint16_t *__restrict__ a_d) {
+    const int64_t quads_per_row = K / 4;
+    const int64_t total = M * quads_per_row;
+    const unsigned lane = threadIdx.x & 31u;
+    // All 32 lanes of a warp stay in the loop together (total is a multiple of 8, and the
+    // stride is a multiple of 32), so the group-of-8 shuffles below are always complete.
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31u); base < total; base += stride) {
+        const int64_t i = base + lane;
+        const bool active = i < total;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        int64_t m = 0, kq = 0;
+        if (active) {
+            m = i / quads_per_row;
+            kq = (i - m * quads_per_row) * 4;
+            const float *p = x + m * ldx + kq;
+            if (vec) {
+                v = __ldg(reinterpret_cast<const float4 *>(p));
+            } else {
+                v.x = __ldg(p); v.y = __ldg(p + 1); v.z = __ldg(p + 2); v.w = __ldg(p + 3);
+            }
+        }
+        float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        if (active) {
+            const float d = q8_scale(amax);
+            const float id = inv_or_zero(d);
+            const uint32_t packed = (uint32_t)(q8_code(v.x, id) & 0xFF) | ((uint32_t)(q8_code(v.y, id) & 0xFF) << 8) |
+                                    ((uint32_t)(q8_code(v.z, id) & 0xFF) << 16) |
+                                    ((uint32_t)(q8_code(v.w, id) & 0xFF) << 24);
+            *reinterpret_cast<uint32_t *>(a_q + m * K + kq) = packed;
+            if ((lane & 7u) == 0) a_d[m * (K / 32) + kq / 32] = __half_as_ushort(__float2half_rn(d));
+        }
+    }
+}
+
+// One thread per flat output block (32 input elements).  Model-load helper: simple, not tuned.
+__global__ void __launch_bounds__(128) quantize_weight_kernel(int type, const float *__restrict__ w, int64_t N,
+                                                              int64_t K, int64_t ldw, uint8_t *__restrict__ flat,
+                                                              Lut16 lut) {
+    const int64_t nb = K / 32;
+    const int64_t total = N * nb;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / nb, b = i - n * nb;
+        const float *x = w + n * ldw + b * 32;
+        float xs[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 v = __ldg(reinterpret_cast<const float4 *>(x + j));
+            xs[j] = v.x; xs[j + 1] = v.y; xs[j + 2] = v.z; xs[j + 3] = v.w;
+        }
+        float amax = 0.0f, m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (fabsf(xs[j]) > amax) { amax = fabsf(xs[j]); m = xs[j]; }
+        }
+        const int bb = (type == QMM_Q8_0) ? kBlock8Bytes : kBlock4Bytes;
+        uint16_t *out = reinterpret_cast<uint16_t *>(flat + i * bb);   // 2-byte aligned
+        int codes[32];
+        float d;
+        if (type == QMM_Q8_0) {
+            d = q8_scale(amax);
+            const float id = inv_or_zero(d);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) codes[j] = q8_code(xs[j], id);
+            out[0] = __half_as_ushort(__float2half_rn(d));
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) out[1 + j / 2] = (uint16_t)((codes[j] & 0xFF) | ((codes[j + 1] & 0xFF) << 8));
+            continue;
+        }
+        if (type == QMM_Q4_0) {
+            d = __fdiv_rn(m, -8.0f);
+            const float id = inv_or_zero(d);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float v = __fadd_rn(__fmul_rn(xs[j], id), 8.5f);
+                int c;
+                if (!(v >= 0.0f)) c = 0;                 // NaN or negative
+                else if (v >= 15.0f) c = 15;
+                else c = __float2int_rz(v);              // truncation toward zero
+                codes[j] = c;
+            }
+            out[0] = __half_as_ushort(__float2half_rn(d));
+        } else {
+            d = __fdiv_rn(m, (float)lut.v[0]);
+            const __half d16 = __float2half_rn(d);
+            const float ds = __half2float(d16);
+            float levels[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) levels[q] = __fmul_rn(ds, (float)lut.v[q]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                int best = 0;
+                float best_err = INFINITY;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float e = fabsf(__fsub_rn(xs[j], levels[q]));
+                    if (e < best_err) { best_err = e; best = q; }
+                }
+                codes[j] = best;
+            }
+            out[0] = __half_as_ushort(d16);
+        }
+        // nibble byte j holds element j (low) and element j+16 (high)
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            const uint32_t b0 = (uint32_t)(codes[j] & 15) | ((uint32_t)(codes[j + 16] & 15) << 4);
+            const uint32_t b1 = (uint32_t)(codes[j + 1] & 15) | ((uint32_t)(codes[j + 17] & 15) << 4);
+            out[1 + j / 2] = (uint16_t)(b0 | (b1 << 8));
+        }
+    }
+}
+
+int grid_for(int64_t work, int threads) {
+    int64_t g = (work + threads - 1) / threads;
+    if (g > 152 * 32) g = 152 * 32;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_act(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *a_q, uint16_t *a_d,
+                                cudaStream_t s) {
+    const int threads = 256;
+    const int64_t quads = M * (K / 4);
+    const int grid = grid_for(quads, threads);
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) && (ldx % 4 == 0);
+    if (vec) quantize_act_kernel<true><<<grid, threads, 0, s>>>(x, M, K, ldx, a_q, a_d);
+    else quantize_act_kernel<false><<<grid, threads, 0, s>>>(x, M, K, ldx, a_q, a_d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weight(qmm_type t, const float *w, int64_t N, int64_t K, int64_t ldw, uint8_t *flat,
+                                   cudaStream_t s) {
+    const int threads = 128;
+    const int grid = grid_for(N * (K / 32), threads);
+    quantize_weight_kernel<<<grid, threads, 0, s>>>((int)t, w, N, K, ldw, flat, iq4nl_lut());
+    return cudaGetLastError();
+}
+
+}  // namespace qmm

@@ -1,0 +1,133 @@
+// repack.cu -- flat GGML rows <-> 32-row tiles ("Tiled Weight Formats": "Tile Dimensions and Grid
+// Layout", "Block-32 Quantized Formats").  Load-time kernels: read and write the weight once.
+//
+// Thread mapping: one thread per (tile, tile row).  A warp covers the 32 rows of one tile, so each
+// per-column-pair store of the warp is one contiguous run (32 bytes for 4-bit tiles, 64 for Q8_0).
+#include "qmm_internal.cuh"
+
+namespace qmm {
+namespace {
+
+__device__ __forceinline__ uint32_t ld_u16(const uint8_t *p) { return *reinterpret_cast<const uint16_t *>(p); }
+
+template <int TYPE>
+__global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ flat, int64_t n_k_tiles, int64_t N,
+                                                     int64_t n_tiles, uint8_t *__restrict__ tiled) {
+    constexpr bool k8 = (TYPE == QMM_Q8_0);
+    constexpr int bb = k8 ? kBlock8Bytes : kBlock4Bytes;
+    constexpr int ts = k8 ? kTile8Bytes : kTile4Bytes;
+    constexpr int soff = k8 ? kScale8Off : kScale4Off;
+    const int64_t total = n_tiles * 32;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = i >> 5;
+        const int r = (int)(i & 31);
+        const int64_t ct = tile / n_k_tiles, kt = tile - ct * n_k_tiles;
+        const int64_t n = ct * 32 + r;
+        uint8_t *t = tiled + tile * ts;
+        if (n >= N) {                                   // padding row: all zero
+            if (k8) {
+#pragma unroll
+                for (int cp = 0; cp < 16; ++cp) *reinterpret_cast<uint16_t *>(t + cp * 64 + 2 * r) = 0;
+            } else {
+#pragma unroll
+                for (int cp = 0; cp < 16; ++cp) t[cp * 32 + r] = 0;
+            }
+            *reinterpret_cast<uint16_t *>(t + soff + 2 * r) = 0;
+            continue;
+        }
+        const uint8_t *blk = flat + (n * n_k_tiles + kt) * bb;
+        if (k8) {
+            // element pair (2cp, 2cp+1) is already adjacent in the flat block
+#pragma unroll
+            for (int cp = 0; cp < 16; ++cp)
+                *reinterpret_cast<uint16_t *>(t + cp * 64 + 2 * r) = (uint16_t)ld_u16(blk + 2 + 2 * cp);
+        } else {
+            uint32_t qs[8];                             // 16 nibble bytes as 8 halfwords
+#pragma unroll
+            for (int h = 0; h < 8; ++h) qs[h] = ld_u16(blk + 2 + 2 * h);
+#pragma unroll
+            for (int cp = 0; cp < 16; ++cp) {
+                // element e: byte e&15 of the block, low nibble for e < 16, high nibble otherwise
+                const int e0 = 2 * cp, e1 = 2 * cp + 1;
+                const uint32_t b0 = (qs[(e0 & 15) >> 1] >> (8 * (e0 & 1))) & 0xFF;
+                const uint32_t b1 = (qs[(e1 & 15) >> 1] >> (8 * (e1 & 1))) & 0xFF;
+                const uint32_t c0 = (e0 < 16) ? (b0 & 15) : (b0 >> 4);
+                const uint32_t c1 = (e1 < 16) ? (b1 & 15) : (b1 >> 4);
+                t[cp * 32 + r] = (uint8_t)(c0 | (c1 << 4));
+            }
+        }
+        *reinterpret_cast<uint16_t *>(t + soff + 2 * r) = (uint16_t)ld_u16(blk);
+    }
+}
+
+template <int TYPE>
+__global__ void __launch_bounds__(256) unpack_kernel(const uint8_t *__restrict__ tiled, int64_t n_k_tiles, int64_t N,
+                                                     uint8_t *__restrict__ flat) {
+    constexpr bool k8 = (TYPE == QMM_Q8_0);
+    constexpr int bb = k8 ? kBlock8Bytes : kBlock4Bytes;
+    constexpr int ts = k8 ? kTile8Bytes : kTile4Bytes;
+    constexpr int soff = k8 ? kScale8Off : kScale4Off;
+    const int64_t total = N * n_k_tiles;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / n_k_tiles, kt = i - n * n_k_tiles;
+        const int64_t ct = n >> 5;
+        const int r = (int)(n & 31);
+        const uint8_t *t = tiled + (ct * n_k_tiles + kt) * ts;
+        uint16_t *blk = reinterpret_cast<uint16_t *>(flat + i * bb);
+        blk[0] = (uint16_t)ld_u16(t + soff + 2 * r);
+        if (k8) {
+#pragma unroll
+            for (int cp = 0; cp < 16; ++cp) blk[1 + cp] = (uint16_t)ld_u16(t + cp * 64 + 2 * r);
+        } else {
+            uint32_t codes[32];
+#pragma unroll
+            for (int cp = 0; cp < 16; ++cp) {
+                const uint32_t b = t[cp * 32 + r];
+                codes[2 * cp] = b & 15;
+                codes[2 * cp + 1] = b >> 4;
+            }
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const uint32_t lo = codes[j] | (codes[j + 16] << 4);
+                const uint32_t hi = codes[j + 1] | (codes[j + 17] << 4);
+                blk[1 + j / 2] = (uint16_t)(lo | (hi << 8));
+            }
+        }
+    }
+}
+
+int grid_for(int64_t work, int threads) {
+    int64_t g = (work + threads - 1) / threads;
+    if (g > 152 * 16) g = 152 * 16;
+    if (g < 1) g = 1;
+    return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_repack(qmm_type t, const uint8_t *flat, int64_t K, int64_t N, uint8_t *tiled, cudaStream_t s) {
+    const int64_t nkt = K / 32, nct = (N + 31) / 32;
+    const int64_t n_tiles = nkt * nct;
+    const int threads = 256;
+    const int grid = grid_for(n_tiles * 32, threads);
+    switch (t) {
+        case QMM_Q4_0: repack_kernel<QMM_Q4_0><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
+        case QMM_IQ4_NL: repack_kernel<QMM_IQ4_NL><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
+        default: repack_kernel<QMM_Q8_0><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, uint8_t *flat, cudaStream_t s) {
+    const int64_t nkt = K / 32;
+    const int threads = 256;
+    const int grid = grid_for(N * nkt, threads);
+    switch (t) {
+        case QMM_Q4_0: unpack_kernel<QMM_Q4_0><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
+        case QMM_IQ4_NL: unpack_kernel<QMM_IQ4_NL><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
+        default: unpack_kernel<QMM_Q8_0><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace qmm

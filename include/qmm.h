@@ -1,0 +1,161 @@
+/*
+ * qmm.h -- C ABI of libqmm: matrix multiply over block-32 quantized weights stored in 32-row tiles,
+ * with activations dynamically quantized to Q8_0 blocks, on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Layouts follow "Hexagon backend developer details", section "Tiled Weight Formats":
+ *   - "Tile Dimensions and Grid Layout": a weight of logical shape [ne0 = K, ne1 = N] is cut into
+ *     tiles of 32 rows (N) x 32 columns (K).  n_k_tiles = K/32, n_col_tiles = (N+31)/32,
+ *     tile_idx = ct*n_k_tiles + kt and the tile starts at byte tile_idx*tile_size.
+ *   - "Block-32 Quantized Formats": Q4_0 and IQ4_NL tiles are 576 bytes (byte cp*32+row holds
+ *     column 2cp in its low nibble and 2cp+1 in its high nibble, cp = 0..15; 32 FP16 row scales at
+ *     bytes 512..575); Q8_0 tiles are 1088 bytes (bytes cp*64+2*row and cp*64+2*row+1 hold columns
+ *     2cp and 2cp+1 as int8; 32 FP16 row scales at bytes 1024..1087).  IQ4_NL quants are indices
+ *     into a 16-entry non-linear table.
+ *
+ * Conventions for every call below:
+ *   - Pointers named *_dev are device pointers; the caller owns every buffer and the stream.  The
+ *     library allocates no device memory and keeps no per-call state.
+ *   - Calls that take a stream only validate their arguments on the host and enqueue work on that
+ *     stream; they return before the GPU has run.  `stream` is a cudaStream_t (NULL = legacy
+ *     default stream).  Calls on different streams with distinct outputs may run concurrently.
+ *   - Argument errors are reported before anything is enqueued; a failed launch returns
+ *     QMM_ERR_CUDA.  Nothing is thrown and nothing aborts across this interface.
+ *   - fp16 values are IEEE binary16 bit patterns in uint16_t, little-endian in memory.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                        /* cudaStream_t is `struct CUstream_st *` */
+typedef struct CUstream_st *qmm_stream_t;
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_INVALID_ARG = 1,   /* a size, stride or required pointer is invalid */
+    QMM_ERR_UNSUPPORTED = 2,   /* type or path not implemented */
+    QMM_ERR_MISALIGNED = 3,    /* a pointer or stride violates the stated alignment */
+    QMM_ERR_CUDA = 4,          /* the CUDA runtime reported an error at launch */
+    QMM_ERR_TIMEOUT = 5        /* a kernel gave up waiting on its own pipeline (see qmm_device_status) */
+} qmm_status;
+
+typedef enum { QMM_Q4_0 = 0, QMM_Q8_0 = 1, QMM_IQ4_NL = 2 } qmm_type;
+
+/* Which kernel qmm_matmul_path runs: AUTO picks the decode matvec for M <= qmm_decode_max_m()
+ * and the tensor-core GEMM otherwise. */
+typedef enum { QMM_PATH_AUTO = 0, QMM_PATH_MATVEC = 1, QMM_PATH_GEMM = 2 } qmm_path;
+
+/* Human-readable name of a status code (static string, never NULL). */
+QMM_API const char *qmm_status_str(qmm_status st);
+
+/* Bytes of one flat GGML block of 32 weights: 18 (Q4_0, IQ4_NL: fp16 d + 16 nibble bytes, element
+ * j in the low nibble of byte j, element j+16 in its high nibble) or 34 (Q8_0: fp16 d + 32 int8).
+ * 0 for an unknown type. */
+QMM_API size_t qmm_block_size(qmm_type t);
+
+/* Bytes of one tile ("Block-32 Quantized Formats"): 576 (Q4_0, IQ4_NL) or 1088 (Q8_0); 0 if unknown. */
+QMM_API size_t qmm_tile_size(qmm_type t);
+
+/* Bytes of the tiled weight [K, N] ("Tile Dimensions and Grid Layout"):
+ * n_col_tiles * n_k_tiles * tile_size.  0 if K <= 0, K % 32 != 0, N <= 0 or the type is unknown. */
+QMM_API size_t qmm_tiled_size(qmm_type t, int64_t K, int64_t N);
+
+/* Bytes of the flat weight: N rows of K/32 GGML blocks.  0 on the same invalid inputs. */
+QMM_API size_t qmm_flat_size(qmm_type t, int64_t K, int64_t N);
+
+/* The 16-entry IQ4_NL table the kernels use (int8 values, ascending).  The pages name the table
+ * (iq4_nl_to_fp16_lut) without printing it; the built-in one is the 16-level Lloyd-Max quantizer of
+ * a unit normal scaled to +-127.  Writes 16 bytes to `out`. */
+QMM_API void qmm_iq4nl_table(int8_t out[16]);
+
+/* Largest activation row count M that QMM_PATH_AUTO sends to the decode matvec. */
+QMM_API int64_t qmm_decode_max_m(void);
+
+/*
+ * qmm_quantize_weight -- fp32 weight rows -> flat GGML blocks (model-load helper, not the hot path).
+ *   w_dev      fp32, N rows of K values, row n at w_dev + n*ldw; 16-byte aligned, ldw % 4 == 0.
+ *   w_flat_dev output, qmm_flat_size(t, K, N) bytes, row-major blocks; 2-byte aligned.
+ * Rules per 32-element block (x = the block, m = its signed element of largest magnitude, first on
+ * ties): Q8_0 d = max|x|/127, q = round-half-away(x/d) (computed as x * (1/d));  Q4_0 d = m/-8,
+ * q = min(15, trunc(x*(1/d) + 8.5));  IQ4_NL d = m/table[0], q = the table index whose level
+ * fp16(d)*table[q] is nearest to x (lowest index on ties).  d is stored rounded to fp16.
+ * Errors: INVALID_ARG (N <= 0, K <= 0, K % 32, ldw < K, NULL), UNSUPPORTED (type), MISALIGNED.
+ */
+QMM_API qmm_status qmm_quantize_weight(qmm_type t, const float *w_dev, int64_t N, int64_t K, int64_t ldw,
+                               void *w_flat_dev, qmm_stream_t stream);
+
+/*
+ * qmm_repack -- flat GGML rows -> tiles ("Tiled Weight Formats"; the pages repack at model load,
+ * in set_tensor() or rt-repack).
+ *   w_flat_dev  N rows of K/32 blocks (qmm_flat_size bytes); 2-byte aligned.
+ *   w_tiled_dev output, qmm_tiled_size bytes; 16-byte aligned.  Rows past N in the last column tile
+ *               are written as zero bytes (scale 0, quants 0).  The buffers must not overlap.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED.  Bit-exact, lossless.
+ */
+QMM_API qmm_status qmm_repack(qmm_type t, const void *w_flat_dev, int64_t K, int64_t N, void *w_tiled_dev,
+                      qmm_stream_t stream);
+
+/* qmm_unpack -- inverse of qmm_repack (tiles -> flat rows); used to check a tiled buffer. Same
+ * arguments and alignment rules with the roles of the two buffers swapped. */
+QMM_API qmm_status qmm_unpack(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N, void *w_flat_dev,
+                      qmm_stream_t stream);
+
+/*
+ * qmm_quantize_act -- dynamic Q8_0 quantization of activations (the pages quantize activations into
+ * Q8_0 blocks before the matmul; "Memory buffers").
+ *   x_dev  fp32, M rows of K values, row m at x_dev + m*ldx; 4-byte aligned (16-byte aligned with
+ *          ldx % 4 == 0 takes the vectorised path).
+ *   a_q_dev output int8 [M][K] (row stride K); 16-byte aligned.
+ *   a_d_dev output fp16 bits [M][K/32], the scale of each block; 4-byte aligned.
+ * Per block of 32: amax = max|x|, d = amax/127, id = (d != 0) ? 1/d : 0, q = round half away from
+ * zero of x*id, clamped to [-127, 127] (a NaN product gives 0); a_d = fp16(d).  IEEE fp32 division
+ * and rounding, no fused multiply-add, no flush-to-zero.  Inputs must be finite.
+ * Errors: INVALID_ARG (M <= 0, K <= 0, K % 32, ldx < K, NULL), MISALIGNED.
+ */
+QMM_API qmm_status qmm_quantize_act(const float *x_dev, int64_t M, int64_t K, int64_t ldx, int8_t *a_q_dev,
+                            uint16_t *a_d_dev, qmm_stream_t stream);
+
+/*
+ * qmm_matmul -- Y = A * W^T over tiled weights:
+ *   Y[m, n] = sum_b fp32(d_w[n, b]) * fp32(d_a[m, b]) * S_b[m, n],
+ *   S_b[m, n] = sum_{j<32} w_int[n, 32b+j] * a_q[m, 32b+j]  (exact integer block dot products),
+ *   w_int = q-8 (Q4_0), q (Q8_0), table[q] (IQ4_NL).
+ *   w_tiled_dev  qmm_tiled_size bytes from qmm_repack; 16-byte aligned.
+ *   a_q_dev, a_d_dev  as written by qmm_quantize_act for M rows and the same K.
+ *   y_dev  fp32 output, y[m*ldy + n] for n < N (other columns untouched); 4-byte aligned.
+ * Accumulation is fp32 in a fixed order (results are reproducible run to run); the error against
+ * the exact value is at most about n_k_tiles * 2^-24 * sum_k |w_k * x_k| (dequantized).
+ * Errors: INVALID_ARG (sizes, ldy < N, NULL), UNSUPPORTED, MISALIGNED, CUDA.
+ */
+QMM_API qmm_status qmm_matmul(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N, const int8_t *a_q_dev,
+                      const uint16_t *a_d_dev, int64_t M, float *y_dev, int64_t ldy, qmm_stream_t stream);
+
+/* qmm_matmul_path -- qmm_matmul with the kernel chosen by the caller.  QMM_PATH_MATVEC accepts any
+ * M (rows are processed in groups of qmm_decode_max_m()); QMM_PATH_GEMM any M >= 1. */
+QMM_API qmm_status qmm_matmul_path(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N,
+                           const int8_t *a_q_dev, const uint16_t *a_d_dev, int64_t M, float *y_dev,
+                           int64_t ldy, qmm_path path, qmm_stream_t stream);
+
+/*
+ * qmm_device_status -- synchronizes `stream`, then returns and clears the library's device status
+ * word for the current device: QMM_OK, or QMM_ERR_TIMEOUT when a pipelined kernel gave up on one of
+ * its bounded waits (its outputs are then undefined).  QMM_ERR_CUDA if the synchronization fails.
+ */
+QMM_API qmm_status qmm_device_status(qmm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -1,0 +1,66 @@
+"""Helpers for the GPU parity tests: run one workload through the CUDA path (libqmm, via the binding)
+and through the CPU oracle, on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+
+TYPES = ["q4_0", "q8_0", "iq4_nl"]
+
+
+def torch_mod():
+    import torch
+
+    return torch
+
+
+def dev_u8(a: np.ndarray):
+    torch = torch_mod()
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.uint8).reshape(-1)).cuda()
+
+
+def gpu_prepare_weight(type_, w: np.ndarray):
+    """fp32 [N, K] -> (flat, tiled) on the GPU through qmm_quantize_weight + qmm_repack."""
+    import block_quantized_matmul_gb300 as qmm
+
+    torch = torch_mod()
+    N, K = w.shape
+    w_d = torch.from_numpy(np.ascontiguousarray(w)).cuda()
+    flat = torch.empty(qmm.flat_size(type_, K, N), dtype=torch.uint8, device="cuda")
+    tiled = torch.full((qmm.tiled_size(type_, K, N),), 0xA5, dtype=torch.uint8, device="cuda")
+    qmm.qmm_quantize_weight(type_, w_d, N, K, K, flat)
+    qmm.qmm_repack(type_, flat, K, N, tiled)
+    return flat, tiled
+
+
+def gpu_quantize_act(x: np.ndarray):
+    import block_quantized_matmul_gb300 as qmm
+
+    torch = torch_mod()
+    M, K = x.shape
+    x_d = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    a_q = torch.full((M, K), 99, dtype=torch.int8, device="cuda")
+    a_d = torch.full((M, K // 32), 0x7E00, dtype=torch.int16, device="cuda")
+    qmm.qmm_quantize_act(x_d, M, K, K, a_q, a_d)
+    return a_q, a_d
+
+
+def gpu_matmul(type_, tiled, K, N, a_q, a_d, M, path=0, ldy=None):
+    import block_quantized_matmul_gb300 as qmm
+
+    torch = torch_mod()
+    ldy = N if ldy is None else ldy
+    y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    qmm.qmm_matmul_path(type_, tiled, K, N, a_q, a_d, M, y, ldy, path)
+    torch.cuda.synchronize()
+    return y
+
+
+def assert_within_bound(y_gpu: np.ndarray, y_ref: np.ndarray, bound: np.ndarray, what=""):
+    """|gpu - oracle| <= 1e-5 * sum_k |w_k x_k| + 1e-6, element by element."""
+    err = np.abs(y_gpu.astype(np.float64) - y_ref)
+    tol = 1e-5 * bound + 1e-6
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance, e.g. at {idx.tolist()}: "
+                             f"gpu={y_gpu[tuple(idx[0])]}, ref={y_ref[tuple(idx[0])]}, tol={tol[tuple(idx[0])]}")

@@ -1,0 +1,120 @@
+"""Host-side checks of libqmm that need no GPU: exported symbols, size queries, argument errors.
+
+Every call below fails validation before anything is launched, so no CUDA device is touched.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_quantized_matmul_gb300 as qmm
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qmm.h")
+INVALID, UNSUPPORTED, MISALIGNED = 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def L():
+    from block_quantized_matmul_gb300 import build
+
+    build.build()
+    return qmm.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"QMM_API[^;(]*?\b(qmm_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    for required in ("qmm_repack", "qmm_quantize_act", "qmm_matmul", "qmm_tiled_size", "qmm_tile_size",
+                     "qmm_status_str", "qmm_unpack"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_sizes(L):
+    assert qmm.tile_size("q4_0") == 576 and qmm.tile_size("iq4_nl") == 576 and qmm.tile_size("q8_0") == 1088
+    assert qmm.block_size("q4_0") == 18 and qmm.block_size("q8_0") == 34
+    assert qmm.tiled_size("q4_0", 4096, 4096) == 9437184
+    assert qmm.tiled_size("q8_0", 4096, 14336) == 62390272
+    assert qmm.tiled_size("q8_0", 4096, 128256) == 558170112
+    assert qmm.tiled_size("q4_0", 64, 33) == 4 * 576
+    assert qmm.flat_size("q8_0", 64, 33) == 33 * 2 * 34
+    assert qmm.tiled_size("q4_0", 33, 64) == 0 and qmm.tiled_size("q4_0", 0, 64) == 0
+    assert qmm.tiled_size("q4_0", 64, 0) == 0 and qmm.tiled_size(7, 64, 64) == 0
+    assert L.qmm_tile_size(9) == 0
+    assert qmm.decode_max_m() >= 8
+
+
+def test_iq4nl_table_matches_the_oracle(L, orc):
+    assert qmm.iq4nl_table() == list(orc.iq4nl_table())
+
+
+def test_status_strings(L):
+    for st in range(6):
+        assert L.qmm_status_str(st)
+    assert L.qmm_status_str(99) == b"unknown status"
+
+
+P = 1 << 20          # a fake, 16-byte aligned, non-null address (never dereferenced: validation fails first)
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, P, 0, 64, P, P, 1, P, 64, None), INVALID),      # K = 0
+    ((0, P, 48, 64, P, P, 1, P, 64, None), INVALID),     # K % 32
+    ((0, P, 64, 0, P, P, 1, P, 64, None), INVALID),      # N = 0
+    ((0, P, 64, 64, P, P, 0, P, 64, None), INVALID),     # M = 0
+    ((0, P, 64, 64, P, P, -3, P, 64, None), INVALID),    # M < 0
+    ((0, P, 64, 64, P, P, 1, P, 63, None), INVALID),     # ldy < N
+    ((0, None, 64, 64, P, P, 1, P, 64, None), INVALID),  # NULL weight
+    ((0, P, 64, 64, None, P, 1, P, 64, None), INVALID),  # NULL a_q
+    ((0, P, 64, 64, P, None, 1, P, 64, None), INVALID),  # NULL a_d
+    ((0, P, 64, 64, P, P, 1, None, 64, None), INVALID),  # NULL y
+    ((5, P, 64, 64, P, P, 1, P, 64, None), UNSUPPORTED),  # unknown type
+    ((0, P + 8, 64, 64, P, P, 1, P, 64, None), MISALIGNED),
+    ((0, P, 64, 64, P + 4, P, 1, P, 64, None), MISALIGNED),
+    ((0, P, 64, 64, P, P + 2, 1, P, 64, None), MISALIGNED),
+    ((0, P, 64, 64, P, P, 1, P + 2, 64, None), MISALIGNED),
+])
+def test_matmul_argument_errors(L, args, expect):
+    assert L.qmm_matmul(*args) == expect
+
+
+def test_matmul_path_rejects_unknown_path(L):
+    assert L.qmm_matmul_path(0, P, 64, 64, P, P, 1, P, 64, 7, None) == UNSUPPORTED
+
+
+def test_quantize_act_argument_errors(L):
+    assert L.qmm_quantize_act(P, 0, 64, 64, P, P, None) == INVALID
+    assert L.qmm_quantize_act(P, 2, 40, 64, P, P, None) == INVALID
+    assert L.qmm_quantize_act(P, 2, 64, 32, P, P, None) == INVALID
+    assert L.qmm_quantize_act(None, 2, 64, 64, P, P, None) == INVALID
+    assert L.qmm_quantize_act(P + 1, 2, 64, 64, P, P, None) == MISALIGNED
+    assert L.qmm_quantize_act(P, 2, 64, 64, P + 4, P, None) == MISALIGNED
+    assert L.qmm_quantize_act(P, 2, 64, 64, P, P + 2, None) == MISALIGNED
+
+
+def test_repack_and_quantize_weight_argument_errors(L):
+    assert L.qmm_repack(0, P, 48, 64, P, None) == INVALID
+    assert L.qmm_repack(0, None, 64, 64, P, None) == INVALID
+    assert L.qmm_repack(3, P, 64, 64, P, None) == UNSUPPORTED
+    assert L.qmm_repack(0, P + 1, 64, 64, P, None) == MISALIGNED
+    assert L.qmm_repack(0, P, 64, 64, P + 8, None) == MISALIGNED
+    assert L.qmm_unpack(1, P + 8, 64, 64, P, None) == MISALIGNED
+    assert L.qmm_unpack(1, P, 64, -1, P, None) == INVALID
+    assert L.qmm_quantize_weight(0, P, 64, 64, 60, P, None) == INVALID      # ldw < K
+    assert L.qmm_quantize_weight(0, P, 64, 64, 66, P, None) == MISALIGNED   # ldw % 4
+    assert L.qmm_quantize_weight(0, P + 4, 64, 64, 64, P, None) == MISALIGNED
+    assert L.qmm_quantize_weight(9, P, 64, 64, 64, P, None) == UNSUPPORTED
+
+
+def test_binding_raises_on_error(L):
+    with pytest.raises(qmm.QmmError):
+        qmm.qmm_matmul("q4_0", P, 48, 64, P, P, 1, P, 64, stream=0)
