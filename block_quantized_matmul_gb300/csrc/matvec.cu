@@ -1,387 +1,523 @@
-// matvec.cu -- decode-shaped matmul (M <= 16 activation rows) over 32-row weight tiles.
+// matvec.cu -- decode-shaped matmul (M <= 16 activation rows per pass) over 32-row weight tiles.
 //
 // What it computes ("Hexagon backend developer details", "Tiled Weight Formats"):
 //   Y[m, n] = sum_b fp32(d_w[n,b]) * fp32(d_a[m,b]) * S_b[m,n],  S_b = sum_j w_int[n,32b+j] * a_q[m,32b+j]
 // with w_int = q-8 (Q4_0), q (Q8_0), table[q] (IQ4_NL) read from the tile layouts of "Block-32
-// Quantized Formats".  The pages' own decode kernel is an HVX 32x1 / 32x2 vector dot product against
-// Q8_0 activation tiles; on GB300 the block dot products run on the tensor cores instead.
+// Quantized Formats".  The pages' decode kernel is an HVX 32x1 / 32x2 vector dot product fed by a
+// DDR -> DMA -> VTCM multi-buffered pipeline ("DDR -> DMA -> VTCM Execution Pipeline"); this is the
+// GB300 counterpart of both.
 //
 // GB300 design:
-//   * Weight bytes are streamed once from HBM with 4/8-byte vector loads straight into registers;
-//     each warp owns one column tile (32 rows) and a strided subset of its K tiles.
-//   * Quants are decoded to fp16 holding the exact integer value (|v| <= 127), activations are the
-//     int8 quants as fp16, and `mma.sync.m16n8k16` with fp32 accumulation produces the exact integer
-//     block sums S_b (every partial sum is an integer below 2^24).  fp16 mma runs at ~4x the rate of
-//     the int8 mma.sync path on sm_103a, and int8 tcgen05 does not exist there.
-//   * Dot products within a block do not depend on the order of k, nor on which logical mma row a
-//     weight row occupies: each thread takes the 4 tile rows 4g..4g+3 of one 4-byte word and the
-//     column pairs cp = t, t+4, t+8, t+12, so every load is a whole word of the tile.
-//   * Per block, the fp32 result is rescaled by d_w*d_a in registers and accumulated in fp32.
-//   * Split-K across the CTAs of a thread-block cluster; partial sums are added in a fixed order
-//     through distributed shared memory, so results are bit-reproducible (no atomics).
-#include <cooperative_groups.h>
-
+//   * Persistent CTAs (one or two per SM) each own a set of column tiles.  The K tiles of a column
+//     tile are contiguous in memory (tile_idx = ct*n_k_tiles + kt), so one producer warp streams them
+//     with 1-D cp.async.bulk copies of 8 tiles into a deep shared-memory ring (mbarrier
+//     complete_tx / consumer release) -- the pipelined multi-buffering of the pages, with the TMA
+//     engine as the DMA queue.
+//   * 8 consumer warps take one tile of each stage.  Quants become fp16 holding exact integers
+//     (biased: 1024+q or 1152+q, see decode_*), activations are staged once per CTA as fp16 in the
+//     mma fragment order, and mma.sync.m16n8k16 (fp32 accumulate) yields block sums that are exact
+//     integers; subtracting the exact per-(token, block) bias gives S_b.  fp16 mma.sync runs at ~4x
+//     the int8 mma.sync rate on sm_103a, where int8 tcgen05 does not exist.
+//   * Per block the fp32 result is rescaled by d_w*d_a with packed f32x2 arithmetic and accumulated.
+//   * No atomics and no scratch memory: each column tile is reduced across the 8 warps in a fixed
+//     order; if the staged activations would not fit, K is processed in passes that add into y.
 #include "qmm_internal.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace qmm {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kChunkTiles = 32;          // K tiles of activations staged in shared memory at a time
-constexpr int kActPad = 8;               // halfs of padding per staged activation row (bank spread)
-constexpr int kLutCopies = 16;           // IQ4_NL byte->half2 table copies (spreads banks)
-constexpr int kUnroll = 4;               // tiles loaded ahead per warp
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = 32 * (1 + kConsumerWarps);     // warp 0 = producer
+constexpr int kTilesPerStage = kConsumerWarps;          // one tile per consumer warp per stage
+constexpr int kLutCopies = 16;
+constexpr int kActBudget = 64 * 1024;                   // bytes of staged activations per CTA
+constexpr int kSmemLimit = 227 * 1024;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
-struct MatvecParams {
+struct MvParams {
     const uint8_t *tiled;
     const int8_t *a_q;
     const uint16_t *a_d;
     float *y;
-    int64_t nkt;          // K / 32
-    int64_t N;
-    int64_t ldy;
-    int M;                // activation rows in this launch (<= 8 * NF)
-    int kt_per_cta;       // K tiles handled by one CTA of the split
-    int ksplit;           // CTAs per column tile (= cluster size along y)
+    int64_t K, nkt, N, ldy, n_col_tiles;
+    int M;            // tokens in this launch (<= 8 * NF)
+    int kt0, nkc;     // K-tile range of this pass: [kt0, kt0 + nkc)
+    int accumulate;   // 0: y = result, 1: y += result
+    int stages;       // ring depth
     Lut16 lut;
 };
 
-__device__ __forceinline__ uint32_t ldg_u32(const uint8_t *p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
+__device__ unsigned g_mv_status = 0;   // set when a bounded wait gave up (reported with the GEMM's word)
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
-__device__ __forceinline__ uint2 ldg_u64(const uint8_t *p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-    return v;
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            *abort = 1;
+            atomicOr(&g_mv_status, 1u);
+            return false;
+        }
+    }
+}
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > kWaitLimitNs / 4) return;
+    }
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void consumer_sync() {      // named barrier over the 8 consumer warps
+    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-// Q4_0 byte i of a tile word -> half2(lo - 8, hi - 8), exact.  The byte is copied into both 16-bit
-// halves; the low nibble becomes the mantissa of 1024 + lo, the high nibble that of 1024 + 16*hi,
-// and one fp16 fma removes the offsets.
-template <int I>
-__device__ __forceinline__ uint32_t q4_pair(uint32_t w) {
-    const uint32_t y = __byte_perm(w, 0u, 0x4040u | (I << 8) | I);
-    uint32_t h;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(y), "r"(0x00F0000Fu), "r"(0x64006400u));  // (y & b) | c
-    const __half2 r = __hfma2(bits_h2(h), __halves2half2(__float2half_rn(1.0f), __float2half_rn(0.0625f)),
-                              __halves2half2(__float2half_rn(-1032.0f), __float2half_rn(-72.0f)));
-    return h2_bits(r);
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+    unsigned long long v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(a), "f"(b));
+    return v;
+}
+__device__ __forceinline__ void unpack2(unsigned long long v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
-// Q8_0: two int8 of one row (bytes I, I+1 of w) -> half2, exact: (b ^ 0x80) is b + 128 as an
-// unsigned byte, placed in the mantissa of 1024; subtracting 1152 leaves b.
-template <int SEL>
-__device__ __forceinline__ uint32_t q8_pair(uint32_t w_xor) {
-    const uint32_t h = __byte_perm(w_xor, 0x64646464u, SEL);
-    const __half2 r = __hsub2(bits_h2(h), __halves2half2(__float2half_rn(1152.0f), __float2half_rn(1152.0f)));
-    return h2_bits(r);
-}
-
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Raw bytes of one tile held by one thread.
-template <int TYPE>
-struct TileRegs;
-template <>
-struct TileRegs<QMM_Q8_0> {
-    uint2 q[4];
-    uint2 sc;
-};
-template <int TYPE>
-struct TileRegs {
-    uint32_t q[4];
-    uint2 sc;
-};
-
-template <int TYPE>
-__device__ __forceinline__ void load_tile(TileRegs<TYPE> &r, const uint8_t *tp, int g, int t) {
-    if constexpr (TYPE == QMM_Q8_0) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) r.q[q] = ldg_u64(tp + (t + 4 * q) * 64 + 8 * g);
-        r.sc = ldg_u64(tp + kScale8Off + 8 * g);
-    } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) r.q[q] = ldg_u32(tp + (t + 4 * q) * 32 + 4 * g);
-        r.sc = ldg_u64(tp + kScale4Off + 8 * g);
-    }
+// ---- weight decode: 16 half2 H[q][r] = (column 2cp, 2cp+1) of tile row 4g+r, cp = t + 4q ----
+// Q4_0: byte -> half2(1024 + lo, 1024 + 16*hi).  With the odd-column activations staged divided by
+// 16 (exact), the mma sums (1024+lo)*a_even + (64+hi)*a_odd; the bias 1032*sum(a_even) +
+// 72*sum(a_odd) (which also removes the -8 offset) is subtracted per token and block.
+template <int I>
+__device__ __forceinline__ uint32_t q4_biased(uint32_t w) {
+    const uint32_t y = __byte_perm(w, 0u, 0x4040u | (I << 8) | I);
+    uint32_t h;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(y), "r"(0x00F0000Fu), "r"(0x64006400u));
+    return h;
 }
+// Q8_0: two int8 -> half2(1152 + b0, 1152 + b1) (b ^ 0x80 = b + 128 placed in the mantissa of 1024);
+// bias 1152*sum(a) per token and block.
+template <int SEL>
+__device__ __forceinline__ uint32_t q8_biased(uint32_t w_xor) { return __byte_perm(w_xor, 0x64646464u, SEL); }
 
-// Decode to H[q][i]: half2 of (column 2cp, 2cp+1) for tile row 4g+i, column pair cp = t + 4q.
 template <int TYPE>
-__device__ __forceinline__ void decode_tile(const TileRegs<TYPE> &r, uint32_t (&H)[4][4], const uint32_t *lut_s,
-                                            int copy) {
+__device__ __forceinline__ void decode_tile(const uint8_t *tile, int g, int t, uint32_t (&H)[4][4],
+                                            const uint32_t *lut_lane) {
     if constexpr (TYPE == QMM_Q8_0) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint32_t x = r.q[q].x ^ 0x80808080u, z = r.q[q].y ^ 0x80808080u;
-            H[q][0] = q8_pair<0x4140>(x);
-            H[q][1] = q8_pair<0x4342>(x);
-            H[q][2] = q8_pair<0x4140>(z);
-            H[q][3] = q8_pair<0x4342>(z);
-        }
-    } else if constexpr (TYPE == QMM_Q4_0) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            H[q][0] = q4_pair<0>(r.q[q]);
-            H[q][1] = q4_pair<1>(r.q[q]);
-            H[q][2] = q4_pair<2>(r.q[q]);
-            H[q][3] = q4_pair<3>(r.q[q]);
+            const uint2 v = *reinterpret_cast<const uint2 *>(tile + (t + 4 * q) * 64 + 8 * g);
+            const uint32_t x = v.x ^ 0x80808080u, z = v.y ^ 0x80808080u;
+            H[q][0] = q8_biased<0x4140>(x);
+            H[q][1] = q8_biased<0x4342>(x);
+            H[q][2] = q8_biased<0x4140>(z);
+            H[q][3] = q8_biased<0x4342>(z);
         }
     } else {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(tile + (t + 4 * q) * 32 + 4 * g);
+            if constexpr (TYPE == QMM_Q4_0) {
+                H[q][0] = q4_biased<0>(w);
+                H[q][1] = q4_biased<1>(w);
+                H[q][2] = q4_biased<2>(w);
+                H[q][3] = q4_biased<3>(w);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t b = (r.q[q] >> (8 * i)) & 0xFFu;
-                H[q][i] = lut_s[b * kLutCopies + copy];
+                for (int r = 0; r < 4; ++r) H[q][r] = lut_lane[((w >> (8 * r)) & 0xFFu) * kLutCopies];
             }
         }
     }
+}
+
+// Token stride of the staged activations in uint4 units: an odd multiple of 4, so the 8 lanes of a
+// quarter-warp (2 tokens x 4 column groups) read 8 distinct 16-byte bank groups.
+__host__ __device__ inline int act_tok_stride(int nkc) { return nkc * 4 + ((nkc & 1) ? 0 : 4); }
+
+// Shared-memory layout (offsets in bytes from a 128-byte aligned base).
+struct MvLayout {
+    int ring, bars, act, da, corr, red, lut, total;
+};
+template <int TYPE, int NF>
+__host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
+    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    MvLayout L;
+    int off = 0;
+    L.ring = off;  off += stages * kTilesPerStage * TS;
+    off = (off + 15) & ~15;
+    L.bars = off;  off += 2 * stages * 8 + 16;
+    off = (off + 15) & ~15;
+    L.act = off;   off += M * act_tok_stride(nkc) * 16;     // [M][stride] uint4 (16 half2 per block)
+    L.da = off;    off += nkc * 8 * NF * 4;                 // [nkc][8*NF] float
+    L.corr = off;  off += nkc * 8 * NF * 4;                 // [nkc][8*NF] float
+    L.red = off;   off += kConsumerWarps * 2 * NF * 4 * 32 * 4;
+    L.lut = off;   off += (TYPE == QMM_IQ4_NL) ? 256 * kLutCopies * 4 : 0;
+    L.total = off;
+    return L;
 }
 
 template <int TYPE, int NF>
-__global__ void __launch_bounds__(kThreads) matvec_kernel(const MatvecParams p) {
+__global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvParams p) {
     constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    constexpr int SOFF = (TYPE == QMM_Q8_0) ? kScale8Off : kScale4Off;
     constexpr int TOK = 8 * NF;
-    constexpr int ROW_H = kChunkTiles * 32 + kActPad;       // staged activation row stride (halfs)
-
-    extern __shared__ __align__(16) uint8_t smem[];
-    __half *act_s = reinterpret_cast<__half *>(smem);                                   // [TOK][ROW_H]
-    float *da_s = reinterpret_cast<float *>(smem + TOK * ROW_H * 2);                     // [TOK][kChunkTiles]
-    float *red_s = da_s + TOK * kChunkTiles;                                             // [kWarps][2][NF][4][32]
-    uint32_t *lut_s = reinterpret_cast<uint32_t *>(red_s + kWarps * 2 * NF * 4 * 32);     // [256][kLutCopies]
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    const MvLayout L = mv_layout<TYPE, NF>(p.M, p.nkc, p.stages);
+    uint8_t *ring = smem + L.ring;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + p.stages;
+    volatile int *abort = reinterpret_cast<volatile int *>(empty + p.stages);
+    uint4 *act_s = reinterpret_cast<uint4 *>(smem + L.act);      // [M][act_tok_stride] uint4
+    const int tok_stride = act_tok_stride(p.nkc);
+    float *da_s = reinterpret_cast<float *>(smem + L.da);         // [nkc][TOK]
+    float *corr_s = reinterpret_cast<float *>(smem + L.corr);     // [nkc][TOK]
+    float *red_s = reinterpret_cast<float *>(smem + L.red);
+    uint32_t *lut_s = reinterpret_cast<uint32_t *>(smem + L.lut);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int64_t ct = blockIdx.x;
-    const int64_t kt_begin = (int64_t)blockIdx.y * p.kt_per_cta;
-    const int64_t kt_end = (kt_begin + p.kt_per_cta < p.nkt) ? kt_begin + p.kt_per_cta : p.nkt;
+    const int stages = p.stages;
+    const int nkc = p.nkc;
 
-    if constexpr (TYPE == QMM_IQ4_NL) {
-        for (int i = threadIdx.x; i < 256 * kLutCopies; i += kThreads) {
-            const int b = i / kLutCopies;
-            const __half2 v = __halves2half2(__int2half_rn(p.lut.v[b & 15]), __int2half_rn(p.lut.v[b >> 4]));
-            lut_s[i] = h2_bits(v);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), kConsumerWarps);
         }
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ============================== producer ==============================
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t ct = blockIdx.x; ct < p.n_col_tiles && ok; ct += gridDim.x) {
+            const uint8_t *src = p.tiled + (ct * p.nkt + p.kt0) * TS;
+            for (int j0 = 0; j0 < nkc; j0 += kTilesPerStage, ++it) {
+                const int s = (int)(it % (uint32_t)stages);
+                const uint32_t ph = (it / (uint32_t)stages) & 1u;
+                if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort)) { ok = false; break; }
+                if (lane == 0) {
+                    const int nt = (nkc - j0) < kTilesPerStage ? (nkc - j0) : kTilesPerStage;
+                    const uint32_t bytes = (uint32_t)(nt * TS);
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    bulk_g2s(smem_u32(ring + s * kTilesPerStage * TS), src + (int64_t)j0 * TS, bytes, fb);
+                }
+                __syncwarp();
+            }
+        }
+        // copies in flight land before the CTA may exit
+        if (lane == 0 && it > 0) {
+            const uint32_t last = it - 1;
+            for (uint32_t k = 0; k < (uint32_t)stages && k <= last; ++k) {
+                const uint32_t i = last - k;
+                wait_drain(smem_u32(&full[i % stages]), (i / stages) & 1u);
+            }
+        }
+        return;
     }
 
-    float acc[2][NF][4];
-#pragma unroll
-    for (int rb = 0; rb < 2; ++rb)
-#pragma unroll
-        for (int nf = 0; nf < NF; ++nf)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[rb][nf][c] = 0.0f;
+    // ============================== consumers ==============================
+    const int cw = warp - 1;                  // consumer warp 0..7
+    const int ctid = threadIdx.x - 32;        // 0..255
+    const int g = lane >> 2, t = lane & 3;
 
-    const uint8_t *col_base = p.tiled + (size_t)ct * p.nkt * TS;
-
-    for (int64_t c0 = kt_begin; c0 < kt_end; c0 += kChunkTiles) {
-        const int nt = (int)((kt_end - c0) < kChunkTiles ? (kt_end - c0) : kChunkTiles);
-        // ---- stage activations of this chunk: int8 -> fp16 (exact), rows >= M zero ----
-        __syncthreads();
-        {
-            const int words_per_row = nt * 8;                  // 4 int8 per word
-            for (int i = threadIdx.x; i < TOK * words_per_row; i += kThreads) {
-                const int tok = i / words_per_row, wi = i - tok * words_per_row;
-                uint32_t v = 0;
-                if (tok < p.M) v = __ldg(reinterpret_cast<const uint32_t *>(p.a_q + (int64_t)tok * p.nkt * 32 + c0 * 32) + wi);
-                const __half2 lo = __halves2half2(__int2half_rn((int8_t)(v & 0xFF)), __int2half_rn((int8_t)((v >> 8) & 0xFF)));
-                const __half2 hi = __halves2half2(__int2half_rn((int8_t)((v >> 16) & 0xFF)), __int2half_rn((int8_t)(v >> 24)));
-                uint2 st;
-                st.x = h2_bits(lo);
-                st.y = h2_bits(hi);
-                *reinterpret_cast<uint2 *>(act_s + tok * ROW_H + wi * 4) = st;
-            }
-            for (int i = threadIdx.x; i < TOK * nt; i += kThreads) {
-                const int tok = i / nt, j = i - tok * nt;
-                float d = 0.0f;
-                if (tok < p.M) d = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + c0 + j]));
-                da_s[tok * kChunkTiles + j] = d;
-            }
+    // ---- stage activations once: per (token, block) 16 half2 in fragment order, plus the
+    //      per-block scale and the exact bias of the biased weight decode ----
+    if constexpr (TYPE == QMM_IQ4_NL) {
+        for (int i = ctid; i < 256 * kLutCopies; i += kConsumerWarps * 32) {
+            const int b = i / kLutCopies;
+            lut_s[i] = h2_bits(__halves2half2(__int2half_rn(p.lut.v[b & 15]), __int2half_rn(p.lut.v[b >> 4])));
         }
-        __syncthreads();
+    }
+    for (int i = ctid; i < TOK * nkc; i += kConsumerWarps * 32) {
+        const int j = i / TOK, tok = i - j * TOK;
+        float d = 0.0f, corr = 0.0f;
+        if (tok < p.M) {
+            const int64_t kt = p.kt0 + j;
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.a_q + (int64_t)tok * p.K + kt * 32);
+            const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+            const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            int sum_even = 0, sum_odd = 0;
+            uint32_t hp[16];                 // half2 of column pair cp, in cp order
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int a0 = (int)(int8_t)((wv[wi] >> (16 * h)) & 0xFF);
+                    const int a1 = (int)(int8_t)((wv[wi] >> (16 * h + 8)) & 0xFF);
+                    sum_even += a0;
+                    sum_odd += a1;
+                    const float f1 = (TYPE == QMM_Q4_0) ? (float)a1 * 0.0625f : (float)a1;   // exact
+                    hp[2 * wi + h] = h2_bits(__halves2half2(__float2half_rn((float)a0), __float2half_rn(f1)));
+                }
+            }
+            // fragment order: position 4t + q holds column pair t + 4q
+            uint4 *dst = act_s + tok * tok_stride + j * 4;
+#pragma unroll
+            for (int tt = 0; tt < 4; ++tt) dst[tt] = make_uint4(hp[tt], hp[tt + 4], hp[tt + 8], hp[tt + 12]);
+            d = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
+            if (TYPE == QMM_Q4_0) corr = 1032.0f * (float)sum_even + 72.0f * (float)sum_odd;
+            else if (TYPE == QMM_Q8_0) corr = 1152.0f * (float)(sum_even + sum_odd);
+        }
+        da_s[j * TOK + tok] = d;
+        corr_s[j * TOK + tok] = corr;
+    }
+    consumer_sync();
 
-        // ---- each warp takes tiles j = warp, warp + kWarps, ... of the chunk, kUnroll at a time ----
-        for (int j0 = warp * kUnroll; j0 < nt; j0 += kWarps * kUnroll) {
-            TileRegs<TYPE> regs[kUnroll];
+    // After a timed-out wait a warp stops waiting and computing but keeps the loop structure, so
+    // every consumer warp still reaches the same named barriers.
+    const uint32_t *lut_lane = lut_s + (lane & (kLutCopies - 1));
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t ct = blockIdx.x; ct < p.n_col_tiles; ct += gridDim.x) {
+        unsigned long long acc[2][NF][2];     // [rb][nf][row pair half]: (tok 2t, 2t+1) of rows 4g+2rb(+1)
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u)
-                if (j0 + u < nt) load_tile<TYPE>(regs[u], col_base + (size_t)(c0 + j0 + u) * TS, g, t);
+        for (int rb = 0; rb < 2; ++rb)
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int j = j0 + u;
-                if (j >= nt) break;
+            for (int nf = 0; nf < NF; ++nf) acc[rb][nf][0] = acc[rb][nf][1] = 0ull;
+
+        for (int j0 = 0; j0 < nkc; j0 += kTilesPerStage, ++it) {
+            const int s = (int)(it % (uint32_t)stages);
+            const uint32_t ph = (it / (uint32_t)stages) & 1u;
+            if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
+            const int j = j0 + cw;
+            if (ok && j < nkc) {
+                const uint8_t *tile = ring + (s * kTilesPerStage + cw) * TS;
                 uint32_t H[4][4];
-                decode_tile<TYPE>(regs[u], H, lut_s, lane & (kLutCopies - 1));
-                const float dw[4] = {__half2float(__ushort_as_half((uint16_t)(regs[u].sc.x & 0xFFFF))),
-                                     __half2float(__ushort_as_half((uint16_t)(regs[u].sc.x >> 16))),
-                                     __half2float(__ushort_as_half((uint16_t)(regs[u].sc.y & 0xFFFF))),
-                                     __half2float(__ushort_as_half((uint16_t)(regs[u].sc.y >> 16)))};
+                decode_tile<TYPE>(tile, g, t, H, lut_lane);
+                const uint2 sc = *reinterpret_cast<const uint2 *>(tile + SOFF + 8 * g);
+                const float2 dw01 = __half22float2(bits_h2(sc.x));      // rows 4g, 4g+1
+                const float2 dw23 = __half22float2(bits_h2(sc.y));      // rows 4g+2, 4g+3
+                const float dwr[4] = {dw01.x, dw01.y, dw23.x, dw23.y};
 #pragma unroll
                 for (int nf = 0; nf < NF; ++nf) {
-                    const __half *arow = act_s + (8 * nf + g) * ROW_H + j * 32;
-                    // b registers: column pair cp = t + 4q -> halfs 2cp, 2cp+1 of the block
-                    const uint32_t b00 = *reinterpret_cast<const uint32_t *>(arow + 2 * t);
-                    const uint32_t b01 = *reinterpret_cast<const uint32_t *>(arow + 2 * (t + 4));
-                    const uint32_t b10 = *reinterpret_cast<const uint32_t *>(arow + 2 * (t + 8));
-                    const uint32_t b11 = *reinterpret_cast<const uint32_t *>(arow + 2 * (t + 12));
-                    const float da0 = da_s[(8 * nf + 2 * t) * kChunkTiles + j];
-                    const float da1 = da_s[(8 * nf + 2 * t + 1) * kChunkTiles + j];
+                    const int tok = 8 * nf + g;
+                    uint4 b = make_uint4(0, 0, 0, 0);
+                    if (tok < p.M) b = act_s[tok * tok_stride + j * 4 + t];
+                    const float2 da = *reinterpret_cast<const float2 *>(da_s + j * TOK + 8 * nf + 2 * t);
+                    const float2 cr = *reinterpret_cast<const float2 *>(corr_s + j * TOK + 8 * nf + 2 * t);
+                    const unsigned long long ncorr = pack2(-cr.x, -cr.y);
+                    const unsigned long long da2 = pack2(da.x, da.y);
 #pragma unroll
                     for (int rb = 0; rb < 2; ++rb) {
                         float c[4] = {0.f, 0.f, 0.f, 0.f};
-                        const uint32_t a0[4] = {H[0][2 * rb], H[0][2 * rb + 1], H[1][2 * rb], H[1][2 * rb + 1]};
-                        const uint32_t a1[4] = {H[2][2 * rb], H[2][2 * rb + 1], H[3][2 * rb], H[3][2 * rb + 1]};
-                        mma16816(c, a0, b00, b01);
-                        mma16816(c, a1, b10, b11);
-                        // c0: (row 4g+2rb, tok 2t) c1: (row 4g+2rb, tok 2t+1) c2/c3: row 4g+2rb+1
-                        acc[rb][nf][0] = fmaf(c[0], dw[2 * rb] * da0, acc[rb][nf][0]);
-                        acc[rb][nf][1] = fmaf(c[1], dw[2 * rb] * da1, acc[rb][nf][1]);
-                        acc[rb][nf][2] = fmaf(c[2], dw[2 * rb + 1] * da0, acc[rb][nf][2]);
-                        acc[rb][nf][3] = fmaf(c[3], dw[2 * rb + 1] * da1, acc[rb][nf][3]);
+                        mma16816(c, H[0][2 * rb], H[0][2 * rb + 1], H[1][2 * rb], H[1][2 * rb + 1], b.x, b.y);
+                        mma16816(c, H[2][2 * rb], H[2][2 * rb + 1], H[3][2 * rb], H[3][2 * rb + 1], b.z, b.w);
+                        // c0,c1: row 4g+2rb, tokens 2t,2t+1;  c2,c3: row 4g+2rb+1
+                        const unsigned long long s01 = fadd2(pack2(c[0], c[1]), ncorr);
+                        const unsigned long long s23 = fadd2(pack2(c[2], c[3]), ncorr);
+                        const unsigned long long p01 = fmul2(pack2(dwr[2 * rb], dwr[2 * rb]), da2);
+                        const unsigned long long p23 = fmul2(pack2(dwr[2 * rb + 1], dwr[2 * rb + 1]), da2);
+                        acc[rb][nf][0] = ffma2(s01, p01, acc[rb][nf][0]);
+                        acc[rb][nf][1] = ffma2(s23, p23, acc[rb][nf][1]);
                     }
                 }
             }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(smem_u32(&empty[s]));
         }
-    }
 
-    // ---- reduce the warps of this CTA in a fixed order ----
-#pragma unroll
-    for (int rb = 0; rb < 2; ++rb)
-#pragma unroll
-        for (int nf = 0; nf < NF; ++nf)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) red_s[(((warp * 2 + rb) * NF + nf) * 4 + c) * 32 + lane] = acc[rb][nf][c];
-    __syncthreads();
-    if (warp == 0) {
+        // ---- reduce the 8 warps in a fixed order, write (or add into) y ----
 #pragma unroll
         for (int rb = 0; rb < 2; ++rb)
 #pragma unroll
             for (int nf = 0; nf < NF; ++nf)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float s = red_s[(((0 * 2 + rb) * NF + nf) * 4 + c) * 32 + lane];
-#pragma unroll
-                    for (int w = 1; w < kWarps; ++w) s += red_s[(((w * 2 + rb) * NF + nf) * 4 + c) * 32 + lane];
-                    red_s[(((0 * 2 + rb) * NF + nf) * 4 + c) * 32 + lane] = s;   // CTA partial in slot 0
-                    acc[rb][nf][c] = s;
+                for (int h = 0; h < 2; ++h) {
+                    float a, b;
+                    unpack2(acc[rb][nf][h], a, b);
+                    red_s[((((cw * 2 + rb) * NF + nf) * 2 + h) * 2 + 0) * 32 + lane] = a;
+                    red_s[((((cw * 2 + rb) * NF + nf) * 2 + h) * 2 + 1) * 32 + lane] = b;
                 }
-    }
-
-    if (p.ksplit > 1) {
-        // ---- add the partials of the cluster's CTAs (rank order) through distributed smem ----
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        if (cluster.block_rank() == 0 && warp == 0) {
-            for (int rk = 1; rk < p.ksplit; ++rk) {
-                const float *peer = cluster.map_shared_rank(red_s, rk);
+        consumer_sync();
+        if (cw == 0) {
 #pragma unroll
-                for (int rb = 0; rb < 2; ++rb)
+            for (int rb = 0; rb < 2; ++rb)
 #pragma unroll
-                    for (int nf = 0; nf < NF; ++nf)
+                for (int nf = 0; nf < NF; ++nf)
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) acc[rb][nf][c] += peer[((rb * NF + nf) * 4 + c) * 32 + lane];
-            }
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            float sum = 0.0f;
+#pragma unroll
+                            for (int w = 0; w < kConsumerWarps; ++w)
+                                sum += red_s[((((w * 2 + rb) * NF + nf) * 2 + h) * 2 + e) * 32 + lane];
+                            const int row = 4 * g + 2 * rb + h;
+                            const int tok = 8 * nf + 2 * t + e;
+                            const int64_t n = ct * 32 + row;
+                            if (ok && tok < p.M && n < p.N) {
+                                float *dst = p.y + (int64_t)tok * p.ldy + n;
+                                *dst = p.accumulate ? (*dst + sum) : sum;
+                            }
+                        }
         }
-        cluster.sync();
-        if (cluster.block_rank() != 0) return;
-    }
-
-    if (warp == 0) {
-#pragma unroll
-        for (int rb = 0; rb < 2; ++rb)
-#pragma unroll
-            for (int nf = 0; nf < NF; ++nf)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int row = 4 * g + 2 * rb + (c >> 1);
-                    const int tok = 8 * nf + 2 * t + (c & 1);
-                    const int64_t n = ct * 32 + row;
-                    if (tok < p.M && n < p.N) p.y[(int64_t)tok * p.ldy + n] = acc[rb][nf][c];
-                }
+        consumer_sync();
     }
 }
 
+struct Plan {
+    int nf, nkc, stages, ctas_per_sm;
+    size_t smem;
+};
+
 template <int TYPE, int NF>
-size_t smem_bytes() {
-    constexpr int TOK = 8 * NF;
-    size_t b = (size_t)TOK * (kChunkTiles * 32 + kActPad) * 2 + (size_t)TOK * kChunkTiles * 4 +
-               (size_t)kWarps * 2 * NF * 4 * 32 * 4;
-    if (TYPE == QMM_IQ4_NL) b += 256 * kLutCopies * 4;
-    return b;
+Plan plan_for(int M, int64_t nkt) {
+    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    Plan pl;
+    pl.nf = NF;
+    int64_t nkc = kActBudget / (64 * (int64_t)M);
+    if (nkc > nkt) nkc = nkt;
+    if (nkc < 1) nkc = 1;
+    pl.nkc = (int)nkc;
+    const int fixed = mv_layout<TYPE, NF>(M, pl.nkc, 0).total + 128;
+    const int stage_bytes = kTilesPerStage * TS + 16;
+    // two CTAs per SM when a useful ring still fits in half the shared memory
+    int stages2 = (kSmemLimit / 2 - 1024 - fixed) / stage_bytes;
+    if (stages2 >= 6) {
+        pl.stages = stages2 > 12 ? 12 : stages2;
+        pl.ctas_per_sm = 2;
+    } else {
+        int st = (kSmemLimit - 1024 - fixed) / stage_bytes;
+        pl.stages = st > 16 ? 16 : st;
+        pl.ctas_per_sm = 1;
+    }
+    if (pl.stages < 2) pl.stages = 2;
+    pl.smem = (size_t)mv_layout<TYPE, NF>(M, pl.nkc, pl.stages).total + 128;
+    return pl;
+}
+
+int num_sms() {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms <= 0) sms = 152;
+    }
+    return sms;
 }
 
 template <int TYPE, int NF>
-cudaError_t launch_typed(const MatvecParams &p0, int64_t n_col_tiles, cudaStream_t s) {
-    MatvecParams p = p0;
+cudaError_t run(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
+                int64_t ldy, cudaStream_t s) {
+    const int64_t nkt = K / 32, nct = (N + 31) / 32;
+    const Plan pl = plan_for<TYPE, NF>(M, nkt);
     auto kern = matvec_kernel<TYPE, NF>;
-    const size_t smem = smem_bytes<TYPE, NF>();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)n_col_tiles, (unsigned)p.ksplit, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = (unsigned)p.ksplit;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    int64_t grid = (int64_t)num_sms() * pl.ctas_per_sm;
+    if (grid > nct) grid = nct;
+    for (int64_t kt0 = 0; kt0 < nkt; kt0 += pl.nkc) {
+        MvParams p;
+        p.tiled = tiled;
+        p.a_q = a_q;
+        p.a_d = a_d;
+        p.y = y;
+        p.K = K;
+        p.nkt = nkt;
+        p.N = N;
+        p.ldy = ldy;
+        p.n_col_tiles = nct;
+        p.M = M;
+        p.kt0 = (int)kt0;
+        p.nkc = (int)((nkt - kt0) < pl.nkc ? (nkt - kt0) : pl.nkc);
+        p.accumulate = kt0 > 0;
+        p.stages = pl.stages;
+        p.lut = iq4nl_lut();
+        kern<<<(unsigned)grid, kThreads, pl.smem, s>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t launch_matvec(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                           const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s) {
-    const int64_t nkt = K / 32, nct = (N + 31) / 32;
-    // Split K over up to 8 CTAs (one cluster) so that the grid holds several CTAs per SM.
-    const int64_t target_ctas = 152 * 8;
-    int ksplit = 1;
-    while (ksplit < 8 && nct * ksplit < target_ctas && nkt / (ksplit * 2) >= kUnroll) ksplit *= 2;
-    const int kpc = (int)((nkt + ksplit - 1) / ksplit);
-    ksplit = (int)((nkt + kpc - 1) / kpc);      // no empty CTAs
+    const int64_t nkt = K / 32;
     for (int64_t m0 = 0; m0 < M; m0 += kDecodeMaxM) {
         const int mm = (int)((M - m0) < kDecodeMaxM ? (M - m0) : kDecodeMaxM);
-        MatvecParams p;
-        p.tiled = tiled;
-        p.a_q = a_q + m0 * K;
-        p.a_d = a_d + m0 * nkt;
-        p.y = y + m0 * ldy;
-        p.nkt = nkt;
-        p.N = N;
-        p.ldy = ldy;
-        p.M = mm;
-        p.kt_per_cta = kpc;
-        p.ksplit = ksplit;
-        p.lut = iq4nl_lut();
+        const int8_t *aq = a_q + m0 * K;
+        const uint16_t *ad = a_d + m0 * nkt;
+        float *yy = y + m0 * ldy;
         cudaError_t e;
         const bool two = mm > 8;
         switch (t) {
-            case QMM_Q4_0: e = two ? launch_typed<QMM_Q4_0, 2>(p, nct, s) : launch_typed<QMM_Q4_0, 1>(p, nct, s); break;
-            case QMM_IQ4_NL: e = two ? launch_typed<QMM_IQ4_NL, 2>(p, nct, s) : launch_typed<QMM_IQ4_NL, 1>(p, nct, s); break;
-            default: e = two ? launch_typed<QMM_Q8_0, 2>(p, nct, s) : launch_typed<QMM_Q8_0, 1>(p, nct, s); break;
+            case QMM_Q4_0: e = two ? run<QMM_Q4_0, 2>(tiled, K, N, aq, ad, mm, yy, ldy, s) : run<QMM_Q4_0, 1>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
+            case QMM_IQ4_NL: e = two ? run<QMM_IQ4_NL, 2>(tiled, K, N, aq, ad, mm, yy, ldy, s) : run<QMM_IQ4_NL, 1>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
+            default: e = two ? run<QMM_Q8_0, 2>(tiled, K, N, aq, ad, mm, yy, ldy, s) : run<QMM_Q8_0, 1>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
         }
         if (e != cudaSuccess) return e;
     }
-    return cudaGetLastError();
+    return cudaSuccess;
+}
+
+cudaError_t read_and_clear_matvec_status(unsigned *out, cudaStream_t s) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_mv_status, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyToSymbolAsync(g_mv_status, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(s);
 }
 
 }  // namespace qmm

@@ -124,10 +124,11 @@ qmm_status qmm_matmul(qmm_type t, const void *w_tiled, int64_t K, int64_t N, con
 }
 
 qmm_status qmm_device_status(qmm_stream_t stream) {
-    unsigned v = 0;
+    unsigned v = 0, w = 0;
     cudaError_t e = read_and_clear_device_status(&v, cs(stream));
+    if (e == cudaSuccess) e = read_and_clear_matvec_status(&w, cs(stream));
     if (e != cudaSuccess) return QMM_ERR_CUDA;
-    return v ? QMM_ERR_TIMEOUT : QMM_OK;
+    return (v | w) ? QMM_ERR_TIMEOUT : QMM_OK;
 }
 
 }  // extern "C"
