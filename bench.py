@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the tiled block-32 quantized matmul hot path on GB300.
+
+Headline workload: Q8_0 tiled matvec, K=4096, N=14336, batch 1 (an FFN up-projection shape).
+One step = one pass of the hot path over one batch: dynamic Q8_0 quantization of the activation
+(qmm_quantize_act) followed by the matmul over the tiled weight (qmm_matmul, decode kernel) and its
+fp32 output.  The weight is repacked once beforehand, as at model load.
+
+  value   weight-tile bytes per step / device time per step (GB/s), inputs resident in HBM;
+          K consecutive steps timed with CUDA events, rotating through enough weight copies that the
+          working set exceeds the 129 MB L2 (no step hits a weight left in L2 by the previous one).
+  e2e     the same metric through the C ABI with host buffers: each step copies its activation
+          from pinned host memory, runs both calls and reads the output back.
+  roofline  the decode matvec alone: algorithmic bytes (weight tiles + activation quants and
+          scales + fp32 output) per launch / mean launch time from CUDA events, against the
+          measured HBM copy bandwidth.
+  other_configs  the remaining workloads, each as its own step (prefill GEMM in TFLOP/s).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 129 * 1024 * 1024
+HEADLINE = ("q8_0", 4096, 14336, 1)
+OTHERS = [("q4_0", 4096, 4096, 1), ("iq4_nl", 4096, 4096, 8), ("q8_0", 4096, 128256, 1),
+          ("q4_0", 4096, 14336, 512), ("q8_0", 4096, 128256, 128)]
+METRIC = "tiled Q4_0/Q8_0 matvec weight GB/s (% HBM peak); prefill int8 GEMM TOPS"
+
+
+def workload_name(type_, K, N, M):
+    kind = "prefill_gemm" if M > 16 else ("matvec" if M == 1 else "matmul")
+    return f"{type_}_{kind}_K{K}_N{N}_M{M}"
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(os.path.join(ROOT, "block_quantized_matmul_gb300", "csrc"))):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(ROOT, "block_quantized_matmul_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """dram bytes per launch from a committed ncu capture, if it was taken on the current kernels."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        ent = rec.get(workload)
+        if ent and ent.get("source_hash") == kernel_source_hash():
+            return ent.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------------
+class Workload:
+    def __init__(self, torch, qmm, type_, K, N, M, seed=0, copies=None):
+        self.torch, self.qmm = torch, qmm
+        self.type_, self.K, self.N, self.M = type_, K, N, M
+        self.tiled_bytes = qmm.tiled_size(type_, K, N)
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed)
+        # weights ~ N(0, 0.02^2), quantized and repacked once on the GPU (model-load path)
+        flat = torch.empty(qmm.flat_size(type_, K, N), dtype=torch.uint8, device="cuda")
+        rows = max(1, (256 << 20) // (4 * K))
+        for r0 in range(0, N, rows):
+            r1 = min(N, r0 + rows)
+            w = torch.randn(r1 - r0, K, device="cuda", generator=g) * 0.02
+            qmm.qmm_quantize_weight(type_, w, r1 - r0, K, K,
+                                    flat[r0 * (K // 32) * qmm.block_size(type_):])
+            del w
+        self.copies = copies or max(2, -(-3 * L2_BYTES // self.tiled_bytes) if self.tiled_bytes < 3 * L2_BYTES else 2)
+        self.tiled = []
+        for _ in range(self.copies):
+            t = torch.empty(self.tiled_bytes, dtype=torch.uint8, device="cuda")
+            qmm.qmm_repack(type_, flat, K, N, t)
+            self.tiled.append(t)
+        del flat
+        # activations ~ N(0,1), 1 % outliers x20 for the prefill workload
+        self.n_act = 4
+        xs = torch.randn(self.n_act, M, K, device="cuda", generator=g)
+        if M > 16:
+            mask = torch.rand(self.n_act, M, K, device="cuda", generator=g) < 0.01
+            xs = torch.where(mask, xs * 20.0, xs)
+        self.x = xs.contiguous()
+        self.a_q = torch.empty((M, K), dtype=torch.int8, device="cuda")
+        self.a_d = torch.empty((M, K // 32), dtype=torch.int16, device="cuda")
+        self.y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        # prefill shapes take the tensor-core path with a caller workspace (qmm_matmul_ws)
+        self.ws_bytes = qmm.matmul_workspace_size(M, K) if M > qmm.decode_max_m() else 0
+        self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device="cuda") if self.ws_bytes else None
+        self.ws_ptr = (self.ws.data_ptr() + (-self.ws.data_ptr()) % 256) if self.ws_bytes else None
+        torch.cuda.synchronize()
+
+    def step(self, i, stream):
+        self.qmm.qmm_quantize_act(self.x[i % self.n_act], self.M, self.K, self.K, self.a_q, self.a_d, stream=stream)
+        self.matmul_only(i, stream)
+
+    def matmul_only(self, i, stream):
+        if self.ws_bytes:
+            self.qmm.qmm_matmul_ws(self.type_, self.tiled[i % self.copies], self.K, self.N, self.a_q, self.a_d, self.M,
+                                   self.y, self.N, self.ws_ptr, self.ws_bytes, stream=stream)
+        else:
+            self.qmm.qmm_matmul(self.type_, self.tiled[i % self.copies], self.K, self.N, self.a_q, self.a_d, self.M,
+                                self.y, self.N, stream=stream)
+
+    def algorithmic_bytes(self):
+        return self.tiled_bytes + self.M * self.K + self.M * (self.K // 32) * 2 + self.M * self.N * 4
+
+    def flops(self):
+        return 2.0 * self.M * self.N * self.K
+
+
+def time_steps(torch, fn, steps, stream):
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(steps):
+        fn(i, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps        # ms per step
+
+
+def kernel_time(torch, wl, steps, stream):
+    """Mean duration of the matmul kernel alone: events around each launch on its stream."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        ev[i][0].record(stream)
+        wl.matmul_only(i, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
+def run_gpu(args):
+    import torch
+
+    import block_quantized_matmul_gb300 as qmm
+    from block_quantized_matmul_gb300 import build
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    build.build()
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    stream = torch.cuda.Stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # ---------------- headline workload ----------------
+    type_, K, N, M = HEADLINE
+    wl = Workload(torch, qmm, type_, K, N, M)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            wl.step(i, stream)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        barrier()
+        ms = time_steps(torch, wl.step, args.steps, stream)
+        barrier()
+        # keep the GPU busy a little longer so the clock record is not empty on short runs
+        extra = 0
+        t_end = time.time() + 0.5
+        while time.time() < t_end:
+            for i in range(200):
+                wl.step(i, stream)
+            extra += 200
+        torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = wl.tiled_bytes * world / (ms * 1e-3) / 1e9
+
+    # roofline of the decode kernel
+    kms = kernel_time(torch, wl, max(20, min(args.steps, 200)), stream)
+    achieved = wl.algorithmic_bytes() / (kms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                "traffic": recorded_traffic(workload_name(*HEADLINE)), "kernel_us": round(kms * 1e3, 3)}
+
+    # end to end through the C ABI with host buffers
+    x_host = torch.empty((wl.n_act, M, K), dtype=torch.float32).pin_memory()
+    x_host.copy_(wl.x.cpu())
+    y_host = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((M, K), dtype=torch.float32, device="cuda")
+
+    def e2e_step(i, s):
+        x_dev.copy_(x_host[i % wl.n_act], non_blocking=True)
+        qmm.qmm_quantize_act(x_dev, M, K, K, wl.a_q, wl.a_d, stream=s)
+        qmm.qmm_matmul(type_, wl.tiled[i % wl.copies], K, N, wl.a_q, wl.a_d, M, wl.y, N, stream=s)
+        y_host.copy_(wl.y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i, stream)
+        torch.cuda.synchronize()
+        e2e_ms = time_steps(torch, e2e_step, args.steps, stream)
+    e2e = {"value": round(wl.tiled_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(e2e_ms, 5)}
+
+    # ---------------- other workloads ----------------
+    others = []
+    if not args.headline_only:
+        del wl
+        torch.cuda.empty_cache()
+        for cfg in OTHERS:
+            o = Workload(torch, qmm, *cfg)
+            with torch.cuda.stream(stream):
+                for i in range(max(3, args.warmup)):
+                    o.step(i, stream)
+            torch.cuda.synchronize()
+            n = max(10, min(args.steps, 200 if cfg[3] > 16 else 1000))
+            oms = time_steps(torch, o.step, n, stream)
+            okms = kernel_time(torch, o, min(n, 100), stream)
+            ent = {"workload": workload_name(*cfg), "ms_per_step": round(oms, 5), "kernel_us": round(okms * 1e3, 3),
+                   "weight_GBps": round(o.tiled_bytes / (oms * 1e-3) / 1e9, 1)}
+            kbytes = o.algorithmic_bytes() / (okms * 1e-3) / 1e9
+            ent["roofline_hbm"] = {"achieved": round(kbytes, 1), "peak": hbm_peak, "unit": "GB/s",
+                                   "frac": round(kbytes / hbm_peak, 4)}
+            if cfg[3] > 16:
+                tf = o.flops() / (okms * 1e-3) / 1e12
+                ent["TFLOPs"] = round(tf, 1)
+                ent["roofline_tensor"] = {"achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                                          "frac": round(tf / bf16_peak, 4),
+                                          "note": "fp16 tcgen05 MMA on exact integer operands (no int8 tcgen05 "
+                                                  "on sm_103a); peak = measured bf16 burst"}
+            others.append(ent)
+            del o
+            torch.cuda.empty_cache()
+    status = qmm.qmm_device_status()
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8",
+        "arith": "Q8_0 weights x int8 activations: exact integer block sums on fp16 tensor cores, fp32 scaling",
+        "data": "synthetic (seeded: weights N(0,0.02^2) -> Q8_0 tiles, activations N(0,1))",
+        "config": {"workload": workload_name(*HEADLINE), "type": type_, "K": K, "N": N, "M": M,
+                   "step": "qmm_quantize_act + qmm_matmul (decode matvec)",
+                   "l2": f"{wl_copies_note(qmm, type_, K, N)}", "parallelism": f"replica x{world}"},
+        "pct_hbm_peak": round(value / hbm_peak * 100, 2),
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": (args.steps) * (1 + 1),
+        "clocks": clk.summary(),
+        "device_status": status,
+        "other_configs": others,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(HEADLINE, budget_s=args.cpu_seconds) if not args.no_cpu else None
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def wl_copies_note(qmm, type_, K, N):
+    tb = qmm.tiled_size(type_, K, N)
+    copies = max(2, -(-3 * L2_BYTES // tb) if tb < 3 * L2_BYTES else 2)
+    return f"inputs larger than L2: {copies} rotating weight copies x {tb} B = {copies * tb} B > 129 MB L2"
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle timing (reported baseline; also the --impl reference arm)
+# ---------------------------------------------------------------------------------------------
+def cpu_baseline(cfg, budget_s=15.0, rows=1024):
+    import numpy as np
+
+    import oracle
+    from block_quantized_matmul_gb300 import synth
+
+    type_, K, N, M = cfg
+    rows = min(rows, N)
+    w = synth.weights(rows, K)
+    x = synth.activations(M, K)
+    tiled = oracle.repack(type_, oracle.quantize_rows(type_, w), K, rows)
+    bytes_per_pass = oracle.tiled_bytes(type_, K, rows)
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        a_q, a_d = oracle.quantize_act(x)
+        oracle.matmul(type_, tiled, K, rows, a_q, a_d)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or passes >= 10000:
+            break
+    gbps = bytes_per_pass * passes / el / 1e9
+    return {"value": round(gbps, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{workload_name(*cfg)}: first {rows} of {N} weight rows ({bytes_per_pass} tile bytes), "
+                      f"{passes} passes of act-quant + matmul in {el:.1f} s, single-threaded C oracle",
+            "host_cores_available": os.cpu_count()}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_step = max(1.0, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(HEADLINE, budget_s=per_step)
+    t0 = time.perf_counter()
+    vals = [cpu_baseline(HEADLINE, budget_s=per_step) for _ in range(args.steps)]
+    el = time.perf_counter() - t0
+    v = sum(r["value"] for r in vals) / len(vals)
+    type_, K, N, M = HEADLINE
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 5), "unit": "GB/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64/f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": workload_name(*HEADLINE), "type": type_, "K": K, "N": N, "M": M},
+            "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": round(v, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_profile(args):
+    """Set up one workload and launch its matmul kernel warmup + steps times (for ncu captures)."""
+    import torch
+
+    import block_quantized_matmul_gb300 as qmm
+    from block_quantized_matmul_gb300 import build
+
+    torch.cuda.set_device(0)
+    build.build()
+    cfg = {workload_name(*c): c for c in [HEADLINE] + OTHERS}[args.profile]
+    wl = Workload(torch, qmm, *cfg, copies=1)
+    stream = torch.cuda.current_stream()
+    wl.step(0, stream)
+    for i in range(args.warmup + args.steps):
+        wl.matmul_only(i, stream)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps + 1,
+                      "status": qmm.qmm_device_status()}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", default=None, help="launch one workload's matmul kernel only (for ncu)")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--headline-only", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

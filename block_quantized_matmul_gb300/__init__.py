@@ -19,6 +19,7 @@ __all__ = [
     "block_size", "tile_size", "tiled_size", "flat_size", "iq4nl_table", "decode_max_m",
     "qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
     "qmm_matmul_path", "qmm_device_status", "PATH_AUTO", "PATH_MATVEC", "PATH_GEMM",
+    "matmul_workspace_size", "qmm_matmul_ws",
 ]
 
 Q4_0, Q8_0, IQ4_NL = 0, 1, 2
@@ -65,8 +66,11 @@ def lib():
         L.qmm_matmul.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp]
         L.qmm_matmul_path.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, i32, vp]
         L.qmm_device_status.argtypes = [vp]
+        L.qmm_matmul_workspace_size.argtypes = [i64, i64]
+        L.qmm_matmul_workspace_size.restype = sz
+        L.qmm_matmul_ws.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp, sz, vp]
         for fn in ("qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
-                   "qmm_matmul_path", "qmm_device_status"):
+                   "qmm_matmul_path", "qmm_device_status", "qmm_matmul_ws"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -155,6 +159,16 @@ def qmm_matmul_path(type_, w_tiled, K: int, N: int, a_q, a_d, M: int, y, ldy: in
                     stream=None) -> None:
     _check("qmm_matmul_path", lib().qmm_matmul_path(_t(type_), _ptr(w_tiled), K, N, _ptr(a_q), _ptr(a_d), M,
                                                     _ptr(y), ldy, int(path), _stream(stream)))
+
+
+def matmul_workspace_size(M: int, K: int) -> int:
+    return int(lib().qmm_matmul_workspace_size(M, K))
+
+
+def qmm_matmul_ws(type_, w_tiled, K: int, N: int, a_q, a_d, M: int, y, ldy: int, workspace, workspace_bytes: int,
+                  stream=None) -> None:
+    _check("qmm_matmul_ws", lib().qmm_matmul_ws(_t(type_), _ptr(w_tiled), K, N, _ptr(a_q), _ptr(a_d), M, _ptr(y), ldy,
+                                                _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
 def qmm_device_status(stream=None) -> int:

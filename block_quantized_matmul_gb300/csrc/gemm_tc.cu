@@ -13,15 +13,21 @@
 //     y += S_b * P_b, using packed fma.rn.f32x2.
 //
 // Tile: 128 weight rows (4 column tiles, the UMMA M dimension) x 128 tokens (UMMA N), all of K.
-// Warp roles (448 threads):
-//   warp 0      producer: cp.async.bulk copies of the 4 raw weight tiles and the 128 activation rows of
-//               block kt into a 4-stage raw ring (mbarrier complete_tx).
+// Warp roles (448 threads), one 4-stage ring of paired raw + operand buffers per CTA:
+//   warp 0      producer: cp.async.bulk of the 4 raw weight tiles of block kt and a 2-D TMA load of
+//               the block's 128 token rows (mbarrier complete_tx).
 //   warp 1      TMEM owner and MMA issuer (one thread): 3 MMAs per block into a 2-stage TMEM ring.
-//   warps 2-5   converters: raw bytes -> fp16 operands in the canonical K-major 64-byte-swizzled
-//               layout (3-stage ring), plus the d_w / d_a columns of the scale-product operands.
+//   warps 2-5   converters: thread c turns weight row c of the raw tiles into fp16 in the canonical
+//               K-major 64-byte-swizzled layout and writes the d_w / d_a columns of the
+//               scale-product operands (and, for int8 activations, converts token row c).
 //   warps 6-13  rescale: tcgen05.ld of S_b and P_b, y += S_b*P_b in registers, then the fp32 store.
+// Two token-operand variants: int8 quants converted in the kernel (no scratch memory), or a prepared
+// fp16 copy in a caller workspace that TMA writes directly in the swizzled operand layout (every
+// token tile is then converted once instead of once per weight tile).
 // Every mbarrier wait is bounded in time; on expiry the kernel records QMM_ERR_TIMEOUT in a device
 // status word, lets its copies and MMAs in flight land, frees TMEM and returns.
+#include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched through the runtime)
+
 #include "qmm_internal.cuh"
 
 namespace qmm {
@@ -32,8 +38,7 @@ __device__ unsigned g_device_status = 0;   // non-zero once a bounded wait gave 
 
 constexpr int BM = 128;                    // weight rows per CTA
 constexpr int BN = 128;                    // tokens per CTA
-constexpr int kRawStages = 4;
-constexpr int kOpStages = 3;
+constexpr int kStages = 4;                 // paired raw + operand stages
 constexpr int kTmemStages = 2;
 constexpr int kTmemCols = 512;             // 2 stages x (S 128 + P 128) fp32 columns
 constexpr int kConvWarp0 = 2, kNumConvWarps = 4;
@@ -42,7 +47,7 @@ constexpr int kThreads = (kRescaleWarp0 + kNumRescaleWarps) * 32;
 constexpr int kOpBytes = BM * 64;          // one 128 x 32 fp16 operand (64-byte rows)
 constexpr int kOpStageBytes = 4 * kOpBytes;    // A (weights), B (tokens), AP (d_w), BP (d_a)
 constexpr int kRawWBytes = 4 * kTile8Bytes;    // 4 raw tiles (Q8_0 worst case)
-constexpr int kRawABytes = BN * 32;            // 128 activation rows of one block
+constexpr int kRawABytes = BN * 32;            // 128 int8 activation rows of one block (or 128 fp16 scales)
 constexpr int kRawStageBytes = kRawWBytes + kRawABytes;
 constexpr int kLutCopies = 16;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
@@ -124,6 +129,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  : "memory");
 }
 
+// 2-D tensor copy: box {32 bytes of K, 128 token rows} of the int8 activations; rows past M are
+// zero-filled by the TMA unit.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -200,23 +214,31 @@ __device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
 // ---------------------------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------------------------
-template <int TYPE>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmParams p) {
+// ACT: how the token operand reaches shared memory.
+//   kActInt8      the int8 quants are copied raw (2-D TMA) and converted by the converter warps;
+//   kActPrepared  a prepared fp16 copy of the quants (exact integers) is copied by TMA straight into
+//                 the 64-byte-swizzled operand layout, and the block scales come transposed
+//                 ([K/32][M_pad] fp16), one 256-byte row per block.
+enum { kActInt8 = 0, kActPrepared = 1 };
+
+template <int TYPE, int ACT>
+// 14 warps put 4 warps on some SM sub-partitions, whose 16K-register files then allow at most
+// 128 registers per thread.
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap act_map, const __grid_constant__ CUtensorMap da_map) {
     constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
     constexpr int SOFF = (TYPE == QMM_Q8_0) ? kScale8Off : kScale4Off;
 
     extern __shared__ uint8_t smem_raw[];
-    // 1024-byte aligned base for the operand stages
     const uint32_t raw_base_u32 = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_base_u32 & 1023u)) & 1023u);
-    uint8_t *op_s = smem;                                                     // kOpStages x kOpStageBytes
-    uint8_t *raw_s = op_s + kOpStages * kOpStageBytes;                        // kRawStages x kRawStageBytes
-    uint32_t *lut_s = reinterpret_cast<uint32_t *>(raw_s + kRawStages * kRawStageBytes);   // IQ4_NL only
+    uint8_t *op_s = smem;                                                     // kStages x kOpStageBytes
+    uint8_t *raw_s = op_s + kStages * kOpStageBytes;                          // kStages x kRawStageBytes
+    uint32_t *lut_s = reinterpret_cast<uint32_t *>(raw_s + kStages * kRawStageBytes);   // IQ4_NL only
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(lut_s) +
                                                   (TYPE == QMM_IQ4_NL ? 256 * kLutCopies * 4 : 0));
-    uint64_t *raw_full = bars, *raw_empty = bars + kRawStages;
-    uint64_t *op_full = bars + 2 * kRawStages, *op_empty = op_full + kOpStages;
-    uint64_t *tm_full = op_empty + kOpStages, *tm_empty = tm_full + kTmemStages;
+    uint64_t *full = bars, *op_full = bars + kStages, *empty = bars + 2 * kStages;
+    uint64_t *tm_full = bars + 3 * kStages, *tm_empty = tm_full + kTmemStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tm_empty + kTmemStages);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -229,13 +251,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmParams p) {
 
     // ---- set-up: barriers, zeroed scale-product operands, IQ4_NL table, TMEM ----
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRawStages; ++s) { mbar_init(smem_u32(&raw_full[s]), 1); mbar_init(smem_u32(&raw_empty[s]), kNumConvWarps * 32); }
-        for (int s = 0; s < kOpStages; ++s) { mbar_init(smem_u32(&op_full[s]), kNumConvWarps * 32); mbar_init(smem_u32(&op_empty[s]), 1); }
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&op_full[s]), kNumConvWarps * 32);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
         for (int s = 0; s < kTmemStages; ++s) { mbar_init(smem_u32(&tm_full[s]), 1); mbar_init(smem_u32(&tm_empty[s]), kNumRescaleWarps * 32); }
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int s = 0; s < kOpStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
         uint4 *zp = reinterpret_cast<uint4 *>(op_s + s * kOpStageBytes + 2 * kOpBytes);   // AP and BP
         for (int i = threadIdx.x; i < 2 * kOpBytes / 16; i += kThreads) zp[i] = make_uint4(0, 0, 0, 0);
     }
@@ -259,43 +284,54 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmParams p) {
 
     if (warp == 0) {
         // ================================ producer ================================
-        uint32_t issued[kRawStages] = {0, 0, 0, 0};
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&act_map)) : "memory");
+            if (ACT == kActPrepared) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&da_map)) : "memory");
+        }
+        uint32_t issued[kStages];
+#pragma unroll
+        for (int s = 0; s < kStages; ++s) issued[s] = 0;
         for (int64_t kt = 0; kt < nkt; ++kt) {
-            const int s = (int)(kt % kRawStages);
-            const uint32_t ph = (uint32_t)((kt / kRawStages) & 1);
-            if (!wait_warp(smem_u32(&raw_empty[s]), ph ^ 1u, abort)) break;
-            const uint32_t full = smem_u32(&raw_full[s]);
-            if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(n_tiles * TS + n_tok * 32));
+            const int s = (int)(kt % kStages);
+            const uint32_t ph = (uint32_t)((kt / kStages) & 1);
+            if (!wait_warp(smem_u32(&empty[s]), ph ^ 1u, abort)) break;
+            const uint32_t fb = smem_u32(&full[s]);
+            const uint32_t raw = smem_u32(raw_s + s * kRawStageBytes);
+            const uint32_t act_bytes = (ACT == kActPrepared) ? (uint32_t)(kOpBytes + 2 * BN) : (uint32_t)kRawABytes;
+            if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(n_tiles * TS) + act_bytes);
             __syncwarp();
-            const uint32_t dst_w = smem_u32(raw_s + s * kRawStageBytes);
-            if (lane < n_tiles)
-                bulk_g2s(dst_w + lane * TS, p.tiled + ((ct0 + lane) * nkt + kt) * TS, TS, full);
-            for (int r = lane; r < n_tok; r += 32)
-                bulk_g2s(dst_w + kRawWBytes + r * 32, p.a_q + (m0 + r) * p.K + kt * 32, 32, full);
+            if (lane < n_tiles) bulk_g2s(raw + lane * TS, p.tiled + ((ct0 + lane) * nkt + kt) * TS, TS, fb);
+            if (lane == 0) {
+                if (ACT == kActPrepared) {
+                    tma_load_2d(smem_u32(op_s + s * kOpStageBytes + kOpBytes), &act_map, (int)(kt * 32), (int)m0, fb);
+                    tma_load_2d(raw + kRawWBytes, &da_map, (int)m0, (int)kt, fb);
+                } else {
+                    tma_load_2d(raw + kRawWBytes, &act_map, (int)(kt * 32), (int)m0, fb);
+                }
+            }
             issued[s] += 1;
         }
-        // let every copy issued land before the CTA can exit
-        for (int s = 0; s < kRawStages; ++s)
-            if (issued[s]) wait_drain(smem_u32(&raw_full[s]), (issued[s] - 1) & 1u);
+        for (int s = 0; s < kStages; ++s)
+            if (issued[s]) wait_drain(smem_u32(&full[s]), (issued[s] - 1) & 1u);
     } else if (warp == 1) {
         // ================================ MMA issuer ================================
         uint32_t committed[kTmemStages] = {0, 0};
         for (int64_t kt = 0; kt < nkt; ++kt) {
-            const int os = (int)(kt % kOpStages);
-            const uint32_t oph = (uint32_t)((kt / kOpStages) & 1);
+            const int s = (int)(kt % kStages);
+            const uint32_t ph = (uint32_t)((kt / kStages) & 1);
             const int ts = (int)(kt % kTmemStages);
             const uint32_t tph = (uint32_t)((kt / kTmemStages) & 1);
-            if (!wait_warp(smem_u32(&op_full[os]), oph, abort)) break;
+            if (!wait_warp(smem_u32(&op_full[s]), ph, abort)) break;
             if (!wait_warp(smem_u32(&tm_empty[ts]), tph ^ 1u, abort)) break;
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t a = smem_u32(op_s + os * kOpStageBytes);
+                const uint32_t a = smem_u32(op_s + s * kOpStageBytes);
                 const uint32_t b = a + kOpBytes, ap = a + 2 * kOpBytes, bp = a + 3 * kOpBytes;
                 const uint32_t d_s = tmem_base + (uint32_t)(ts * 256);
                 mma_f16(d_s, smem_desc_sw64(a), smem_desc_sw64(b), 0u);
                 mma_f16(d_s, smem_desc_sw64(a + 32), smem_desc_sw64(b + 32), 1u);
                 mma_f16(d_s + 128, smem_desc_sw64(ap), smem_desc_sw64(bp), 0u);
-                mma_commit(smem_u32(&op_empty[os]));
+                mma_commit(smem_u32(&empty[s]));
                 mma_commit(smem_u32(&tm_full[ts]));
             }
             __syncwarp();
@@ -305,87 +341,91 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmParams p) {
             if (committed[s]) wait_drain(smem_u32(&tm_full[s]), (committed[s] - 1) & 1u);
     } else if (warp < kRescaleWarp0) {
         // ================================ converters ================================
-        const int c = threadIdx.x - kConvWarp0 * 32;        // 0..127
-        const int q = c >> 5;                               // local column tile of this thread's weight word
-        const int j = (c & 31) >> 2;                        // rows 4j..4j+3 of that tile
-        const int cq = c & 3;                               // column pairs 4cq..4cq+3 (k 8cq..8cq+7)
-        const int copy = lane & (kLutCopies - 1);
+        // Thread c owns weight row c (tile q = c/32, tile row c%32) and token row c of the block.
+        const int c = threadIdx.x - kConvWarp0 * 32;
+        const int q = c >> 5, tr = c & 31;
+        const bool w_ok = q < n_tiles;
+        const uint32_t *lut_lane = lut_s + (lane & (kLutCopies - 1));
         const bool tok_ok = c < n_tok;
-        uint16_t da_next = tok_ok ? p.a_d[(m0 + c) * nkt + 0] : (uint16_t)0;
-        for (int64_t kt = 0; kt < nkt; ++kt) {
-            const int rs = (int)(kt % kRawStages);
-            const uint32_t rph = (uint32_t)((kt / kRawStages) & 1);
-            const int os = (int)(kt % kOpStages);
-            const uint32_t oph = (uint32_t)((kt / kOpStages) & 1);
-            const uint16_t da = da_next;
-            if (tok_ok && kt + 1 < nkt) da_next = p.a_d[(m0 + c) * nkt + kt + 1];
-            if (!wait_bounded(smem_u32(&raw_full[rs]), rph, abort)) break;
-            if (!wait_bounded(smem_u32(&op_empty[os]), oph ^ 1u, abort)) break;
-            const uint8_t *raw = raw_s + rs * kRawStageBytes;
-            uint8_t *op = op_s + os * kOpStageBytes;
-            // -- weights: 4 rows x 8 columns per thread --
-            uint32_t h[4][4];                               // [row offset][column pair offset]
-            if (q < n_tiles) {
-                const uint8_t *tile = raw + q * TS;
-                if constexpr (TYPE == QMM_Q8_0) {
+        // int8 path: block scales of this token, loaded 8 blocks ahead
+        uint16_t da_cur[8], da_nxt[8];
+        if (ACT == kActInt8) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(tile + (4 * cq + i) * 64 + 8 * j);
-                        i8x4_to_h2x2(v.x, h[0][i], h[1][i]);
-                        i8x4_to_h2x2(v.y, h[2][i], h[3][i]);
-                    }
-                } else {
+            for (int u = 0; u < 8; ++u) {
+                da_cur[u] = (tok_ok && u < nkt) ? p.a_d[(m0 + c) * nkt + u] : (uint16_t)0;
+                da_nxt[u] = (tok_ok && 8 + u < nkt) ? p.a_d[(m0 + c) * nkt + 8 + u] : (uint16_t)0;
+            }
+        }
+        bool ok = true;
+        for (int64_t kb = 0; kb < nkt && ok; kb += 8) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t w = *reinterpret_cast<const uint32_t *>(tile + (4 * cq + i) * 32 + 4 * j);
-                        if constexpr (TYPE == QMM_Q4_0) {
-                            h[0][i] = q4_byte_to_h2<0>(w);
-                            h[1][i] = q4_byte_to_h2<1>(w);
-                            h[2][i] = q4_byte_to_h2<2>(w);
-                            h[3][i] = q4_byte_to_h2<3>(w);
-                        } else {
+            for (int u = 0; u < 8; ++u) {
+                const int64_t kt = kb + u;
+                if (kt >= nkt || !ok) break;
+                const int s = (int)(kt % kStages);
+                const uint32_t ph = (uint32_t)((kt / kStages) & 1);
+                if (!wait_bounded(smem_u32(&full[s]), ph, abort)) { ok = false; break; }
+                const uint8_t *raw = raw_s + s * kRawStageBytes;
+                uint8_t *op = op_s + s * kOpStageBytes;
+                // -- weight row c: 32 columns -> 16 half2 in column order --
+                uint32_t h[16];
+                uint16_t dw = 0;
+                if (w_ok) {
+                    const uint8_t *tile = raw + q * TS;
+                    if constexpr (TYPE == QMM_Q8_0) {
 #pragma unroll
-                            for (int rr = 0; rr < 4; ++rr) h[rr][i] = lut_s[((w >> (8 * rr)) & 0xFFu) * kLutCopies + copy];
+                        for (int cp = 0; cp < 16; ++cp) {
+                            const uint32_t v = *reinterpret_cast<const uint16_t *>(tile + cp * 64 + 2 * tr);
+                            uint32_t lo, hi;
+                            i8x4_to_h2x2(v, lo, hi);
+                            h[cp] = lo;
+                        }
+                    } else {
+#pragma unroll
+                        for (int cp = 0; cp < 16; ++cp) {
+                            const uint32_t b = tile[cp * 32 + tr];
+                            if constexpr (TYPE == QMM_Q4_0) h[cp] = q4_byte_to_h2<0>(b);
+                            else h[cp] = lut_lane[b * kLutCopies];
                         }
                     }
+                    dw = *reinterpret_cast<const uint16_t *>(tile + SOFF + 2 * tr);
+                } else {
+#pragma unroll
+                    for (int cp = 0; cp < 16; ++cp) h[cp] = 0u;
                 }
-            } else {
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) h[rr][i] = 0u;
-            }
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const int row = 32 * q + 4 * j + rr;
-                *reinterpret_cast<uint4 *>(op + sw64_off(row, cq)) = make_uint4(h[rr][0], h[rr][1], h[rr][2], h[rr][3]);
-            }
-            // -- d_w of weight row c into column 0 of the AP operand --
-            {
-                const int tq = c >> 5, tr = c & 31;
-                const uint16_t dw = (tq < n_tiles) ? *reinterpret_cast<const uint16_t *>(raw + tq * TS + SOFF + 2 * tr) : (uint16_t)0;
+                for (int ch = 0; ch < 4; ++ch)
+                    *reinterpret_cast<uint4 *>(op + sw64_off(c, ch)) = make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
                 *reinterpret_cast<uint16_t *>(op + 2 * kOpBytes + sw64_off(c, 0)) = dw;
-            }
-            // -- activations: token row c, 32 int8 -> 32 fp16 --
-            {
-                uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-                if (tok_ok) {
-                    v0 = *reinterpret_cast<const uint4 *>(raw + kRawWBytes + c * 32);
-                    v1 = *reinterpret_cast<const uint4 *>(raw + kRawWBytes + c * 32 + 16);
-                }
-                const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                // -- token row c --
+                uint16_t da;
+                if constexpr (ACT == kActPrepared) {
+                    da = *reinterpret_cast<const uint16_t *>(raw + kRawWBytes + 2 * c);
+                } else {
+                    da = da_cur[u];
+                    uint4 v0 = *reinterpret_cast<const uint4 *>(raw + kRawWBytes + c * 32);
+                    uint4 v1 = *reinterpret_cast<const uint4 *>(raw + kRawWBytes + c * 32 + 16);
+                    const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t a0, a1, a2, a3;
-                    i8x4_to_h2x2(wv[2 * ch], a0, a1);
-                    i8x4_to_h2x2(wv[2 * ch + 1], a2, a3);
-                    *reinterpret_cast<uint4 *>(op + kOpBytes + sw64_off(c, ch)) = make_uint4(a0, a1, a2, a3);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t a0, a1, a2, a3;
+                        i8x4_to_h2x2(wv[2 * ch], a0, a1);
+                        i8x4_to_h2x2(wv[2 * ch + 1], a2, a3);
+                        *reinterpret_cast<uint4 *>(op + kOpBytes + sw64_off(c, ch)) = make_uint4(a0, a1, a2, a3);
+                    }
                 }
                 *reinterpret_cast<uint16_t *>(op + 3 * kOpBytes + sw64_off(c, 0)) = da;
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&op_full[s]));
             }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&op_full[os]));
-            mbar_arrive(smem_u32(&raw_empty[rs]));
+            if (ACT == kActInt8) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    da_cur[u] = da_nxt[u];
+                    const int64_t kn = kb + 16 + u;
+                    da_nxt[u] = (tok_ok && kn < nkt) ? p.a_d[(m0 + c) * nkt + kn] : (uint16_t)0;
+                }
+            }
         }
     } else {
         // ================================ rescale ================================
@@ -404,12 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmParams p) {
             const uint32_t t_s = tmem_base + ((uint32_t)(32 * qd) << 16) + (uint32_t)(ts * 256 + 64 * half);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                uint32_t s[16], pr[16];
-                tmem_ld16(t_s + 16 * cc, s);
-                tmem_ld16(t_s + 128 + 16 * cc, pr);
+                uint32_t sv[16], pv[16];
+                tmem_ld16(t_s + 16 * cc, sv);
+                tmem_ld16(t_s + 128 + 16 * cc, pv);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) ffma2(y[16 * cc + e], y[16 * cc + e + 1], s[e], s[e + 1], pr[e], pr[e + 1]);
+                for (int e = 0; e < 16; e += 2) ffma2(y[16 * cc + e], y[16 * cc + e + 1], sv[e], sv[e + 1], pv[e], pv[e + 1]);
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&tm_empty[ts]));
@@ -434,29 +474,92 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmParams p) {
     }
 }
 
-template <int TYPE>
-size_t gemm_smem_bytes() {
-    size_t b = 1024 + (size_t)kOpStages * kOpStageBytes + (size_t)kRawStages * kRawStageBytes;
-    if (TYPE == QMM_IQ4_NL) b += 256 * kLutCopies * 4;
-    b += (2 * kRawStages + 2 * kOpStages + 2 * kTmemStages) * 8 + 16;
-    return b;
+// Prepares the token operand for kActPrepared: a_h[m][k] = fp16(a_q[m][k]) (exact) and
+// a_dT[kt][m] = a_d[m][kt] for m < M_pad (zero for m >= M).
+__global__ void __launch_bounds__(256) prepare_act_kernel(const int8_t *__restrict__ a_q, const uint16_t *__restrict__ a_d,
+                                                          int64_t M, int64_t K, int64_t M_pad, __half *__restrict__ a_h,
+                                                          uint16_t *__restrict__ a_dT) {
+    const int64_t nkt = K / 32;
+    const int64_t quads = M * K / 4;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < quads; i += stride) {
+        const uint32_t w = __ldg(reinterpret_cast<const uint32_t *>(a_q) + i);
+        uint32_t lo, hi;
+        const uint32_t x = w ^ 0x80808080u;
+        const __half2 bias = __halves2half2(__float2half_rn(1152.0f), __float2half_rn(1152.0f));
+        lo = h2_bits(__hsub2(bits_h2(__byte_perm(x, 0x64646464u, 0x4140u)), bias));
+        hi = h2_bits(__hsub2(bits_h2(__byte_perm(x, 0x64646464u, 0x4342u)), bias));
+        reinterpret_cast<uint2 *>(a_h)[i] = make_uint2(lo, hi);
+    }
+    const int64_t nd = nkt * M_pad;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nd; i += stride) {
+        const int64_t kt = i / M_pad, m = i - kt * M_pad;
+        a_dT[i] = (m < M) ? a_d[m * nkt + kt] : (uint16_t)0;
+    }
 }
 
 template <int TYPE>
-cudaError_t launch_typed(const GemmParams &p, cudaStream_t s) {
-    auto kern = gemm_kernel<TYPE>;
+size_t gemm_smem_bytes() {
+    size_t b = 1024 + (size_t)kStages * (kOpStageBytes + kRawStageBytes);
+    if (TYPE == QMM_IQ4_NL) b += 256 * kLutCopies * 4;
+    b += (3 * kStages + 2 * kTmemStages) * 8 + 16;
+    return b;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D tensor map: rows of `inner` elements (row stride `row_bytes`), box {box_inner, box_rows}.
+cudaError_t make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int TYPE, int ACT>
+cudaError_t launch_typed(const GemmParams &p, const CUtensorMap &act_map, const CUtensorMap &da_map, cudaStream_t s) {
+    auto kern = gemm_kernel<TYPE, ACT>;
     const size_t smem = gemm_smem_bytes<TYPE>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((p.n_col_tiles + 3) / 4), (unsigned)((p.M + BN - 1) / BN), 1);
-    kern<<<grid, kThreads, smem, s>>>(p);
+    kern<<<grid, kThreads, smem, s>>>(p, act_map, da_map);
     return cudaGetLastError();
 }
 
-}  // namespace
+template <int ACT>
+cudaError_t dispatch(qmm_type t, const GemmParams &p, const CUtensorMap &am, const CUtensorMap &dm, cudaStream_t s) {
+    switch (t) {
+        case QMM_Q4_0: return launch_typed<QMM_Q4_0, ACT>(p, am, dm, s);
+        case QMM_IQ4_NL: return launch_typed<QMM_IQ4_NL, ACT>(p, am, dm, s);
+        default: return launch_typed<QMM_Q8_0, ACT>(p, am, dm, s);
+    }
+}
 
-cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
-                        int64_t M, float *y, int64_t ldy, cudaStream_t s) {
+GemmParams make_params(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int64_t M,
+                       float *y, int64_t ldy) {
     GemmParams p;
     p.tiled = tiled;
     p.a_q = a_q;
@@ -469,12 +572,51 @@ cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, 
     p.ldy = ldy;
     p.n_col_tiles = (N + 31) / 32;
     p.lut = iq4nl_lut();
+    return p;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
+                        int64_t M, float *y, int64_t ldy, cudaStream_t s) {
     if ((M + BN - 1) / BN > 65535) return cudaErrorInvalidValue;
-    switch (t) {
-        case QMM_Q4_0: return launch_typed<QMM_Q4_0>(p, s);
-        case QMM_IQ4_NL: return launch_typed<QMM_IQ4_NL>(p, s);
-        default: return launch_typed<QMM_Q8_0>(p, s);
+    const GemmParams p = make_params(tiled, K, N, a_q, a_d, M, y, ldy);
+    alignas(64) CUtensorMap am, dm;
+    cudaError_t e = make_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, (uint64_t)K, (uint64_t)M, (uint64_t)K, 32, BN,
+                                CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    dm = am;   // unused by this variant
+    return dispatch<kActInt8>(t, p, am, dm, s);
+}
+
+size_t gemm_workspace_bytes(int64_t M, int64_t K) {
+    const int64_t m_pad = (M + 7) / 8 * 8;
+    return (size_t)M * (size_t)K * 2 + (size_t)(K / 32) * (size_t)m_pad * 2 + 256;
+}
+
+cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
+                           const uint16_t *a_d, int64_t M, float *y, int64_t ldy, void *ws, cudaStream_t s) {
+    if ((M + BN - 1) / BN > 65535) return cudaErrorInvalidValue;
+    const int64_t nkt = K / 32, m_pad = (M + 7) / 8 * 8;
+    __half *a_h = static_cast<__half *>(ws);
+    uint16_t *a_dT = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + ((size_t)M * K * 2 + 255) / 256 * 256);
+    {
+        const int64_t work = M * K / 4 > nkt * m_pad ? M * K / 4 : nkt * m_pad;
+        int64_t grid = (work + 255) / 256;
+        if (grid > 152 * 8) grid = 152 * 8;
+        prepare_act_kernel<<<(unsigned)grid, 256, 0, s>>>(a_q, a_d, M, K, m_pad, a_h, a_dT);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
+    const GemmParams p = make_params(tiled, K, N, a_q, a_d, M, y, ldy);
+    alignas(64) CUtensorMap am, dm;
+    cudaError_t e = make_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a_h, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 32,
+                                BN, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (e != cudaSuccess) return e;
+    e = make_map_2d(&dm, CU_TENSOR_MAP_DATA_TYPE_UINT16, a_dT, (uint64_t)m_pad, (uint64_t)nkt, (uint64_t)m_pad * 2, BN, 1,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    return dispatch<kActPrepared>(t, p, am, dm, s);
 }
 
 cudaError_t read_and_clear_device_status(unsigned *out, cudaStream_t s) {

@@ -10,10 +10,10 @@
 // GB300 design:
 //   * Persistent CTAs (one or two per SM) each own a set of column tiles.  The K tiles of a column
 //     tile are contiguous in memory (tile_idx = ct*n_k_tiles + kt), so one producer warp streams them
-//     with 1-D cp.async.bulk copies of 8 tiles into a deep shared-memory ring (mbarrier
+//     with 1-D cp.async.bulk copies of 16 tiles into a deep shared-memory ring (mbarrier
 //     complete_tx / consumer release) -- the pipelined multi-buffering of the pages, with the TMA
 //     engine as the DMA queue.
-//   * 8 consumer warps take one tile of each stage.  Quants become fp16 holding exact integers
+//   * 8 consumer warps take two tiles of each 16-tile stage (two independent chains per warp).  Quants become fp16 holding exact integers
 //     (biased: 1024+q or 1152+q, see decode_*), activations are staged once per CTA as fp16 in the
 //     mma fragment order, and mma.sync.m16n8k16 (fp32 accumulate) yields block sums that are exact
 //     integers; subtracting the exact per-(token, block) bias gives S_b.  fp16 mma.sync runs at ~4x
@@ -28,7 +28,8 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);     // warp 0 = producer
-constexpr int kTilesPerStage = kConsumerWarps;          // one tile per consumer warp per stage
+constexpr int kTilesPerWarp = 2;                        // independent tiles per warp per stage (ILP)
+constexpr int kTilesPerStage = kConsumerWarps * kTilesPerWarp;
 constexpr int kLutCopies = 16;
 constexpr int kActBudget = 64 * 1024;                   // bytes of staged activations per CTA
 constexpr int kSmemLimit = 227 * 1024;
@@ -337,36 +338,50 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvParams p) {
             const int s = (int)(it % (uint32_t)stages);
             const uint32_t ph = (it / (uint32_t)stages) & 1u;
             if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
-            const int j = j0 + cw;
-            if (ok && j < nkc) {
-                const uint8_t *tile = ring + (s * kTilesPerStage + cw) * TS;
-                uint32_t H[4][4];
-                decode_tile<TYPE>(tile, g, t, H, lut_lane);
-                const uint2 sc = *reinterpret_cast<const uint2 *>(tile + SOFF + 8 * g);
-                const float2 dw01 = __half22float2(bits_h2(sc.x));      // rows 4g, 4g+1
-                const float2 dw23 = __half22float2(bits_h2(sc.y));      // rows 4g+2, 4g+3
-                const float dwr[4] = {dw01.x, dw01.y, dw23.x, dw23.y};
+            if (ok) {
+                // tiles cw and cw + 8 of this stage, decoded and contracted side by side
+                uint32_t H[kTilesPerWarp][4][4];
+                float dwr[kTilesPerWarp][4];
+                bool live[kTilesPerWarp];
 #pragma unroll
-                for (int nf = 0; nf < NF; ++nf) {
-                    const int tok = 8 * nf + g;
-                    uint4 b = make_uint4(0, 0, 0, 0);
-                    if (tok < p.M) b = act_s[tok * tok_stride + j * 4 + t];
-                    const float2 da = *reinterpret_cast<const float2 *>(da_s + j * TOK + 8 * nf + 2 * t);
-                    const float2 cr = *reinterpret_cast<const float2 *>(corr_s + j * TOK + 8 * nf + 2 * t);
-                    const unsigned long long ncorr = pack2(-cr.x, -cr.y);
-                    const unsigned long long da2 = pack2(da.x, da.y);
+                for (int u = 0; u < kTilesPerWarp; ++u) {
+                    const int jt = j0 + cw + kConsumerWarps * u;
+                    live[u] = jt < nkc;
+                    const uint8_t *tile = ring + (s * kTilesPerStage + cw + kConsumerWarps * u) * TS;
+                    if (live[u]) {
+                        decode_tile<TYPE>(tile, g, t, H[u], lut_lane);
+                        const uint2 sc = *reinterpret_cast<const uint2 *>(tile + SOFF + 8 * g);
+                        const float2 dw01 = __half22float2(bits_h2(sc.x));      // rows 4g, 4g+1
+                        const float2 dw23 = __half22float2(bits_h2(sc.y));      // rows 4g+2, 4g+3
+                        dwr[u][0] = dw01.x; dwr[u][1] = dw01.y; dwr[u][2] = dw23.x; dwr[u][3] = dw23.y;
+                    }
+                }
 #pragma unroll
-                    for (int rb = 0; rb < 2; ++rb) {
-                        float c[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma16816(c, H[0][2 * rb], H[0][2 * rb + 1], H[1][2 * rb], H[1][2 * rb + 1], b.x, b.y);
-                        mma16816(c, H[2][2 * rb], H[2][2 * rb + 1], H[3][2 * rb], H[3][2 * rb + 1], b.z, b.w);
-                        // c0,c1: row 4g+2rb, tokens 2t,2t+1;  c2,c3: row 4g+2rb+1
-                        const unsigned long long s01 = fadd2(pack2(c[0], c[1]), ncorr);
-                        const unsigned long long s23 = fadd2(pack2(c[2], c[3]), ncorr);
-                        const unsigned long long p01 = fmul2(pack2(dwr[2 * rb], dwr[2 * rb]), da2);
-                        const unsigned long long p23 = fmul2(pack2(dwr[2 * rb + 1], dwr[2 * rb + 1]), da2);
-                        acc[rb][nf][0] = ffma2(s01, p01, acc[rb][nf][0]);
-                        acc[rb][nf][1] = ffma2(s23, p23, acc[rb][nf][1]);
+                for (int u = 0; u < kTilesPerWarp; ++u) {
+                    if (!live[u]) continue;
+                    const int j = j0 + cw + kConsumerWarps * u;
+#pragma unroll
+                    for (int nf = 0; nf < NF; ++nf) {
+                        const int tok = 8 * nf + g;
+                        uint4 b = make_uint4(0, 0, 0, 0);
+                        if (tok < p.M) b = act_s[tok * tok_stride + j * 4 + t];
+                        const float2 da = *reinterpret_cast<const float2 *>(da_s + j * TOK + 8 * nf + 2 * t);
+                        const float2 cr = *reinterpret_cast<const float2 *>(corr_s + j * TOK + 8 * nf + 2 * t);
+                        const unsigned long long ncorr = pack2(-cr.x, -cr.y);
+                        const unsigned long long da2 = pack2(da.x, da.y);
+#pragma unroll
+                        for (int rb = 0; rb < 2; ++rb) {
+                            float c[4] = {0.f, 0.f, 0.f, 0.f};
+                            mma16816(c, H[u][0][2 * rb], H[u][0][2 * rb + 1], H[u][1][2 * rb], H[u][1][2 * rb + 1], b.x, b.y);
+                            mma16816(c, H[u][2][2 * rb], H[u][2][2 * rb + 1], H[u][3][2 * rb], H[u][3][2 * rb + 1], b.z, b.w);
+                            // c0,c1: row 4g+2rb, tokens 2t,2t+1;  c2,c3: row 4g+2rb+1
+                            const unsigned long long s01 = fadd2(pack2(c[0], c[1]), ncorr);
+                            const unsigned long long s23 = fadd2(pack2(c[2], c[3]), ncorr);
+                            const unsigned long long p01 = fmul2(pack2(dwr[u][2 * rb], dwr[u][2 * rb]), da2);
+                            const unsigned long long p23 = fmul2(pack2(dwr[u][2 * rb + 1], dwr[u][2 * rb + 1]), da2);
+                            acc[rb][nf][0] = ffma2(s01, p01, acc[rb][nf][0]);
+                            acc[rb][nf][1] = ffma2(s23, p23, acc[rb][nf][1]);
+                        }
                     }
                 }
             }
@@ -431,7 +446,7 @@ Plan plan_for(int M, int64_t nkt) {
     const int stage_bytes = kTilesPerStage * TS + 16;
     // two CTAs per SM when a useful ring still fits in half the shared memory
     int stages2 = (kSmemLimit / 2 - 1024 - fixed) / stage_bytes;
-    if (stages2 >= 6) {
+    if (stages2 >= 4) {
         pl.stages = stages2 > 12 ? 12 : stages2;
         pl.ctas_per_sm = 2;
     } else {

@@ -123,6 +123,23 @@ qmm_status qmm_matmul(qmm_type t, const void *w_tiled, int64_t K, int64_t N, con
     return qmm_matmul_path(t, w_tiled, K, N, a_q, a_d, M, y, ldy, QMM_PATH_AUTO, stream);
 }
 
+size_t qmm_matmul_workspace_size(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0 || (K % 32) != 0 || M > kMaxDim || K > kMaxDim) return 0;
+    return gemm_workspace_bytes(M, K);
+}
+
+qmm_status qmm_matmul_ws(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
+                         int64_t M, float *y, int64_t ldy, void *workspace, size_t workspace_bytes,
+                         qmm_stream_t stream) {
+    qmm_status st = check_matmul(t, w_tiled, K, N, a_q, a_d, M, y, ldy);
+    if (st != QMM_OK) return st;
+    const uint8_t *w = static_cast<const uint8_t *>(w_tiled);
+    if (M <= kDecodeMaxM) return from_cuda(launch_matvec(t, w, K, N, a_q, a_d, M, y, ldy, cs(stream)));
+    if (!workspace || workspace_bytes < gemm_workspace_bytes(M, K)) return QMM_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return QMM_ERR_MISALIGNED;
+    return from_cuda(launch_gemm_ws(t, w, K, N, a_q, a_d, M, y, ldy, workspace, cs(stream)));
+}
+
 qmm_status qmm_device_status(qmm_stream_t stream) {
     unsigned v = 0, w = 0;
     cudaError_t e = read_and_clear_device_status(&v, cs(stream));

@@ -147,6 +147,26 @@ QMM_API qmm_status qmm_matmul_path(qmm_type t, const void *w_tiled_dev, int64_t 
                            const int8_t *a_q_dev, const uint16_t *a_d_dev, int64_t M, float *y_dev,
                            int64_t ldy, qmm_path path, qmm_stream_t stream);
 
+/* Bytes of device workspace qmm_matmul_ws needs for M activation rows of length K (0 if invalid). */
+QMM_API size_t qmm_matmul_workspace_size(int64_t M, int64_t K);
+
+/*
+ * qmm_matmul_ws -- qmm_matmul with caller-provided scratch memory for the tensor-core path.
+ *   workspace_dev  >= qmm_matmul_workspace_size(M, K) bytes, 256-byte aligned, owned by the caller;
+ *                  its contents on entry do not matter and are overwritten.  Calls that overlap on the
+ *                  GPU must use different workspaces.
+ * For M > qmm_decode_max_m() the activation quants are first rewritten into the workspace as fp16
+ * holding the same integers (plus a transposed copy of the block scales), which the GEMM then loads
+ * with TMA directly in its operand layout; each token tile is converted once instead of once per
+ * weight tile.  Results equal qmm_matmul's within the stated bound.  For smaller M the workspace is
+ * not touched.  Errors: those of qmm_matmul, plus INVALID_ARG (workspace missing or too small) and
+ * MISALIGNED (workspace not 256-byte aligned).
+ */
+QMM_API qmm_status qmm_matmul_ws(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N,
+                                 const int8_t *a_q_dev, const uint16_t *a_d_dev, int64_t M, float *y_dev,
+                                 int64_t ldy, void *workspace_dev, size_t workspace_bytes,
+                                 qmm_stream_t stream);
+
 /*
  * qmm_device_status -- synchronizes `stream`, then returns and clears the library's device status
  * word for the current device: QMM_OK, or QMM_ERR_TIMEOUT when a pipelined kernel gave up on one of

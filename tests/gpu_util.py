@@ -64,3 +64,18 @@ def assert_within_bound(y_gpu: np.ndarray, y_ref: np.ndarray, bound: np.ndarray,
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance, e.g. at {idx.tolist()}: "
                              f"gpu={y_gpu[tuple(idx[0])]}, ref={y_ref[tuple(idx[0])]}, tol={tol[tuple(idx[0])]}")
+
+
+def gpu_matmul_ws(type_, tiled, K, N, a_q, a_d, M, ldy=None, fill=0x5A):
+    """qmm_matmul_ws with a freshly allocated (and deliberately dirty) workspace."""
+    import block_quantized_matmul_gb300 as qmm
+
+    torch = torch_mod()
+    ldy = N if ldy is None else ldy
+    y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    nbytes = qmm.matmul_workspace_size(M, K)
+    ws = torch.full((nbytes + 256,), fill, dtype=torch.uint8, device="cuda")
+    off = (-ws.data_ptr()) % 256
+    qmm.qmm_matmul_ws(type_, tiled, K, N, a_q, a_d, M, y, ldy, ws.data_ptr() + off, nbytes)
+    torch.cuda.synchronize()
+    return y

@@ -118,3 +118,14 @@ def test_repack_and_quantize_weight_argument_errors(L):
 def test_binding_raises_on_error(L):
     with pytest.raises(qmm.QmmError):
         qmm.qmm_matmul("q4_0", P, 48, 64, P, P, 1, P, 64, stream=0)
+
+
+def test_matmul_ws_argument_errors(L):
+    need = L.qmm_matmul_workspace_size(64, 256)
+    assert need >= 64 * 256 * 2
+    assert L.qmm_matmul_workspace_size(0, 256) == 0 and L.qmm_matmul_workspace_size(64, 48) == 0
+    # M > 16 takes the GEMM path, which needs the workspace
+    assert L.qmm_matmul_ws(0, P, 256, 64, P, P, 64, P, 64, None, need, None) == INVALID
+    assert L.qmm_matmul_ws(0, P, 256, 64, P, P, 64, P, 64, P, need - 1, None) == INVALID
+    assert L.qmm_matmul_ws(0, P, 256, 64, P, P, 64, P, 64, P + 16, need, None) == MISALIGNED
+    assert L.qmm_matmul_ws(0, P, 48, 64, P, P, 64, P, 64, P, need, None) == INVALID

@@ -8,7 +8,8 @@ import numpy as np
 import pytest
 
 from block_quantized_matmul_gb300 import synth
-from tests.gpu_util import TYPES, assert_within_bound, gpu_matmul, gpu_prepare_weight, gpu_quantize_act, torch_mod
+from tests.gpu_util import (TYPES, assert_within_bound, gpu_matmul, gpu_matmul_ws, gpu_prepare_weight,
+                            gpu_quantize_act, torch_mod)
 
 pytestmark = pytest.mark.gpu
 GEMM = 2
@@ -25,7 +26,7 @@ def torch():
     return t
 
 
-def _case(torch, orc, type_, N, K, M, outliers=True, ldy=None):
+def _case(torch, orc, type_, N, K, M, outliers=True, ldy=None, ws=False):
     import block_quantized_matmul_gb300 as qmm
 
     w = synth.weights(N, K, seed=5 * N + K)
@@ -35,9 +36,12 @@ def _case(torch, orc, type_, N, K, M, outliers=True, ldy=None):
     y_ref, bound = orc.matmul(type_, tiled_ref, K, N, q_ref, d_ref)
     _, tiled_d = gpu_prepare_weight(type_, w)
     a_q, a_d = gpu_quantize_act(x)
-    y = gpu_matmul(type_, tiled_d, K, N, a_q, a_d, M, path=GEMM, ldy=ldy).cpu().numpy()
+    if ws:
+        y = gpu_matmul_ws(type_, tiled_d, K, N, a_q, a_d, M, ldy=ldy).cpu().numpy()
+    else:
+        y = gpu_matmul(type_, tiled_d, K, N, a_q, a_d, M, path=GEMM, ldy=ldy).cpu().numpy()
     assert qmm.qmm_device_status() == 0
-    assert_within_bound(y[:, :N], y_ref, bound, f"gemm {type_} N={N} K={K} M={M}")
+    assert_within_bound(y[:, :N], y_ref, bound, f"gemm {type_} N={N} K={K} M={M} ws={ws}")
     if ldy is not None and ldy > N:
         assert np.isnan(y[:, N:]).all()
     return y
@@ -48,6 +52,32 @@ def _case(torch, orc, type_, N, K, M, outliers=True, ldy=None):
 @pytest.mark.parametrize("N,K", [(128, 64), (100, 256), (544, 1024)])
 def test_gemm_parity(torch, orc, type_, M, N, K):
     _case(torch, orc, type_, N, K, M)
+
+
+@pytest.mark.parametrize("type_", TYPES)
+@pytest.mark.parametrize("M", [17, 128, 129, 300])
+@pytest.mark.parametrize("N,K", [(100, 256), (544, 1024)])
+def test_gemm_workspace_parity(torch, orc, type_, M, N, K):
+    _case(torch, orc, type_, N, K, M, ws=True)
+
+
+@pytest.mark.parametrize("type_", TYPES)
+def test_gemm_workspace_ragged(torch, orc, type_):
+    _case(torch, orc, type_, 33, 32, 19, ws=True)              # one K tile, M not a multiple of 8
+    _case(torch, orc, type_, 31, 96, 130, ldy=48, ws=True)
+    _case(torch, orc, type_, 4100, 128, 40, ws=True)
+
+
+def test_gemm_workspace_matches_in_kernel_path(torch):
+    # same integers and scales -> the two token-operand variants give identical results
+    w = synth.weights(512, 1024, seed=21)
+    x = synth.activations(200, 1024, seed=22, outliers=True)
+    _, tiled = gpu_prepare_weight("q4_0", w)
+    a_q, a_d = gpu_quantize_act(x)
+    y1 = gpu_matmul("q4_0", tiled, 1024, 512, a_q, a_d, 200, path=GEMM)
+    y2 = gpu_matmul_ws("q4_0", tiled, 1024, 512, a_q, a_d, 200)
+    y3 = gpu_matmul_ws("q4_0", tiled, 1024, 512, a_q, a_d, 200, fill=0xFF)
+    assert torch.equal(y1, y2) and torch.equal(y2, y3)
 
 
 @pytest.mark.parametrize("type_", TYPES)
@@ -96,6 +126,8 @@ def test_gemm_full_size_sampled(torch, orc, type_, K, N, M):
         assert np.array_equal(tiled_d[s:s + step].cpu().numpy(), tiled_ref[s:s + step]), f"tiles @ {s}"
     a_q, a_d = gpu_quantize_act(x)
     y = gpu_matmul(type_, tiled_d, K, N, a_q, a_d, M, path=0).cpu().numpy()
+    y_ws = gpu_matmul_ws(type_, tiled_d, K, N, a_q, a_d, M).cpu().numpy()
+    assert np.array_equal(y, y_ws)
     assert qmm.qmm_device_status() == 0
     rng = np.random.default_rng(1)
     n_ct = (N + 31) // 32
