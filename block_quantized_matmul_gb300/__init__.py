@@ -19,7 +19,7 @@ __all__ = [
     "block_size", "tile_size", "tiled_size", "flat_size", "iq4nl_table", "decode_max_m",
     "qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
     "qmm_matmul_path", "qmm_device_status", "PATH_AUTO", "PATH_MATVEC", "PATH_GEMM",
-    "matmul_workspace_size", "qmm_matmul_ws",
+    "matmul_workspace_size", "qmm_matmul_ws", "qmm_matmul_noalloc", "matmul_noalloc_max_workspace",
 ]
 
 Q4_0, Q8_0, IQ4_NL = 0, 1, 2
@@ -69,8 +69,11 @@ def lib():
         L.qmm_matmul_workspace_size.argtypes = [i64, i64]
         L.qmm_matmul_workspace_size.restype = sz
         L.qmm_matmul_ws.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp, sz, vp]
+        L.qmm_matmul_noalloc.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp]
+        L.qmm_matmul_noalloc_max_workspace.argtypes = []
+        L.qmm_matmul_noalloc_max_workspace.restype = sz
         for fn in ("qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
-                   "qmm_matmul_path", "qmm_device_status", "qmm_matmul_ws"):
+                   "qmm_matmul_path", "qmm_device_status", "qmm_matmul_ws", "qmm_matmul_noalloc"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -169,6 +172,17 @@ def qmm_matmul_ws(type_, w_tiled, K: int, N: int, a_q, a_d, M: int, y, ldy: int,
                   stream=None) -> None:
     _check("qmm_matmul_ws", lib().qmm_matmul_ws(_t(type_), _ptr(w_tiled), K, N, _ptr(a_q), _ptr(a_d), M, _ptr(y), ldy,
                                                 _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def qmm_matmul_noalloc(type_, w_tiled, K: int, N: int, a_q, a_d, M: int, y, ldy: int, stream=None) -> None:
+    """For callers that cannot allocate device memory: the tensor-core path's workspace is the
+    library's fixed per-device scratch array (see include/qmm.h); overlapping calls race on it."""
+    _check("qmm_matmul_noalloc", lib().qmm_matmul_noalloc(_t(type_), _ptr(w_tiled), K, N, _ptr(a_q), _ptr(a_d), M,
+                                                          _ptr(y), ldy, _stream(stream)))
+
+
+def matmul_noalloc_max_workspace() -> int:
+    return int(lib().qmm_matmul_noalloc_max_workspace())
 
 
 def qmm_device_status(stream=None) -> int:

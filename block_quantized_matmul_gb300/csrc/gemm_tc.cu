@@ -28,6 +28,8 @@
 // status word, lets its copies and MMAs in flight land, frees TMEM and returns.
 #include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched through the runtime)
 
+#include <mutex>
+
 #include "qmm_internal.cuh"
 
 namespace qmm {
@@ -617,6 +619,41 @@ cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t 
                     CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     return dispatch<kActPrepared>(t, p, am, dm, s);
+}
+
+// ---------------------------------------------------------------------------------------------
+// No-allocation variant of the workspace path.
+// Some callers cannot allocate device memory: code running under a custom allocator or memory pool
+// that must not see foreign allocations, inference runtimes that pre-plan every byte of device
+// memory, or programs that must not touch the CUDA allocator in a latency-critical section.  For
+// them the workspace lives in this fixed, file-scope device array instead of a caller buffer.  The
+// array exists once per device for as long as the library stays loaded; its contents persist from
+// call to call, and calls that overlap on the GPU share (and race on) it.
+// ---------------------------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the scratch array on the current device.  The host-side symbol is only a
+// stand-in for the device variable, so the address is looked up once per device (with that device
+// current) and cached.
+cudaError_t noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
 }
 
 cudaError_t read_and_clear_device_status(unsigned *out, cudaStream_t s) {

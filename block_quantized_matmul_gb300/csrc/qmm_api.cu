@@ -140,6 +140,20 @@ qmm_status qmm_matmul_ws(qmm_type t, const void *w_tiled, int64_t K, int64_t N, 
     return from_cuda(launch_gemm_ws(t, w, K, N, a_q, a_d, M, y, ldy, workspace, cs(stream)));
 }
 
+qmm_status qmm_matmul_noalloc(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const int8_t *a_q,
+                              const uint16_t *a_d, int64_t M, float *y, int64_t ldy, qmm_stream_t stream) {
+    qmm_status st = check_matmul(t, w_tiled, K, N, a_q, a_d, M, y, ldy);
+    if (st != QMM_OK) return st;
+    const uint8_t *w = static_cast<const uint8_t *>(w_tiled);
+    if (M <= kDecodeMaxM) return from_cuda(launch_matvec(t, w, K, N, a_q, a_d, M, y, ldy, cs(stream)));
+    if (gemm_workspace_bytes(M, K) > kNoAllocScratchBytes) return QMM_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    if (noalloc_scratch(&scratch) != cudaSuccess) return QMM_ERR_CUDA;
+    return from_cuda(launch_gemm_ws(t, w, K, N, a_q, a_d, M, y, ldy, scratch, cs(stream)));
+}
+
+size_t qmm_matmul_noalloc_max_workspace(void) { return kNoAllocScratchBytes; }
+
 qmm_status qmm_device_status(qmm_stream_t stream) {
     unsigned v = 0, w = 0;
     cudaError_t e = read_and_clear_device_status(&v, cs(stream));

@@ -51,6 +51,11 @@ cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, 
 cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                            const uint16_t *a_d, int64_t M, float *y, int64_t ldy, void *ws, cudaStream_t s);
 size_t gemm_workspace_bytes(int64_t M, int64_t K);
+
+// Fixed device scratch used by qmm_matmul_noalloc (bytes, per device).
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+constexpr int kMaxDevices = 64;
+cudaError_t noalloc_scratch(void **out);
 cudaError_t read_and_clear_device_status(unsigned *out, cudaStream_t s);   // tensor-core GEMM
 cudaError_t read_and_clear_matvec_status(unsigned *out, cudaStream_t s);   // decode matvec
 

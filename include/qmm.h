@@ -168,6 +168,33 @@ QMM_API qmm_status qmm_matmul_ws(qmm_type t, const void *w_tiled_dev, int64_t K,
                                  qmm_stream_t stream);
 
 /*
+ * qmm_matmul_noalloc -- qmm_matmul_ws for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists for users of this library.
+ *
+ * Some callers may not allocate device memory: code running inside a custom allocator or memory
+ * pool that must not see foreign allocations, serving runtimes that plan every byte of device memory
+ * up front, or sections that must not enter the CUDA allocator at all.  This call takes the same
+ * inputs and outputs as qmm_matmul and allocates nothing: for M > qmm_decode_max_m() the
+ * tensor-core path's workspace is a fixed scratch array of qmm_matmul_noalloc_max_workspace() bytes
+ * (8 MiB) that the library holds on every GPU that loads it, until the process exits.
+ *   - Sizes: if qmm_matmul_workspace_size(M, K) exceeds that limit the call returns
+ *     QMM_ERR_INVALID_ARG without launching anything (e.g. M*K up to about 4M elements fits).
+ *   - The first call with M > qmm_decode_max_m() on a device looks up the scratch array's device
+ *     address with that device current and caches it; make that first call before any stream capture.
+ *   - The scratch array is shared by all calls and keeps the last call's contents; nothing in it
+ *     needs to start at zero (each call rewrites what it reads).  Calls that overlap on the GPU (on
+ *     different streams, or from different threads) race on it and must be serialized by the caller.
+ *   - For M <= qmm_decode_max_m() no scratch is used (the decode kernel needs none).
+ * Errors: those of qmm_matmul, plus INVALID_ARG for sizes beyond the scratch limit.
+ */
+QMM_API qmm_status qmm_matmul_noalloc(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N,
+                                      const int8_t *a_q_dev, const uint16_t *a_d_dev, int64_t M,
+                                      float *y_dev, int64_t ldy, qmm_stream_t stream);
+
+/* Size in bytes of the fixed scratch array qmm_matmul_noalloc uses (per device). */
+QMM_API size_t qmm_matmul_noalloc_max_workspace(void);
+
+/*
  * qmm_device_status -- synchronizes `stream`, then returns and clears the library's device status
  * word for the current device: QMM_OK, or QMM_ERR_TIMEOUT when a pipelined kernel gave up on one of
  * its bounded waits (its outputs are then undefined).  QMM_ERR_CUDA if the synchronization fails.
