@@ -20,7 +20,8 @@
  *   - Activation quantization (Q8_0, per 32 elements): amax = max|x|, d = amax/127, id = d ? 1/d : 0,
  *     q = round-half-away(x*id) clamped to [-127,127] (a NaN product, 0*inf, gives 0), stored d = fp16(d).
  *   - Weight quantizers (test-data generation): Q4_0 takes the signed element of largest magnitude m,
- *     d = m/-8, id = d ? 1/d : 0, q = min(15, trunc(x*id + 8.5)); Q8_0 uses the activation rule;
+ *     d = m/-8, id = d ? 1/d : 0, q = min(15, trunc(x*id + 8.5)) (0 for a NaN or negative value);
+ *     Q8_0 uses the activation rule;
  *     IQ4_NL takes d = m/lut[0], d16 = fp16(d), and for each x the index i minimising
  *     |x - f32(d16)*lut[i]| (lowest index on ties).
  *   - The IQ4_NL table itself is not printed on the pages; callers pass the table in.
@@ -193,9 +194,10 @@ static void quantize_block_q4_0(const float *x, uint8_t *codes, uint16_t *d16)
     float id = (d != 0.0f) ? 1.0f / d : 0.0f;
     for (int j = 0; j < 32; ++j) {
         float v = x[j] * id + 8.5f;          /* two roundings: product, then sum (no FMA) */
-        int c = (int)v;                      /* truncation toward zero; v >= 0.5 here */
-        if (c > 15) c = 15;
-        if (c < 0) c = 0;
+        int c;
+        if (!(v >= 0.0f)) c = 0;             /* NaN (0 * inf) or negative */
+        else if (v >= 15.0f) c = 15;         /* min(15, .) taken before the conversion */
+        else c = (int)v;                     /* truncation toward zero */
         codes[j] = (uint8_t)c;
     }
     *d16 = orc_f32_to_f16(d);
