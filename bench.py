@@ -7,13 +7,14 @@ One step = one pass of the hot path over one batch: dynamic Q8_0 quantization of
 fp32 output.  The weight is repacked once beforehand, as at model load.
 
   value   weight-tile bytes per step / device time per step (GB/s), inputs resident in HBM;
-          K consecutive steps timed with CUDA events, rotating through enough weight copies that the
-          working set exceeds the 129 MB L2 (no step hits a weight left in L2 by the previous one).
+          K consecutive steps captured in one CUDA graph and timed with CUDA events on the launching
+          stream, rotating through enough weight copies that the working set exceeds the 129 MB L2
+          (no step hits a weight left in L2 by the previous one).
   e2e     the same metric through the C ABI with host buffers: each step copies its activation
           from pinned host memory, runs both calls and reads the output back.
   roofline  the decode matvec alone: algorithmic bytes (weight tiles + activation quants and
-          scales + fp32 output) per launch / mean launch time from CUDA events, against the
-          measured HBM copy bandwidth.
+          scales + fp32 output) per launch / mean launch time (a graph of back-to-back launches
+          timed with CUDA events), against the measured HBM copy bandwidth.
   other_configs  the remaining workloads, each as its own step (prefill GEMM in TFLOP/s).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -192,7 +193,32 @@ class Workload:
         return 2.0 * self.M * self.N * self.K
 
 
+def capture(torch, fn, n, stream):
+    """CUDA graph of n consecutive calls fn(0..n-1) on `stream` (no host work left in the loop)."""
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n):
+            fn(i, stream)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(torch, g, stream, n):
+    """Device time per call of a captured graph of n calls: events on the launching stream."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n        # ms per call
+
+
 def time_steps(torch, fn, steps, stream):
+    """Eager loop (host launch overhead included), events on the launching stream."""
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -205,15 +231,11 @@ def time_steps(torch, fn, steps, stream):
 
 
 def kernel_time(torch, wl, steps, stream):
-    """Mean duration of the matmul kernel alone: events around each launch on its stream."""
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    torch.cuda.synchronize()
-    for i in range(steps):
-        ev[i][0].record(stream)
-        wl.matmul_only(i, stream)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in ev) / steps
+    """Mean duration of the matmul call alone: a graph of `steps` back-to-back launches (rotating
+    weight copies), timed with events on the launching stream."""
+    g = capture(torch, wl.matmul_only, steps, stream)
+    time_graph(torch, g, stream, steps)            # warm replay
+    return time_graph(torch, g, stream, steps)
 
 
 def run_gpu(args):
@@ -248,18 +270,21 @@ def run_gpu(args):
         for i in range(args.warmup):
             wl.step(i, stream)
     torch.cuda.synchronize()
+    # The K timed steps run as one CUDA graph (act-quant + matmul per step, rotating weights), so the
+    # measurement is the device time of the hot path, not Python launch overhead.
+    graph = capture(torch, wl.step, args.steps, stream)
+    time_graph(torch, graph, stream, args.steps)         # warm-up replay
     with ClockSampler(local) as clk:
         barrier()
-        ms = time_steps(torch, wl.step, args.steps, stream)
+        ms = time_graph(torch, graph, stream, args.steps)
         barrier()
         # keep the GPU busy a little longer so the clock record is not empty on short runs
-        extra = 0
         t_end = time.time() + 0.5
         while time.time() < t_end:
-            for i in range(200):
-                wl.step(i, stream)
-            extra += 200
-        torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                graph.replay()
+            torch.cuda.synchronize()
+    del graph
     if world > 1:
         t = torch.tensor([ms], device="cuda")
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -304,9 +329,12 @@ def run_gpu(args):
                 for i in range(max(3, args.warmup)):
                     o.step(i, stream)
             torch.cuda.synchronize()
-            n = max(10, min(args.steps, 200 if cfg[3] > 16 else 1000))
-            oms = time_steps(torch, o.step, n, stream)
-            okms = kernel_time(torch, o, min(n, 100), stream)
+            n = max(10, min(args.steps, 100 if cfg[3] > 16 else 1000))
+            og = capture(torch, o.step, n, stream)
+            time_graph(torch, og, stream, n)
+            oms = time_graph(torch, og, stream, n)
+            del og
+            okms = kernel_time(torch, o, min(n, 200), stream)
             ent = {"workload": workload_name(*cfg), "ms_per_step": round(oms, 5), "kernel_us": round(okms * 1e3, 3),
                    "weight_GBps": round(o.tiled_bytes / (oms * 1e-3) / 1e9, 1)}
             kbytes = o.algorithmic_bytes() / (okms * 1e-3) / 1e9

@@ -13,17 +13,21 @@
 //     y += S_b * P_b, using packed fma.rn.f32x2.
 //
 // Tile: 128 weight rows (4 column tiles, the UMMA M dimension) x 128 tokens (UMMA N), all of K.
-// Warp roles (448 threads), one 4-stage ring of paired raw + operand buffers per CTA:
-//   warp 0      producer: cp.async.bulk of the 4 raw weight tiles of block kt and a 2-D TMA load of
-//               the block's 128 token rows (mbarrier complete_tx).
-//   warp 1      TMEM owner and MMA issuer (one thread): 3 MMAs per block into a 2-stage TMEM ring.
-//   warps 2-5   converters: thread c turns weight row c of the raw tiles into fp16 in the canonical
-//               K-major 64-byte-swizzled layout and writes the d_w / d_a columns of the
-//               scale-product operands (and, for int8 activations, converts token row c).
+// The pipeline moves K in pairs of 32-wide blocks; TMEM holds S and P of two single blocks.
+// Warp roles (480 threads):
+//   warp 0      W producer: per block pair, one 3-D TMA of the 4 x 2 raw weight tiles plus one TMA of
+//               the pair's token data (fp16 scales, or the raw int8 rows), into a W ring.
+//   warp 1      TMEM owner and MMA issuer (one thread): per block, 2 MMAs for S_b and 1 for P_b into a
+//               2-slot TMEM ring.
+//   warps 2-5   converters: thread c turns weight row c of the pair into fp16 in the canonical K-major
+//               128-byte-swizzled layout and writes the d_w / d_a columns of the scale-product
+//               operands (and, for int8 activations, converts token row c).
 //   warps 6-13  rescale: tcgen05.ld of S_b and P_b, y += S_b*P_b in registers, then the fp32 store.
+//   warp 14     B producer (prepared variant): one 128-byte-swizzled TMA of the fp16 token operand of
+//               the pair, straight into the layout the MMA reads.
 // Two token-operand variants: int8 quants converted in the kernel (no scratch memory), or a prepared
-// fp16 copy in a caller workspace that TMA writes directly in the swizzled operand layout (every
-// token tile is then converted once instead of once per weight tile).
+// fp16 copy in a caller workspace (every token tile is then converted once instead of once per
+// weight tile).
 // Every mbarrier wait is bounded in time; on expiry the kernel records QMM_ERR_TIMEOUT in a device
 // status word, lets its copies and MMAs in flight land, frees TMEM and returns.
 #include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched through the runtime)
@@ -40,17 +44,14 @@ __device__ unsigned g_device_status = 0;   // non-zero once a bounded wait gave 
 
 constexpr int BM = 128;                    // weight rows per CTA
 constexpr int BN = 128;                    // tokens per CTA
-constexpr int kStages = 4;                 // paired raw + operand stages
-constexpr int kTmemStages = 2;
-constexpr int kTmemCols = 512;             // 2 stages x (S 128 + P 128) fp32 columns
+constexpr int kTmemStages = 4;
+constexpr int kTmemCols = 512;             // 4 slots x 128 fp32 columns (S of one block each)
 constexpr int kConvWarp0 = 2, kNumConvWarps = 4;
 constexpr int kRescaleWarp0 = 6, kNumRescaleWarps = 8;
-constexpr int kThreads = (kRescaleWarp0 + kNumRescaleWarps) * 32;
-constexpr int kOpBytes = BM * 64;          // one 128 x 32 fp16 operand (64-byte rows)
-constexpr int kOpStageBytes = 4 * kOpBytes;    // A (weights), B (tokens), AP (d_w), BP (d_a)
-constexpr int kRawWBytes = 4 * kTile8Bytes;    // 4 raw tiles (Q8_0 worst case)
-constexpr int kRawABytes = BN * 32;            // 128 int8 activation rows of one block (or 128 fp16 scales)
-constexpr int kRawStageBytes = kRawWBytes + kRawABytes;
+constexpr int kBProducerWarp = kRescaleWarp0 + kNumRescaleWarps;    // warp 14
+constexpr int kThreads = (kBProducerWarp + 1) * 32;
+constexpr int kOpBytes = BM * 64;          // 128 rows x 64 bytes: one K block (SW64) or the scale columns
+constexpr int kOp2Bytes = BM * 128;        // 128 rows x 128 bytes: a block pair (SW128)
 constexpr int kLutCopies = 16;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
 
@@ -95,19 +96,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait.  Gives up (returning false) when `abort` is raised by another warp or after
-// kWaitLimitNs, in which case it raises `abort` and the device status word itself.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+// kWaitLimitNs, in which case it raises `abort` and the device status word itself.  The fast path
+// (phase already complete) is inline; the timer is read only every 64 polls of the slow path.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort) {
     const unsigned long long t0 = globaltimer();
-    while (true) {
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            atomicOr(&g_device_status, 1u);
-            return false;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                atomicOr(&g_device_status, 1u);
+                return false;
+            }
         }
     }
+}
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, abort);
 }
 
 // Warp-uniform bounded wait: every lane waits, and the warp gives up together if any lane did, so
@@ -140,6 +147,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -149,6 +163,12 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+
+// Same for rows of 128 bytes with the 128-byte swizzle (8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both K-major, M = 128, N = BN.
@@ -174,6 +194,36 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ unsigned long long pack2f(float a, float b) {
+    unsigned long long v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(a), "f"(b));
+    return v;
+}
+__device__ __forceinline__ unsigned long long pack2u(uint32_t a, uint32_t b) {
+    unsigned long long v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(a), "r"(b));
+    return v;
+}
+__device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ void unpack2f(unsigned long long v, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long ffma2p(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// (y0, y1) += t * s, elementwise
+__device__ __forceinline__ void ffma2_acc(float &y0, float &y1, unsigned long long t, unsigned long long s) {
+    unsigned long long yv;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(yv) : "f"(y0), "f"(y1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(yv) : "l"(t), "l"(s));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(y0), "=f"(y1) : "l"(yv));
+}
 __device__ __forceinline__ void ffma2(float &y0, float &y1, uint32_t s0, uint32_t s1, uint32_t p0, uint32_t p1) {
     unsigned long long yv, sv, pv;
     asm("mov.b64 %0, {%1, %2};" : "=l"(yv) : "f"(y0), "f"(y1));
@@ -207,6 +257,12 @@ __device__ __forceinline__ uint32_t q4_byte_to_h2(uint32_t w) {
                            __halves2half2(__float2half_rn(-1032.0f), __float2half_rn(-72.0f))));
 }
 
+// Byte offset of (row, 16-byte chunk) in a 128 x 128-byte K-major operand with the 128-byte swizzle
+// (chunk index XOR the row's low 3 bits; 8-row groups of 1024 bytes).
+__device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
+    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
 // Byte offset of (row, 16-byte chunk) in a 128 x 64-byte K-major operand with the 64-byte swizzle
 // (chunk index XOR bits 1..2 of the row; 8-row groups of 512 bytes).
 __device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
@@ -223,24 +279,70 @@ __device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
 //                 ([K/32][M_pad] fp16), one 256-byte row per block.
 enum { kActInt8 = 0, kActPrepared = 1 };
 
+// Shared-memory plan: three decoupled rings whose stages each cover a pair of K blocks.
+//   W ring   W producer -> converters: the raw weight tiles [4 column tiles][2 blocks] (one 3-D TMA)
+//            and the pair's token data: 2 x 128 fp16 scales (prepared variant) or 128 rows x 64 int8
+//            (int8 variant);
+//   B ring   B producer -> MMA (prepared variant only): the fp16 token operand of the pair, 128 rows x
+//            128 bytes, swizzled by the TMA unit;
+//   op ring  converters -> MMA and rescale: A (weights, 128 x 128 B, 128-byte swizzle), for the int8
+//            variant B (128 x 128 B), and the pair's fp32 scales d_w[2][128] and d_a[2][128].  A stage
+//            is released by the rescale warps once they have applied both blocks' scales (the MMAs
+//            that read A and B have completed by then).
 template <int TYPE, int ACT>
-// 14 warps put 4 warps on some SM sub-partitions, whose 16K-register files then allow at most
+struct GemmPlan {
+    static constexpr bool kPrep = ACT == kActPrepared;
+    static constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    static constexpr int kWTiles = 8 * TS;                                   // [4 ct][2 kt] raw tiles
+    static constexpr int kWTok = kPrep ? 2 * BN * 2 : BN * 64;              // fp16 scales or int8 rows
+    static constexpr int kWStageBytes = (kWTiles + kWTok + 127) / 128 * 128;
+    static constexpr int kScaleBytes = 2 * 2 * 128 * 4;                     // d_w[2][128], d_a[2][128]
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOp2Bytes;                                  // int8 variant only
+    static constexpr int kOffScale = kPrep ? kOp2Bytes : 2 * kOp2Bytes;
+    static constexpr int kOpStage = (kOffScale + kScaleBytes + 1023) / 1024 * 1024;
+    static constexpr int kOpStages = 3;
+    static constexpr int kBStages = kPrep ? 4 : 0;
+    static constexpr int kBRing = kBStages > 0 ? kBStages : 1;               // modulus, never 0
+    static constexpr int kLutBytes = (TYPE == QMM_IQ4_NL) ? 256 * kLutCopies * 4 : 0;
+    static constexpr int kFixed = kOpStages * kOpStage + kBStages * kOp2Bytes + kLutBytes + 1024 + 512;
+    static constexpr int kWStagesFit = (227 * 1024 - kFixed) / kWStageBytes;
+    static constexpr int kWStages = kWStagesFit > 8 ? 8 : kWStagesFit;
+    // byte offsets from the 1024-aligned base
+    static constexpr int kOp = 0;
+    static constexpr int kB = kOp + kOpStages * kOpStage;
+    static constexpr int kW = kB + kBStages * kOp2Bytes;
+    static constexpr int kLut = kW + kWStages * kWStageBytes;
+    static constexpr int kBars = kLut + kLutBytes;
+    static constexpr int kNumBars = 2 * kWStages + 2 * kBStages + 2 * kOpStages + 2 * kTmemStages;
+    static constexpr int kEnd = kBars + kNumBars * 8 + 16;
+    static constexpr size_t kSmem = 1024 + (size_t)kEnd;
+    static_assert(kWStages >= 3, "W ring too shallow");
+};
+
+// 15 warps put 4 warps on some SM sub-partitions, whose 16K-register files then allow at most
 // 128 registers per thread.
+template <int TYPE, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap act_map, const __grid_constant__ CUtensorMap da_map) {
-    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap act_map,
+            const __grid_constant__ CUtensorMap da_map) {
+    using P = GemmPlan<TYPE, ACT>;
+    constexpr int TS = P::TS;
     constexpr int SOFF = (TYPE == QMM_Q8_0) ? kScale8Off : kScale4Off;
+    constexpr int WS = P::kWStages, BR = P::kBRing, OS = P::kOpStages;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_base_u32 = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_base_u32 & 1023u)) & 1023u);
-    uint8_t *op_s = smem;                                                     // kStages x kOpStageBytes
-    uint8_t *raw_s = op_s + kStages * kOpStageBytes;                          // kStages x kRawStageBytes
-    uint32_t *lut_s = reinterpret_cast<uint32_t *>(raw_s + kStages * kRawStageBytes);   // IQ4_NL only
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(lut_s) +
-                                                  (TYPE == QMM_IQ4_NL ? 256 * kLutCopies * 4 : 0));
-    uint64_t *full = bars, *op_full = bars + kStages, *empty = bars + 2 * kStages;
-    uint64_t *tm_full = bars + 3 * kStages, *tm_empty = tm_full + kTmemStages;
+    uint8_t *op_s = smem + P::kOp;
+    uint8_t *b_s = smem + P::kB;
+    uint8_t *w_s = smem + P::kW;
+    uint32_t *lut_s = reinterpret_cast<uint32_t *>(smem + P::kLut);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P::kBars);
+    uint64_t *w_full = bars, *w_empty = bars + WS;
+    uint64_t *b_full = bars + 2 * WS, *b_empty = b_full + P::kBStages;
+    uint64_t *op_full = bars + 2 * WS + 2 * P::kBStages, *op_empty = op_full + OS;
+    uint64_t *tm_full = op_empty + OS, *tm_empty = tm_full + kTmemStages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tm_empty + kTmemStages);
     volatile int *abort = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -250,21 +352,20 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap act_map, con
     const int n_tiles = (int)((p.n_col_tiles - ct0) < 4 ? (p.n_col_tiles - ct0) : 4);
     const int n_tok = (int)((p.M - m0) < BN ? (p.M - m0) : BN);
     const int64_t nkt = p.nkt;
+    const int nkt32 = (int)p.nkt;
+    const int npairs = (nkt32 + 1) >> 1;
 
-    // ---- set-up: barriers, zeroed scale-product operands, IQ4_NL table, TMEM ----
+    // ---- set-up: barriers, IQ4_NL table, TMEM ----
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
+        for (int s = 0; s < WS; ++s) { mbar_init(smem_u32(&w_full[s]), 1); mbar_init(smem_u32(&w_empty[s]), kNumConvWarps * 32); }
+        for (int s = 0; s < P::kBStages; ++s) { mbar_init(smem_u32(&b_full[s]), 1); mbar_init(smem_u32(&b_empty[s]), 1); }
+        for (int s = 0; s < OS; ++s) {
             mbar_init(smem_u32(&op_full[s]), kNumConvWarps * 32);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&op_empty[s]), kNumRescaleWarps * 32);
         }
         for (int s = 0; s < kTmemStages; ++s) { mbar_init(smem_u32(&tm_full[s]), 1); mbar_init(smem_u32(&tm_empty[s]), kNumRescaleWarps * 32); }
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    for (int s = 0; s < kStages; ++s) {
-        uint4 *zp = reinterpret_cast<uint4 *>(op_s + s * kOpStageBytes + 2 * kOpBytes);   // AP and BP
-        for (int i = threadIdx.x; i < 2 * kOpBytes / 16; i += kThreads) zp[i] = make_uint4(0, 0, 0, 0);
     }
     if constexpr (TYPE == QMM_IQ4_NL) {
         for (int i = threadIdx.x; i < 256 * kLutCopies; i += kThreads) {
@@ -278,186 +379,241 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap act_map, con
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        // ================================ producer ================================
+        // ============================== W producer ==============================
         if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&act_map)) : "memory");
-            if (ACT == kActPrepared) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&da_map)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&w_map)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(P::kPrep ? &da_map : &act_map)) : "memory");
         }
-        uint32_t issued[kStages];
-#pragma unroll
-        for (int s = 0; s < kStages; ++s) issued[s] = 0;
-        for (int64_t kt = 0; kt < nkt; ++kt) {
-            const int s = (int)(kt % kStages);
-            const uint32_t ph = (uint32_t)((kt / kStages) & 1);
-            if (!wait_warp(smem_u32(&empty[s]), ph ^ 1u, abort)) break;
-            const uint32_t fb = smem_u32(&full[s]);
-            const uint32_t raw = smem_u32(raw_s + s * kRawStageBytes);
-            const uint32_t act_bytes = (ACT == kActPrepared) ? (uint32_t)(kOpBytes + 2 * BN) : (uint32_t)kRawABytes;
-            if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(n_tiles * TS) + act_bytes);
-            __syncwarp();
-            if (lane < n_tiles) bulk_g2s(raw + lane * TS, p.tiled + ((ct0 + lane) * nkt + kt) * TS, TS, fb);
+        int issued = 0, s = 0;
+        uint32_t ph = 0;
+        for (int pr = 0; pr < npairs; ++pr) {
+            if (!wait_warp(smem_u32(&w_empty[s]), ph ^ 1u, abort)) break;
             if (lane == 0) {
-                if (ACT == kActPrepared) {
-                    tma_load_2d(smem_u32(op_s + s * kOpStageBytes + kOpBytes), &act_map, (int)(kt * 32), (int)m0, fb);
-                    tma_load_2d(raw + kRawWBytes, &da_map, (int)m0, (int)kt, fb);
-                } else {
-                    tma_load_2d(raw + kRawWBytes, &act_map, (int)(kt * 32), (int)m0, fb);
-                }
+                const uint32_t fb = smem_u32(&w_full[s]);
+                const uint32_t dst = smem_u32(w_s + s * P::kWStageBytes);
+                mbar_arrive_expect_tx(fb, (uint32_t)(P::kWTiles + P::kWTok));
+                tma_load_3d(dst, &w_map, 0, 2 * pr, (int)ct0, fb);
+                if (P::kPrep) tma_load_2d(dst + P::kWTiles, &da_map, (int)m0, 2 * pr, fb);
+                else tma_load_2d(dst + P::kWTiles, &act_map, 64 * pr, (int)m0, fb);
             }
-            issued[s] += 1;
+            __syncwarp();
+            issued = pr + 1;
+            if (++s == WS) { s = 0; ph ^= 1u; }
         }
-        for (int s = 0; s < kStages; ++s)
-            if (issued[s]) wait_drain(smem_u32(&full[s]), (issued[s] - 1) & 1u);
+        // let every copy issued land before the CTA can exit
+        for (int i = (issued > WS ? issued - WS : 0); i < issued; ++i)
+            wait_drain(smem_u32(&w_full[i % WS]), (uint32_t)((i / WS) & 1));
+    } else if (warp == kBProducerWarp) {
+        // ============================== B producer ==============================
+        if (P::kPrep) {
+            int issued = 0, s = 0;
+            uint32_t ph = 0;
+            for (int pr = 0; pr < npairs; ++pr) {
+                if (!wait_warp(smem_u32(&b_empty[s]), ph ^ 1u, abort)) break;
+                if (lane == 0) {
+                    const uint32_t fb = smem_u32(&b_full[s]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)kOp2Bytes);
+                    tma_load_2d(smem_u32(b_s + s * kOp2Bytes), &act_map, 64 * pr, (int)m0, fb);
+                }
+                __syncwarp();
+                issued = pr + 1;
+                if (++s == BR) { s = 0; ph ^= 1u; }
+            }
+            for (int i = (issued > BR ? issued - BR : 0); i < issued; ++i)
+                wait_drain(smem_u32(&b_full[i % BR]), (uint32_t)((i / BR) & 1));
+        }
     } else if (warp == 1) {
         // ================================ MMA issuer ================================
-        uint32_t committed[kTmemStages] = {0, 0};
-        for (int64_t kt = 0; kt < nkt; ++kt) {
-            const int s = (int)(kt % kStages);
-            const uint32_t ph = (uint32_t)((kt / kStages) & 1);
-            const int ts = (int)(kt % kTmemStages);
-            const uint32_t tph = (uint32_t)((kt / kTmemStages) & 1);
-            if (!wait_warp(smem_u32(&op_full[s]), ph, abort)) break;
-            if (!wait_warp(smem_u32(&tm_empty[ts]), tph ^ 1u, abort)) break;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t a = smem_u32(op_s + s * kOpStageBytes);
-                const uint32_t b = a + kOpBytes, ap = a + 2 * kOpBytes, bp = a + 3 * kOpBytes;
-                const uint32_t d_s = tmem_base + (uint32_t)(ts * 256);
-                mma_f16(d_s, smem_desc_sw64(a), smem_desc_sw64(b), 0u);
-                mma_f16(d_s, smem_desc_sw64(a + 32), smem_desc_sw64(b + 32), 1u);
-                mma_f16(d_s + 128, smem_desc_sw64(ap), smem_desc_sw64(bp), 0u);
-                mma_commit(smem_u32(&empty[s]));
-                mma_commit(smem_u32(&tm_full[ts]));
+        int committed = 0;
+        int os = 0, bs = 0, ts = 0;
+        uint32_t oph = 0, bph = 0, tph = 0;
+        bool ok = true;
+        for (int pr = 0; pr < npairs && ok; ++pr) {
+            if (!wait_warp(smem_u32(&op_full[os]), oph, abort)) break;
+            if (P::kPrep && !wait_warp(smem_u32(&b_full[bs]), bph, abort)) break;
+            const uint32_t op = smem_u32(op_s + os * P::kOpStage);
+            const uint32_t bbase = P::kPrep ? smem_u32(b_s + bs * kOp2Bytes) : op + P::kOffB;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if (2 * pr + j >= nkt32) break;
+                if (!wait_warp(smem_u32(&tm_empty[ts]), tph ^ 1u, abort)) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a = op + P::kOffA + 64 * j, b = bbase + 64 * j;
+                    const uint32_t d_s = tmem_base + (uint32_t)(ts * BN);
+                    mma_f16(d_s, smem_desc_sw128(a), smem_desc_sw128(b), 0u);
+                    mma_f16(d_s, smem_desc_sw128(a + 32), smem_desc_sw128(b + 32), 1u);
+                    mma_commit(smem_u32(&tm_full[ts]));
+                }
+                __syncwarp();
+                committed += 1;
+                if (++ts == kTmemStages) { ts = 0; tph ^= 1u; }
             }
-            __syncwarp();
-            committed[ts] += 1;
+            if (!ok) break;
+            if (P::kPrep) {
+                if (lane == 0) mma_commit(smem_u32(&b_empty[bs]));
+                __syncwarp();
+                if (++bs == BR) { bs = 0; bph ^= 1u; }
+            }
+            if (++os == OS) { os = 0; oph ^= 1u; }
         }
-        for (int s = 0; s < kTmemStages; ++s)
-            if (committed[s]) wait_drain(smem_u32(&tm_full[s]), (committed[s] - 1) & 1u);
+        for (int i = (committed > kTmemStages ? committed - kTmemStages : 0); i < committed; ++i)
+            wait_drain(smem_u32(&tm_full[i % kTmemStages]), (uint32_t)((i / kTmemStages) & 1));
     } else if (warp < kRescaleWarp0) {
         // ================================ converters ================================
-        // Thread c owns weight row c (tile q = c/32, tile row c%32) and token row c of the block.
+        // Thread c owns weight row c (tile q = c/32, tile row c%32) and token row c of the pair.
         const int c = threadIdx.x - kConvWarp0 * 32;
         const int q = c >> 5, tr = c & 31;
         const bool w_ok = q < n_tiles;
         const uint32_t *lut_lane = lut_s + (lane & (kLutCopies - 1));
         const bool tok_ok = c < n_tok;
-        // int8 path: block scales of this token, loaded 8 blocks ahead
+        // int8 variant: block scales of this token, loaded 8 blocks (4 pairs) ahead
         uint16_t da_cur[8], da_nxt[8];
-        if (ACT == kActInt8) {
+        if (!P::kPrep) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                da_cur[u] = (tok_ok && u < nkt) ? p.a_d[(m0 + c) * nkt + u] : (uint16_t)0;
-                da_nxt[u] = (tok_ok && 8 + u < nkt) ? p.a_d[(m0 + c) * nkt + 8 + u] : (uint16_t)0;
+                da_cur[u] = (tok_ok && u < nkt32) ? p.a_d[(m0 + c) * nkt + u] : (uint16_t)0;
+                da_nxt[u] = (tok_ok && 8 + u < nkt32) ? p.a_d[(m0 + c) * nkt + 8 + u] : (uint16_t)0;
             }
         }
         bool ok = true;
-        for (int64_t kb = 0; kb < nkt && ok; kb += 8) {
+        int ws = 0, os = 0;
+        uint32_t wph = 0, oph = 0;
+        for (int pg = 0; pg < npairs && ok; pg += 4) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int64_t kt = kb + u;
-                if (kt >= nkt || !ok) break;
-                const int s = (int)(kt % kStages);
-                const uint32_t ph = (uint32_t)((kt / kStages) & 1);
-                if (!wait_bounded(smem_u32(&full[s]), ph, abort)) { ok = false; break; }
-                const uint8_t *raw = raw_s + s * kRawStageBytes;
-                uint8_t *op = op_s + s * kOpStageBytes;
-                // -- weight row c: 32 columns -> 16 half2 in column order --
-                uint32_t h[16];
-                uint16_t dw = 0;
-                if (w_ok) {
-                    const uint8_t *tile = raw + q * TS;
-                    if constexpr (TYPE == QMM_Q8_0) {
+            for (int u = 0; u < 4; ++u) {
+                const int pr = pg + u;
+                if (pr >= npairs || !ok) break;
+                if (!wait_bounded(smem_u32(&w_full[ws]), wph, abort)) { ok = false; break; }
+                if (!wait_bounded(smem_u32(&op_empty[os]), oph ^ 1u, abort)) { ok = false; break; }
+                const uint8_t *raw = w_s + ws * P::kWStageBytes;
+                uint8_t *op = op_s + os * P::kOpStage;
+                float *sc = reinterpret_cast<float *>(op + P::kOffScale);        // [d_w 2][128], [d_a 2][128]
 #pragma unroll
-                        for (int cp = 0; cp < 16; ++cp) {
-                            const uint32_t v = *reinterpret_cast<const uint16_t *>(tile + cp * 64 + 2 * tr);
-                            uint32_t lo, hi;
-                            i8x4_to_h2x2(v, lo, hi);
-                            h[cp] = lo;
+                for (int j = 0; j < 2; ++j) {
+                    // -- weight row c of block j: 32 columns -> 16 half2 in column order --
+                    uint32_t h[16];
+                    uint16_t dw = 0;
+                    if (w_ok) {
+                        const uint8_t *tile = raw + (q * 2 + j) * TS;
+                        if constexpr (TYPE == QMM_Q8_0) {
+#pragma unroll
+                            for (int cp = 0; cp < 16; ++cp) {
+                                const uint32_t v = *reinterpret_cast<const uint16_t *>(tile + cp * 64 + 2 * tr);
+                                uint32_t lo, hi;
+                                i8x4_to_h2x2(v, lo, hi);
+                                h[cp] = lo;
+                            }
+                        } else {
+#pragma unroll
+                            for (int cp = 0; cp < 16; ++cp) {
+                                const uint32_t b = tile[cp * 32 + tr];
+                                if constexpr (TYPE == QMM_Q4_0) h[cp] = q4_byte_to_h2<0>(b);
+                                else h[cp] = lut_lane[b * kLutCopies];
+                            }
                         }
+                        dw = *reinterpret_cast<const uint16_t *>(tile + SOFF + 2 * tr);
                     } else {
 #pragma unroll
-                        for (int cp = 0; cp < 16; ++cp) {
-                            const uint32_t b = tile[cp * 32 + tr];
-                            if constexpr (TYPE == QMM_Q4_0) h[cp] = q4_byte_to_h2<0>(b);
-                            else h[cp] = lut_lane[b * kLutCopies];
+                        for (int cp = 0; cp < 16; ++cp) h[cp] = 0u;
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+                        *reinterpret_cast<uint4 *>(op + P::kOffA + sw128_off(c, 4 * j + ch)) =
+                            make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
+                    sc[j * 128 + c] = __half2float(__ushort_as_half(dw));
+                    // -- token row c of block j --
+                    uint16_t da;
+                    if constexpr (P::kPrep) {
+                        da = *reinterpret_cast<const uint16_t *>(raw + P::kWTiles + 2 * (j * BN + c));
+                    } else {
+                        da = da_cur[2 * u + j];
+                        const uint4 v0 = *reinterpret_cast<const uint4 *>(raw + P::kWTiles + c * 64 + 32 * j);
+                        const uint4 v1 = *reinterpret_cast<const uint4 *>(raw + P::kWTiles + c * 64 + 32 * j + 16);
+                        const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+                        for (int ch = 0; ch < 4; ++ch) {
+                            uint32_t a0, a1, a2, a3;
+                            i8x4_to_h2x2(wv[2 * ch], a0, a1);
+                            i8x4_to_h2x2(wv[2 * ch + 1], a2, a3);
+                            *reinterpret_cast<uint4 *>(op + P::kOffB + sw128_off(c, 4 * j + ch)) =
+                                make_uint4(a0, a1, a2, a3);
                         }
                     }
-                    dw = *reinterpret_cast<const uint16_t *>(tile + SOFF + 2 * tr);
-                } else {
-#pragma unroll
-                    for (int cp = 0; cp < 16; ++cp) h[cp] = 0u;
+                    sc[256 + j * 128 + c] = __half2float(__ushort_as_half(da));
                 }
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    *reinterpret_cast<uint4 *>(op + sw64_off(c, ch)) = make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
-                *reinterpret_cast<uint16_t *>(op + 2 * kOpBytes + sw64_off(c, 0)) = dw;
-                // -- token row c --
-                uint16_t da;
-                if constexpr (ACT == kActPrepared) {
-                    da = *reinterpret_cast<const uint16_t *>(raw + kRawWBytes + 2 * c);
-                } else {
-                    da = da_cur[u];
-                    uint4 v0 = *reinterpret_cast<const uint4 *>(raw + kRawWBytes + c * 32);
-                    uint4 v1 = *reinterpret_cast<const uint4 *>(raw + kRawWBytes + c * 32 + 16);
-                    const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t a0, a1, a2, a3;
-                        i8x4_to_h2x2(wv[2 * ch], a0, a1);
-                        i8x4_to_h2x2(wv[2 * ch + 1], a2, a3);
-                        *reinterpret_cast<uint4 *>(op + kOpBytes + sw64_off(c, ch)) = make_uint4(a0, a1, a2, a3);
-                    }
-                }
-                *reinterpret_cast<uint16_t *>(op + 3 * kOpBytes + sw64_off(c, 0)) = da;
                 fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&op_full[s]));
+                mbar_arrive(smem_u32(&op_full[os]));
+                mbar_arrive(smem_u32(&w_empty[ws]));
+                if (++ws == WS) { ws = 0; wph ^= 1u; }
+                if (++os == OS) { os = 0; oph ^= 1u; }
             }
-            if (ACT == kActInt8) {
+            if (!P::kPrep) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     da_cur[u] = da_nxt[u];
-                    const int64_t kn = kb + 16 + u;
-                    da_nxt[u] = (tok_ok && kn < nkt) ? p.a_d[(m0 + c) * nkt + kn] : (uint16_t)0;
+                    const int kn = 2 * pg + 16 + u;
+                    da_nxt[u] = (tok_ok && kn < nkt32) ? p.a_d[(m0 + c) * nkt + kn] : (uint16_t)0;
                 }
             }
         }
     } else {
         // ================================ rescale ================================
+        // y[m] += (S_b[n][m] * d_a[m]) * d_w[n] for this thread's weight row n and 64 token columns.
         const int rw = warp - kRescaleWarp0;
         const int qd = warp & 3;                     // TMEM lane quadrant this warp may access
         const int half = rw >> 2;                    // token columns 64*half .. 64*half+63
+        const int row = 32 * qd + lane;              // weight row within the tile (= TMEM lane)
         float y[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) y[i] = 0.0f;
         bool ok = true;
-        for (int64_t kt = 0; kt < nkt; ++kt) {
-            const int ts = (int)(kt % kTmemStages);
-            const uint32_t tph = (uint32_t)((kt / kTmemStages) & 1);
+        int ts = 0, os = 0;
+        uint32_t tph = 0, oph = 0;
+        for (int kt = 0; kt < nkt32; ++kt) {
+            const int j = kt & 1;
             if (!wait_warp(smem_u32(&tm_full[ts]), tph, abort)) { ok = false; break; }
+            // the pair's scales were written before op_full completed (already complete here)
+            if (j == 0 && !wait_warp(smem_u32(&op_full[os]), oph, abort)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t t_s = tmem_base + ((uint32_t)(32 * qd) << 16) + (uint32_t)(ts * 256 + 64 * half);
+            const float *sc = reinterpret_cast<const float *>(op_s + os * P::kOpStage + P::kOffScale);
+            const float dw = sc[j * 128 + row];
+            const unsigned long long dw2 = pack2f(dw, dw);
+            const float4 *da4 = reinterpret_cast<const float4 *>(sc + 256 + j * 128 + 64 * half);
+            const uint32_t t_s = tmem_base + ((uint32_t)(32 * qd) << 16) + (uint32_t)(ts * BN + 64 * half);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
-                uint32_t sv[16], pv[16];
+                uint32_t sv[16];
                 tmem_ld16(t_s + 16 * cc, sv);
-                tmem_ld16(t_s + 128 + 16 * cc, pv);
+                float4 da[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) da[e] = da4[4 * cc + e];
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) ffma2(y[16 * cc + e], y[16 * cc + e + 1], sv[e], sv[e + 1], pv[e], pv[e + 1]);
+                for (int e = 0; e < 4; ++e) {
+                    const unsigned long long t0 = fmul2(pack2u(sv[4 * e], sv[4 * e + 1]), pack2f(da[e].x, da[e].y));
+                    const unsigned long long t1 = fmul2(pack2u(sv[4 * e + 2], sv[4 * e + 3]), pack2f(da[e].z, da[e].w));
+                    ffma2_acc(y[16 * cc + 4 * e], y[16 * cc + 4 * e + 1], t0, dw2);
+                    ffma2_acc(y[16 * cc + 4 * e + 2], y[16 * cc + 4 * e + 3], t1, dw2);
+                }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&tm_empty[ts]));
+            if (++ts == kTmemStages) { ts = 0; tph ^= 1u; }
+            if (j == 1 || kt + 1 == nkt32) {
+                // both blocks of the pair applied: the operand stage (A, B and the scales) is free
+                mbar_arrive(smem_u32(&op_empty[os]));
+                if (++os == OS) { os = 0; oph ^= 1u; }
+            }
         }
         if (ok) {
-            const int64_t n = (ct0 * 32) + 32 * qd + lane;
+            const int64_t n = (ct0 * 32) + row;
             if (n < p.N) {
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
@@ -500,14 +656,6 @@ __global__ void __launch_bounds__(256) prepare_act_kernel(const int8_t *__restri
     }
 }
 
-template <int TYPE>
-size_t gemm_smem_bytes() {
-    size_t b = 1024 + (size_t)kStages * (kOpStageBytes + kRawStageBytes);
-    if (TYPE == QMM_IQ4_NL) b += 256 * kLutCopies * 4;
-    b += (3 * kStages + 2 * kTmemStages) * 8 + 16;
-    return b;
-}
-
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -540,14 +688,35 @@ cudaError_t make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ba
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// 3-D tensor map of the tiled weight viewed as [n_col_tiles][n_k_tiles][tile bytes / 8] of 8-byte
+// words: one box = the 4 column tiles x 2 K tiles of a block pair (column tiles past the end read
+// as zeros).
+cudaError_t make_weight_map(CUtensorMap *map, const uint8_t *tiled, int tile_bytes, int64_t nkt, int64_t nct) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {(cuuint64_t)(tile_bytes / 8), (cuuint64_t)nkt, (cuuint64_t)nct};
+    const cuuint64_t strides[2] = {(cuuint64_t)tile_bytes, (cuuint64_t)nkt * (cuuint64_t)tile_bytes};
+    const cuuint32_t box[3] = {(cuuint32_t)(tile_bytes / 8), 2, 4};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint8_t *>(tiled), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int TYPE, int ACT>
 cudaError_t launch_typed(const GemmParams &p, const CUtensorMap &act_map, const CUtensorMap &da_map, cudaStream_t s) {
+    using P = GemmPlan<TYPE, ACT>;
+    static_assert(P::kSmem <= 227 * 1024, "shared memory plan too large");
     auto kern = gemm_kernel<TYPE, ACT>;
-    const size_t smem = gemm_smem_bytes<TYPE>();
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static int attr_done[4] = {0, 0, 0, 0};
+    cudaError_t e = ensure_smem_limit(kern, P::kSmem, attr_done);
+    if (e != cudaSuccess) return e;
+    alignas(64) CUtensorMap w_map;
+    e = make_weight_map(&w_map, p.tiled, P::TS, p.nkt, p.n_col_tiles);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((p.n_col_tiles + 3) / 4), (unsigned)((p.M + BN - 1) / BN), 1);
-    kern<<<grid, kThreads, smem, s>>>(p, act_map, da_map);
+    kern<<<grid, kThreads, P::kSmem, s>>>(p, w_map, act_map, da_map);
     return cudaGetLastError();
 }
 
@@ -584,7 +753,7 @@ cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, 
     if ((M + BN - 1) / BN > 65535) return cudaErrorInvalidValue;
     const GemmParams p = make_params(tiled, K, N, a_q, a_d, M, y, ldy);
     alignas(64) CUtensorMap am, dm;
-    cudaError_t e = make_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, (uint64_t)K, (uint64_t)M, (uint64_t)K, 32, BN,
+    cudaError_t e = make_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, (uint64_t)K, (uint64_t)M, (uint64_t)K, 64, BN,
                                 CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     dm = am;   // unused by this variant
@@ -612,10 +781,10 @@ cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t 
     }
     const GemmParams p = make_params(tiled, K, N, a_q, a_d, M, y, ldy);
     alignas(64) CUtensorMap am, dm;
-    cudaError_t e = make_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a_h, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 32,
-                                BN, CU_TENSOR_MAP_SWIZZLE_64B);
+    cudaError_t e = make_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a_h, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64,
+                                BN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
-    e = make_map_2d(&dm, CU_TENSOR_MAP_DATA_TYPE_UINT16, a_dT, (uint64_t)m_pad, (uint64_t)nkt, (uint64_t)m_pad * 2, BN, 1,
+    e = make_map_2d(&dm, CU_TENSOR_MAP_DATA_TYPE_UINT16, a_dT, (uint64_t)m_pad, (uint64_t)nkt, (uint64_t)m_pad * 2, BN, 2,
                     CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     return dispatch<kActPrepared>(t, p, am, dm, s);

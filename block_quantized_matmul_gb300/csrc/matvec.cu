@@ -8,28 +8,27 @@
 // GB300 counterpart of both.
 //
 // GB300 design:
-//   * Persistent CTAs (one or two per SM) each own a set of column tiles.  The K tiles of a column
+//   * Persistent CTAs (one wide or two narrow per SM) each own a set of column tiles.  The K tiles of a column
 //     tile are contiguous in memory (tile_idx = ct*n_k_tiles + kt), so one producer warp streams them
-//     with 1-D cp.async.bulk copies of 16 tiles into a deep shared-memory ring (mbarrier
+//     with 1-D cp.async.bulk copies of one stage (2 tiles per consumer warp) into a deep ring (mbarrier
 //     complete_tx / consumer release) -- the pipelined multi-buffering of the pages, with the TMA
 //     engine as the DMA queue.
-//   * 8 consumer warps take two tiles of each 16-tile stage (two independent chains per warp).  Quants become fp16 holding exact integers
+//   * 8 or 16 consumer warps take two tiles each of every stage (two independent chains per warp).  Quants become fp16 holding exact integers
 //     (biased: 1024+q or 1152+q, see decode_*), activations are staged once per CTA as fp16 in the
 //     mma fragment order, and mma.sync.m16n8k16 (fp32 accumulate) yields block sums that are exact
 //     integers; subtracting the exact per-(token, block) bias gives S_b.  fp16 mma.sync runs at ~4x
 //     the int8 mma.sync rate on sm_103a, where int8 tcgen05 does not exist.
 //   * Per block the fp32 result is rescaled by d_w*d_a with packed f32x2 arithmetic and accumulated.
-//   * No atomics and no scratch memory: each column tile is reduced across the 8 warps in a fixed
+//   * Launched as a programmatic dependent: weight streaming overlaps the end of the preceding grid
+//     (the activation quantizer), and only the activation staging waits for it.
+//   * No atomics and no scratch memory: each column tile is reduced across the warps in a fixed
 //     order; if the staged activations would not fit, K is processed in passes that add into y.
 #include "qmm_internal.cuh"
 
 namespace qmm {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (1 + kConsumerWarps);     // warp 0 = producer
 constexpr int kTilesPerWarp = 2;                        // independent tiles per warp per stage (ILP)
-constexpr int kTilesPerStage = kConsumerWarps * kTilesPerWarp;
 constexpr int kLutCopies = 16;
 constexpr int kActBudget = 64 * 1024;                   // bytes of staged activations per CTA
 constexpr int kSmemLimit = 227 * 1024;
@@ -74,18 +73,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Bounded wait.  Gives up (returning false) when `abort` is raised by another warp or after
+// kWaitLimitNs, in which case it raises `abort` and the device status word itself.  The fast path
+// (phase already complete) is inline; the timer is read only every 64 polls of the slow path.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort) {
     const unsigned long long t0 = globaltimer();
-    while (true) {
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            *abort = 1;
-            atomicOr(&g_mv_status, 1u);
-            return false;
+        if ((it & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                atomicOr(&g_mv_status, 1u);
+                return false;
+            }
         }
     }
+}
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, abort);
 }
 __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
@@ -98,8 +105,9 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
-__device__ __forceinline__ void consumer_sync() {      // named barrier over the 8 consumer warps
-    asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+template <int CW>
+__device__ __forceinline__ void consumer_sync() {      // named barrier over the consumer warps
+    asm volatile("bar.sync 1, %0;" ::"r"(CW * 32) : "memory");
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -192,9 +200,10 @@ __host__ __device__ inline int act_tok_stride(int nkc) { return nkc * 4 + ((nkc 
 struct MvLayout {
     int ring, bars, act, da, corr, red, lut, total;
 };
-template <int TYPE, int NF>
+template <int TYPE, int NF, int CW>
 __host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
     constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    constexpr int kTilesPerStage = CW * kTilesPerWarp;
     MvLayout L;
     int off = 0;
     L.ring = off;  off += stages * kTilesPerStage * TS;
@@ -204,20 +213,24 @@ __host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
     L.act = off;   off += M * act_tok_stride(nkc) * 16;     // [M][stride] uint4 (16 half2 per block)
     L.da = off;    off += nkc * 8 * NF * 4;                 // [nkc][8*NF] float
     L.corr = off;  off += nkc * 8 * NF * 4;                 // [nkc][8*NF] float
-    L.red = off;   off += kConsumerWarps * 2 * NF * 4 * 32 * 4;
+    L.red = off;   off += CW * 2 * NF * 4 * 32 * 4;
     L.lut = off;   off += (TYPE == QMM_IQ4_NL) ? 256 * kLutCopies * 4 : 0;
     L.total = off;
     return L;
 }
 
-template <int TYPE, int NF>
-__global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvParams p) {
+// CW consumer warps per CTA: 8 (two CTAs per SM) for grids with many column tiles, 16 (one wide CTA
+// per SM) for small ones.
+template <int TYPE, int NF, int CW>
+__global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const MvParams p) {
+    constexpr int kConsumerWarps = CW;
+    constexpr int kTilesPerStage = CW * kTilesPerWarp;
     constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
     constexpr int SOFF = (TYPE == QMM_Q8_0) ? kScale8Off : kScale4Off;
     constexpr int TOK = 8 * NF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-    const MvLayout L = mv_layout<TYPE, NF>(p.M, p.nkc, p.stages);
+    const MvLayout L = mv_layout<TYPE, NF, CW>(p.M, p.nkc, p.stages);
     uint8_t *ring = smem + L.ring;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + p.stages;
@@ -279,6 +292,11 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvParams p) {
     const int ctid = threadIdx.x - 32;        // 0..255
     const int g = lane >> 2, t = lane & 3;
 
+    // The weights never depend on the kernel launched just before on the stream, so the producer
+    // starts streaming at once; the activations may, so the consumers wait for that grid first
+    // (a no-op unless this grid was launched as its programmatic dependent).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     // ---- stage activations once: per (token, block) 16 half2 in fragment order, plus the
     //      per-block scale and the exact bias of the biased weight decode ----
     if constexpr (TYPE == QMM_IQ4_NL) {
@@ -320,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvParams p) {
         da_s[j * TOK + tok] = d;
         corr_s[j * TOK + tok] = corr;
     }
-    consumer_sync();
+    consumer_sync<CW>();
 
     // After a timed-out wait a warp stops waiting and computing but keeps the loop structure, so
     // every consumer warp still reaches the same named barriers.
@@ -401,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvParams p) {
                     red_s[((((cw * 2 + rb) * NF + nf) * 2 + h) * 2 + 0) * 32 + lane] = a;
                     red_s[((((cw * 2 + rb) * NF + nf) * 2 + h) * 2 + 1) * 32 + lane] = b;
                 }
-        consumer_sync();
+        consumer_sync<CW>();
         if (cw == 0) {
 #pragma unroll
             for (int rb = 0; rb < 2; ++rb)
@@ -424,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 2) matvec_kernel(const MvParams p) {
                             }
                         }
         }
-        consumer_sync();
+        consumer_sync<CW>();
     }
 }
 
@@ -433,29 +451,25 @@ struct Plan {
     size_t smem;
 };
 
-template <int TYPE, int NF>
+template <int TYPE, int NF, int CW>
 Plan plan_for(int M, int64_t nkt) {
     constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    constexpr int kTilesPerStage = CW * kTilesPerWarp;
     Plan pl;
     pl.nf = NF;
     int64_t nkc = kActBudget / (64 * (int64_t)M);
     if (nkc > nkt) nkc = nkt;
     if (nkc < 1) nkc = 1;
     pl.nkc = (int)nkc;
-    const int fixed = mv_layout<TYPE, NF>(M, pl.nkc, 0).total + 128;
+    const int fixed = mv_layout<TYPE, NF, CW>(M, pl.nkc, 0).total + 128;
     const int stage_bytes = kTilesPerStage * TS + 16;
-    // two CTAs per SM when a useful ring still fits in half the shared memory
-    int stages2 = (kSmemLimit / 2 - 1024 - fixed) / stage_bytes;
-    if (stages2 >= 4) {
-        pl.stages = stages2 > 12 ? 12 : stages2;
-        pl.ctas_per_sm = 2;
-    } else {
-        int st = (kSmemLimit - 1024 - fixed) / stage_bytes;
-        pl.stages = st > 16 ? 16 : st;
-        pl.ctas_per_sm = 1;
-    }
+    // CW = 16: one wide CTA per SM (all of shared memory); CW = 8: two CTAs per SM (half each)
+    const int budget = (CW == 16) ? kSmemLimit : kSmemLimit / 2;
+    int st = (budget - 1024 - fixed) / stage_bytes;
+    pl.stages = st > 12 ? 12 : st;
+    pl.ctas_per_sm = 16 / CW;
     if (pl.stages < 2) pl.stages = 2;
-    pl.smem = (size_t)mv_layout<TYPE, NF>(M, pl.nkc, pl.stages).total + 128;
+    pl.smem = (size_t)mv_layout<TYPE, NF, CW>(M, pl.nkc, pl.stages).total + 128;
     return pl;
 }
 
@@ -470,13 +484,14 @@ int num_sms() {
     return sms;
 }
 
-template <int TYPE, int NF>
-cudaError_t run(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
-                int64_t ldy, cudaStream_t s) {
+template <int TYPE, int NF, int CW>
+cudaError_t run_cw(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
+                   int64_t ldy, cudaStream_t s) {
     const int64_t nkt = K / 32, nct = (N + 31) / 32;
-    const Plan pl = plan_for<TYPE, NF>(M, nkt);
-    auto kern = matvec_kernel<TYPE, NF>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    const Plan pl = plan_for<TYPE, NF, CW>(M, nkt);
+    auto kern = matvec_kernel<TYPE, NF, CW>;
+    static int attr_done[4] = {0, 0, 0, 0};
+    cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
     if (e != cudaSuccess) return e;
     int64_t grid = (int64_t)num_sms() * pl.ctas_per_sm;
     if (grid > nct) grid = nct;
@@ -497,11 +512,32 @@ cudaError_t run(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, c
         p.accumulate = kt0 > 0;
         p.stages = pl.stages;
         p.lut = iq4nl_lut();
-        kern<<<(unsigned)grid, kThreads, pl.smem, s>>>(p);
-        e = cudaGetLastError();
+        // programmatic dependent launch: may start while the previous grid on the stream is still
+        // running (only if that grid allows it); the kernel waits before it reads activations or y
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.blockDim = dim3(32 * (1 + CW), 1, 1);
+        cfg.dynamicSmemBytes = pl.smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, p);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// Many column tiles: two narrow CTAs per SM hide latency best; few: one wide CTA per SM streams each
+// column tile twice as fast, which keeps the rounds of a small grid short and balanced.
+template <int TYPE, int NF>
+cudaError_t run(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
+                int64_t ldy, cudaStream_t s) {
+    const int64_t nct = (N + 31) / 32;
+    if (nct >= (int64_t)num_sms() * 8) return run_cw<TYPE, NF, 8>(tiled, K, N, a_q, a_d, M, y, ldy, s);
+    return run_cw<TYPE, NF, 16>(tiled, K, N, a_q, a_d, M, y, ldy, s);
 }
 
 }  // namespace

@@ -59,6 +59,22 @@ cudaError_t noalloc_scratch(void **out);
 cudaError_t read_and_clear_device_status(unsigned *out, cudaStream_t s);   // tensor-core GEMM
 cudaError_t read_and_clear_matvec_status(unsigned *out, cudaStream_t s);   // decode matvec
 
+// Raises a kernel's dynamic shared-memory limit once per device (the attribute is per device and
+// per function, and setting it on every call costs host time on the launch path).
+// `done_mask` must be a static owned by the caller's (kernel-specific) launcher: bit d is set once the
+// attribute is in place on device d (devices 0..127; others set it on every call).
+template <typename Kern>
+inline cudaError_t ensure_smem_limit(Kern kern, size_t bytes, int (&done_mask)[4]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cacheable = dev >= 0 && dev < 128;
+    if (cacheable && (__atomic_load_n(&done_mask[dev >> 5], __ATOMIC_ACQUIRE) >> (dev & 31)) & 1) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && cacheable) __atomic_fetch_or(&done_mask[dev >> 5], 1 << (dev & 31), __ATOMIC_RELEASE);
+    return e;
+}
+
 // Largest M handled by one decode-matvec launch (two 8-token mma fragments).
 constexpr int kDecodeMaxM = 16;
 

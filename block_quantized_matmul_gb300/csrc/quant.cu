@@ -26,6 +26,9 @@ template <bool vec>
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x, int64_t M, int64_t K,
                                                            int64_t ldx, int8_t *__restrict__ a_q,
                                                            uint16_t *__restrict__ a_d) {
+    // Lets a dependent grid launched after this one (the matmul) start its independent work -- streaming
+    // weights -- right away; it still waits for this grid to finish before reading a_q / a_d.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t quads_per_row = K / 4;
     const int64_t total = M * quads_per_row;
     const unsigned lane = threadIdx.x & 31u;
