@@ -29,6 +29,7 @@ namespace qmm {
 namespace {
 
 constexpr int kTilesPerWarp = 2;                        // independent tiles per warp per stage (ILP)
+constexpr int kDp4aMaxM = 4;                            // tokens up to which the int8 dot-product path runs
 constexpr int kLutCopies = 16;
 constexpr int kActBudget = 64 * 1024;                   // bytes of staged activations per CTA
 constexpr int kSmemLimit = 227 * 1024;
@@ -105,6 +106,41 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// Producer warp: streams the K tiles [kt0, kt0 + nkc) of every column tile this CTA owns into the
+// ring, one stage of TPS consecutive tiles per 1-D bulk copy, and returns once the copies in
+// flight have landed.
+template <int TS, int TPS>
+__device__ __forceinline__ void produce(const MvParams &p, uint8_t *ring, uint64_t *full, uint64_t *empty,
+                                        volatile int *abort, int lane) {
+    const int stages = p.stages, nkc = p.nkc;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t ct = blockIdx.x; ct < p.n_col_tiles && ok; ct += gridDim.x) {
+        const uint8_t *src = p.tiled + (ct * p.nkt + p.kt0) * TS;
+        for (int j0 = 0; j0 < nkc; j0 += TPS, ++it) {
+            const int s = (int)(it % (uint32_t)stages);
+            const uint32_t ph = (it / (uint32_t)stages) & 1u;
+            if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort)) { ok = false; break; }
+            if (lane == 0) {
+                const int nt = (nkc - j0) < TPS ? (nkc - j0) : TPS;
+                const uint32_t bytes = (uint32_t)(nt * TS);
+                const uint32_t fb = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(fb, bytes);
+                bulk_g2s(smem_u32(ring + s * TPS * TS), src + (int64_t)j0 * TS, bytes, fb);
+            }
+            __syncwarp();
+        }
+    }
+    // copies in flight land before the CTA may exit
+    if (lane == 0 && it > 0) {
+        const uint32_t last = it - 1;
+        for (uint32_t k = 0; k < (uint32_t)stages && k <= last; ++k) {
+            const uint32_t i = last - k;
+            wait_drain(smem_u32(&full[i % stages]), (i / stages) & 1u);
+        }
+    }
+}
+
 template <int CW>
 __device__ __forceinline__ void consumer_sync() {      // named barrier over the consumer warps
     asm volatile("bar.sync 1, %0;" ::"r"(CW * 32) : "memory");
@@ -257,33 +293,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     __syncthreads();
 
     if (warp == 0) {
-        // ============================== producer ==============================
-        uint32_t it = 0;
-        bool ok = true;
-        for (int64_t ct = blockIdx.x; ct < p.n_col_tiles && ok; ct += gridDim.x) {
-            const uint8_t *src = p.tiled + (ct * p.nkt + p.kt0) * TS;
-            for (int j0 = 0; j0 < nkc; j0 += kTilesPerStage, ++it) {
-                const int s = (int)(it % (uint32_t)stages);
-                const uint32_t ph = (it / (uint32_t)stages) & 1u;
-                if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort)) { ok = false; break; }
-                if (lane == 0) {
-                    const int nt = (nkc - j0) < kTilesPerStage ? (nkc - j0) : kTilesPerStage;
-                    const uint32_t bytes = (uint32_t)(nt * TS);
-                    const uint32_t fb = smem_u32(&full[s]);
-                    mbar_arrive_expect_tx(fb, bytes);
-                    bulk_g2s(smem_u32(ring + s * kTilesPerStage * TS), src + (int64_t)j0 * TS, bytes, fb);
-                }
-                __syncwarp();
-            }
-        }
-        // copies in flight land before the CTA may exit
-        if (lane == 0 && it > 0) {
-            const uint32_t last = it - 1;
-            for (uint32_t k = 0; k < (uint32_t)stages && k <= last; ++k) {
-                const uint32_t i = last - k;
-                wait_drain(smem_u32(&full[i % stages]), (i / stages) & 1u);
-            }
-        }
+        produce<TS, kTilesPerStage>(p, ring, full, empty, abort, lane);
         return;
     }
 
@@ -446,31 +456,260 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     }
 }
 
+// ================= small-M path: int8 dot products straight from the tile bytes =================
+// For a handful of tokens the fp16 decode above costs more issue slots than the weight bytes take
+// to arrive.  Here the quants stay 8-bit: lane (i, j) = (lane & 7, lane >> 3) of a warp owns tile
+// rows 4i..4i+3 and column pairs cp = 4j..4j+3 of one tile, gathers each row's bytes into int8x4
+// words with a 4x4 byte transpose (Q4_0 / IQ4_NL: byte cp*32 + row; Q8_0: bytes cp*64 + 2*row,
+// +1) and takes dp4a against the int8 activations.  The column pairs are visited in the rotated
+// order cp_c = 4j + ((c + j) & 3), which puts the 32 lanes' shared-memory words in distinct banks;
+// the activations are staged once per CTA in that same order, so the rotation costs nothing later.
+//   Q4_0:   low and high nibbles are two int8x4 words (0..15) of the even and odd columns; the -8
+//           offset enters as the dp4a chain's start value -8 * (sum of the lane's 8 activations).
+//   IQ4_NL: each nibble indexes the 16-entry table held in 4 registers with two byte permutes and
+//           a third that picks the half by the index's top bit.
+//   Q8_0:   the int8 quants are the operands as they are.
+// Each lane keeps, per token, fp32 sums for its 4 rows: y += float(S) * (d_w * d_a), where S, the
+// product of the two fp16 scales and float(S) are exact; the four column quarters and then the
+// warps are added in a fixed order at the end of a column tile.
+
+// Row words of one tile for lane (i, j): R[r][0], R[r][1] are the int8x4 weights of row 4i + r in
+// the staged activation order (see stage_act_dp4a).
+template <int TYPE>
+__device__ __forceinline__ void tile_rows_dp4a(const uint8_t *tile, int i, int j, uint32_t (&R)[4][2],
+                                               const uint32_t (&tb)[4]) {
+    if constexpr (TYPE == QMM_Q8_0) {
+        uint2 w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint2 *>(tile + (4 * j + ((c + j) & 3)) * 64 + 8 * i);
+        // w[c].x = (row 4i: col 2cp, 2cp+1; row 4i+1: col 2cp, 2cp+1), w[c].y likewise rows 4i+2, 4i+3
+        R[0][0] = __byte_perm(w[0].x, w[1].x, 0x5410); R[0][1] = __byte_perm(w[2].x, w[3].x, 0x5410);
+        R[1][0] = __byte_perm(w[0].x, w[1].x, 0x7632); R[1][1] = __byte_perm(w[2].x, w[3].x, 0x7632);
+        R[2][0] = __byte_perm(w[0].y, w[1].y, 0x5410); R[2][1] = __byte_perm(w[2].y, w[3].y, 0x5410);
+        R[3][0] = __byte_perm(w[0].y, w[1].y, 0x7632); R[3][1] = __byte_perm(w[2].y, w[3].y, 0x7632);
+    } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) w[c] = *reinterpret_cast<const uint32_t *>(tile + (4 * j + ((c + j) & 3)) * 32 + 4 * i);
+        // 4x4 byte transpose: T[r] = byte r (tile row 4i + r) of w[0..3]
+        const uint32_t x01 = __byte_perm(w[0], w[1], 0x5140), x23 = __byte_perm(w[2], w[3], 0x5140);
+        const uint32_t y01 = __byte_perm(w[0], w[1], 0x7362), y23 = __byte_perm(w[2], w[3], 0x7362);
+        uint32_t T[4];
+        T[0] = __byte_perm(x01, x23, 0x5410);
+        T[1] = __byte_perm(x01, x23, 0x7632);
+        T[2] = __byte_perm(y01, y23, 0x5410);
+        T[3] = __byte_perm(y01, y23, 0x7632);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            if constexpr (TYPE == QMM_Q4_0) {
+                R[r][0] = T[r] & 0x0F0F0F0Fu;             // even columns 2cp_c
+                R[r][1] = (T[r] >> 4) & 0x0F0F0F0Fu;      // odd columns 2cp_c + 1
+            } else {
+                // nibbles in column order: lo(b0), hi(b0), lo(b1), hi(b1) | lo(b2), hi(b2), lo(b3), hi(b3)
+                const uint32_t m = T[r] & 0x77777777u;                         // index & 7 per nibble
+                const uint32_t sel0 = ((T[r] >> 1) & 0x4444u) | 0x3210u;       // + 4 where index & 8
+                const uint32_t sel1 = ((T[r] >> 17) & 0x4444u) | 0x3210u;
+                const uint32_t m1 = m >> 16;
+                R[r][0] = __byte_perm(__byte_perm(tb[0], tb[1], m), __byte_perm(tb[2], tb[3], m), sel0);
+                R[r][1] = __byte_perm(__byte_perm(tb[0], tb[1], m1), __byte_perm(tb[2], tb[3], m1), sel1);
+            }
+        }
+    }
+}
+
+// Staged activation record of (token, block, quarter j): the 8 int8 of columns 8j..8j+7 as two
+// int8x4 words in the order of tile_rows_dp4a, the dp4a start value, and fp32(d_a).
+__device__ __forceinline__ uint4 stage_act_dp4a(int type, const int8_t *a8, int j, float da) {
+    const uint2 v = *reinterpret_cast<const uint2 *>(a8 + 8 * j);
+    unsigned long long V = (unsigned long long)v.x | ((unsigned long long)v.y << 32);
+    if (j) V = (V >> (16 * j)) | (V << (64 - 16 * j));       // column pair c <- local pair (c + j) & 3
+    const uint32_t lo = (uint32_t)V, hi = (uint32_t)(V >> 32);
+    uint4 rec;
+    int corr = 0;
+    if (type == QMM_Q4_0) {
+        rec.x = __byte_perm(lo, hi, 0x6420);      // even columns
+        rec.y = __byte_perm(lo, hi, 0x7531);      // odd columns
+#pragma unroll
+        for (int b = 0; b < 8; ++b) corr += (int)a8[8 * j + b];
+        corr *= -8;
+    } else {
+        rec.x = lo;
+        rec.y = hi;
+    }
+    rec.z = (uint32_t)corr;
+    rec.w = __float_as_uint(da);
+    return rec;
+}
+
+struct Dp4aLayout {
+    int ring, bars, act, red, total;
+};
+template <int TYPE, int MT, int CW>
+__host__ __device__ inline Dp4aLayout dp4a_layout(int nkc, int stages) {
+    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    Dp4aLayout L;
+    int off = 0;
+    L.ring = off;  off += stages * CW * kTilesPerWarp * TS;
+    off = (off + 15) & ~15;
+    L.bars = off;  off += 2 * stages * 8 + 16;
+    off = (off + 15) & ~15;
+    L.act = off;   off += MT * nkc * 4 * 16;                 // [MT][nkc][4] uint4
+    L.red = off;   off += CW * MT * 32 * 4;                  // [CW][MT][32] float
+    L.total = off;
+    return L;
+}
+
+// MT = token capacity (1, 2 or 4); p.M <= MT tokens are live.
+template <int TYPE, int MT, int CW>
+__global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(const MvParams p) {
+    constexpr int kTilesPerStage = CW * kTilesPerWarp;
+    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    constexpr int SOFF = (TYPE == QMM_Q8_0) ? kScale8Off : kScale4Off;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    const Dp4aLayout L = dp4a_layout<TYPE, MT, CW>(p.nkc, p.stages);
+    uint8_t *ring = smem + L.ring;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + p.stages;
+    volatile int *abort = reinterpret_cast<volatile int *>(empty + p.stages);
+    uint4 *act_s = reinterpret_cast<uint4 *>(smem + L.act);
+    float *red_s = reinterpret_cast<float *>(smem + L.red);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int stages = p.stages, nkc = p.nkc;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), CW);
+        }
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        produce<TS, kTilesPerStage>(p, ring, full, empty, abort, lane);
+        return;
+    }
+
+    const int cw = warp - 1, ctid = threadIdx.x - 32;
+    const int i = lane & 7, j = lane >> 3;
+
+    // the activations may come from the grid launched just before this one (see produce)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int e = ctid; e < MT * nkc * 4; e += CW * 32) {
+        const int tok = e / (nkc * 4), rem = e - tok * nkc * 4, jt = rem >> 2, q = rem & 3;
+        uint4 rec = make_uint4(0u, 0u, 0u, 0u);
+        if (tok < p.M) {
+            const int64_t kt = p.kt0 + jt;
+            const float da = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
+            rec = stage_act_dp4a(TYPE, p.a_q + (int64_t)tok * p.K + kt * 32, q, da);
+        }
+        act_s[e] = rec;
+    }
+    uint32_t tb[4] = {0u, 0u, 0u, 0u};
+    if constexpr (TYPE == QMM_IQ4_NL) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) tb[w] |= ((uint32_t)(p.lut.v[4 * w + b] & 0xFF)) << (8 * b);
+    }
+    consumer_sync<CW>();
+
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t ct = blockIdx.x; ct < p.n_col_tiles; ct += gridDim.x) {
+        unsigned long long acc[MT][2];           // per token: rows (4i, 4i+1), (4i+2, 4i+3)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = 0ull;
+
+        for (int j0 = 0; j0 < nkc; j0 += kTilesPerStage, ++it) {
+            const int s = (int)(it % (uint32_t)stages);
+            const uint32_t ph = (it / (uint32_t)stages) & 1u;
+            if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
+            if (ok) {
+#pragma unroll
+                for (int u = 0; u < kTilesPerWarp; ++u) {
+                    const int jt = j0 + cw + CW * u;
+                    if (jt >= nkc) continue;
+                    const uint8_t *tile = ring + (s * kTilesPerStage + cw + CW * u) * TS;
+                    uint32_t R[4][2];
+                    tile_rows_dp4a<TYPE>(tile, i, j, R, tb);
+                    const uint2 sc = *reinterpret_cast<const uint2 *>(tile + SOFF + 8 * i);
+                    const float2 d01 = __half22float2(bits_h2(sc.x)), d23 = __half22float2(bits_h2(sc.y));
+                    const unsigned long long dw01 = pack2(d01.x, d01.y), dw23 = pack2(d23.x, d23.y);
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) {
+                        if (t >= p.M) break;
+                        const uint4 a = act_s[(t * nkc + jt) * 4 + j];
+                        int S[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) S[r] = __dp4a((int)R[r][0], (int)a.x, __dp4a((int)R[r][1], (int)a.y, (int)a.z));
+                        const float da = __uint_as_float(a.w);
+                        const unsigned long long da2 = pack2(da, da);
+                        acc[t][0] = ffma2(pack2((float)S[0], (float)S[1]), fmul2(dw01, da2), acc[t][0]);
+                        acc[t][1] = ffma2(pack2((float)S[2], (float)S[3]), fmul2(dw23, da2), acc[t][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        }
+
+        // ---- quarters (lanes i, i+8, i+16, i+24), then warps, in a fixed order ----
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            float v[4];
+            unpack2(acc[t][0], v[0], v[1]);
+            unpack2(acc[t][1], v[2], v[3]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                v[r] += __shfl_xor_sync(0xffffffffu, v[r], 8);
+                v[r] += __shfl_xor_sync(0xffffffffu, v[r], 16);
+            }
+            if (j == 0) *reinterpret_cast<float4 *>(red_s + (cw * MT + t) * 32 + 4 * i) = make_float4(v[0], v[1], v[2], v[3]);
+        }
+        consumer_sync<CW>();
+        if (cw < MT && cw < p.M) {
+            const int t = cw;
+            float sum = 0.0f;
+#pragma unroll
+            for (int w = 0; w < CW; ++w) sum += red_s[(w * MT + t) * 32 + lane];
+            const int64_t n = ct * 32 + lane;
+            if (ok && n < p.N) {
+                float *dst = p.y + (int64_t)t * p.ldy + n;
+                *dst = p.accumulate ? (*dst + sum) : sum;
+            }
+        }
+        consumer_sync<CW>();
+    }
+}
+
 struct Plan {
-    int nf, nkc, stages, ctas_per_sm;
+    int nkc, stages, ctas_per_sm;
     size_t smem;
 };
 
-template <int TYPE, int NF, int CW>
-Plan plan_for(int M, int64_t nkt) {
-    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+// Ring depth from what is left of the CTA's share of shared memory: CW = 16 runs one wide CTA per
+// SM (all of it), CW = 8 two narrow CTAs per SM (half each).
+template <int TS, int CW>
+Plan plan_ring(int nkc, int fixed_bytes) {
     constexpr int kTilesPerStage = CW * kTilesPerWarp;
     Plan pl;
-    pl.nf = NF;
-    int64_t nkc = kActBudget / (64 * (int64_t)M);
+    pl.nkc = nkc;
+    const int stage_bytes = kTilesPerStage * TS + 16;
+    const int budget = (CW == 16) ? kSmemLimit : kSmemLimit / 2;
+    const int st = (budget - 1024 - fixed_bytes - 128) / stage_bytes;
+    pl.stages = st > 12 ? 12 : (st < 2 ? 2 : st);
+    pl.ctas_per_sm = 16 / CW;
+    return pl;
+}
+
+int chunk_tiles(int64_t nkt, int64_t bytes_per_tile) {
+    int64_t nkc = kActBudget / bytes_per_tile;
     if (nkc > nkt) nkc = nkt;
     if (nkc < 1) nkc = 1;
-    pl.nkc = (int)nkc;
-    const int fixed = mv_layout<TYPE, NF, CW>(M, pl.nkc, 0).total + 128;
-    const int stage_bytes = kTilesPerStage * TS + 16;
-    // CW = 16: one wide CTA per SM (all of shared memory); CW = 8: two CTAs per SM (half each)
-    const int budget = (CW == 16) ? kSmemLimit : kSmemLimit / 2;
-    int st = (budget - 1024 - fixed) / stage_bytes;
-    pl.stages = st > 12 ? 12 : st;
-    pl.ctas_per_sm = 16 / CW;
-    if (pl.stages < 2) pl.stages = 2;
-    pl.smem = (size_t)mv_layout<TYPE, NF, CW>(M, pl.nkc, pl.stages).total + 128;
-    return pl;
+    return (int)nkc;
 }
 
 int num_sms() {
@@ -484,15 +723,13 @@ int num_sms() {
     return sms;
 }
 
-template <int TYPE, int NF, int CW>
-cudaError_t run_cw(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
-                   int64_t ldy, cudaStream_t s) {
+// Launch `kern` once per K pass (passes after the first add into y).  Each launch is a programmatic
+// dependent of the grid before it on the stream: it may start while that grid is still running (if
+// that grid allows it), and the kernel waits for it before reading activations or y.
+template <typename Kern>
+cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const uint8_t *tiled, int64_t K, int64_t N,
+                          const int8_t *a_q, const uint16_t *a_d, int M, float *y, int64_t ldy, cudaStream_t s) {
     const int64_t nkt = K / 32, nct = (N + 31) / 32;
-    const Plan pl = plan_for<TYPE, NF, CW>(M, nkt);
-    auto kern = matvec_kernel<TYPE, NF, CW>;
-    static int attr_done[4] = {0, 0, 0, 0};
-    cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
-    if (e != cudaSuccess) return e;
     int64_t grid = (int64_t)num_sms() * pl.ctas_per_sm;
     if (grid > nct) grid = nct;
     for (int64_t kt0 = 0; kt0 < nkt; kt0 += pl.nkc) {
@@ -512,11 +749,9 @@ cudaError_t run_cw(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q
         p.accumulate = kt0 > 0;
         p.stages = pl.stages;
         p.lut = iq4nl_lut();
-        // programmatic dependent launch: may start while the previous grid on the stream is still
-        // running (only if that grid allows it); the kernel waits before it reads activations or y
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid, 1, 1);
-        cfg.blockDim = dim3(32 * (1 + CW), 1, 1);
+        cfg.blockDim = dim3((unsigned)threads, 1, 1);
         cfg.dynamicSmemBytes = pl.smem;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
@@ -524,20 +759,56 @@ cudaError_t run_cw(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kern, p);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
-// Many column tiles: two narrow CTAs per SM hide latency best; few: one wide CTA per SM streams each
-// column tile twice as fast, which keeps the rounds of a small grid short and balanced.
-template <int TYPE, int NF>
+template <int TYPE, int NF, int CW>
+cudaError_t run_mma(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
+                    int64_t ldy, cudaStream_t s) {
+    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    const int nkc = chunk_tiles(K / 32, 64 * (int64_t)M);
+    Plan pl = plan_ring<TS, CW>(nkc, mv_layout<TYPE, NF, CW>(M, nkc, 0).total);
+    pl.smem = (size_t)mv_layout<TYPE, NF, CW>(M, nkc, pl.stages).total + 128;
+    auto kern = matvec_kernel<TYPE, NF, CW>;
+    static int attr_done[4] = {0, 0, 0, 0};
+    const cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
+    if (e != cudaSuccess) return e;
+    return launch_passes(kern, 32 * (1 + CW), pl, tiled, K, N, a_q, a_d, M, y, ldy, s);
+}
+
+template <int TYPE, int MT, int CW>
+cudaError_t run_dp4a(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M,
+                     float *y, int64_t ldy, cudaStream_t s) {
+    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    const int nkc = chunk_tiles(K / 32, 64 * (int64_t)MT);
+    Plan pl = plan_ring<TS, CW>(nkc, dp4a_layout<TYPE, MT, CW>(nkc, 0).total);
+    pl.smem = (size_t)dp4a_layout<TYPE, MT, CW>(nkc, pl.stages).total + 128;
+    auto kern = matvec_dp4a_kernel<TYPE, MT, CW>;
+    static int attr_done[4] = {0, 0, 0, 0};
+    const cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
+    if (e != cudaSuccess) return e;
+    return launch_passes(kern, 32 * (1 + CW), pl, tiled, K, N, a_q, a_d, M, y, ldy, s);
+}
+
+// Up to kDp4aMaxM tokens: int8 dot products; more: fp16 mma.sync.  Many column tiles: two narrow
+// CTAs per SM hide latency best; few: one wide CTA per SM streams each column tile twice as fast,
+// which keeps the rounds of a small grid short and balanced.
+template <int TYPE>
 cudaError_t run(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
                 int64_t ldy, cudaStream_t s) {
-    const int64_t nct = (N + 31) / 32;
-    if (nct >= (int64_t)num_sms() * 8) return run_cw<TYPE, NF, 8>(tiled, K, N, a_q, a_d, M, y, ldy, s);
-    return run_cw<TYPE, NF, 16>(tiled, K, N, a_q, a_d, M, y, ldy, s);
+    const bool narrow = (N + 31) / 32 >= (int64_t)num_sms() * 8;
+#define QMM_MV_ARGS tiled, K, N, a_q, a_d, M, y, ldy, s
+    if (M <= kDp4aMaxM) {
+        if (M == 1) return narrow ? run_dp4a<TYPE, 1, 8>(QMM_MV_ARGS) : run_dp4a<TYPE, 1, 16>(QMM_MV_ARGS);
+        if (M == 2) return narrow ? run_dp4a<TYPE, 2, 8>(QMM_MV_ARGS) : run_dp4a<TYPE, 2, 16>(QMM_MV_ARGS);
+        return narrow ? run_dp4a<TYPE, 4, 8>(QMM_MV_ARGS) : run_dp4a<TYPE, 4, 16>(QMM_MV_ARGS);
+    }
+    if (M <= 8) return narrow ? run_mma<TYPE, 1, 8>(QMM_MV_ARGS) : run_mma<TYPE, 1, 16>(QMM_MV_ARGS);
+    return narrow ? run_mma<TYPE, 2, 8>(QMM_MV_ARGS) : run_mma<TYPE, 2, 16>(QMM_MV_ARGS);
+#undef QMM_MV_ARGS
 }
 
 }  // namespace
@@ -551,11 +822,10 @@ cudaError_t launch_matvec(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N
         const uint16_t *ad = a_d + m0 * nkt;
         float *yy = y + m0 * ldy;
         cudaError_t e;
-        const bool two = mm > 8;
         switch (t) {
-            case QMM_Q4_0: e = two ? run<QMM_Q4_0, 2>(tiled, K, N, aq, ad, mm, yy, ldy, s) : run<QMM_Q4_0, 1>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
-            case QMM_IQ4_NL: e = two ? run<QMM_IQ4_NL, 2>(tiled, K, N, aq, ad, mm, yy, ldy, s) : run<QMM_IQ4_NL, 1>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
-            default: e = two ? run<QMM_Q8_0, 2>(tiled, K, N, aq, ad, mm, yy, ldy, s) : run<QMM_Q8_0, 1>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
+            case QMM_Q4_0: e = run<QMM_Q4_0>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
+            case QMM_IQ4_NL: e = run<QMM_IQ4_NL>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
+            default: e = run<QMM_Q8_0>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
         }
         if (e != cudaSuccess) return e;
     }

@@ -117,7 +117,7 @@ def _parity_case(torch, orc, type_, N, K, M, path, outliers=False, ldy=None):
 
 
 @pytest.mark.parametrize("type_", TYPES)
-@pytest.mark.parametrize("M", [1, 2, 7, 8, 9, 16, 17])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 9, 16, 17])
 @pytest.mark.parametrize("N,K", [(100, 256), (33, 1056), (300, 4096)])
 def test_matvec_parity(torch, orc, type_, M, N, K):
     _parity_case(torch, orc, type_, N, K, M, path=1)
@@ -128,6 +128,13 @@ def test_matvec_ragged_and_ldy(torch, orc, type_):
     _parity_case(torch, orc, type_, 1, 32, 1, path=1)          # one row, one tile
     _parity_case(torch, orc, type_, 31, 64, 3, path=1, ldy=40)  # ldy > N
     _parity_case(torch, orc, type_, 65, 32 * 37, 5, path=1, outliers=True)
+
+
+@pytest.mark.parametrize("type_", TYPES)
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_matvec_k_passes(torch, orc, type_, M):
+    """K long enough that the staged activations take several passes that add into y."""
+    _parity_case(torch, orc, type_, 70, 32 * 1100, M, path=1)
 
 
 def test_matvec_is_deterministic(torch, orc):
