@@ -172,11 +172,28 @@ class Workload:
         self.ws_bytes = qmm.matmul_workspace_size(M, K) if M > qmm.decode_max_m() else 0
         self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device="cuda") if self.ws_bytes else None
         self.ws_ptr = (self.ws.data_ptr() + (-self.ws.data_ptr()) % 256) if self.ws_bytes else None
+        self.fused = M <= qmm.decode_max_m()
         torch.cuda.synchronize()
 
     def step(self, i, stream):
+        """One pass of the hot path: activation quantization + matmul + epilogue.  Decode shapes run
+        it as one kernel (qmm_matmul_f32), prefill shapes as quantize + tensor-core GEMM."""
+        if self.fused:
+            self.qmm.qmm_matmul_f32(self.type_, self.tiled[i % self.copies], self.K, self.N, self.x[i % self.n_act],
+                                    self.K, self.M, self.y, self.N, stream=stream)
+        else:
+            self.step_two_call(i, stream)
+
+    def step_two_call(self, i, stream):
         self.qmm.qmm_quantize_act(self.x[i % self.n_act], self.M, self.K, self.K, self.a_q, self.a_d, stream=stream)
         self.matmul_only(i, stream)
+
+    def kernel_only(self, i, stream):
+        """The dominant kernel alone: the fused decode kernel, or the GEMM."""
+        if self.fused:
+            self.step(i, stream)
+        else:
+            self.matmul_only(i, stream)
 
     def matmul_only(self, i, stream):
         if self.ws_bytes:
@@ -187,7 +204,24 @@ class Workload:
                                 self.y, self.N, stream=stream)
 
     def algorithmic_bytes(self):
-        return self.tiled_bytes + self.M * self.K + self.M * (self.K // 32) * 2 + self.M * self.N * 4
+        """Bytes the dominant kernel must move once: the weight tiles, its activation input (fp32 rows
+        for the fused decode kernel, int8 quants + fp16 scales for the GEMM) and the fp32 output."""
+        act = self.M * self.K * 4 if self.fused else self.M * self.K + self.M * (self.K // 32) * 2
+        return self.tiled_bytes + act + self.M * self.N * 4
+
+    def launches_per_step(self):
+        """Kernels of this library launched by one step: the fused decode kernel once per 16-row group
+        and K pass (K is split only beyond its 64 KB activation staging budget), or quantize +
+        activation prepare + GEMM."""
+        if not self.fused:
+            return 3
+        n, nkt = 0, self.K // 32
+        for m0 in range(0, self.M, 16):
+            mm = min(16, self.M - m0)
+            mt = mm if mm > 4 else (mm if mm <= 2 else 4)
+            nkc = max(1, min(nkt, 65536 // (64 * mt)))
+            n += -(-nkt // nkc)
+        return n
 
     def flops(self):
         return 2.0 * self.M * self.N * self.K
@@ -231,9 +265,9 @@ def time_steps(torch, fn, steps, stream):
 
 
 def kernel_time(torch, wl, steps, stream):
-    """Mean duration of the matmul call alone: a graph of `steps` back-to-back launches (rotating
+    """Mean duration of the dominant kernel alone: a graph of `steps` back-to-back launches (rotating
     weight copies), timed with events on the launching stream."""
-    g = capture(torch, wl.matmul_only, steps, stream)
+    g = capture(torch, wl.kernel_only, steps, stream)
     time_graph(torch, g, stream, steps)            # warm replay
     return time_graph(torch, g, stream, steps)
 
@@ -270,8 +304,9 @@ def run_gpu(args):
         for i in range(args.warmup):
             wl.step(i, stream)
     torch.cuda.synchronize()
-    # The K timed steps run as one CUDA graph (act-quant + matmul per step, rotating weights), so the
-    # measurement is the device time of the hot path, not Python launch overhead.
+    # The K timed steps run as one CUDA graph (act-quant + matmul per step, fused into one kernel for
+    # this decode shape; rotating weights), so the measurement is the device time of the hot path,
+    # not Python launch overhead.
     graph = capture(torch, wl.step, args.steps, stream)
     time_graph(torch, graph, stream, args.steps)         # warm-up replay
     with ClockSampler(local) as clk:
@@ -298,6 +333,15 @@ def run_gpu(args):
                 "frac": round(achieved / hbm_peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                 "traffic": recorded_traffic(workload_name(*HEADLINE)), "kernel_us": round(kms * 1e3, 3)}
 
+    # the same step as two calls (qmm_quantize_act, then qmm_matmul): for comparison only
+    g2 = capture(torch, wl.step_two_call, args.steps, stream)
+    time_graph(torch, g2, stream, args.steps)
+    two_ms = time_graph(torch, g2, stream, args.steps)
+    del g2
+    two_call = {"ms_per_step": round(two_ms, 5), "value": round(wl.tiled_bytes / (two_ms * 1e-3) / 1e9, 1),
+                "unit": "GB/s", "step": "qmm_quantize_act + qmm_matmul (two kernels)"}
+    wl_launches = wl.launches_per_step()
+
     # end to end through the C ABI with host buffers
     x_host = torch.empty((wl.n_act, M, K), dtype=torch.float32).pin_memory()
     x_host.copy_(wl.x.cpu())
@@ -306,8 +350,7 @@ def run_gpu(args):
 
     def e2e_step(i, s):
         x_dev.copy_(x_host[i % wl.n_act], non_blocking=True)
-        qmm.qmm_quantize_act(x_dev, M, K, K, wl.a_q, wl.a_d, stream=s)
-        qmm.qmm_matmul(type_, wl.tiled[i % wl.copies], K, N, wl.a_q, wl.a_d, M, wl.y, N, stream=s)
+        qmm.qmm_matmul_f32(type_, wl.tiled[i % wl.copies], K, N, x_dev, K, M, wl.y, N, stream=s)
         y_host.copy_(wl.y, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -359,12 +402,13 @@ def run_gpu(args):
         "arith": "Q8_0 weights x int8 activations: exact integer block sums on fp16 tensor cores, fp32 scaling",
         "data": "synthetic (seeded: weights N(0,0.02^2) -> Q8_0 tiles, activations N(0,1))",
         "config": {"workload": workload_name(*HEADLINE), "type": type_, "K": K, "N": N, "M": M,
-                   "step": "qmm_quantize_act + qmm_matmul (decode matvec)",
+                   "step": "qmm_matmul_f32: activation quantization fused into the decode kernel",
                    "l2": f"{wl_copies_note(qmm, type_, K, N)}", "parallelism": f"replica x{world}"},
         "pct_hbm_peak": round(value / hbm_peak * 100, 2),
         "roofline": roofline,
         "e2e": e2e,
-        "gpu_launches": (args.steps) * (1 + 1),
+        "two_call_step": two_call,
+        "gpu_launches": args.steps * wl_launches,
         "clocks": clk.summary(),
         "device_status": status,
         "other_configs": others,
@@ -436,7 +480,7 @@ def run_reference(args):
 
 
 def run_profile(args):
-    """Set up one workload and launch its matmul kernel warmup + steps times (for ncu captures)."""
+    """Set up one workload and launch its dominant kernel warmup + steps times (for ncu captures)."""
     import torch
 
     import block_quantized_matmul_gb300 as qmm
@@ -449,7 +493,7 @@ def run_profile(args):
     stream = torch.cuda.current_stream()
     wl.step(0, stream)
     for i in range(args.warmup + args.steps):
-        wl.matmul_only(i, stream)
+        wl.kernel_only(i, stream)
     torch.cuda.synchronize()
     print(json.dumps({"profile": args.profile, "launches": args.warmup + args.steps + 1,
                       "status": qmm.qmm_device_status()}))

@@ -64,6 +64,7 @@ def lib():
         L.qmm_unpack.argtypes = [i32, vp, i64, i64, vp, vp]
         L.qmm_quantize_act.argtypes = [vp, i64, i64, i64, vp, vp, vp]
         L.qmm_matmul.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp]
+        L.qmm_matmul_f32.argtypes = [i32, vp, i64, i64, vp, i64, i64, vp, i64, vp]
         L.qmm_matmul_path.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, i32, vp]
         L.qmm_device_status.argtypes = [vp]
         L.qmm_matmul_workspace_size.argtypes = [i64, i64]
@@ -73,7 +74,7 @@ def lib():
         L.qmm_matmul_noalloc_max_workspace.argtypes = []
         L.qmm_matmul_noalloc_max_workspace.restype = sz
         for fn in ("qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
-                   "qmm_matmul_path", "qmm_device_status", "qmm_matmul_ws", "qmm_matmul_noalloc"):
+                   "qmm_matmul_path", "qmm_device_status", "qmm_matmul_ws", "qmm_matmul_noalloc", "qmm_matmul_f32"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -156,6 +157,11 @@ def qmm_quantize_act(x, M: int, K: int, ldx: int, a_q, a_d, stream=None) -> None
 def qmm_matmul(type_, w_tiled, K: int, N: int, a_q, a_d, M: int, y, ldy: int, stream=None) -> None:
     _check("qmm_matmul", lib().qmm_matmul(_t(type_), _ptr(w_tiled), K, N, _ptr(a_q), _ptr(a_d), M, _ptr(y), ldy,
                                           _stream(stream)))
+
+
+def qmm_matmul_f32(type_, w_tiled, K: int, N: int, x, ldx: int, M: int, y, ldy: int, stream=None) -> None:
+    _check("qmm_matmul_f32", lib().qmm_matmul_f32(_t(type_), _ptr(w_tiled), K, N, _ptr(x), ldx, M, _ptr(y), ldy,
+                                                  _stream(stream)))
 
 
 def qmm_matmul_path(type_, w_tiled, K: int, N: int, a_q, a_d, M: int, y, ldy: int, path: int,

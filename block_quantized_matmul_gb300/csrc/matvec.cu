@@ -46,6 +46,9 @@ struct MvParams {
     int accumulate;   // 0: y = result, 1: y += result
     int stages;       // ring depth
     Lut16 lut;
+    const float *x;   // fused activation quantization: fp32 rows (a_q / a_d unused), else nullptr
+    int64_t ldx;
+    int x_vec;        // x 16-byte aligned and ldx % 4 == 0: float4 loads
 };
 
 __device__ unsigned g_mv_status = 0;   // set when a bounded wait gave up (reported with the GEMM's word)
@@ -146,6 +149,40 @@ __device__ __forceinline__ void consumer_sync() {      // named barrier over the
     asm volatile("bar.sync 1, %0;" ::"r"(CW * 32) : "memory");
 }
 
+// Fused activation quantization.  The 4 lanes q = 0..3 of an aligned lane quad quantize one block
+// of 32 (columns 8q..8q+7 each) by the rule of qmm_quantize_act, sharing amax through two
+// shuffles; every lane of the warp must call this (dead lanes pass live = false).  Returns the 8
+// int8 codes (columns 8q..8q+7, in order) and sets da = fp32(fp16(d)).
+__device__ __forceinline__ uint2 quantize_quarter(const MvParams &p, bool live, int tok, int64_t kt, int q, float &da) {
+    float v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = 0.0f;
+    if (live) {
+        const float *src = p.x + (int64_t)tok * p.ldx + kt * 32 + 8 * q;
+        if (p.x_vec) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(src)), b = __ldg(reinterpret_cast<const float4 *>(src + 4));
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __ldg(src + k);
+        }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = q8_scale(amax), id = inv_or_zero(d);
+    uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        lo |= (uint32_t)(q8_code(v[k], id) & 0xFF) << (8 * k);
+        hi |= (uint32_t)(q8_code(v[k + 4], id) & 0xFF) << (8 * k);
+    }
+    da = __half2float(__float2half_rn(d));
+    return make_uint2(lo, hi);
+}
+
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
@@ -228,6 +265,21 @@ __device__ __forceinline__ void decode_tile(const uint8_t *tile, int g, int t, u
     }
 }
 
+// Staged fp16 activation pair (column 2cp, 2cp+1) for the biased decode: the odd column is divided
+// by 16 (exact) for Q4_0, whose high nibble is decoded as 16*hi.
+template <int TYPE>
+__device__ __forceinline__ uint32_t act_pair(int a0, int a1) {
+    const float f1 = (TYPE == QMM_Q4_0) ? (float)a1 * 0.0625f : (float)a1;
+    return h2_bits(__halves2half2(__float2half_rn((float)a0), __float2half_rn(f1)));
+}
+// The exact bias of the biased weight decode for one (token, block).
+template <int TYPE>
+__device__ __forceinline__ float act_bias(int sum_even, int sum_odd) {
+    if (TYPE == QMM_Q4_0) return 1032.0f * (float)sum_even + 72.0f * (float)sum_odd;
+    if (TYPE == QMM_Q8_0) return 1152.0f * (float)(sum_even + sum_odd);
+    return 0.0f;
+}
+
 // Token stride of the staged activations in uint4 units: an odd multiple of 4, so the 8 lanes of a
 // quarter-warp (2 tokens x 4 column groups) read 8 distinct 16-byte bank groups.
 __host__ __device__ inline int act_tok_stride(int nkc) { return nkc * 4 + ((nkc & 1) ? 0 : 4); }
@@ -257,7 +309,7 @@ __host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
 
 // CW consumer warps per CTA: 8 (two CTAs per SM) for grids with many column tiles, 16 (one wide CTA
 // per SM) for small ones.
-template <int TYPE, int NF, int CW>
+template <int TYPE, int NF, int CW, bool FUSED>
 __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const MvParams p) {
     constexpr int kConsumerWarps = CW;
     constexpr int kTilesPerStage = CW * kTilesPerWarp;
@@ -291,6 +343,9 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // A grid launched after this one as a programmatic dependent may start now: it waits for this
+    // grid to complete before it reads anything this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         produce<TS, kTilesPerStage>(p, ring, full, empty, abort, lane);
@@ -315,38 +370,72 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
             lut_s[i] = h2_bits(__halves2half2(__int2half_rn(p.lut.v[b & 15]), __int2half_rn(p.lut.v[b >> 4])));
         }
     }
-    for (int i = ctid; i < TOK * nkc; i += kConsumerWarps * 32) {
-        const int j = i / TOK, tok = i - j * TOK;
-        float d = 0.0f, corr = 0.0f;
-        if (tok < p.M) {
-            const int64_t kt = p.kt0 + j;
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.a_q + (int64_t)tok * p.K + kt * 32);
-            const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-            const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            int sum_even = 0, sum_odd = 0;
-            uint32_t hp[16];                 // half2 of column pair cp, in cp order
+    if constexpr (!FUSED) {
+        for (int i = ctid; i < TOK * nkc; i += kConsumerWarps * 32) {
+            const int j = i / TOK, tok = i - j * TOK;
+            float d = 0.0f, corr = 0.0f;
+            if (tok < p.M) {
+                const int64_t kt = p.kt0 + j;
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.a_q + (int64_t)tok * p.K + kt * 32);
+                const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                int sum_even = 0, sum_odd = 0;
+                uint32_t hp[16];                 // half2 of column pair cp, in cp order
 #pragma unroll
-            for (int wi = 0; wi < 8; ++wi) {
+                for (int wi = 0; wi < 8; ++wi) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int a0 = (int)(int8_t)((wv[wi] >> (16 * h)) & 0xFF);
-                    const int a1 = (int)(int8_t)((wv[wi] >> (16 * h + 8)) & 0xFF);
-                    sum_even += a0;
-                    sum_odd += a1;
-                    const float f1 = (TYPE == QMM_Q4_0) ? (float)a1 * 0.0625f : (float)a1;   // exact
-                    hp[2 * wi + h] = h2_bits(__halves2half2(__float2half_rn((float)a0), __float2half_rn(f1)));
+                    for (int h = 0; h < 2; ++h) {
+                        const int a0 = (int)(int8_t)((wv[wi] >> (16 * h)) & 0xFF);
+                        const int a1 = (int)(int8_t)((wv[wi] >> (16 * h + 8)) & 0xFF);
+                        sum_even += a0;
+                        sum_odd += a1;
+                        hp[2 * wi + h] = act_pair<TYPE>(a0, a1);
+                    }
                 }
-            }
-            // fragment order: position 4t + q holds column pair t + 4q
-            uint4 *dst = act_s + tok * tok_stride + j * 4;
+                // fragment order: position 4t + q holds column pair t + 4q
+                uint4 *dst = act_s + tok * tok_stride + j * 4;
 #pragma unroll
-            for (int tt = 0; tt < 4; ++tt) dst[tt] = make_uint4(hp[tt], hp[tt + 4], hp[tt + 8], hp[tt + 12]);
-            d = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
-            if (TYPE == QMM_Q4_0) corr = 1032.0f * (float)sum_even + 72.0f * (float)sum_odd;
-            else if (TYPE == QMM_Q8_0) corr = 1152.0f * (float)(sum_even + sum_odd);
+                for (int tt = 0; tt < 4; ++tt) dst[tt] = make_uint4(hp[tt], hp[tt + 4], hp[tt + 8], hp[tt + 12]);
+                d = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
+                corr = act_bias<TYPE>(sum_even, sum_odd);
+            }
+            da_s[j * TOK + tok] = d;
+            corr_s[j * TOK + tok] = corr;
         }
-        da_s[j * TOK + tok] = d;
-        corr_s[j * TOK + tok] = corr;
+    } else {
+        // 4 lanes per (block, token), 8 columns each; lane q holds column pairs 4q..4q+3, which go to
+        // word q of fragment positions 0..3
+        const int total = TOK * nkc * 4;
+        for (int base = cw * 32; base < total; base += kConsumerWarps * 32) {
+            const int e = base + lane, q = e & 3, jt = (e >> 2) / TOK, tok = (e >> 2) - jt * TOK;
+            const bool live = e < total && tok < p.M;
+            float d;
+            const uint2 c = quantize_quarter(p, live, tok, p.kt0 + jt, q, d);
+            int sum_even = 0, sum_odd = 0;
+            uint32_t hp[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w = u < 2 ? c.x : c.y;
+                const int a0 = (int)(int8_t)((w >> (16 * (u & 1))) & 0xFF);
+                const int a1 = (int)(int8_t)((w >> (16 * (u & 1) + 8)) & 0xFF);
+                sum_even += a0;
+                sum_odd += a1;
+                hp[u] = act_pair<TYPE>(a0, a1);
+            }
+            sum_even += __shfl_xor_sync(0xffffffffu, sum_even, 1);
+            sum_odd += __shfl_xor_sync(0xffffffffu, sum_odd, 1);
+            sum_even += __shfl_xor_sync(0xffffffffu, sum_even, 2);
+            sum_odd += __shfl_xor_sync(0xffffffffu, sum_odd, 2);
+            if (live) {
+                uint32_t *dst = reinterpret_cast<uint32_t *>(act_s + tok * tok_stride + jt * 4);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) dst[4 * u + q] = hp[u];
+            }
+            if (e < total && q == 0) {
+                da_s[jt * TOK + tok] = live ? d : 0.0f;
+                corr_s[jt * TOK + tok] = live ? act_bias<TYPE>(sum_even, sum_odd) : 0.0f;
+            }
+        }
     }
     consumer_sync<CW>();
 
@@ -474,7 +563,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
 // warps are added in a fixed order at the end of a column tile.
 
 // Row words of one tile for lane (i, j): R[r][0], R[r][1] are the int8x4 weights of row 4i + r in
-// the staged activation order (see stage_act_dp4a).
+// the staged activation order (see dp4a_record).
 template <int TYPE>
 __device__ __forceinline__ void tile_rows_dp4a(const uint8_t *tile, int i, int j, uint32_t (&R)[4][2],
                                                const uint32_t (&tb)[4]) {
@@ -517,10 +606,9 @@ __device__ __forceinline__ void tile_rows_dp4a(const uint8_t *tile, int i, int j
     }
 }
 
-// Staged activation record of (token, block, quarter j): the 8 int8 of columns 8j..8j+7 as two
+// Staged activation record of (token, block, quarter j): the 8 int8 v of columns 8j..8j+7 as two
 // int8x4 words in the order of tile_rows_dp4a, the dp4a start value, and fp32(d_a).
-__device__ __forceinline__ uint4 stage_act_dp4a(int type, const int8_t *a8, int j, float da) {
-    const uint2 v = *reinterpret_cast<const uint2 *>(a8 + 8 * j);
+__device__ __forceinline__ uint4 dp4a_record(int type, uint2 v, int j, float da) {
     unsigned long long V = (unsigned long long)v.x | ((unsigned long long)v.y << 32);
     if (j) V = (V >> (16 * j)) | (V << (64 - 16 * j));       // column pair c <- local pair (c + j) & 3
     const uint32_t lo = (uint32_t)V, hi = (uint32_t)(V >> 32);
@@ -529,9 +617,7 @@ __device__ __forceinline__ uint4 stage_act_dp4a(int type, const int8_t *a8, int 
     if (type == QMM_Q4_0) {
         rec.x = __byte_perm(lo, hi, 0x6420);      // even columns
         rec.y = __byte_perm(lo, hi, 0x7531);      // odd columns
-#pragma unroll
-        for (int b = 0; b < 8; ++b) corr += (int)a8[8 * j + b];
-        corr *= -8;
+        corr = -8 * __dp4a((int)v.x, 0x01010101, __dp4a((int)v.y, 0x01010101, 0));
     } else {
         rec.x = lo;
         rec.y = hi;
@@ -560,7 +646,7 @@ __host__ __device__ inline Dp4aLayout dp4a_layout(int nkc, int stages) {
 }
 
 // MT = token capacity (1, 2 or 4); p.M <= MT tokens are live.
-template <int TYPE, int MT, int CW>
+template <int TYPE, int MT, int CW, bool FUSED>
 __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(const MvParams p) {
     constexpr int kTilesPerStage = CW * kTilesPerWarp;
     constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
@@ -586,6 +672,9 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // A grid launched after this one as a programmatic dependent may start now: it waits for this
+    // grid to complete before it reads anything this grid writes.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         produce<TS, kTilesPerStage>(p, ring, full, empty, abort, lane);
@@ -597,15 +686,29 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
 
     // the activations may come from the grid launched just before this one (see produce)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int e = ctid; e < MT * nkc * 4; e += CW * 32) {
-        const int tok = e / (nkc * 4), rem = e - tok * nkc * 4, jt = rem >> 2, q = rem & 3;
-        uint4 rec = make_uint4(0u, 0u, 0u, 0u);
-        if (tok < p.M) {
-            const int64_t kt = p.kt0 + jt;
-            const float da = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
-            rec = stage_act_dp4a(TYPE, p.a_q + (int64_t)tok * p.K + kt * 32, q, da);
+    if constexpr (!FUSED) {
+        for (int e = ctid; e < MT * nkc * 4; e += CW * 32) {
+            const int tok = e / (nkc * 4), rem = e - tok * nkc * 4, jt = rem >> 2, q = rem & 3;
+            uint4 rec = make_uint4(0u, 0u, 0u, 0u);
+            if (tok < p.M) {
+                const int64_t kt = p.kt0 + jt;
+                const float da = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
+                const uint2 v = *reinterpret_cast<const uint2 *>(p.a_q + (int64_t)tok * p.K + kt * 32 + 8 * q);
+                rec = dp4a_record(TYPE, v, q, da);
+            }
+            act_s[e] = rec;
         }
-        act_s[e] = rec;
+    } else {
+        // record e = (token, block, quarter) is made by lane quad e & ~3 (all lanes of a warp iterate together)
+        const int total = MT * nkc * 4;
+        for (int base = cw * 32; base < total; base += CW * 32) {
+            const int e = base + lane;
+            const int tok = e / (nkc * 4), rem = e - tok * nkc * 4, jt = rem >> 2, q = rem & 3;
+            const bool live = e < total && tok < p.M;
+            float da;
+            const uint2 v = quantize_quarter(p, live, tok, p.kt0 + jt, q, da);
+            if (e < total) act_s[e] = live ? dp4a_record(TYPE, v, q, da) : make_uint4(0u, 0u, 0u, 0u);
+        }
     }
     uint32_t tb[4] = {0u, 0u, 0u, 0u};
     if constexpr (TYPE == QMM_IQ4_NL) {
@@ -728,15 +831,18 @@ int num_sms() {
 // that grid allows it), and the kernel waits for it before reading activations or y.
 template <typename Kern>
 cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const uint8_t *tiled, int64_t K, int64_t N,
-                          const int8_t *a_q, const uint16_t *a_d, int M, float *y, int64_t ldy, cudaStream_t s) {
+                          const ActSrc &a, int M, float *y, int64_t ldy, cudaStream_t s) {
     const int64_t nkt = K / 32, nct = (N + 31) / 32;
     int64_t grid = (int64_t)num_sms() * pl.ctas_per_sm;
     if (grid > nct) grid = nct;
     for (int64_t kt0 = 0; kt0 < nkt; kt0 += pl.nkc) {
         MvParams p;
         p.tiled = tiled;
-        p.a_q = a_q;
-        p.a_d = a_d;
+        p.a_q = a.a_q;
+        p.a_d = a.a_d;
+        p.x = a.x;
+        p.ldx = a.ldx;
+        p.x_vec = a.x != nullptr && (reinterpret_cast<uintptr_t>(a.x) & 15u) == 0 && a.ldx % 4 == 0;
         p.y = y;
         p.K = K;
         p.nkt = nkt;
@@ -765,71 +871,90 @@ cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const uint8_t 
     return cudaSuccess;
 }
 
-template <int TYPE, int NF, int CW>
-cudaError_t run_mma(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
-                    int64_t ldy, cudaStream_t s) {
+template <int TYPE, int NF, int CW, bool FUSED>
+cudaError_t run_mma(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a, int M, float *y, int64_t ldy,
+                    cudaStream_t s) {
     constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
     const int nkc = chunk_tiles(K / 32, 64 * (int64_t)M);
     Plan pl = plan_ring<TS, CW>(nkc, mv_layout<TYPE, NF, CW>(M, nkc, 0).total);
     pl.smem = (size_t)mv_layout<TYPE, NF, CW>(M, nkc, pl.stages).total + 128;
-    auto kern = matvec_kernel<TYPE, NF, CW>;
+    auto kern = matvec_kernel<TYPE, NF, CW, FUSED>;
     static int attr_done[4] = {0, 0, 0, 0};
     const cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
     if (e != cudaSuccess) return e;
-    return launch_passes(kern, 32 * (1 + CW), pl, tiled, K, N, a_q, a_d, M, y, ldy, s);
+    return launch_passes(kern, 32 * (1 + CW), pl, tiled, K, N, a, M, y, ldy, s);
 }
 
-template <int TYPE, int MT, int CW>
-cudaError_t run_dp4a(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M,
-                     float *y, int64_t ldy, cudaStream_t s) {
+template <int TYPE, int MT, int CW, bool FUSED>
+cudaError_t run_dp4a(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a, int M, float *y, int64_t ldy,
+                     cudaStream_t s) {
     constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
     const int nkc = chunk_tiles(K / 32, 64 * (int64_t)MT);
     Plan pl = plan_ring<TS, CW>(nkc, dp4a_layout<TYPE, MT, CW>(nkc, 0).total);
     pl.smem = (size_t)dp4a_layout<TYPE, MT, CW>(nkc, pl.stages).total + 128;
-    auto kern = matvec_dp4a_kernel<TYPE, MT, CW>;
+    auto kern = matvec_dp4a_kernel<TYPE, MT, CW, FUSED>;
     static int attr_done[4] = {0, 0, 0, 0};
     const cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
     if (e != cudaSuccess) return e;
-    return launch_passes(kern, 32 * (1 + CW), pl, tiled, K, N, a_q, a_d, M, y, ldy, s);
+    return launch_passes(kern, 32 * (1 + CW), pl, tiled, K, N, a, M, y, ldy, s);
 }
 
 // Up to kDp4aMaxM tokens: int8 dot products; more: fp16 mma.sync.  Many column tiles: two narrow
 // CTAs per SM hide latency best; few: one wide CTA per SM streams each column tile twice as fast,
 // which keeps the rounds of a small grid short and balanced.
-template <int TYPE>
-cudaError_t run(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
-                int64_t ldy, cudaStream_t s) {
+template <int TYPE, bool FUSED>
+cudaError_t run(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a, int M, float *y, int64_t ldy,
+                cudaStream_t s) {
     const bool narrow = (N + 31) / 32 >= (int64_t)num_sms() * 8;
-#define QMM_MV_ARGS tiled, K, N, a_q, a_d, M, y, ldy, s
+#define QMM_MV_ARGS tiled, K, N, a, M, y, ldy, s
     if (M <= kDp4aMaxM) {
-        if (M == 1) return narrow ? run_dp4a<TYPE, 1, 8>(QMM_MV_ARGS) : run_dp4a<TYPE, 1, 16>(QMM_MV_ARGS);
-        if (M == 2) return narrow ? run_dp4a<TYPE, 2, 8>(QMM_MV_ARGS) : run_dp4a<TYPE, 2, 16>(QMM_MV_ARGS);
-        return narrow ? run_dp4a<TYPE, 4, 8>(QMM_MV_ARGS) : run_dp4a<TYPE, 4, 16>(QMM_MV_ARGS);
+        if (M == 1) return narrow ? run_dp4a<TYPE, 1, 8, FUSED>(QMM_MV_ARGS) : run_dp4a<TYPE, 1, 16, FUSED>(QMM_MV_ARGS);
+        if (M == 2) return narrow ? run_dp4a<TYPE, 2, 8, FUSED>(QMM_MV_ARGS) : run_dp4a<TYPE, 2, 16, FUSED>(QMM_MV_ARGS);
+        return narrow ? run_dp4a<TYPE, 4, 8, FUSED>(QMM_MV_ARGS) : run_dp4a<TYPE, 4, 16, FUSED>(QMM_MV_ARGS);
     }
-    if (M <= 8) return narrow ? run_mma<TYPE, 1, 8>(QMM_MV_ARGS) : run_mma<TYPE, 1, 16>(QMM_MV_ARGS);
-    return narrow ? run_mma<TYPE, 2, 8>(QMM_MV_ARGS) : run_mma<TYPE, 2, 16>(QMM_MV_ARGS);
+    if (M <= 8) return narrow ? run_mma<TYPE, 1, 8, FUSED>(QMM_MV_ARGS) : run_mma<TYPE, 1, 16, FUSED>(QMM_MV_ARGS);
+    return narrow ? run_mma<TYPE, 2, 8, FUSED>(QMM_MV_ARGS) : run_mma<TYPE, 2, 16, FUSED>(QMM_MV_ARGS);
 #undef QMM_MV_ARGS
+}
+
+// Groups of at most kDecodeMaxM rows, one launch sequence each.
+template <bool FUSED>
+cudaError_t run_groups(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a, int64_t M, float *y,
+                       int64_t ldy, cudaStream_t s) {
+    const int64_t nkt = K / 32;
+    for (int64_t m0 = 0; m0 < M; m0 += kDecodeMaxM) {
+        const int mm = (int)((M - m0) < kDecodeMaxM ? (M - m0) : kDecodeMaxM);
+        ActSrc g = a;
+        if (FUSED) {
+            g.x = a.x + m0 * a.ldx;
+        } else {
+            g.a_q = a.a_q + m0 * K;
+            g.a_d = a.a_d + m0 * nkt;
+        }
+        float *yy = y + m0 * ldy;
+        cudaError_t e;
+        switch (t) {
+            case QMM_Q4_0: e = run<QMM_Q4_0, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
+            case QMM_IQ4_NL: e = run<QMM_IQ4_NL, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
+            default: e = run<QMM_Q8_0, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t launch_matvec(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                           const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s) {
-    const int64_t nkt = K / 32;
-    for (int64_t m0 = 0; m0 < M; m0 += kDecodeMaxM) {
-        const int mm = (int)((M - m0) < kDecodeMaxM ? (M - m0) : kDecodeMaxM);
-        const int8_t *aq = a_q + m0 * K;
-        const uint16_t *ad = a_d + m0 * nkt;
-        float *yy = y + m0 * ldy;
-        cudaError_t e;
-        switch (t) {
-            case QMM_Q4_0: e = run<QMM_Q4_0>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
-            case QMM_IQ4_NL: e = run<QMM_IQ4_NL>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
-            default: e = run<QMM_Q8_0>(tiled, K, N, aq, ad, mm, yy, ldy, s); break;
-        }
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+    const ActSrc a = {a_q, a_d, nullptr, 0};
+    return run_groups<false>(t, tiled, K, N, a, M, y, ldy, s);
+}
+
+cudaError_t launch_matvec_fused(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
+                                int64_t M, float *y, int64_t ldy, cudaStream_t s) {
+    const ActSrc a = {nullptr, nullptr, x, ldx};
+    return run_groups<true>(t, tiled, K, N, a, M, y, ldy, s);
 }
 
 cudaError_t read_and_clear_matvec_status(unsigned *out, cudaStream_t s) {

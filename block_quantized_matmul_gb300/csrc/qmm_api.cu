@@ -123,6 +123,16 @@ qmm_status qmm_matmul(qmm_type t, const void *w_tiled, int64_t K, int64_t N, con
     return qmm_matmul_path(t, w_tiled, K, N, a_q, a_d, M, y, ldy, QMM_PATH_AUTO, stream);
 }
 
+qmm_status qmm_matmul_f32(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
+                          int64_t M, float *y, int64_t ldy, qmm_stream_t stream) {
+    if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
+    if (!valid_kn(K, N) || M <= 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim || ldx < K || ldx > kMaxDim || ldy < N)
+        return QMM_ERR_INVALID_ARG;
+    if (!w_tiled || !x || !y) return QMM_ERR_INVALID_ARG;
+    if (!aligned(w_tiled, 16) || !aligned(x, 4) || !aligned(y, 4)) return QMM_ERR_MISALIGNED;
+    return from_cuda(launch_matvec_fused(t, static_cast<const uint8_t *>(w_tiled), K, N, x, ldx, M, y, ldy, cs(stream)));
+}
+
 size_t qmm_matmul_workspace_size(int64_t M, int64_t K) {
     if (M <= 0 || K <= 0 || (K % 32) != 0 || M > kMaxDim || K > kMaxDim) return 0;
     return gemm_workspace_bytes(M, K);

@@ -35,6 +35,29 @@ inline Lut16 iq4nl_lut() {
     return l;
 }
 
+// ---- the dynamic Q8_0 activation rule, per block of 32 (also the Q8_0 weight rule) ----
+// amax = max|x|, d = amax/127, id = d ? 1/d : 0, q = round half away from zero of x*id clamped to
+// [-127, 127] (a NaN product, 0*inf after 1/d overflowed, gives 0); the stored scale is fp16(d).
+// IEEE-rounded fp32 intrinsics throughout, so nothing is contracted or reassociated.
+__device__ __forceinline__ float q8_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
+__device__ __forceinline__ float inv_or_zero(float d) { return d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f; }
+__device__ __forceinline__ int q8_code(float x, float id) {
+    float v = __fmul_rn(x, id);
+    if (isnan(v)) return 0;
+    float r = roundf(v);                       // halfway cases away from zero
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return (int)r;
+}
+
+// Activation source of the decode kernels: quantized rows (a_q, a_d) or fp32 rows x quantized
+// inside the kernel (x != nullptr).
+struct ActSrc {
+    const int8_t *a_q;
+    const uint16_t *a_d;
+    const float *x;
+    int64_t ldx;
+};
+
 // Launchers (each returns cudaGetLastError() after enqueueing).
 cudaError_t launch_quantize_act(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *a_q,
                                 uint16_t *a_d, cudaStream_t s);
@@ -46,6 +69,8 @@ cudaError_t launch_unpack(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N
                           cudaStream_t s);
 cudaError_t launch_matvec(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                           const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
+cudaError_t launch_matvec_fused(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
+                                int64_t M, float *y, int64_t ldy, cudaStream_t s);
 cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                         const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
 cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,

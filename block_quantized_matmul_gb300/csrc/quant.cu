@@ -9,25 +9,18 @@
 namespace qmm {
 namespace {
 
-__device__ __forceinline__ int q8_code(float x, float id) {
-    float v = __fmul_rn(x, id);
-    if (isnan(v)) return 0;                    // 0 * inf when 1/d overflowed
-    float r = roundf(v);                       // halfway cases away from zero
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return (int)r;
-}
-
-__device__ __forceinline__ float q8_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
-__device__ __forceinline__ float inv_or_zero(float d) { return d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f; }
-
 // 8 threads per 32-element block, 4 consecutive elements per thread.  Grid-stride over all
 // M*K/4 element quads.  `vec` selects float4 loads (x 16-byte aligned, ldx % 4 == 0).
 template <bool vec>
 __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restrict__ x, int64_t M, int64_t K,
                                                            int64_t ldx, int8_t *__restrict__ a_q,
                                                            uint16_t *__restrict__ a_d) {
-    // Lets a dependent grid launched after this one (the matmul) start its independent work -- streaming
-    // weights -- right away; it still waits for this grid to finish before reading a_q / a_d.
+    // This grid is launched as a programmatic dependent: x may be written by the grid before it on
+    // the stream (and a_q / a_d still read by it), so wait for that grid to complete first.  Only
+    // then let the dependent matmul start streaming weights: anything the earlier grids wrote, the
+    // weights included, is visible by now.  The matmul still waits for this grid before it reads
+    // a_q / a_d.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t quads_per_row = K / 4;
     const int64_t total = M * quads_per_row;
@@ -158,9 +151,20 @@ cudaError_t launch_quantize_act(const float *x, int64_t M, int64_t K, int64_t ld
     const int64_t quads = M * (K / 4);
     const int grid = grid_for(quads, threads);
     const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) && (ldx % 4 == 0);
-    if (vec) quantize_act_kernel<true><<<grid, threads, 0, s>>>(x, M, K, ldx, a_q, a_d);
-    else quantize_act_kernel<false><<<grid, threads, 0, s>>>(x, M, K, ldx, a_q, a_d);
-    return cudaGetLastError();
+    // programmatic dependent launch: the launch overlaps the tail of the grid before it on the stream
+    // (if that grid allows it); the kernel waits for that grid before touching memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (vec) return cudaLaunchKernelEx(&cfg, quantize_act_kernel<true>, x, M, K, ldx, a_q, a_d);
+    return cudaLaunchKernelEx(&cfg, quantize_act_kernel<false>, x, M, K, ldx, a_q, a_d);
 }
 
 cudaError_t launch_quantize_weight(qmm_type t, const float *w, int64_t N, int64_t K, int64_t ldw, uint8_t *flat,

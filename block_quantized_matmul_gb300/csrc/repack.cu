@@ -58,6 +58,9 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
         }
         *reinterpret_cast<uint16_t *>(t + soff + 2 * r) = (uint16_t)ld_u16(blk);
     }
+    // The decode matmul streams tiles before it waits for the kernel before it on the stream, so the
+    // tiles must be visible device-wide by the time this grid's blocks have exited.
+    __threadfence();
 }
 
 template <int TYPE>

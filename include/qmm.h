@@ -136,10 +136,37 @@ QMM_API qmm_status qmm_quantize_act(const float *x_dev, int64_t M, int64_t K, in
  *   y_dev  fp32 output, y[m*ldy + n] for n < N (other columns untouched); 4-byte aligned.
  * Accumulation is fp32 in a fixed order (results are reproducible run to run); the error against
  * the exact value is at most about n_k_tiles * 2^-24 * sum_k |w_k * x_k| (dequantized).
+ * Launch overlap (M <= qmm_decode_max_m()): the decode kernel is a programmatic dependent launch.
+ * It may start while the kernel before it on the stream is finishing, and it starts streaming the
+ * weight tiles at once; it waits for that kernel to complete before it reads a_q, a_d or y.  So
+ * the tiles must not be written by the kernel launched immediately before this call if that
+ * kernel itself lets dependents start early.  Tiles from qmm_repack (which makes its stores
+ * visible before it exits), from a copy, or from any earlier kernel are fine.  qmm_quantize_act
+ * is launched the same way and waits before it reads x.
  * Errors: INVALID_ARG (sizes, ldy < N, NULL), UNSUPPORTED, MISALIGNED, CUDA.
  */
 QMM_API qmm_status qmm_matmul(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N, const int8_t *a_q_dev,
                       const uint16_t *a_d_dev, int64_t M, float *y_dev, int64_t ldy, qmm_stream_t stream);
+
+/*
+ * qmm_matmul_f32 -- the same product with the activation quantization fused into the decode kernel:
+ * Y = Q8_0(x) * W^T, x given as fp32 rows.  The pages quantize the activations into Q8_0 blocks in
+ * VTCM inside the op before the weight loop ("Memory buffers"); here every CTA quantizes the rows
+ * it needs into shared memory while its weight stream starts.
+ *   w_tiled_dev  as for qmm_matmul.
+ *   x_dev  fp32, M rows of K values, row m at x_dev + m*ldx; 4-byte aligned (16-byte aligned with
+ *          ldx % 4 == 0 takes the vectorised loads).  Inputs must be finite.
+ *   y_dev  fp32 output as for qmm_matmul.
+ * The quantization is the rule of qmm_quantize_act, bit for bit, and the result equals
+ * qmm_quantize_act followed by qmm_matmul (same kernels' arithmetic, same order) for
+ * M <= qmm_decode_max_m().  Meant for decode shapes: larger M runs the decode kernel on groups
+ * of qmm_decode_max_m() rows, far slower than quantize + the tensor-core GEMM.  Nothing is
+ * written but y; no workspace.  Launch overlap as for qmm_matmul (x is read only after the
+ * preceding kernel has completed).
+ * Errors: INVALID_ARG (sizes, ldx < K, ldy < N, NULL), UNSUPPORTED, MISALIGNED, CUDA.
+ */
+QMM_API qmm_status qmm_matmul_f32(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N, const float *x_dev,
+                                  int64_t ldx, int64_t M, float *y_dev, int64_t ldy, qmm_stream_t stream);
 
 /* qmm_matmul_path -- qmm_matmul with the kernel chosen by the caller.  QMM_PATH_MATVEC accepts any
  * M (rows are processed in groups of qmm_decode_max_m()); QMM_PATH_GEMM any M >= 1. */

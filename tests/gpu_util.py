@@ -79,3 +79,21 @@ def gpu_matmul_ws(type_, tiled, K, N, a_q, a_d, M, ldy=None, fill=0x5A):
     qmm.qmm_matmul_ws(type_, tiled, K, N, a_q, a_d, M, y, ldy, ws.data_ptr() + off, nbytes)
     torch.cuda.synchronize()
     return y
+
+
+def gpu_matmul_f32(type_, tiled, K, N, x: np.ndarray, ldx=None, ldy=None, x_offset=0):
+    """qmm_matmul_f32 (activation quantization fused into the decode kernel) on fp32 rows x [M, K].
+    x is placed in a row-padded device buffer (row stride ldx) starting x_offset floats in."""
+    import block_quantized_matmul_gb300 as qmm
+
+    torch = torch_mod()
+    M = x.shape[0]
+    ldx = K if ldx is None else ldx
+    ldy = N if ldy is None else ldy
+    buf = torch.full((x_offset + M * ldx,), float("nan"), dtype=torch.float32, device="cuda")
+    rows = buf[x_offset:].view(M, ldx)
+    rows[:, :K] = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    y = torch.full((M, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    qmm.qmm_matmul_f32(type_, tiled, K, N, rows, ldx, M, y, ldy)
+    torch.cuda.synchronize()
+    return y

@@ -129,3 +129,18 @@ def test_matmul_ws_argument_errors(L):
     assert L.qmm_matmul_ws(0, P, 256, 64, P, P, 64, P, 64, P, need - 1, None) == INVALID
     assert L.qmm_matmul_ws(0, P, 256, 64, P, P, 64, P, 64, P + 16, need, None) == MISALIGNED
     assert L.qmm_matmul_ws(0, P, 48, 64, P, P, 64, P, 64, P, need, None) == INVALID
+
+
+def test_matmul_f32_argument_errors(L):
+    f = L.qmm_matmul_f32
+    assert f(0, P, 48, 64, P, 64, 1, P, 64, None) == INVALID     # K % 32
+    assert f(0, P, 64, 64, P, 63, 1, P, 64, None) == INVALID     # ldx < K
+    assert f(0, P, 64, 64, P, 64, 0, P, 64, None) == INVALID     # M = 0
+    assert f(0, P, 64, 64, P, 64, 1, P, 63, None) == INVALID     # ldy < N
+    assert f(0, None, 64, 64, P, 64, 1, P, 64, None) == INVALID  # NULL weight
+    assert f(0, P, 64, 64, None, 64, 1, P, 64, None) == INVALID  # NULL x
+    assert f(0, P, 64, 64, P, 64, 1, None, 64, None) == INVALID  # NULL y
+    assert f(4, P, 64, 64, P, 64, 1, P, 64, None) == UNSUPPORTED
+    assert f(0, P + 8, 64, 64, P, 64, 1, P, 64, None) == MISALIGNED
+    assert f(0, P, 64, 64, P + 2, 64, 1, P, 64, None) == MISALIGNED
+    assert f(0, P, 64, 64, P, 64, 1, P + 1, 64, None) == MISALIGNED
