@@ -176,3 +176,27 @@ def test_full_size_sampled(torch, orc, type_, K, N, M):
     ys, bs = orc.matmul_at(type_, tiled_ref, K, q_ref, d_ref, ms, ns)
     assert_within_bound(y[ms, ns], ys, bs, f"{type_} {K}x{N} M={M}")
     assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("type_", TYPES)
+@pytest.mark.parametrize("M", [1, 8, 40])
+def test_column_shards_match_the_full_product(torch, orc, type_, M):
+    """A rank's contiguous range of column tiles is itself a tiled weight: its product, written at
+    column n0 with the full ldy, equals those columns of the full product bit for bit."""
+    from block_quantized_matmul_gb300 import shard
+
+    K, N = 320, 200
+    w = synth.weights(N, K, seed=21)
+    x = synth.activations(M, K, seed=22)
+    _, tiled = gpu_prepare_weight(type_, w)
+    a_q, a_d = gpu_quantize_act(x)
+    full = gpu_matmul(type_, tiled, K, N, a_q, a_d, M, path=0)
+    import block_quantized_matmul_gb300 as qmm
+
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    for r in range(3):
+        sh = shard.shard(type_, K, N, r, 3)
+        if sh.n_local:
+            qmm.qmm_matmul(type_, tiled[sh.byte_offset:], K, sh.n_local, a_q, a_d, M, y[:, sh.n0:], N)
+    torch.cuda.synchronize()
+    assert torch.equal(y, full)
