@@ -111,11 +111,17 @@ class ClockSampler:
 
 
 def kernel_source_hash():
+    """Hash of the kernel sources with comments and blank lines removed (a comment edit does not
+    change the kernels the recorded counters were taken on)."""
+    import re
+
     h = hashlib.sha256()
     for name in sorted(os.listdir(os.path.join(ROOT, "block_quantized_matmul_gb300", "csrc"))):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(ROOT, "block_quantized_matmul_gb300", "csrc", name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(ROOT, "block_quantized_matmul_gb300", "csrc", name)) as f:
+                text = re.sub(r"//[^\n]*", "", f.read())
+            code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+            h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -7,22 +7,21 @@
 //   * int8 tcgen05 (kind::i8) does not exist on sm_103a, so quants are expanded to fp16 holding the
 //     exact integer (|w| <= 127, |a| <= 127) and contracted with tcgen05.mma.kind::f16; every partial
 //     sum of a 32-element block is an integer below 2^24, so the fp32 accumulator in TMEM is exact.
-//   * The per-block scale product P_b[n,m] = d_w[n,b] * d_a[m,b] is itself a (rank-1) matrix
-//     product: a third MMA with d_w and d_a in column 0 of otherwise-zero fp16 operands writes it,
-//     exactly, next to S_b in TMEM.  The CUDA cores then do one fp32 FMA per element and block,
-//     y += S_b * P_b, using packed fma.rn.f32x2.
+//   * Each block's sums S_b go to their own TMEM slot; the CUDA cores then apply the two scales,
+//     y += (S_b * d_a) * d_w, with packed mul.rn.f32x2 / fma.rn.f32x2 in registers.
 //
 // Tile: 128 weight rows (4 column tiles, the UMMA M dimension) x 128 tokens (UMMA N), all of K.
-// The pipeline moves K in pairs of 32-wide blocks; TMEM holds S and P of two single blocks.
+// The pipeline moves K in pairs of 32-wide blocks; TMEM holds S of four single blocks (4 x 128
+// columns).
 // Warp roles (480 threads):
 //   warp 0      W producer: per block pair, one 3-D TMA of the 4 x 2 raw weight tiles plus one TMA of
 //               the pair's token data (fp16 scales, or the raw int8 rows), into a W ring.
-//   warp 1      TMEM owner and MMA issuer (one thread): per block, 2 MMAs for S_b and 1 for P_b into a
-//               2-slot TMEM ring.
+//   warp 1      TMEM owner and MMA issuer (one thread): per block, 2 MMAs (K = 16 each) into a
+//               4-slot TMEM ring.
 //   warps 2-5   converters: thread c turns weight row c of the pair into fp16 in the canonical K-major
-//               128-byte-swizzled layout and writes the d_w / d_a columns of the scale-product
-//               operands (and, for int8 activations, converts token row c).
-//   warps 6-13  rescale: tcgen05.ld of S_b and P_b, y += S_b*P_b in registers, then the fp32 store.
+//               128-byte-swizzled layout and writes the pair's fp32 d_w / d_a (and, for int8
+//               activations, converts token row c).
+//   warps 6-13  rescale: tcgen05.ld of S_b, y += (S_b * d_a) * d_w in registers, then the fp32 store.
 //   warp 14     B producer (prepared variant): one 128-byte-swizzled TMA of the fp16 token operand of
 //               the pair, straight into the layout the MMA reads.
 // Two token-operand variants: int8 quants converted in the kernel (no scratch memory), or a prepared
