@@ -178,7 +178,9 @@ class Workload:
         self.ws_bytes = qmm.matmul_workspace_size(M, K) if M > qmm.decode_max_m() else 0
         self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device="cuda") if self.ws_bytes else None
         self.ws_ptr = (self.ws.data_ptr() + (-self.ws.data_ptr()) % 256) if self.ws_bytes else None
-        self.fused = M <= qmm.decode_max_m()
+        # decode shapes up to 4 tokens run the fused kernel (qmm_matmul_f32); from 5 tokens on the two
+        # calls are faster (the fused kernel quantizes all M rows in every CTA)
+        self.fused = M <= 4
         torch.cuda.synchronize()
 
     def step(self, i, stream):
@@ -195,7 +197,7 @@ class Workload:
         self.matmul_only(i, stream)
 
     def kernel_only(self, i, stream):
-        """The dominant kernel alone: the fused decode kernel, or the GEMM."""
+        """The dominant kernel alone: the fused decode kernel, the decode kernel or the GEMM."""
         if self.fused:
             self.step(i, stream)
         else:
@@ -216,12 +218,12 @@ class Workload:
         return self.tiled_bytes + act + self.M * self.N * 4
 
     def launches_per_step(self):
-        """Kernels of this library launched by one step: the fused decode kernel once per 16-row group
-        and K pass (K is split only beyond its 64 KB activation staging budget), or quantize +
-        activation prepare + GEMM."""
-        if not self.fused:
+        """Kernels of this library launched by one step: the decode kernel once per 16-row group and K
+        pass (K is split only beyond its 64 KB activation staging budget), plus the activation
+        quantizer unless it is fused; or quantize + activation prepare + GEMM."""
+        if self.M > 16:
             return 3
-        n, nkt = 0, self.K // 32
+        n, nkt = (0 if self.fused else 1), self.K // 32
         for m0 in range(0, self.M, 16):
             mm = min(16, self.M - m0)
             mt = mm if mm > 4 else (mm if mm <= 2 else 4)
