@@ -7,8 +7,8 @@ it, and it shares no code with the product: the arithmetic lives in ``oracle/ora
 ``oracle.build()``; this module only marshals numpy arrays through ctypes.
 
 What it follows ("Hexagon backend developer details", "Tiled Weight Formats"): the tile grid of
-"Tile Dimensions and Grid Layout" and the Q4_0 / Q8_0 / IQ4_NL tile byte layouts of "Block-32
-Quantized Formats".  The readings taken where the pages are silent are listed in ``oracle.c``.
+"Tile Dimensions and Grid Layout" and the Q4_0 / Q8_0 / IQ4_NL / MXFP4 tile byte layouts of
+"Block-32 Quantized Formats".  The readings taken where the pages are silent are listed in ``oracle.c``.
 """
 from __future__ import annotations
 
@@ -19,8 +19,8 @@ import threading
 
 import numpy as np
 
-Q4_0, Q8_0, IQ4_NL = 0, 1, 2
-TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL}
+Q4_0, Q8_0, IQ4_NL, MXFP4 = 0, 1, 2, 3
+TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL, "mxfp4": MXFP4}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -50,6 +50,8 @@ def _load():
             lib.orc_f16_to_f32.restype = ctypes.c_float
             lib.orc_f32_to_f16.argtypes = [ctypes.c_float]
             lib.orc_f32_to_f16.restype = ctypes.c_uint16
+            lib.orc_e8m0_to_f16_bits.argtypes = [i32]
+            lib.orc_e8m0_to_f16_bits.restype = ctypes.c_uint16
             for fn in ("orc_block_bytes", "orc_tile_bytes"):
                 getattr(lib, fn).argtypes = [i32]
                 getattr(lib, fn).restype = i64
@@ -102,6 +104,11 @@ def f16_to_f32(h: int) -> float:
 
 def f32_to_f16(x: float) -> int:
     return int(_load().orc_f32_to_f16(float(x)))
+
+
+def e8m0_to_f16_bits(e: int) -> int:
+    """The MXFP4 row scale as fp16 bits (the pages' clamp(e - 112, 0, 30) << 10)."""
+    return int(_load().orc_e8m0_to_f16_bits(int(e)))
 
 
 def block_bytes(type_) -> int:

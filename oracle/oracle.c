@@ -12,6 +12,9 @@
  *     cp*32+row = (q[row][2cp+1] << 4) | q[row][2cp], FP16 row scales at 512+2*row) and the Q8_0
  *     1088-byte tile (bytes cp*64+2*row+0/1 = q[row][2cp] / q[row][2cp+1], FP16 row scales at
  *     1024+2*row); IQ4_NL dequantizes through a 16-entry non-linear table times the row scale.
+ *     The MXFP4 544-byte tile keeps the Q4_0 nibble layout for 4-bit E2M1 codes and stores one E8M0
+ *     exponent byte per row at 512+row; it dequantizes as the FP4 value of the code times the
+ *     power-of-two fp16 scale whose bits are clamp(e - 112, 0, 30) << 10.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   - Flat (untiled) rows are GGML blocks: Q4_0 / IQ4_NL = {fp16 d; u8 qs[16]} (18 B), element j in
@@ -25,6 +28,12 @@
  *     IQ4_NL takes d = m/lut[0], d16 = fp16(d), and for each x the index i minimising
  *     |x - f32(d16)*lut[i]| (lowest index on ties).
  *   - The IQ4_NL table itself is not printed on the pages; callers pass the table in.
+ *   - MXFP4: the flat block is {u8 e; u8 qs[16]} (17 B, nibble order as Q4_0); the FP4 table is the
+ *     OCP E2M1 code set {0, 0.5, 1, 1.5, 2, 3, 4, 6} with a sign bit (code = s<<3 | e<<1 | m).
+ *     Integer weights are twice the FP4 value (0..12 with sign) and the block scale is half the
+ *     fp16 scale, which is the same product.  Quantizer (test data): e = floor(log2 amax) - 2 + 127
+ *     (0 for an all-zero block, clamped to 0..254), then the nearest FP4 level under the dequantizing
+ *     scale, lowest code on ties.
  *   - Matmul: Y[m,n] = sum_b f64(d_w[n,b]) * f64(d_a[m,b]) * S_b[m,n], where S_b is the exact integer
  *     dot product of the block's integer weights (q-8, q, lut[q]) and activation quants.  The oracle
  *     also returns B[m,n] = sum_b sum_j |d_w*w_int * d_a*q_a|, the scale of the error bound.
@@ -36,7 +45,26 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORC_Q4_0 = 0, ORC_Q8_0 = 1, ORC_IQ4_NL = 2 };
+enum { ORC_Q4_0 = 0, ORC_Q8_0 = 1, ORC_IQ4_NL = 2, ORC_MXFP4 = 3 };
+
+/* OCP Microscaling FP4 (E2M1): code = sign<<3 | exponent<<1 | mantissa; value = 0.5 * mantissa for
+ * exponent 0, else 2^(exponent-1) * (1 + mantissa/2).  Twice the value, as an integer. */
+static int e2m1_twice(int code)
+{
+    int ex = (code >> 1) & 3, mant = code & 1;
+    int v2 = (ex == 0) ? mant : (1 << (ex - 1)) * (2 + mant);   /* 2 * value */
+    return (code & 8) ? -v2 : v2;
+}
+
+/* The pages' E8M0 -> fp16 conversion: fp16 bits clamp(e - 112, 0, 30) << 10, a power of two
+ * (2^(e-127) for 113 <= e <= 142), 0 for e <= 112 and 2^15 from e = 142 on. */
+uint16_t orc_e8m0_to_f16_bits(int e)
+{
+    int f = e - 112;
+    if (f < 0) f = 0;
+    if (f > 30) f = 30;
+    return (uint16_t)(f << 10);
+}
 
 /* The oracle's own copy of the 16-entry IQ4_NL table.  The pages name the table but print no values;
  * this stand-in is the 16-level Lloyd-Max quantizer of a unit normal, scaled so that its outermost
@@ -108,6 +136,7 @@ int64_t orc_block_bytes(int type)
 {
     if (type == ORC_Q4_0 || type == ORC_IQ4_NL) return 18;  /* fp16 d + 16 bytes of nibbles */
     if (type == ORC_Q8_0) return 34;                        /* fp16 d + 32 int8 */
+    if (type == ORC_MXFP4) return 17;                       /* E8M0 e + 16 bytes of nibbles */
     return 0;
 }
 
@@ -115,6 +144,7 @@ int64_t orc_tile_bytes(int type)
 {
     if (type == ORC_Q4_0 || type == ORC_IQ4_NL) return 576;  /* 512 quant bytes + 32 fp16 scales */
     if (type == ORC_Q8_0) return 1088;                       /* 1024 quant bytes + 32 fp16 scales */
+    if (type == ORC_MXFP4) return 544;                       /* 512 quant bytes + 32 E8M0 exponents */
     return 0;
 }
 
@@ -134,18 +164,23 @@ int64_t orc_tiled_bytes(int type, int64_t K, int64_t N)
 static uint16_t load_u16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 static void store_u16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (uint8_t)(v >> 8); }
 
+/* Bytes before the quants in a flat block: the fp16 scale, or MXFP4's one exponent byte. */
+static int flat_head(int type) { return type == ORC_MXFP4 ? 1 : 2; }
+
 static int flat_code(int type, const uint8_t *blk, int j)
 {
-    if (type == ORC_Q8_0) return (int)(int8_t)blk[2 + j];
-    if (j < 16) return blk[2 + j] & 0x0F;
-    return blk[2 + (j - 16)] >> 4;
+    const uint8_t *qs = blk + flat_head(type);
+    if (type == ORC_Q8_0) return (int)(int8_t)qs[j];
+    if (j < 16) return qs[j] & 0x0F;
+    return qs[j - 16] >> 4;
 }
 
 static void flat_set_code(int type, uint8_t *blk, int j, int code)
 {
-    if (type == ORC_Q8_0) { blk[2 + j] = (uint8_t)(int8_t)code; return; }
-    if (j < 16) blk[2 + j] = (uint8_t)((blk[2 + j] & 0xF0) | (code & 0x0F));
-    else blk[2 + (j - 16)] = (uint8_t)((blk[2 + (j - 16)] & 0x0F) | ((code & 0x0F) << 4));
+    uint8_t *qs = blk + flat_head(type);
+    if (type == ORC_Q8_0) { qs[j] = (uint8_t)(int8_t)code; return; }
+    if (j < 16) qs[j] = (uint8_t)((qs[j] & 0xF0) | (code & 0x0F));
+    else qs[j - 16] = (uint8_t)((qs[j - 16] & 0x0F) | ((code & 0x0F) << 4));
 }
 
 /* Integer weight value of a code: Q4_0 q-8, Q8_0 q, IQ4_NL lut[q] (BASELINE dequant rules; IQ4_NL
@@ -154,7 +189,16 @@ static int weight_int(int type, int code, const int8_t *lut)
 {
     if (type == ORC_Q4_0) return code - 8;
     if (type == ORC_Q8_0) return code;
+    if (type == ORC_MXFP4) return e2m1_twice(code & 15);
     return (int)lut[code & 15];
+}
+
+/* Scale of a block's integer weights: the fp16 scale, or for MXFP4 half the fp16 power of two made
+ * from the exponent byte (the integer weights are twice the FP4 values). */
+static double block_scale(int type, const uint8_t *scale_bytes)
+{
+    if (type == ORC_MXFP4) return 0.5 * (double)orc_f16_to_f32(orc_e8m0_to_f16_bits(scale_bytes[0]));
+    return (double)orc_f16_to_f32(load_u16(scale_bytes));
 }
 
 /* ------------------------------------------------------------------------------------------------
@@ -225,6 +269,36 @@ static void quantize_block_iq4_nl(const float *x, const int8_t *lut, uint8_t *co
     }
 }
 
+/* MXFP4 rule: e = floor(log2 amax) - 2 + 127 (so that amax / 2^(e-127) lies in [4, 8)), 0 for an
+ * all-zero block, clamped to 0..254; then the code whose level s * fp4(code) is nearest to x, where s
+ * is the dequantizing scale (the pages' fp16 power of two), lowest code on ties. */
+static void quantize_block_mxfp4(const float *x, uint8_t *codes, uint8_t *e_out)
+{
+    float amax = 0.0f;
+    for (int j = 0; j < 32; ++j)
+        if (fabsf(x[j]) > amax) amax = fabsf(x[j]);
+    int e = 0;
+    if (amax > 0.0f) {
+        int ex;
+        (void)frexpf(amax, &ex);             /* amax = f * 2^ex, f in [0.5, 1): floor(log2 amax) = ex - 1 */
+        e = (ex - 1) - 2 + 127;
+        if (e < 0) e = 0;
+        if (e > 254) e = 254;
+    }
+    *e_out = (uint8_t)e;
+    const float s = orc_f16_to_f32(orc_e8m0_to_f16_bits(e));
+    for (int j = 0; j < 32; ++j) {
+        int best = 0;
+        float best_err = INFINITY;
+        for (int i = 0; i < 16; ++i) {
+            float level = s * (0.5f * (float)e2m1_twice(i));
+            float err = fabsf(x[j] - level);
+            if (err < best_err) { best_err = err; best = i; }
+        }
+        codes[j] = (uint8_t)best;
+    }
+}
+
 /* Quantize N rows of K floats (row n at w + n*K) into flat GGML blocks, row after row. */
 void orc_quantize_rows(int type, const float *w, int64_t N, int64_t K, const int8_t *lut, uint8_t *flat)
 {
@@ -239,6 +313,12 @@ void orc_quantize_rows(int type, const float *w, int64_t N, int64_t K, const int
                 int8_t q[32];
                 orc_quantize_block_q8_0(x, q, &d16);
                 for (int j = 0; j < 32; ++j) flat_set_code(type, blk, j, q[j]);
+            } else if (type == ORC_MXFP4) {
+                uint8_t codes[32], e;
+                quantize_block_mxfp4(x, codes, &e);
+                for (int j = 0; j < 32; ++j) flat_set_code(type, blk, j, codes[j]);
+                blk[0] = e;
+                continue;
             } else {
                 uint8_t codes[32];
                 if (type == ORC_Q4_0) quantize_block_q4_0(x, codes, &d16);
@@ -257,7 +337,7 @@ void orc_dequantize_flat(int type, const uint8_t *flat, int64_t N, int64_t K, co
     for (int64_t n = 0; n < N; ++n)
         for (int64_t b = 0; b < nb; ++b) {
             const uint8_t *blk = flat + (n * nb + b) * bb;
-            double d = (double)orc_f16_to_f32(load_u16(blk));
+            double d = block_scale(type, blk);
             for (int j = 0; j < 32; ++j)
                 out[n * K + b * 32 + j] = d * (double)weight_int(type, flat_code(type, blk, j), lut);
         }
@@ -290,8 +370,12 @@ void orc_repack(int type, const uint8_t *flat, int64_t K, int64_t N, uint8_t *ti
                         tile[cp * 32 + r] = (uint8_t)(((c1 & 0x0F) << 4) | (c0 & 0x0F));
                     }
                 }
-                tile[scale_off + 2 * r + 0] = blk[0];
-                tile[scale_off + 2 * r + 1] = blk[1];
+                if (type == ORC_MXFP4) {
+                    tile[scale_off + r] = blk[0];            /* one exponent byte per row */
+                } else {
+                    tile[scale_off + 2 * r + 0] = blk[0];
+                    tile[scale_off + 2 * r + 1] = blk[1];
+                }
             }
         }
 }
@@ -308,8 +392,12 @@ void orc_unpack(int type, const uint8_t *tiled, int64_t K, int64_t N, uint8_t *f
             const uint8_t *tile = tiled + orc_tile_index(ct, kt, n_k_tiles) * ts;
             uint8_t *blk = flat + (n * n_k_tiles + kt) * bb;
             memset(blk, 0, (size_t)bb);
-            blk[0] = tile[scale_off + 2 * r + 0];
-            blk[1] = tile[scale_off + 2 * r + 1];
+            if (type == ORC_MXFP4) {
+                blk[0] = tile[scale_off + r];
+            } else {
+                blk[0] = tile[scale_off + 2 * r + 0];
+                blk[1] = tile[scale_off + 2 * r + 1];
+            }
             for (int cp = 0; cp < 16; ++cp) {
                 int c0, c1;
                 if (type == ORC_Q8_0) {
@@ -339,13 +427,13 @@ static int tiled_weight(int type, const uint8_t *tiled, int64_t n_k_tiles, int64
     return weight_int(type, code, lut);
 }
 
-static uint16_t tiled_scale(int type, const uint8_t *tiled, int64_t n_k_tiles, int64_t n, int64_t kt)
+static double tiled_scale(int type, const uint8_t *tiled, int64_t n_k_tiles, int64_t n, int64_t kt)
 {
     int64_t ct = n / 32;
     int r = (int)(n % 32);
     const uint8_t *tile = tiled + orc_tile_index(ct, kt, n_k_tiles) * orc_tile_bytes(type);
     int64_t scale_off = (type == ORC_Q8_0) ? 1024 : 512;
-    return load_u16(tile + scale_off + 2 * r);
+    return block_scale(type, tile + scale_off + (type == ORC_MXFP4 ? r : 2 * r));
 }
 
 /* ------------------------------------------------------------------------------------------------
@@ -380,7 +468,7 @@ static void one_output(int type, const uint8_t *tiled, int64_t K, const int8_t *
             s += w * a;
             sabs += (w * a < 0) ? -(w * a) : (w * a);
         }
-        double dw = (double)orc_f16_to_f32(tiled_scale(type, tiled, n_k_tiles, n, b));
+        double dw = tiled_scale(type, tiled, n_k_tiles, n, b);
         double da = (double)orc_f16_to_f32(a_d[m * n_k_tiles + b]);
         acc += dw * da * (double)s;
         bacc += fabs(dw * da) * (double)sabs;

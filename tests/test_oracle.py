@@ -12,7 +12,7 @@ import pytest
 from block_quantized_matmul_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-TYPES = ["q4_0", "q8_0", "iq4_nl"]
+TYPES = ["q4_0", "q8_0", "iq4_nl", "mxfp4"]
 
 
 # ---------------------------------------------------------------------------------------------
@@ -45,6 +45,7 @@ def test_tile_and_block_sizes(orc):
     assert orc.tile_bytes("q8_0") == 1088
     assert 32 * orc.block_bytes("q4_0") == 576 and 32 * orc.block_bytes("iq4_nl") == 576
     assert 32 * orc.block_bytes("q8_0") == 1088
+    assert orc.tile_bytes("mxfp4") == 544 and 32 * orc.block_bytes("mxfp4") == 544
 
 
 @pytest.mark.parametrize("K,N,type_,tiles", [
@@ -90,12 +91,16 @@ def test_one_hot_tile_position(orc, case):
     flat = np.zeros((N, bb), np.uint8)
     raw = code & 0xFF if type_ == "q8_0" else code << fshift
     flat[row, fbyte] = raw
-    flat[row, 0:2] = (0x34, 0x12)              # fp16 scale bits 0x1234 on that row
+    expect = np.zeros(ts, np.uint8)
+    if type_ == "mxfp4":
+        flat[row, 0] = 0x7B                    # E8M0 exponent byte of that row
+        expect[sbyte] = 0x7B
+    else:
+        flat[row, 0:2] = (0x34, 0x12)          # fp16 scale bits 0x1234 on that row
+        expect[sbyte], expect[sbyte + 1] = 0x34, 0x12
     tiled = orc.repack(type_, flat, K, N)
     assert tiled.size == ts
-    expect = np.zeros(ts, np.uint8)
     expect[tbyte] = (code & 0xFF) if type_ == "q8_0" else (code << tshift)
-    expect[sbyte], expect[sbyte + 1] = 0x34, 0x12
     assert np.array_equal(tiled, expect), np.nonzero(tiled != expect)
 
 
@@ -117,6 +122,9 @@ def test_repack_unpack_roundtrip_and_padding(orc, type_, K, N):
                 if type_ == "q8_0":
                     assert all(t[cp * 64 + 2 * r + h] == 0 for cp in range(16) for h in range(2))
                     assert t[1024 + 2 * r] == 0 and t[1025 + 2 * r] == 0
+                elif type_ == "mxfp4":
+                    assert all(t[cp * 32 + r] == 0 for cp in range(16))
+                    assert t[512 + r] == 0
                 else:
                     assert all(t[cp * 32 + r] == 0 for cp in range(16))
                     assert t[512 + 2 * r] == 0 and t[513 + 2 * r] == 0
@@ -213,6 +221,12 @@ def test_weight_quantizer_error_bound(orc, type_):
     elif type_ == "q4_0":
         step = amax / 8
         assert np.all(np.abs(dq - blocks) <= step * (1.0 + 8 * 2.0 ** -11) + 1e-12)
+    elif type_ == "mxfp4":
+        # scale 2^(floor(log2 amax) - 2): levels up to 6 * scale cover amax < 8 * scale except the top
+        # (saturation at 6 * scale); the widest gap below 6 is 2 * scale (between 4 and 6)
+        scale = 2.0 ** (np.floor(np.log2(amax)) - 2)
+        err = np.abs(dq - blocks)
+        assert np.all(err <= np.maximum(scale, amax - 6 * scale) + 1e-12)
     else:
         lut = orc.iq4nl_table().astype(np.float64)
         gaps = np.diff(lut).max()
@@ -319,3 +333,69 @@ def test_iq4_nl_with_offset_table_equals_q4_0(orc):
     y4, b4 = orc.matmul("q4_0", tiled, K, N, a_q, a_d)
     yi, bi = orc.matmul("iq4_nl", tiled, K, N, a_q, a_d, lut=np.arange(16) - 8)
     assert np.array_equal(y4, yi) and np.array_equal(b4, bi)
+
+
+# ---------------------------------------------------------------------------------------------
+# MXFP4: the pages' E8M0 conversion and the OCP E2M1 code set
+# ---------------------------------------------------------------------------------------------
+# OCP Microscaling FP4 (E2M1) values of codes 0..7; codes 8..15 are their negatives (sign bit 3).
+OCP_E2M1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e8m0_scale_follows_the_pages_formula(orc):
+    # "clamp(e - 112, 0, 30) << 10" read as fp16 bits: 2^(e-127) in 113..142, 0 below, 2^15 above.
+    for e in range(256):
+        v = float(np.array([orc.e8m0_to_f16_bits(e)], np.uint16).view(np.float16)[0])
+        if e <= 112:
+            assert v == 0.0
+        elif e <= 142:
+            assert v == 2.0 ** (e - 127)
+        else:
+            assert v == 2.0 ** 15
+    assert orc.e8m0_to_f16_bits(127) == 0x3C00          # 1.0
+
+
+def test_mxfp4_dequant_is_e2m1_times_scale(orc):
+    # Every code at several exponents, decoded from the raw bytes with the OCP table and numpy fp16.
+    flat = np.zeros((16, 17), np.uint8)
+    for r in range(16):
+        flat[r, 0] = 100 + 3 * r                          # exponents 100..145 (some flushed, some clamped)
+        for j in range(32):
+            code = (j + r) % 16
+            if j < 16:
+                flat[r, 1 + j] |= code
+            else:
+                flat[r, 1 + j - 16] |= code << 4
+    deq = orc.dequantize_flat("mxfp4", flat, 16, 32)
+    for r in range(16):
+        e = int(flat[r, 0])
+        s = float(np.array([min(max(e - 112, 0), 30) << 10], np.uint16).view(np.float16)[0])
+        for j in range(32):
+            code = (j + r) % 16
+            v = OCP_E2M1[code & 7] * (-1.0 if code & 8 else 1.0)
+            assert deq[r, j] == v * s, (r, j, code, e)
+
+
+def test_mxfp4_quantizer_exact_values_and_nearest_level(orc):
+    rng = np.random.default_rng(5)
+    # exactly representable blocks come back unchanged (the largest magnitude 6 * 2^k fixes e)
+    levels = np.array(OCP_E2M1 + [-v for v in OCP_E2M1], np.float32)
+    w = np.stack([np.float32(2.0 ** k) * np.concatenate([[np.float32(6.0)], rng.choice(levels, 31)]).astype(np.float32)
+                  for k in range(-6, 7)]).astype(np.float32)
+    flat = orc.quantize_rows("mxfp4", w)
+    assert np.array_equal(orc.dequantize_flat("mxfp4", flat, w.shape[0], 32), w.astype(np.float64))
+    # otherwise each element takes a nearest level of its block's scale (lowest code on ties)
+    w = synth.weights(8, 64)
+    flat = orc.quantize_rows("mxfp4", w)
+    for n in range(8):
+        for b in range(2):
+            blk = flat[n, b * 17:(b + 1) * 17]
+            s = np.float32(np.array([orc.e8m0_to_f16_bits(int(blk[0]))], np.uint16).view(np.float16)[0])
+            lv = np.array([s * np.float32(OCP_E2M1[c & 7] * (-1.0 if c & 8 else 1.0)) for c in range(16)], np.float32)
+            for j in range(32):
+                c = (blk[1 + j] & 15) if j < 16 else (blk[1 + j - 16] >> 4)
+                errs = np.abs(np.float32(w[n, b * 32 + j]) - lv)
+                assert c == int(np.argmax(errs == errs.min()))
+    # an all-zero block gets exponent 0 and code 0 everywhere
+    z = orc.quantize_rows("mxfp4", np.zeros((1, 32), np.float32))
+    assert not z.any()
