@@ -291,7 +291,7 @@ enum { kActInt8 = 0, kActPrepared = 1 };
 template <int TYPE, int ACT>
 struct GemmPlan {
     static constexpr bool kPrep = ACT == kActPrepared;
-    static constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    static constexpr int TS = TileFmt<TYPE>::kBytes;
     static constexpr int kWTiles = 8 * TS;                                   // [4 ct][2 kt] raw tiles
     static constexpr int kWTok = kPrep ? 2 * BN * 2 : BN * 64;              // fp16 scales or int8 rows
     static constexpr int kWStageBytes = (kWTiles + kWTok + 127) / 128 * 128;
@@ -303,7 +303,7 @@ struct GemmPlan {
     static constexpr int kOpStages = 3;
     static constexpr int kBStages = kPrep ? 4 : 0;
     static constexpr int kBRing = kBStages > 0 ? kBStages : 1;               // modulus, never 0
-    static constexpr int kLutBytes = (TYPE == QMM_IQ4_NL) ? 256 * kLutCopies * 4 : 0;
+    static constexpr int kLutBytes = TileFmt<TYPE>::kLut ? 256 * kLutCopies * 4 : 0;
     static constexpr int kFixed = kOpStages * kOpStage + kBStages * kOp2Bytes + kLutBytes + 1024 + 512;
     static constexpr int kWStagesFit = (227 * 1024 - kFixed) / kWStageBytes;
     static constexpr int kWStages = kWStagesFit > 8 ? 8 : kWStagesFit;
@@ -327,7 +327,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
             const __grid_constant__ CUtensorMap da_map) {
     using P = GemmPlan<TYPE, ACT>;
     constexpr int TS = P::TS;
-    constexpr int SOFF = (TYPE == QMM_Q8_0) ? kScale8Off : kScale4Off;
+    constexpr int SOFF = TileFmt<TYPE>::kScaleOff;
     constexpr int WS = P::kWStages, BR = P::kBRing, OS = P::kOpStages;
 
     extern __shared__ uint8_t smem_raw[];
@@ -366,7 +366,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if constexpr (TYPE == QMM_IQ4_NL) {
+    if constexpr (TileFmt<TYPE>::kLut) {
         for (int i = threadIdx.x; i < 256 * kLutCopies; i += kThreads) {
             const int b = i / kLutCopies;
             lut_s[i] = h2_bits(__halves2half2(__int2half_rn(p.lut.v[b & 15]), __int2half_rn(p.lut.v[b >> 4])));
@@ -498,7 +498,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                 for (int j = 0; j < 2; ++j) {
                     // -- weight row c of block j: 32 columns -> 16 half2 in column order --
                     uint32_t h[16];
-                    uint16_t dw = 0;
+                    float dw = 0.0f;
                     if (w_ok) {
                         const uint8_t *tile = raw + (q * 2 + j) * TS;
                         if constexpr (TYPE == QMM_Q8_0) {
@@ -517,7 +517,8 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                                 else h[cp] = lut_lane[b * kLutCopies];
                             }
                         }
-                        dw = *reinterpret_cast<const uint16_t *>(tile + SOFF + 2 * tr);
+                        if constexpr (TileFmt<TYPE>::kE8M0) dw = mx_half_scale(tile[SOFF + tr]);
+                        else dw = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(tile + SOFF + 2 * tr)));
                     } else {
 #pragma unroll
                         for (int cp = 0; cp < 16; ++cp) h[cp] = 0u;
@@ -526,7 +527,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                     for (int ch = 0; ch < 4; ++ch)
                         *reinterpret_cast<uint4 *>(op + P::kOffA + sw128_off(c, 4 * j + ch)) =
                             make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
-                    sc[j * 128 + c] = __half2float(__ushort_as_half(dw));
+                    sc[j * 128 + c] = dw;
                     // -- token row c of block j --
                     uint16_t da;
                     if constexpr (P::kPrep) {
@@ -724,12 +725,13 @@ cudaError_t dispatch(qmm_type t, const GemmParams &p, const CUtensorMap &am, con
     switch (t) {
         case QMM_Q4_0: return launch_typed<QMM_Q4_0, ACT>(p, am, dm, s);
         case QMM_IQ4_NL: return launch_typed<QMM_IQ4_NL, ACT>(p, am, dm, s);
+        case QMM_MXFP4: return launch_typed<QMM_MXFP4, ACT>(p, am, dm, s);
         default: return launch_typed<QMM_Q8_0, ACT>(p, am, dm, s);
     }
 }
 
-GemmParams make_params(const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int64_t M,
-                       float *y, int64_t ldy) {
+GemmParams make_params(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
+                       int64_t M, float *y, int64_t ldy) {
     GemmParams p;
     p.tiled = tiled;
     p.a_q = a_q;
@@ -741,7 +743,7 @@ GemmParams make_params(const uint8_t *tiled, int64_t K, int64_t N, const int8_t 
     p.M = M;
     p.ldy = ldy;
     p.n_col_tiles = (N + 31) / 32;
-    p.lut = iq4nl_lut();
+    p.lut = lut_for(t);
     return p;
 }
 
@@ -750,7 +752,7 @@ GemmParams make_params(const uint8_t *tiled, int64_t K, int64_t N, const int8_t 
 cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
                         int64_t M, float *y, int64_t ldy, cudaStream_t s) {
     if ((M + BN - 1) / BN > 65535) return cudaErrorInvalidValue;
-    const GemmParams p = make_params(tiled, K, N, a_q, a_d, M, y, ldy);
+    const GemmParams p = make_params(t, tiled, K, N, a_q, a_d, M, y, ldy);
     alignas(64) CUtensorMap am, dm;
     cudaError_t e = make_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, (uint64_t)K, (uint64_t)M, (uint64_t)K, 64, BN,
                                 CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -778,7 +780,7 @@ cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t 
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    const GemmParams p = make_params(tiled, K, N, a_q, a_d, M, y, ldy);
+    const GemmParams p = make_params(t, tiled, K, N, a_q, a_d, M, y, ldy);
     alignas(64) CUtensorMap am, dm;
     cudaError_t e = make_map_2d(&am, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a_h, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64,
                                 BN, CU_TENSOR_MAP_SWIZZLE_128B);

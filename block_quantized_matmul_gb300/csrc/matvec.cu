@@ -29,6 +29,10 @@ namespace qmm {
 namespace {
 
 constexpr int kTilesPerWarp = 2;                        // independent tiles per warp per stage (ILP)
+// Independent tiles per warp and stage for the int8 dot-product consumers: 4 where decoding a tile takes
+// many instructions per byte (4-bit codes, table lookups), 2 for the plain Q8_0 bytes (measured).
+template <int TYPE>
+constexpr int kDp4aTilesPerWarp = TYPE == QMM_Q8_0 ? 2 : 4;
 constexpr int kDp4aMaxM = 4;                            // tokens up to which the int8 dot-product path runs
 constexpr int kLutCopies = 16;
 constexpr int kActBudget = 64 * 1024;                   // bytes of staged activations per CTA
@@ -186,6 +190,21 @@ __device__ __forceinline__ uint2 quantize_quarter(const MvParams &p, bool live, 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
+// The scales of tile rows r0 .. r0+3 (r0 a multiple of 4) as fp32: fp16 row scales, or for MXFP4 half
+// the power of two of each row's E8M0 byte (the doubled integer codes carry the other factor 2).
+template <int TYPE>
+__device__ __forceinline__ void row_scales(const uint8_t *scales, int r0, float (&d)[4]) {
+    if constexpr (TileFmt<TYPE>::kE8M0) {
+        const uint32_t e4 = *reinterpret_cast<const uint32_t *>(scales + r0);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) d[r] = mx_half_scale((e4 >> (8 * r)) & 0xFFu);
+    } else {
+        const uint2 sc = *reinterpret_cast<const uint2 *>(scales + 2 * r0);
+        const float2 d01 = __half22float2(bits_h2(sc.x)), d23 = __half22float2(bits_h2(sc.y));
+        d[0] = d01.x; d[1] = d01.y; d[2] = d23.x; d[3] = d23.y;
+    }
+}
+
 __device__ __forceinline__ unsigned long long pack2(float a, float b) {
     unsigned long long v;
     asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(a), "f"(b));
@@ -290,7 +309,7 @@ struct MvLayout {
 };
 template <int TYPE, int NF, int CW>
 __host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
-    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    constexpr int TS = TileFmt<TYPE>::kBytes;
     constexpr int kTilesPerStage = CW * kTilesPerWarp;
     MvLayout L;
     int off = 0;
@@ -302,7 +321,7 @@ __host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
     L.da = off;    off += nkc * 8 * NF * 4;                 // [nkc][8*NF] float
     L.corr = off;  off += nkc * 8 * NF * 4;                 // [nkc][8*NF] float
     L.red = off;   off += CW * 2 * NF * 4 * 32 * 4;
-    L.lut = off;   off += (TYPE == QMM_IQ4_NL) ? 256 * kLutCopies * 4 : 0;
+    L.lut = off;   off += TileFmt<TYPE>::kLut ? 256 * kLutCopies * 4 : 0;
     L.total = off;
     return L;
 }
@@ -313,8 +332,8 @@ template <int TYPE, int NF, int CW, bool FUSED>
 __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const MvParams p) {
     constexpr int kConsumerWarps = CW;
     constexpr int kTilesPerStage = CW * kTilesPerWarp;
-    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
-    constexpr int SOFF = (TYPE == QMM_Q8_0) ? kScale8Off : kScale4Off;
+    constexpr int TS = TileFmt<TYPE>::kBytes;
+    constexpr int SOFF = TileFmt<TYPE>::kScaleOff;
     constexpr int TOK = 8 * NF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
@@ -364,7 +383,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
 
     // ---- stage activations once: per (token, block) 16 half2 in fragment order, plus the
     //      per-block scale and the exact bias of the biased weight decode ----
-    if constexpr (TYPE == QMM_IQ4_NL) {
+    if constexpr (TileFmt<TYPE>::kLut) {
         for (int i = ctid; i < 256 * kLutCopies; i += kConsumerWarps * 32) {
             const int b = i / kLutCopies;
             lut_s[i] = h2_bits(__halves2half2(__int2half_rn(p.lut.v[b & 15]), __int2half_rn(p.lut.v[b >> 4])));
@@ -467,10 +486,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                     const uint8_t *tile = ring + (s * kTilesPerStage + cw + kConsumerWarps * u) * TS;
                     if (live[u]) {
                         decode_tile<TYPE>(tile, g, t, H[u], lut_lane);
-                        const uint2 sc = *reinterpret_cast<const uint2 *>(tile + SOFF + 8 * g);
-                        const float2 dw01 = __half22float2(bits_h2(sc.x));      // rows 4g, 4g+1
-                        const float2 dw23 = __half22float2(bits_h2(sc.y));      // rows 4g+2, 4g+3
-                        dwr[u][0] = dw01.x; dwr[u][1] = dw01.y; dwr[u][2] = dw23.x; dwr[u][3] = dw23.y;
+                        row_scales<TYPE>(tile + SOFF, 4 * g, dwr[u]);            // rows 4g .. 4g+3
                     }
                 }
 #pragma unroll
@@ -630,12 +646,12 @@ __device__ __forceinline__ uint4 dp4a_record(int type, uint2 v, int j, float da)
 struct Dp4aLayout {
     int ring, bars, act, red, total;
 };
-template <int TYPE, int MT, int CW>
+template <int TYPE, int MT, int CW, int TPW>
 __host__ __device__ inline Dp4aLayout dp4a_layout(int nkc, int stages) {
-    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    constexpr int TS = TileFmt<TYPE>::kBytes;
     Dp4aLayout L;
     int off = 0;
-    L.ring = off;  off += stages * CW * kTilesPerWarp * TS;
+    L.ring = off;  off += stages * CW * TPW * TS;
     off = (off + 15) & ~15;
     L.bars = off;  off += 2 * stages * 8 + 16;
     off = (off + 15) & ~15;
@@ -645,15 +661,15 @@ __host__ __device__ inline Dp4aLayout dp4a_layout(int nkc, int stages) {
     return L;
 }
 
-// MT = token capacity (1, 2 or 4); p.M <= MT tokens are live.
-template <int TYPE, int MT, int CW, bool FUSED>
+// MT = token capacity (1, 2 or 4); p.M <= MT tokens are live.  TPW independent tiles per warp and stage.
+template <int TYPE, int MT, int CW, bool FUSED, int TPW>
 __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(const MvParams p) {
-    constexpr int kTilesPerStage = CW * kTilesPerWarp;
-    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
-    constexpr int SOFF = (TYPE == QMM_Q8_0) ? kScale8Off : kScale4Off;
+    constexpr int kTilesPerStage = CW * TPW;
+    constexpr int TS = TileFmt<TYPE>::kBytes;
+    constexpr int SOFF = TileFmt<TYPE>::kScaleOff;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-    const Dp4aLayout L = dp4a_layout<TYPE, MT, CW>(p.nkc, p.stages);
+    const Dp4aLayout L = dp4a_layout<TYPE, MT, CW, TPW>(p.nkc, p.stages);
     uint8_t *ring = smem + L.ring;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + p.stages;
@@ -711,7 +727,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
         }
     }
     uint32_t tb[4] = {0u, 0u, 0u, 0u};
-    if constexpr (TYPE == QMM_IQ4_NL) {
+    if constexpr (TileFmt<TYPE>::kLut) {
 #pragma unroll
         for (int w = 0; w < 4; ++w)
 #pragma unroll
@@ -732,15 +748,15 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
             if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
             if (ok) {
 #pragma unroll
-                for (int u = 0; u < kTilesPerWarp; ++u) {
+                for (int u = 0; u < TPW; ++u) {
                     const int jt = j0 + cw + CW * u;
                     if (jt >= nkc) continue;
                     const uint8_t *tile = ring + (s * kTilesPerStage + cw + CW * u) * TS;
                     uint32_t R[4][2];
                     tile_rows_dp4a<TYPE>(tile, i, j, R, tb);
-                    const uint2 sc = *reinterpret_cast<const uint2 *>(tile + SOFF + 8 * i);
-                    const float2 d01 = __half22float2(bits_h2(sc.x)), d23 = __half22float2(bits_h2(sc.y));
-                    const unsigned long long dw01 = pack2(d01.x, d01.y), dw23 = pack2(d23.x, d23.y);
+                    float dws[4];
+                    row_scales<TYPE>(tile + SOFF, 4 * i, dws);                  // rows 4i .. 4i+3
+                    const unsigned long long dw01 = pack2(dws[0], dws[1]), dw23 = pack2(dws[2], dws[3]);
 #pragma unroll
                     for (int t = 0; t < MT; ++t) {
                         if (t >= p.M) break;
@@ -795,9 +811,9 @@ struct Plan {
 
 // Ring depth from what is left of the CTA's share of shared memory: CW = 16 runs one wide CTA per
 // SM (all of it), CW = 8 two narrow CTAs per SM (half each).
-template <int TS, int CW>
+template <int TS, int CW, int TPW = kTilesPerWarp>
 Plan plan_ring(int nkc, int fixed_bytes) {
-    constexpr int kTilesPerStage = CW * kTilesPerWarp;
+    constexpr int kTilesPerStage = CW * TPW;
     Plan pl;
     pl.nkc = nkc;
     const int stage_bytes = kTilesPerStage * TS + 16;
@@ -830,8 +846,8 @@ int num_sms() {
 // dependent of the grid before it on the stream: it may start while that grid is still running (if
 // that grid allows it), and the kernel waits for it before reading activations or y.
 template <typename Kern>
-cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const uint8_t *tiled, int64_t K, int64_t N,
-                          const ActSrc &a, int M, float *y, int64_t ldy, cudaStream_t s) {
+cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const Lut16 &lut, const uint8_t *tiled, int64_t K,
+                          int64_t N, const ActSrc &a, int M, float *y, int64_t ldy, cudaStream_t s) {
     const int64_t nkt = K / 32, nct = (N + 31) / 32;
     int64_t grid = (int64_t)num_sms() * pl.ctas_per_sm;
     if (grid > nct) grid = nct;
@@ -854,7 +870,7 @@ cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const uint8_t 
         p.nkc = (int)((nkt - kt0) < pl.nkc ? (nkt - kt0) : pl.nkc);
         p.accumulate = kt0 > 0;
         p.stages = pl.stages;
-        p.lut = iq4nl_lut();
+        p.lut = lut;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid, 1, 1);
         cfg.blockDim = dim3((unsigned)threads, 1, 1);
@@ -874,7 +890,7 @@ cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const uint8_t 
 template <int TYPE, int NF, int CW, bool FUSED>
 cudaError_t run_mma(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a, int M, float *y, int64_t ldy,
                     cudaStream_t s) {
-    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    constexpr int TS = TileFmt<TYPE>::kBytes;
     const int nkc = chunk_tiles(K / 32, 64 * (int64_t)M);
     Plan pl = plan_ring<TS, CW>(nkc, mv_layout<TYPE, NF, CW>(M, nkc, 0).total);
     pl.smem = (size_t)mv_layout<TYPE, NF, CW>(M, nkc, pl.stages).total + 128;
@@ -882,21 +898,22 @@ cudaError_t run_mma(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a,
     static int attr_done[4] = {0, 0, 0, 0};
     const cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
     if (e != cudaSuccess) return e;
-    return launch_passes(kern, 32 * (1 + CW), pl, tiled, K, N, a, M, y, ldy, s);
+    return launch_passes(kern, 32 * (1 + CW), pl, lut_for((qmm_type)TYPE), tiled, K, N, a, M, y, ldy, s);
 }
 
 template <int TYPE, int MT, int CW, bool FUSED>
 cudaError_t run_dp4a(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a, int M, float *y, int64_t ldy,
                      cudaStream_t s) {
-    constexpr int TS = (TYPE == QMM_Q8_0) ? kTile8Bytes : kTile4Bytes;
+    constexpr int TS = TileFmt<TYPE>::kBytes;
+    constexpr int TPW = kDp4aTilesPerWarp<TYPE>;
     const int nkc = chunk_tiles(K / 32, 64 * (int64_t)MT);
-    Plan pl = plan_ring<TS, CW>(nkc, dp4a_layout<TYPE, MT, CW>(nkc, 0).total);
-    pl.smem = (size_t)dp4a_layout<TYPE, MT, CW>(nkc, pl.stages).total + 128;
-    auto kern = matvec_dp4a_kernel<TYPE, MT, CW, FUSED>;
+    Plan pl = plan_ring<TS, CW, TPW>(nkc, dp4a_layout<TYPE, MT, CW, TPW>(nkc, 0).total);
+    pl.smem = (size_t)dp4a_layout<TYPE, MT, CW, TPW>(nkc, pl.stages).total + 128;
+    auto kern = matvec_dp4a_kernel<TYPE, MT, CW, FUSED, TPW>;
     static int attr_done[4] = {0, 0, 0, 0};
     const cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
     if (e != cudaSuccess) return e;
-    return launch_passes(kern, 32 * (1 + CW), pl, tiled, K, N, a, M, y, ldy, s);
+    return launch_passes(kern, 32 * (1 + CW), pl, lut_for((qmm_type)TYPE), tiled, K, N, a, M, y, ldy, s);
 }
 
 // Up to kDp4aMaxM tokens: int8 dot products; more: fp16 mma.sync.  Many column tiles: two narrow
@@ -936,6 +953,7 @@ cudaError_t run_groups(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, c
         switch (t) {
             case QMM_Q4_0: e = run<QMM_Q4_0, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
             case QMM_IQ4_NL: e = run<QMM_IQ4_NL, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
+            case QMM_MXFP4: e = run<QMM_MXFP4, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
             default: e = run<QMM_Q8_0, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
         }
         if (e != cudaSuccess) return e;

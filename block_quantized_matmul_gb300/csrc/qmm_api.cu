@@ -13,7 +13,9 @@ using namespace qmm;
 
 namespace {
 
-bool valid_type(qmm_type t) { return t == QMM_Q4_0 || t == QMM_Q8_0 || t == QMM_IQ4_NL; }
+bool valid_type(qmm_type t) { return t == QMM_Q4_0 || t == QMM_Q8_0 || t == QMM_IQ4_NL || t == QMM_MXFP4; }
+// Flat blocks of 18 or 34 bytes are read as halfwords; MXFP4's 17-byte blocks byte by byte.
+uintptr_t flat_align(qmm_type t) { return t == QMM_MXFP4 ? 1 : 2; }
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool valid_kn(int64_t K, int64_t N) { return K > 0 && (K % 32) == 0 && N > 0; }
 cudaStream_t cs(qmm_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -72,14 +74,14 @@ qmm_status qmm_quantize_weight(qmm_type t, const float *w, int64_t N, int64_t K,
                                qmm_stream_t stream) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
     if (!valid_kn(K, N) || K > kMaxDim || N > kMaxDim || ldw < K || !w || !w_flat) return QMM_ERR_INVALID_ARG;
-    if (!aligned(w, 16) || (ldw % 4) != 0 || !aligned(w_flat, 2)) return QMM_ERR_MISALIGNED;
+    if (!aligned(w, 16) || (ldw % 4) != 0 || !aligned(w_flat, flat_align(t))) return QMM_ERR_MISALIGNED;
     return from_cuda(launch_quantize_weight(t, w, N, K, ldw, static_cast<uint8_t *>(w_flat), cs(stream)));
 }
 
 qmm_status qmm_repack(qmm_type t, const void *w_flat, int64_t K, int64_t N, void *w_tiled, qmm_stream_t stream) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
     if (!valid_kn(K, N) || K > kMaxDim || N > kMaxDim || !w_flat || !w_tiled) return QMM_ERR_INVALID_ARG;
-    if (!aligned(w_flat, 2) || !aligned(w_tiled, 16)) return QMM_ERR_MISALIGNED;
+    if (!aligned(w_flat, flat_align(t)) || !aligned(w_tiled, 16)) return QMM_ERR_MISALIGNED;
     return from_cuda(launch_repack(t, static_cast<const uint8_t *>(w_flat), K, N, static_cast<uint8_t *>(w_tiled),
                                    cs(stream)));
 }
@@ -87,7 +89,7 @@ qmm_status qmm_repack(qmm_type t, const void *w_flat, int64_t K, int64_t N, void
 qmm_status qmm_unpack(qmm_type t, const void *w_tiled, int64_t K, int64_t N, void *w_flat, qmm_stream_t stream) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
     if (!valid_kn(K, N) || K > kMaxDim || N > kMaxDim || !w_flat || !w_tiled) return QMM_ERR_INVALID_ARG;
-    if (!aligned(w_flat, 2) || !aligned(w_tiled, 16)) return QMM_ERR_MISALIGNED;
+    if (!aligned(w_flat, flat_align(t)) || !aligned(w_tiled, 16)) return QMM_ERR_MISALIGNED;
     return from_cuda(launch_unpack(t, static_cast<const uint8_t *>(w_tiled), K, N, static_cast<uint8_t *>(w_flat),
                                    cs(stream)));
 }

@@ -4,6 +4,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "../../include/qmm.h"
 
@@ -17,9 +18,20 @@ constexpr int kScale4Off = 512;       // FP16 row scales inside a 4-bit tile
 constexpr int kScale8Off = 1024;      // FP16 row scales inside a Q8_0 tile
 constexpr int kBlock4Bytes = 18;      // flat GGML block: fp16 d + 16 nibble bytes
 constexpr int kBlock8Bytes = 34;      // flat GGML block: fp16 d + 32 int8
+constexpr int kTileMxBytes = 544;     // MXFP4 tile: 512 nibble bytes + 32 E8M0 exponent bytes
+constexpr int kBlockMxBytes = 17;     // flat MXFP4 block: E8M0 e + 16 nibble bytes
 
-inline int tile_bytes(qmm_type t) { return t == QMM_Q8_0 ? kTile8Bytes : kTile4Bytes; }
-inline int block_bytes(qmm_type t) { return t == QMM_Q8_0 ? kBlock8Bytes : kBlock4Bytes; }
+inline int tile_bytes(qmm_type t) { return t == QMM_Q8_0 ? kTile8Bytes : (t == QMM_MXFP4 ? kTileMxBytes : kTile4Bytes); }
+inline int block_bytes(qmm_type t) { return t == QMM_Q8_0 ? kBlock8Bytes : (t == QMM_MXFP4 ? kBlockMxBytes : kBlock4Bytes); }
+
+// Per-type constants for the kernels.
+template <int TYPE>
+struct TileFmt {
+    static constexpr int kBytes = TYPE == QMM_Q8_0 ? kTile8Bytes : (TYPE == QMM_MXFP4 ? kTileMxBytes : kTile4Bytes);
+    static constexpr int kScaleOff = TYPE == QMM_Q8_0 ? kScale8Off : kScale4Off;   // MXFP4: 512 too
+    static constexpr bool kLut = TYPE == QMM_IQ4_NL || TYPE == QMM_MXFP4;         // codes go through a table
+    static constexpr bool kE8M0 = TYPE == QMM_MXFP4;                              // one exponent byte per row
+};
 
 // The built-in IQ4_NL table (16 int8 levels, ascending): 16-level Lloyd-Max quantizer of a unit
 // normal, scaled so the outer levels are -127 and +127, rounded to integers.
@@ -33,6 +45,28 @@ inline Lut16 iq4nl_lut() {
     Lut16 l;
     for (int i = 0; i < 16; ++i) l.v[i] = kIq4nlTable[i];
     return l;
+}
+
+// MXFP4 codes as integers: twice the OCP FP4 (E2M1) value of code = sign<<3 | exponent<<1 | mantissa
+// ({0, 0.5, 1, 1.5, 2, 3, 4, 6} with the sign), so that the block sums stay exact integers.  The
+// matching block scale is half the fp16 scale (mx_half_scale).
+constexpr int8_t kMxfp4Twice[16] = {0, 1, 2, 3, 4, 6, 8, 12, 0, -1, -2, -3, -4, -6, -8, -12};
+inline Lut16 mxfp4_lut() {
+    Lut16 l;
+    for (int i = 0; i < 16; ++i) l.v[i] = kMxfp4Twice[i];
+    return l;
+}
+inline Lut16 lut_for(qmm_type t) { return t == QMM_MXFP4 ? mxfp4_lut() : iq4nl_lut(); }
+
+// The pages' E8M0 -> fp16 scale: fp16 bits f << 10 with f = clamp(e - 112, 0, 30), i.e. 2^(f - 15), or 0
+// when f = 0.  Half of it (the scale of the doubled integer codes) as an exact fp32: 2^(f - 16).
+__host__ __device__ __forceinline__ float mx_half_scale(uint32_t e) {
+    int f = (int)e - 112;
+    f = f < 0 ? 0 : (f > 30 ? 30 : f);
+    const uint32_t bits = f ? (uint32_t)(f + 127 - 16) << 23 : 0u;
+    float v;
+    memcpy(&v, &bits, 4);
+    return v;
 }
 
 // ---- the dynamic Q8_0 activation rule, per block of 32 (also the Q8_0 weight rule) ----

@@ -79,6 +79,36 @@ __global__ void __launch_bounds__(128) quantize_weight_kernel(int type, const fl
         for (int j = 0; j < 32; ++j) {
             if (fabsf(xs[j]) > amax) { amax = fabsf(xs[j]); m = xs[j]; }
         }
+        if (type == QMM_MXFP4) {
+            // e = floor(log2 amax) - 2 + 127 (0 for an all-zero block, at most 254); each code the
+            // nearest level s * fp4(code) under the dequantizing fp16 scale s, lowest code on ties
+            int e = 0;
+            if (amax > 0.0f) {
+                int ex;
+                (void)frexpf(amax, &ex);
+                e = (ex - 1) - 2 + 127;
+                e = e < 0 ? 0 : (e > 254 ? 254 : e);
+            }
+            const float s = 2.0f * mx_half_scale((uint32_t)e);                 // exact power of two (or 0)
+            uint8_t *blk = flat + i * kBlockMxBytes;
+            int codes[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                int best = 0;
+                float best_err = INFINITY;
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float level = __fmul_rn(s, __fmul_rn(0.5f, (float)lut.v[q]));   // lut: doubled FP4 values
+                    const float err = fabsf(__fsub_rn(xs[j], level));
+                    if (err < best_err) { best_err = err; best = q; }
+                }
+                codes[j] = best;
+            }
+            blk[0] = (uint8_t)e;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) blk[1 + j] = (uint8_t)((codes[j] & 15) | ((codes[j + 16] & 15) << 4));
+            continue;
+        }
         const int bb = (type == QMM_Q8_0) ? kBlock8Bytes : kBlock4Bytes;
         uint16_t *out = reinterpret_cast<uint16_t *>(flat + i * bb);   // 2-byte aligned
         int codes[32];
@@ -171,7 +201,7 @@ cudaError_t launch_quantize_weight(qmm_type t, const float *w, int64_t N, int64_
                                    cudaStream_t s) {
     const int threads = 128;
     const int grid = grid_for(N * (K / 32), threads);
-    quantize_weight_kernel<<<grid, threads, 0, s>>>((int)t, w, N, K, ldw, flat, iq4nl_lut());
+    quantize_weight_kernel<<<grid, threads, 0, s>>>((int)t, w, N, K, ldw, flat, lut_for(t));
     return cudaGetLastError();
 }
 

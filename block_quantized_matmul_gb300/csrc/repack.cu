@@ -14,9 +14,10 @@ template <int TYPE>
 __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ flat, int64_t n_k_tiles, int64_t N,
                                                      int64_t n_tiles, uint8_t *__restrict__ tiled) {
     constexpr bool k8 = (TYPE == QMM_Q8_0);
-    constexpr int bb = k8 ? kBlock8Bytes : kBlock4Bytes;
-    constexpr int ts = k8 ? kTile8Bytes : kTile4Bytes;
-    constexpr int soff = k8 ? kScale8Off : kScale4Off;
+    constexpr bool mx = (TYPE == QMM_MXFP4);            // 17-byte blocks: byte access only
+    constexpr int bb = k8 ? kBlock8Bytes : (mx ? kBlockMxBytes : kBlock4Bytes);
+    constexpr int ts = TileFmt<TYPE>::kBytes;
+    constexpr int soff = TileFmt<TYPE>::kScaleOff;
     const int64_t total = n_tiles * 32;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t tile = i >> 5;
@@ -32,7 +33,8 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
 #pragma unroll
                 for (int cp = 0; cp < 16; ++cp) t[cp * 32 + r] = 0;
             }
-            *reinterpret_cast<uint16_t *>(t + soff + 2 * r) = 0;
+            if (mx) t[soff + r] = 0;
+            else *reinterpret_cast<uint16_t *>(t + soff + 2 * r) = 0;
             continue;
         }
         const uint8_t *blk = flat + (n * n_k_tiles + kt) * bb;
@@ -44,7 +46,8 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
         } else {
             uint32_t qs[8];                             // 16 nibble bytes as 8 halfwords
 #pragma unroll
-            for (int h = 0; h < 8; ++h) qs[h] = ld_u16(blk + 2 + 2 * h);
+            for (int h = 0; h < 8; ++h)
+                qs[h] = mx ? ((uint32_t)blk[1 + 2 * h] | ((uint32_t)blk[2 + 2 * h] << 8)) : ld_u16(blk + 2 + 2 * h);
 #pragma unroll
             for (int cp = 0; cp < 16; ++cp) {
                 // element e: byte e&15 of the block, low nibble for e < 16, high nibble otherwise
@@ -56,7 +59,8 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
                 t[cp * 32 + r] = (uint8_t)(c0 | (c1 << 4));
             }
         }
-        *reinterpret_cast<uint16_t *>(t + soff + 2 * r) = (uint16_t)ld_u16(blk);
+        if (mx) t[soff + r] = blk[0];                   // the row's E8M0 exponent
+        else *reinterpret_cast<uint16_t *>(t + soff + 2 * r) = (uint16_t)ld_u16(blk);
     }
     // The decode matmul streams tiles before it waits for the kernel before it on the stream, so the
     // tiles must be visible device-wide by the time this grid's blocks have exited.
@@ -67,15 +71,28 @@ template <int TYPE>
 __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t *__restrict__ tiled, int64_t n_k_tiles, int64_t N,
                                                      uint8_t *__restrict__ flat) {
     constexpr bool k8 = (TYPE == QMM_Q8_0);
-    constexpr int bb = k8 ? kBlock8Bytes : kBlock4Bytes;
-    constexpr int ts = k8 ? kTile8Bytes : kTile4Bytes;
-    constexpr int soff = k8 ? kScale8Off : kScale4Off;
+    constexpr bool mx = (TYPE == QMM_MXFP4);
+    constexpr int bb = k8 ? kBlock8Bytes : (mx ? kBlockMxBytes : kBlock4Bytes);
+    constexpr int ts = TileFmt<TYPE>::kBytes;
+    constexpr int soff = TileFmt<TYPE>::kScaleOff;
     const int64_t total = N * n_k_tiles;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = i / n_k_tiles, kt = i - n * n_k_tiles;
         const int64_t ct = n >> 5;
         const int r = (int)(n & 31);
         const uint8_t *t = tiled + (ct * n_k_tiles + kt) * ts;
+        if (mx) {
+            uint8_t *b8 = flat + i * bb;
+            b8[0] = t[soff + r];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                // element j is the low nibble of byte j, element j + 16 its high nibble
+                const uint32_t lo = (t[(j >> 1) * 32 + r] >> (4 * (j & 1))) & 15;
+                const uint32_t hi = (t[((j + 16) >> 1) * 32 + r] >> (4 * (j & 1))) & 15;
+                b8[1 + j] = (uint8_t)(lo | (hi << 4));
+            }
+            continue;
+        }
         uint16_t *blk = reinterpret_cast<uint16_t *>(flat + i * bb);
         blk[0] = (uint16_t)ld_u16(t + soff + 2 * r);
         if (k8) {
@@ -116,6 +133,7 @@ cudaError_t launch_repack(qmm_type t, const uint8_t *flat, int64_t K, int64_t N,
     switch (t) {
         case QMM_Q4_0: repack_kernel<QMM_Q4_0><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
         case QMM_IQ4_NL: repack_kernel<QMM_IQ4_NL><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
+        case QMM_MXFP4: repack_kernel<QMM_MXFP4><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
         default: repack_kernel<QMM_Q8_0><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
     }
     return cudaGetLastError();
@@ -128,6 +146,7 @@ cudaError_t launch_unpack(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N
     switch (t) {
         case QMM_Q4_0: unpack_kernel<QMM_Q4_0><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
         case QMM_IQ4_NL: unpack_kernel<QMM_IQ4_NL><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
+        case QMM_MXFP4: unpack_kernel<QMM_MXFP4><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
         default: unpack_kernel<QMM_Q8_0><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
     }
     return cudaGetLastError();

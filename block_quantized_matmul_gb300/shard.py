@@ -23,8 +23,11 @@ class Shard:
     byte_len: int       # bytes of this rank's tiles
 
 
+TILE_BYTES = {"q4_0": 576, "iq4_nl": 576, "q8_0": 1088, "mxfp4": 544}
+
+
 def tile_bytes(type_: str) -> int:
-    return 1088 if type_ == "q8_0" else 576
+    return TILE_BYTES[type_]
 
 
 def col_tile_range(n_col_tiles: int, rank: int, world: int) -> tuple[int, int]:

@@ -51,6 +51,18 @@ def test_sizes(L):
     assert qmm.tiled_size("q4_0", 64, 0) == 0 and qmm.tiled_size(7, 64, 64) == 0
     assert L.qmm_tile_size(9) == 0
     assert qmm.decode_max_m() >= 8
+    # MXFP4: 544-byte tiles of 32 rows x 17-byte blocks
+    assert qmm.tile_size("mxfp4") == 544 and qmm.block_size("mxfp4") == 17
+    assert qmm.tiled_size("mxfp4", 4096, 14336) == 448 * 128 * 544
+    assert qmm.flat_size("mxfp4", 64, 33) == 33 * 2 * 17
+
+
+def test_mxfp4_flat_blocks_need_no_alignment(L):
+    # 17-byte blocks are read byte by byte: an odd flat pointer is accepted for MXFP4 (the call then
+    # fails only on the too-large K, before any launch), but not for the 18-byte formats
+    assert L.qmm_repack(3, P + 1, 48, 64, P, None) == INVALID
+    assert L.qmm_repack(0, P + 1, 64, 64, P, None) == MISALIGNED
+    assert L.qmm_repack(3, P, 64, 64, P + 8, None) == MISALIGNED
 
 
 def test_iq4nl_table_matches_the_oracle(L, orc):
@@ -104,7 +116,7 @@ def test_quantize_act_argument_errors(L):
 def test_repack_and_quantize_weight_argument_errors(L):
     assert L.qmm_repack(0, P, 48, 64, P, None) == INVALID
     assert L.qmm_repack(0, None, 64, 64, P, None) == INVALID
-    assert L.qmm_repack(3, P, 64, 64, P, None) == UNSUPPORTED
+    assert L.qmm_repack(6, P, 64, 64, P, None) == UNSUPPORTED
     assert L.qmm_repack(0, P + 1, 64, 64, P, None) == MISALIGNED
     assert L.qmm_repack(0, P, 64, 64, P + 8, None) == MISALIGNED
     assert L.qmm_unpack(1, P + 8, 64, 64, P, None) == MISALIGNED

@@ -55,7 +55,8 @@ def _worker(rank, world, port, type_, K, N, M, out):
         dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("type_,K,N,M", [("q4_0", 64, 100, 3), ("q8_0", 96, 33, 2), ("iq4_nl", 32, 31, 1)])
+@pytest.mark.parametrize("type_,K,N,M", [("q4_0", 64, 100, 3), ("q8_0", 96, 33, 2), ("iq4_nl", 32, 31, 1),
+                                         ("mxfp4", 64, 70, 2)])
 def test_two_rank_column_shards_reassemble_the_product(type_, K, N, M):
     import torch.multiprocessing as mp
 
@@ -86,3 +87,11 @@ def test_shard_ranges():
     assert (last.ct0, last.ct1, last.n0, last.n_local) == (2, 3, 64, 6)
     with pytest.raises(ValueError):
         shard.shard("q4_0", 48, 10, 0, 1)
+    for t in ("q4_0", "q8_0", "iq4_nl", "mxfp4"):
+        assert shard.tile_bytes(t) == orc_tile_bytes(t)
+
+
+def orc_tile_bytes(t):
+    import oracle
+
+    return oracle.tile_bytes(t)
