@@ -7,7 +7,7 @@ it, and it shares no code with the product: the arithmetic lives in ``oracle/ora
 ``oracle.build()``; this module only marshals numpy arrays through ctypes.
 
 What it follows ("Hexagon backend developer details", "Tiled Weight Formats"): the tile grid of
-"Tile Dimensions and Grid Layout" and the Q4_0 / Q8_0 / IQ4_NL / MXFP4 tile byte layouts of
+"Tile Dimensions and Grid Layout" and the Q4_0 / Q8_0 / IQ4_NL / MXFP4 / Q4_1 tile byte layouts of
 "Block-32 Quantized Formats".  The readings taken where the pages are silent are listed in ``oracle.c``.
 """
 from __future__ import annotations
@@ -19,8 +19,8 @@ import threading
 
 import numpy as np
 
-Q4_0, Q8_0, IQ4_NL, MXFP4 = 0, 1, 2, 3
-TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL, "mxfp4": MXFP4}
+Q4_0, Q8_0, IQ4_NL, MXFP4, Q4_1 = 0, 1, 2, 3, 4
+TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL, "mxfp4": MXFP4, "q4_1": Q4_1}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")

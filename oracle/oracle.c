@@ -14,7 +14,9 @@
  *     1024+2*row); IQ4_NL dequantizes through a 16-entry non-linear table times the row scale.
  *     The MXFP4 544-byte tile keeps the Q4_0 nibble layout for 4-bit E2M1 codes and stores one E8M0
  *     exponent byte per row at 512+row; it dequantizes as the FP4 value of the code times the
- *     power-of-two fp16 scale whose bits are clamp(e - 112, 0, 30) << 10.
+ *     power-of-two fp16 scale whose bits are clamp(e - 112, 0, 30) << 10.  The Q4_1 640-byte tile
+ *     keeps the Q4_0 nibble layout and stores the FP16 pair (d, m) of a row at 512+4*row and
+ *     514+4*row.
  *
  * Readings where the pages are silent (each listed in the design notes):
  *   - Flat (untiled) rows are GGML blocks: Q4_0 / IQ4_NL = {fp16 d; u8 qs[16]} (18 B), element j in
@@ -28,6 +30,10 @@
  *     IQ4_NL takes d = m/lut[0], d16 = fp16(d), and for each x the index i minimising
  *     |x - f32(d16)*lut[i]| (lowest index on ties).
  *   - The IQ4_NL table itself is not printed on the pages; callers pass the table in.
+ *   - Q4_1: "m (min)" read as the GGML affine rule, weight = d*q + m; flat block {fp16 d; fp16 m;
+ *     u8 qs[16]} (20 B, nibble order as Q4_0).  So a block adds d_a * m_w * sum_j a_q[j] to the
+ *     product.  Quantizer (test data): min and max of the block, d = (max - min)/15, id = d ? 1/d : 0,
+ *     q = min(15, trunc((x - min)*id + 0.5)) (0 for NaN), d and m = min stored as fp16.
  *   - MXFP4: the flat block is {u8 e; u8 qs[16]} (17 B, nibble order as Q4_0); the FP4 table is the
  *     OCP E2M1 code set {0, 0.5, 1, 1.5, 2, 3, 4, 6} with a sign bit (code = s<<3 | e<<1 | m).
  *     Integer weights are twice the FP4 value (0..12 with sign) and the block scale is half the
@@ -45,7 +51,7 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORC_Q4_0 = 0, ORC_Q8_0 = 1, ORC_IQ4_NL = 2, ORC_MXFP4 = 3 };
+enum { ORC_Q4_0 = 0, ORC_Q8_0 = 1, ORC_IQ4_NL = 2, ORC_MXFP4 = 3, ORC_Q4_1 = 4 };
 
 /* OCP Microscaling FP4 (E2M1): code = sign<<3 | exponent<<1 | mantissa; value = 0.5 * mantissa for
  * exponent 0, else 2^(exponent-1) * (1 + mantissa/2).  Twice the value, as an integer. */
@@ -137,6 +143,7 @@ int64_t orc_block_bytes(int type)
     if (type == ORC_Q4_0 || type == ORC_IQ4_NL) return 18;  /* fp16 d + 16 bytes of nibbles */
     if (type == ORC_Q8_0) return 34;                        /* fp16 d + 32 int8 */
     if (type == ORC_MXFP4) return 17;                       /* E8M0 e + 16 bytes of nibbles */
+    if (type == ORC_Q4_1) return 20;                        /* fp16 d + fp16 m + 16 bytes of nibbles */
     return 0;
 }
 
@@ -145,6 +152,7 @@ int64_t orc_tile_bytes(int type)
     if (type == ORC_Q4_0 || type == ORC_IQ4_NL) return 576;  /* 512 quant bytes + 32 fp16 scales */
     if (type == ORC_Q8_0) return 1088;                       /* 1024 quant bytes + 32 fp16 scales */
     if (type == ORC_MXFP4) return 544;                       /* 512 quant bytes + 32 E8M0 exponents */
+    if (type == ORC_Q4_1) return 640;                        /* 512 quant bytes + 32 fp16 (d, m) pairs */
     return 0;
 }
 
@@ -165,7 +173,7 @@ static uint16_t load_u16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8
 static void store_u16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (uint8_t)(v >> 8); }
 
 /* Bytes before the quants in a flat block: the fp16 scale, or MXFP4's one exponent byte. */
-static int flat_head(int type) { return type == ORC_MXFP4 ? 1 : 2; }
+static int flat_head(int type) { return type == ORC_MXFP4 ? 1 : (type == ORC_Q4_1 ? 4 : 2); }
 
 static int flat_code(int type, const uint8_t *blk, int j)
 {
@@ -190,11 +198,19 @@ static int weight_int(int type, int code, const int8_t *lut)
     if (type == ORC_Q4_0) return code - 8;
     if (type == ORC_Q8_0) return code;
     if (type == ORC_MXFP4) return e2m1_twice(code & 15);
+    if (type == ORC_Q4_1) return code;
     return (int)lut[code & 15];
 }
 
-/* Scale of a block's integer weights: the fp16 scale, or for MXFP4 half the fp16 power of two made
- * from the exponent byte (the integer weights are twice the FP4 values). */
+/* Scale of a block's integer weights: the fp16 scale (Q4_1: d), or for MXFP4 half the fp16 power of
+ * two made from the exponent byte (the integer weights are twice the FP4 values). */
+/* The additive min of a block (Q4_1 only; 0 otherwise). */
+static double block_min(int type, const uint8_t *scale_bytes)
+{
+    if (type == ORC_Q4_1) return (double)orc_f16_to_f32(load_u16(scale_bytes + 2));
+    return 0.0;
+}
+
 static double block_scale(int type, const uint8_t *scale_bytes)
 {
     if (type == ORC_MXFP4) return 0.5 * (double)orc_f16_to_f32(orc_e8m0_to_f16_bits(scale_bytes[0]));
@@ -269,6 +285,28 @@ static void quantize_block_iq4_nl(const float *x, const int8_t *lut, uint8_t *co
     }
 }
 
+/* Q4_1 rule: d = (max - min)/15, q = min(15, trunc((x - min)*(1/d) + 0.5)), m = min. */
+static void quantize_block_q4_1(const float *x, uint8_t *codes, uint16_t *d16, uint16_t *m16)
+{
+    float mn = INFINITY, mx = -INFINITY;
+    for (int j = 0; j < 32; ++j) {
+        if (x[j] < mn) mn = x[j];
+        if (x[j] > mx) mx = x[j];
+    }
+    float d = (mx - mn) / 15.0f;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    for (int j = 0; j < 32; ++j) {
+        float v = (x[j] - mn) * id + 0.5f;   /* three roundings: difference, product, sum (no FMA) */
+        int c;
+        if (!(v >= 0.0f)) c = 0;             /* NaN */
+        else if (v >= 15.0f) c = 15;
+        else c = (int)v;                     /* truncation toward zero */
+        codes[j] = (uint8_t)c;
+    }
+    *d16 = orc_f32_to_f16(d);
+    *m16 = orc_f32_to_f16(mn);
+}
+
 /* MXFP4 rule: e = floor(log2 amax) - 2 + 127 (so that amax / 2^(e-127) lies in [4, 8)), 0 for an
  * all-zero block, clamped to 0..254; then the code whose level s * fp4(code) is nearest to x, where s
  * is the dequantizing scale (the pages' fp16 power of two), lowest code on ties. */
@@ -313,6 +351,12 @@ void orc_quantize_rows(int type, const float *w, int64_t N, int64_t K, const int
                 int8_t q[32];
                 orc_quantize_block_q8_0(x, q, &d16);
                 for (int j = 0; j < 32; ++j) flat_set_code(type, blk, j, q[j]);
+            } else if (type == ORC_Q4_1) {
+                uint8_t codes[32];
+                uint16_t m16;
+                quantize_block_q4_1(x, codes, &d16, &m16);
+                for (int j = 0; j < 32; ++j) flat_set_code(type, blk, j, codes[j]);
+                store_u16(blk + 2, m16);
             } else if (type == ORC_MXFP4) {
                 uint8_t codes[32], e;
                 quantize_block_mxfp4(x, codes, &e);
@@ -337,9 +381,9 @@ void orc_dequantize_flat(int type, const uint8_t *flat, int64_t N, int64_t K, co
     for (int64_t n = 0; n < N; ++n)
         for (int64_t b = 0; b < nb; ++b) {
             const uint8_t *blk = flat + (n * nb + b) * bb;
-            double d = block_scale(type, blk);
+            double d = block_scale(type, blk), mn = block_min(type, blk);
             for (int j = 0; j < 32; ++j)
-                out[n * K + b * 32 + j] = d * (double)weight_int(type, flat_code(type, blk, j), lut);
+                out[n * K + b * 32 + j] = d * (double)weight_int(type, flat_code(type, blk, j), lut) + mn;
         }
 }
 
@@ -372,6 +416,8 @@ void orc_repack(int type, const uint8_t *flat, int64_t K, int64_t N, uint8_t *ti
                 }
                 if (type == ORC_MXFP4) {
                     tile[scale_off + r] = blk[0];            /* one exponent byte per row */
+                } else if (type == ORC_Q4_1) {
+                    for (int i = 0; i < 4; ++i) tile[scale_off + 4 * r + i] = blk[i];   /* d, m */
                 } else {
                     tile[scale_off + 2 * r + 0] = blk[0];
                     tile[scale_off + 2 * r + 1] = blk[1];
@@ -394,6 +440,8 @@ void orc_unpack(int type, const uint8_t *tiled, int64_t K, int64_t N, uint8_t *f
             memset(blk, 0, (size_t)bb);
             if (type == ORC_MXFP4) {
                 blk[0] = tile[scale_off + r];
+            } else if (type == ORC_Q4_1) {
+                for (int i = 0; i < 4; ++i) blk[i] = tile[scale_off + 4 * r + i];
             } else {
                 blk[0] = tile[scale_off + 2 * r + 0];
                 blk[1] = tile[scale_off + 2 * r + 1];
@@ -433,7 +481,14 @@ static double tiled_scale(int type, const uint8_t *tiled, int64_t n_k_tiles, int
     int r = (int)(n % 32);
     const uint8_t *tile = tiled + orc_tile_index(ct, kt, n_k_tiles) * orc_tile_bytes(type);
     int64_t scale_off = (type == ORC_Q8_0) ? 1024 : 512;
-    return block_scale(type, tile + scale_off + (type == ORC_MXFP4 ? r : 2 * r));
+    return block_scale(type, tile + scale_off + (type == ORC_MXFP4 ? r : (type == ORC_Q4_1 ? 4 * r : 2 * r)));
+}
+
+static double tiled_min(int type, const uint8_t *tiled, int64_t n_k_tiles, int64_t n, int64_t kt)
+{
+    if (type != ORC_Q4_1) return 0.0;
+    const uint8_t *tile = tiled + orc_tile_index(n / 32, kt, n_k_tiles) * orc_tile_bytes(type);
+    return block_min(type, tile + 512 + 4 * (n % 32));
 }
 
 /* ------------------------------------------------------------------------------------------------
@@ -460,18 +515,23 @@ static void one_output(int type, const uint8_t *tiled, int64_t K, const int8_t *
     int64_t n_k_tiles = K / 32;
     double acc = 0.0, bacc = 0.0;
     for (int64_t b = 0; b < n_k_tiles; ++b) {
-        int64_t s = 0, sabs = 0;
+        int64_t s = 0, sabs = 0, asum = 0;
+        double dw = tiled_scale(type, tiled, n_k_tiles, n, b);
+        double mw = tiled_min(type, tiled, n_k_tiles, n, b);
+        double da = (double)orc_f16_to_f32(a_d[m * n_k_tiles + b]);
+        double babs = 0.0;
         for (int j = 0; j < 32; ++j) {
             int64_t k = b * 32 + j;
             int64_t w = tiled_weight(type, tiled, n_k_tiles, n, k, lut);
             int64_t a = a_q[m * K + k];
             s += w * a;
+            asum += a;
             sabs += (w * a < 0) ? -(w * a) : (w * a);
+            babs += fabs(dw * (double)w + mw) * fabs((double)a);   /* |dequantized weight| * |a_q| */
         }
-        double dw = tiled_scale(type, tiled, n_k_tiles, n, b);
-        double da = (double)orc_f16_to_f32(a_d[m * n_k_tiles + b]);
-        acc += dw * da * (double)s;
-        bacc += fabs(dw * da) * (double)sabs;
+        /* sum_j (dw*w_j + mw) * da * a_j = da * (dw * S_b + mw * sum_j a_j) */
+        acc += dw * da * (double)s + mw * da * (double)asum;
+        bacc += (type == ORC_Q4_1) ? fabs(da) * babs : fabs(dw * da) * (double)sabs;
     }
     *y = acc;
     *bound = bacc;

@@ -12,7 +12,7 @@ import pytest
 from block_quantized_matmul_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-TYPES = ["q4_0", "q8_0", "iq4_nl", "mxfp4"]
+TYPES = ["q4_0", "q8_0", "iq4_nl", "mxfp4", "q4_1"]
 
 
 # ---------------------------------------------------------------------------------------------
@@ -46,6 +46,7 @@ def test_tile_and_block_sizes(orc):
     assert 32 * orc.block_bytes("q4_0") == 576 and 32 * orc.block_bytes("iq4_nl") == 576
     assert 32 * orc.block_bytes("q8_0") == 1088
     assert orc.tile_bytes("mxfp4") == 544 and 32 * orc.block_bytes("mxfp4") == 544
+    assert orc.tile_bytes("q4_1") == 640 and 32 * orc.block_bytes("q4_1") == 640
 
 
 @pytest.mark.parametrize("K,N,type_,tiles", [
@@ -95,6 +96,9 @@ def test_one_hot_tile_position(orc, case):
     if type_ == "mxfp4":
         flat[row, 0] = 0x7B                    # E8M0 exponent byte of that row
         expect[sbyte] = 0x7B
+    elif type_ == "q4_1":
+        flat[row, 0:4] = (0x34, 0x12, 0x78, 0x56)    # fp16 d = 0x1234, m = 0x5678 on that row
+        expect[sbyte:sbyte + 4] = (0x34, 0x12, 0x78, 0x56)
     else:
         flat[row, 0:2] = (0x34, 0x12)          # fp16 scale bits 0x1234 on that row
         expect[sbyte], expect[sbyte + 1] = 0x34, 0x12
@@ -125,6 +129,9 @@ def test_repack_unpack_roundtrip_and_padding(orc, type_, K, N):
                 elif type_ == "mxfp4":
                     assert all(t[cp * 32 + r] == 0 for cp in range(16))
                     assert t[512 + r] == 0
+                elif type_ == "q4_1":
+                    assert all(t[cp * 32 + r] == 0 for cp in range(16))
+                    assert not t[512 + 4 * r:516 + 4 * r].any()
                 else:
                     assert all(t[cp * 32 + r] == 0 for cp in range(16))
                     assert t[512 + 2 * r] == 0 and t[513 + 2 * r] == 0
@@ -221,6 +228,12 @@ def test_weight_quantizer_error_bound(orc, type_):
     elif type_ == "q4_0":
         step = amax / 8
         assert np.all(np.abs(dq - blocks) <= step * (1.0 + 8 * 2.0 ** -11) + 1e-12)
+    elif type_ == "q4_1":
+        # affine: step (max - min)/15, rounding to nearest (<= step/2) plus the fp16 roundings of d and m
+        mn = blocks.min(axis=2, keepdims=True)
+        mx = blocks.max(axis=2, keepdims=True)
+        step = (mx - mn) / 15
+        assert np.all(np.abs(dq - blocks) <= step * (0.5 + 16 * 2.0 ** -11) + np.abs(mn) * 2.0 ** -11 + 1e-12)
     elif type_ == "mxfp4":
         # scale 2^(floor(log2 amax) - 2): levels up to 6 * scale cover amax < 8 * scale except the top
         # (saturation at 6 * scale); the widest gap below 6 is 2 * scale (between 4 and 6)
@@ -399,3 +412,37 @@ def test_mxfp4_quantizer_exact_values_and_nearest_level(orc):
     # an all-zero block gets exponent 0 and code 0 everywhere
     z = orc.quantize_rows("mxfp4", np.zeros((1, 32), np.float32))
     assert not z.any()
+
+
+# ---------------------------------------------------------------------------------------------
+# Q4_1: weight = d * q + m with the (d, m) pair of the row
+# ---------------------------------------------------------------------------------------------
+def test_q4_1_dequant_is_affine(orc):
+    rng = np.random.default_rng(17)
+    flat = rng.integers(0, 256, size=(8, 3 * 20), dtype=np.uint8)
+    for n in range(8):                     # keep the fp16 pairs finite
+        for b in range(3):
+            flat[n, b * 20 + 1] &= 0x3F
+            flat[n, b * 20 + 3] &= 0xBF
+    deq = orc.dequantize_flat("q4_1", flat, 8, 96)
+    for n in range(8):
+        for b in range(3):
+            blk = flat[n, b * 20:(b + 1) * 20]
+            d, m = np.array([int(blk[0]) | (int(blk[1]) << 8), int(blk[2]) | (int(blk[3]) << 8)], np.uint16).view(np.float16)
+            for j in range(32):
+                q = (blk[4 + j] & 15) if j < 16 else (blk[4 + j - 16] >> 4)
+                assert deq[n, b * 32 + j] == float(d) * q + float(m)
+
+
+def test_q4_1_quantizer_hits_the_block_extremes(orc):
+    w = synth.weights(16, 128, seed=23)
+    flat = orc.quantize_rows("q4_1", w)
+    for n in range(16):
+        for b in range(4):
+            blk = flat[n, b * 20:(b + 1) * 20]
+            x = w[n, b * 32:(b + 1) * 32]
+            d, m = np.array([int(blk[0]) | (int(blk[1]) << 8), int(blk[2]) | (int(blk[3]) << 8)], np.uint16).view(np.float16)
+            assert m == np.float16(x.min())                    # m is the block minimum, rounded to fp16
+            assert d == np.float16((np.float32(x.max()) - np.float32(x.min())) / np.float32(15))
+            codes = [(blk[4 + j] & 15) if j < 16 else (blk[4 + j - 16] >> 4) for j in range(32)]
+            assert codes[int(np.argmin(x))] == 0 and codes[int(np.argmax(x))] == 15
