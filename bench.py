@@ -38,7 +38,9 @@ HEADLINE = ("q8_0", 4096, 14336, 1)
 OTHERS = [("q4_0", 4096, 4096, 1), ("iq4_nl", 4096, 4096, 8), ("q8_0", 4096, 128256, 1),
           ("q4_0", 4096, 14336, 512), ("q8_0", 4096, 128256, 128),
           # MXFP4 tiles (the next format of the pages' tile family), decode and prefill shapes
-          ("mxfp4", 4096, 14336, 1), ("mxfp4", 4096, 14336, 512)]
+          ("mxfp4", 4096, 14336, 1), ("mxfp4", 4096, 14336, 512),
+          # Q4_1 tiles (d and m per row)
+          ("q4_1", 4096, 14336, 1), ("q4_1", 4096, 14336, 512)]
 METRIC = "tiled Q4_0/Q8_0 matvec weight GB/s (% HBM peak); prefill int8 GEMM TOPS"
 
 

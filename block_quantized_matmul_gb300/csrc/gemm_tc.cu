@@ -246,14 +246,15 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t &lo, uint32_t 
     hi = h2_bits(__hsub2(bits_h2(__byte_perm(x, 0x64646464u, 0x4342u)), bias));
 }
 
-// Q4_0 nibble byte (lo = even column, hi = odd column) at byte position I -> half2(lo-8, hi-8).
-template <int I>
+// 4-bit nibble byte (lo = even column, hi = odd column) at byte position I -> half2(lo-OFF, hi-OFF)
+// (OFF = 8 for Q4_0, 0 for Q4_1), exact.
+template <int I, int OFF = 8>
 __device__ __forceinline__ uint32_t q4_byte_to_h2(uint32_t w) {
     const uint32_t y = __byte_perm(w, 0u, 0x4040u | (I << 8) | I);
     uint32_t h;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(y), "r"(0x00F0000Fu), "r"(0x64006400u));
     return h2_bits(__hfma2(bits_h2(h), __halves2half2(__float2half_rn(1.0f), __float2half_rn(0.0625f)),
-                           __halves2half2(__float2half_rn(-1032.0f), __float2half_rn(-72.0f))));
+                           __halves2half2(__float2half_rn(-1024.0f - OFF), __float2half_rn(-64.0f - OFF))));
 }
 
 // Byte offset of (row, 16-byte chunk) in a 128 x 128-byte K-major operand with the 128-byte swizzle
@@ -293,9 +294,12 @@ struct GemmPlan {
     static constexpr bool kPrep = ACT == kActPrepared;
     static constexpr int TS = TileFmt<TYPE>::kBytes;
     static constexpr int kWTiles = 8 * TS;                                   // [4 ct][2 kt] raw tiles
-    static constexpr int kWTok = kPrep ? 2 * BN * 2 : BN * 64;              // fp16 scales or int8 rows
+    static constexpr bool kAff = TileFmt<TYPE>::kAffine;                   // Q4_1: + m_w * d_a * sum(a_q)
+    // token data of a pair: fp16 scales (+ fp32 d_a * sum(a_q) for Q4_1), or the int8 rows
+    static constexpr int kWTok = kPrep ? 2 * BN * 2 + (kAff ? 2 * BN * 4 : 0) : BN * 64;
     static constexpr int kWStageBytes = (kWTiles + kWTok + 127) / 128 * 128;
-    static constexpr int kScaleBytes = 2 * 2 * 128 * 4;                     // d_w[2][128], d_a[2][128]
+    // d_w[2][128], d_a[2][128] (+ Q4_1: m_w[2][128], d_a * sum(a_q)[2][128])
+    static constexpr int kScaleBytes = (kAff ? 4 : 2) * 2 * 128 * 4;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOp2Bytes;                                  // int8 variant only
     static constexpr int kOffScale = kPrep ? kOp2Bytes : 2 * kOp2Bytes;
@@ -324,7 +328,7 @@ struct GemmPlan {
 template <int TYPE, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const __grid_constant__ CUtensorMap act_map,
-            const __grid_constant__ CUtensorMap da_map) {
+            const __grid_constant__ CUtensorMap da_map, const __grid_constant__ CUtensorMap ca_map) {
     using P = GemmPlan<TYPE, ACT>;
     constexpr int TS = P::TS;
     constexpr int SOFF = TileFmt<TYPE>::kScaleOff;
@@ -398,8 +402,12 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                 const uint32_t dst = smem_u32(w_s + s * P::kWStageBytes);
                 mbar_arrive_expect_tx(fb, (uint32_t)(P::kWTiles + P::kWTok));
                 tma_load_3d(dst, &w_map, 0, 2 * pr, (int)ct0, fb);
-                if (P::kPrep) tma_load_2d(dst + P::kWTiles, &da_map, (int)m0, 2 * pr, fb);
-                else tma_load_2d(dst + P::kWTiles, &act_map, 64 * pr, (int)m0, fb);
+                if constexpr (P::kPrep) {
+                    tma_load_2d(dst + P::kWTiles, &da_map, (int)m0, 2 * pr, fb);
+                    if constexpr (P::kAff) tma_load_2d(dst + P::kWTiles + 2 * BN * 2, &ca_map, (int)m0, 2 * pr, fb);
+                } else {
+                    tma_load_2d(dst + P::kWTiles, &act_map, 64 * pr, (int)m0, fb);
+                }
             }
             __syncwarp();
             issued = pr + 1;
@@ -498,7 +506,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                 for (int j = 0; j < 2; ++j) {
                     // -- weight row c of block j: 32 columns -> 16 half2 in column order --
                     uint32_t h[16];
-                    float dw = 0.0f;
+                    float dw = 0.0f, mw = 0.0f;
                     if (w_ok) {
                         const uint8_t *tile = raw + (q * 2 + j) * TS;
                         if constexpr (TYPE == QMM_Q8_0) {
@@ -514,11 +522,19 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                             for (int cp = 0; cp < 16; ++cp) {
                                 const uint32_t b = tile[cp * 32 + tr];
                                 if constexpr (TYPE == QMM_Q4_0) h[cp] = q4_byte_to_h2<0>(b);
+                                else if constexpr (TYPE == QMM_Q4_1) h[cp] = q4_byte_to_h2<0, 0>(b);
                                 else h[cp] = lut_lane[b * kLutCopies];
                             }
                         }
-                        if constexpr (TileFmt<TYPE>::kE8M0) dw = mx_half_scale(tile[SOFF + tr]);
-                        else dw = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(tile + SOFF + 2 * tr)));
+                        if constexpr (TileFmt<TYPE>::kE8M0) {
+                            dw = mx_half_scale(tile[SOFF + tr]);
+                        } else if constexpr (P::kAff) {
+                            const __half2 dm = bits_h2(*reinterpret_cast<const uint32_t *>(tile + SOFF + 4 * tr));
+                            dw = __low2float(dm);
+                            mw = __high2float(dm);
+                        } else {
+                            dw = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t *>(tile + SOFF + 2 * tr)));
+                        }
                     } else {
 #pragma unroll
                         for (int cp = 0; cp < 16; ++cp) h[cp] = 0u;
@@ -528,10 +544,13 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                         *reinterpret_cast<uint4 *>(op + P::kOffA + sw128_off(c, 4 * j + ch)) =
                             make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
                     sc[j * 128 + c] = dw;
+                    if constexpr (P::kAff) sc[512 + j * 128 + c] = mw;
                     // -- token row c of block j --
                     uint16_t da;
+                    float ca = 0.0f;                       // Q4_1: d_a * sum(a_q) of the block
                     if constexpr (P::kPrep) {
                         da = *reinterpret_cast<const uint16_t *>(raw + P::kWTiles + 2 * (j * BN + c));
+                        if constexpr (P::kAff) ca = *reinterpret_cast<const float *>(raw + P::kWTiles + 2 * BN * 2 + 4 * (j * BN + c));
                     } else {
                         da = da_cur[2 * u + j];
                         const uint4 v0 = *reinterpret_cast<const uint4 *>(raw + P::kWTiles + c * 64 + 32 * j);
@@ -545,8 +564,15 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                             *reinterpret_cast<uint4 *>(op + P::kOffB + sw128_off(c, 4 * j + ch)) =
                                 make_uint4(a0, a1, a2, a3);
                         }
+                        if constexpr (P::kAff) {
+                            int asum = 0;
+#pragma unroll
+                            for (int wi = 0; wi < 8; ++wi) asum = __dp4a((int)wv[wi], 0x01010101, asum);
+                            ca = __fmul_rn(__half2float(__ushort_as_half(da)), (float)asum);   // exact (23 bits)
+                        }
                     }
                     sc[256 + j * 128 + c] = __half2float(__ushort_as_half(da));
+                    if constexpr (P::kAff) sc[768 + j * 128 + c] = ca;
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&op_full[os]));
@@ -602,6 +628,17 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                     ffma2_acc(y[16 * cc + 4 * e], y[16 * cc + 4 * e + 1], t0, dw2);
                     ffma2_acc(y[16 * cc + 4 * e + 2], y[16 * cc + 4 * e + 3], t1, dw2);
                 }
+                if constexpr (P::kAff) {
+                    // + m_w * (d_a * sum(a_q)) of the block, per token column
+                    const float4 *ca4 = reinterpret_cast<const float4 *>(sc + 768 + j * 128 + 64 * half);
+                    const unsigned long long mw2 = pack2f(sc[512 + j * 128 + row], sc[512 + j * 128 + row]);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 ca = ca4[4 * cc + e];
+                        ffma2_acc(y[16 * cc + 4 * e], y[16 * cc + 4 * e + 1], pack2f(ca.x, ca.y), mw2);
+                        ffma2_acc(y[16 * cc + 4 * e + 2], y[16 * cc + 4 * e + 3], pack2f(ca.z, ca.w), mw2);
+                    }
+                }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&tm_empty[ts]));
@@ -632,11 +669,12 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
     }
 }
 
-// Prepares the token operand for kActPrepared: a_h[m][k] = fp16(a_q[m][k]) (exact) and
-// a_dT[kt][m] = a_d[m][kt] for m < M_pad (zero for m >= M).
+// Prepares the token operand for kActPrepared: a_h[m][k] = fp16(a_q[m][k]) (exact),
+// a_dT[kt][m] = a_d[m][kt] for m < M_pad (zero for m >= M) and, if cA is given (Q4_1),
+// cA[kt][m] = fp32(a_d[m][kt]) * sum_j a_q[m][32kt + j] (exact: at most 23 significant bits).
 __global__ void __launch_bounds__(256) prepare_act_kernel(const int8_t *__restrict__ a_q, const uint16_t *__restrict__ a_d,
                                                           int64_t M, int64_t K, int64_t M_pad, __half *__restrict__ a_h,
-                                                          uint16_t *__restrict__ a_dT) {
+                                                          uint16_t *__restrict__ a_dT, float *__restrict__ cA) {
     const int64_t nkt = K / 32;
     const int64_t quads = M * K / 4;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -653,6 +691,20 @@ __global__ void __launch_bounds__(256) prepare_act_kernel(const int8_t *__restri
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nd; i += stride) {
         const int64_t kt = i / M_pad, m = i - kt * M_pad;
         a_dT[i] = (m < M) ? a_d[m * nkt + kt] : (uint16_t)0;
+        if (cA) {
+            float v = 0.0f;
+            if (m < M) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(a_q + m * K + kt * 32);
+                const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                int asum = 0;
+                asum = __dp4a((int)v0.x, 0x01010101, asum); asum = __dp4a((int)v0.y, 0x01010101, asum);
+                asum = __dp4a((int)v0.z, 0x01010101, asum); asum = __dp4a((int)v0.w, 0x01010101, asum);
+                asum = __dp4a((int)v1.x, 0x01010101, asum); asum = __dp4a((int)v1.y, 0x01010101, asum);
+                asum = __dp4a((int)v1.z, 0x01010101, asum); asum = __dp4a((int)v1.w, 0x01010101, asum);
+                v = __fmul_rn(__half2float(__ushort_as_half(a_d[m * nkt + kt])), (float)asum);
+            }
+            cA[i] = v;
+        }
     }
 }
 
@@ -705,7 +757,8 @@ cudaError_t make_weight_map(CUtensorMap *map, const uint8_t *tiled, int tile_byt
 }
 
 template <int TYPE, int ACT>
-cudaError_t launch_typed(const GemmParams &p, const CUtensorMap &act_map, const CUtensorMap &da_map, cudaStream_t s) {
+cudaError_t launch_typed(const GemmParams &p, const CUtensorMap &act_map, const CUtensorMap &da_map, const CUtensorMap &ca_map,
+                         cudaStream_t s) {
     using P = GemmPlan<TYPE, ACT>;
     static_assert(P::kSmem <= 227 * 1024, "shared memory plan too large");
     auto kern = gemm_kernel<TYPE, ACT>;
@@ -716,17 +769,19 @@ cudaError_t launch_typed(const GemmParams &p, const CUtensorMap &act_map, const 
     e = make_weight_map(&w_map, p.tiled, P::TS, p.nkt, p.n_col_tiles);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((p.n_col_tiles + 3) / 4), (unsigned)((p.M + BN - 1) / BN), 1);
-    kern<<<grid, kThreads, P::kSmem, s>>>(p, w_map, act_map, da_map);
+    kern<<<grid, kThreads, P::kSmem, s>>>(p, w_map, act_map, da_map, ca_map);
     return cudaGetLastError();
 }
 
 template <int ACT>
-cudaError_t dispatch(qmm_type t, const GemmParams &p, const CUtensorMap &am, const CUtensorMap &dm, cudaStream_t s) {
+cudaError_t dispatch(qmm_type t, const GemmParams &p, const CUtensorMap &am, const CUtensorMap &dm, const CUtensorMap &cm,
+                     cudaStream_t s) {
     switch (t) {
-        case QMM_Q4_0: return launch_typed<QMM_Q4_0, ACT>(p, am, dm, s);
-        case QMM_IQ4_NL: return launch_typed<QMM_IQ4_NL, ACT>(p, am, dm, s);
-        case QMM_MXFP4: return launch_typed<QMM_MXFP4, ACT>(p, am, dm, s);
-        default: return launch_typed<QMM_Q8_0, ACT>(p, am, dm, s);
+        case QMM_Q4_0: return launch_typed<QMM_Q4_0, ACT>(p, am, dm, cm, s);
+        case QMM_IQ4_NL: return launch_typed<QMM_IQ4_NL, ACT>(p, am, dm, cm, s);
+        case QMM_MXFP4: return launch_typed<QMM_MXFP4, ACT>(p, am, dm, cm, s);
+        case QMM_Q4_1: return launch_typed<QMM_Q4_1, ACT>(p, am, dm, cm, s);
+        default: return launch_typed<QMM_Q8_0, ACT>(p, am, dm, cm, s);
     }
 }
 
@@ -758,12 +813,22 @@ cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, 
                                 CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     dm = am;   // unused by this variant
-    return dispatch<kActInt8>(t, p, am, dm, s);
+    return dispatch<kActInt8>(t, p, am, dm, am, s);
 }
+
+// Workspace: fp16 a_q [M][K] | fp16 a_d transposed [K/32][M_pad] | fp32 d_a * sum(a_q) transposed
+// [K/32][M_pad] (used by Q4_1), each region 256-byte aligned.
+namespace {
+size_t ws_dT_off(int64_t M, int64_t K) { return ((size_t)M * (size_t)K * 2 + 255) / 256 * 256; }
+size_t ws_cA_off(int64_t M, int64_t K) {
+    const int64_t m_pad = (M + 7) / 8 * 8;
+    return ws_dT_off(M, K) + ((size_t)(K / 32) * (size_t)m_pad * 2 + 255) / 256 * 256;
+}
+}  // namespace
 
 size_t gemm_workspace_bytes(int64_t M, int64_t K) {
     const int64_t m_pad = (M + 7) / 8 * 8;
-    return (size_t)M * (size_t)K * 2 + (size_t)(K / 32) * (size_t)m_pad * 2 + 256;
+    return ws_cA_off(M, K) + (size_t)(K / 32) * (size_t)m_pad * 4 + 256;
 }
 
 cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
@@ -771,12 +836,14 @@ cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t 
     if ((M + BN - 1) / BN > 65535) return cudaErrorInvalidValue;
     const int64_t nkt = K / 32, m_pad = (M + 7) / 8 * 8;
     __half *a_h = static_cast<__half *>(ws);
-    uint16_t *a_dT = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + ((size_t)M * K * 2 + 255) / 256 * 256);
+    uint16_t *a_dT = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + ws_dT_off(M, K));
+    float *cA = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_cA_off(M, K));
+    const bool need_ca = t == QMM_Q4_1;
     {
         const int64_t work = M * K / 4 > nkt * m_pad ? M * K / 4 : nkt * m_pad;
         int64_t grid = (work + 255) / 256;
         if (grid > 152 * 8) grid = 152 * 8;
-        prepare_act_kernel<<<(unsigned)grid, 256, 0, s>>>(a_q, a_d, M, K, m_pad, a_h, a_dT);
+        prepare_act_kernel<<<(unsigned)grid, 256, 0, s>>>(a_q, a_d, M, K, m_pad, a_h, a_dT, need_ca ? cA : nullptr);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -788,7 +855,13 @@ cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t 
     e = make_map_2d(&dm, CU_TENSOR_MAP_DATA_TYPE_UINT16, a_dT, (uint64_t)m_pad, (uint64_t)nkt, (uint64_t)m_pad * 2, BN, 2,
                     CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
-    return dispatch<kActPrepared>(t, p, am, dm, s);
+    alignas(64) CUtensorMap cm = dm;
+    if (need_ca) {
+        e = make_map_2d(&cm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cA, (uint64_t)m_pad, (uint64_t)nkt, (uint64_t)m_pad * 4, BN, 2,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (e != cudaSuccess) return e;
+    }
+    return dispatch<kActPrepared>(t, p, am, dm, cm, s);
 }
 
 // ---------------------------------------------------------------------------------------------

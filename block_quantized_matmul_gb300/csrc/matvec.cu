@@ -190,11 +190,22 @@ __device__ __forceinline__ uint2 quantize_quarter(const MvParams &p, bool live, 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-// The scales of tile rows r0 .. r0+3 (r0 a multiple of 4) as fp32: fp16 row scales, or for MXFP4 half
-// the power of two of each row's E8M0 byte (the doubled integer codes carry the other factor 2).
+// The scales of tile rows r0 .. r0+3 (r0 a multiple of 4) as fp32: fp16 row scales (Q4_1: the d of each
+// (d, m) pair), or for MXFP4 half the power of two of each row's E8M0 byte (the doubled integer codes
+// carry the other factor 2).  row_mins: the m of Q4_1's pairs.
+template <int TYPE>
+__device__ __forceinline__ void row_mins(const uint8_t *scales, int r0, float (&m)[4]) {
+    const uint4 dm = *reinterpret_cast<const uint4 *>(scales + 4 * r0);
+    m[0] = __high2float(bits_h2(dm.x)); m[1] = __high2float(bits_h2(dm.y));
+    m[2] = __high2float(bits_h2(dm.z)); m[3] = __high2float(bits_h2(dm.w));
+}
 template <int TYPE>
 __device__ __forceinline__ void row_scales(const uint8_t *scales, int r0, float (&d)[4]) {
-    if constexpr (TileFmt<TYPE>::kE8M0) {
+    if constexpr (TileFmt<TYPE>::kAffine) {
+        const uint4 dm = *reinterpret_cast<const uint4 *>(scales + 4 * r0);    // (d, m) of 4 rows
+        d[0] = __low2float(bits_h2(dm.x)); d[1] = __low2float(bits_h2(dm.y));
+        d[2] = __low2float(bits_h2(dm.z)); d[3] = __low2float(bits_h2(dm.w));
+    } else if constexpr (TileFmt<TYPE>::kE8M0) {
         const uint32_t e4 = *reinterpret_cast<const uint32_t *>(scales + r0);
 #pragma unroll
         for (int r = 0; r < 4; ++r) d[r] = mx_half_scale((e4 >> (8 * r)) & 0xFFu);
@@ -271,7 +282,7 @@ __device__ __forceinline__ void decode_tile(const uint8_t *tile, int g, int t, u
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const uint32_t w = *reinterpret_cast<const uint32_t *>(tile + (t + 4 * q) * 32 + 4 * g);
-            if constexpr (TYPE == QMM_Q4_0) {
+            if constexpr (TileFmt<TYPE>::kNibbleInt) {
                 H[q][0] = q4_biased<0>(w);
                 H[q][1] = q4_biased<1>(w);
                 H[q][2] = q4_biased<2>(w);
@@ -288,13 +299,14 @@ __device__ __forceinline__ void decode_tile(const uint8_t *tile, int g, int t, u
 // by 16 (exact) for Q4_0, whose high nibble is decoded as 16*hi.
 template <int TYPE>
 __device__ __forceinline__ uint32_t act_pair(int a0, int a1) {
-    const float f1 = (TYPE == QMM_Q4_0) ? (float)a1 * 0.0625f : (float)a1;
+    const float f1 = TileFmt<TYPE>::kNibbleInt ? (float)a1 * 0.0625f : (float)a1;
     return h2_bits(__halves2half2(__float2half_rn((float)a0), __float2half_rn(f1)));
 }
 // The exact bias of the biased weight decode for one (token, block).
 template <int TYPE>
 __device__ __forceinline__ float act_bias(int sum_even, int sum_odd) {
     if (TYPE == QMM_Q4_0) return 1032.0f * (float)sum_even + 72.0f * (float)sum_odd;
+    if (TYPE == QMM_Q4_1) return 1024.0f * (float)sum_even + 64.0f * (float)sum_odd;   // no -8 offset
     if (TYPE == QMM_Q8_0) return 1152.0f * (float)(sum_even + sum_odd);
     return 0.0f;
 }
@@ -305,7 +317,7 @@ __host__ __device__ inline int act_tok_stride(int nkc) { return nkc * 4 + ((nkc 
 
 // Shared-memory layout (offsets in bytes from a 128-byte aligned base).
 struct MvLayout {
-    int ring, bars, act, da, corr, red, lut, total;
+    int ring, bars, act, da, corr, asum, red, lut, total;
 };
 template <int TYPE, int NF, int CW>
 __host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
@@ -320,6 +332,7 @@ __host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
     L.act = off;   off += M * act_tok_stride(nkc) * 16;     // [M][stride] uint4 (16 half2 per block)
     L.da = off;    off += nkc * 8 * NF * 4;                 // [nkc][8*NF] float
     L.corr = off;  off += nkc * 8 * NF * 4;                 // [nkc][8*NF] float
+    L.asum = off;  off += TileFmt<TYPE>::kAffine ? nkc * 8 * NF * 4 : 0;   // Q4_1: [nkc][8*NF] sum of a_q
     L.red = off;   off += CW * 2 * NF * 4 * 32 * 4;
     L.lut = off;   off += TileFmt<TYPE>::kLut ? 256 * kLutCopies * 4 : 0;
     L.total = off;
@@ -346,6 +359,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     const int tok_stride = act_tok_stride(p.nkc);
     float *da_s = reinterpret_cast<float *>(smem + L.da);         // [nkc][TOK]
     float *corr_s = reinterpret_cast<float *>(smem + L.corr);     // [nkc][TOK]
+    float *asum_s = reinterpret_cast<float *>(smem + L.asum);     // [nkc][TOK] (Q4_1 only)
     float *red_s = reinterpret_cast<float *>(smem + L.red);
     uint32_t *lut_s = reinterpret_cast<uint32_t *>(smem + L.lut);
 
@@ -392,7 +406,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     if constexpr (!FUSED) {
         for (int i = ctid; i < TOK * nkc; i += kConsumerWarps * 32) {
             const int j = i / TOK, tok = i - j * TOK;
-            float d = 0.0f, corr = 0.0f;
+            float d = 0.0f, corr = 0.0f, asum = 0.0f;
             if (tok < p.M) {
                 const int64_t kt = p.kt0 + j;
                 const uint4 *src = reinterpret_cast<const uint4 *>(p.a_q + (int64_t)tok * p.K + kt * 32);
@@ -417,9 +431,11 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                 for (int tt = 0; tt < 4; ++tt) dst[tt] = make_uint4(hp[tt], hp[tt + 4], hp[tt + 8], hp[tt + 12]);
                 d = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
                 corr = act_bias<TYPE>(sum_even, sum_odd);
+                asum = (float)(sum_even + sum_odd);
             }
             da_s[j * TOK + tok] = d;
             corr_s[j * TOK + tok] = corr;
+            if constexpr (TileFmt<TYPE>::kAffine) asum_s[j * TOK + tok] = asum;
         }
     } else {
         // 4 lanes per (block, token), 8 columns each; lane q holds column pairs 4q..4q+3, which go to
@@ -453,6 +469,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
             if (e < total && q == 0) {
                 da_s[jt * TOK + tok] = live ? d : 0.0f;
                 corr_s[jt * TOK + tok] = live ? act_bias<TYPE>(sum_even, sum_odd) : 0.0f;
+                if constexpr (TileFmt<TYPE>::kAffine) asum_s[jt * TOK + tok] = live ? (float)(sum_even + sum_odd) : 0.0f;
             }
         }
     }
@@ -478,6 +495,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                 // tiles cw and cw + 8 of this stage, decoded and contracted side by side
                 uint32_t H[kTilesPerWarp][4][4];
                 float dwr[kTilesPerWarp][4];
+                float mwr[kTilesPerWarp][4];              // Q4_1 row mins
                 bool live[kTilesPerWarp];
 #pragma unroll
                 for (int u = 0; u < kTilesPerWarp; ++u) {
@@ -487,6 +505,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                     if (live[u]) {
                         decode_tile<TYPE>(tile, g, t, H[u], lut_lane);
                         row_scales<TYPE>(tile + SOFF, 4 * g, dwr[u]);            // rows 4g .. 4g+3
+                        if constexpr (TileFmt<TYPE>::kAffine) row_mins<TYPE>(tile + SOFF, 4 * g, mwr[u]);
                     }
                 }
 #pragma unroll
@@ -502,6 +521,11 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                         const float2 cr = *reinterpret_cast<const float2 *>(corr_s + j * TOK + 8 * nf + 2 * t);
                         const unsigned long long ncorr = pack2(-cr.x, -cr.y);
                         const unsigned long long da2 = pack2(da.x, da.y);
+                        unsigned long long as2 = 0ull;
+                        if constexpr (TileFmt<TYPE>::kAffine) {
+                            const float2 as = *reinterpret_cast<const float2 *>(asum_s + j * TOK + 8 * nf + 2 * t);
+                            as2 = pack2(as.x, as.y);
+                        }
 #pragma unroll
                         for (int rb = 0; rb < 2; ++rb) {
                             float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -514,6 +538,13 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                             const unsigned long long p23 = fmul2(pack2(dwr[u][2 * rb + 1], dwr[u][2 * rb + 1]), da2);
                             acc[rb][nf][0] = ffma2(s01, p01, acc[rb][nf][0]);
                             acc[rb][nf][1] = ffma2(s23, p23, acc[rb][nf][1]);
+                            if constexpr (TileFmt<TYPE>::kAffine) {
+                                // + m_w * d_a * sum(a_q) of the block, per row and token
+                                const unsigned long long m01 = fmul2(pack2(mwr[u][2 * rb], mwr[u][2 * rb]), da2);
+                                const unsigned long long m23 = fmul2(pack2(mwr[u][2 * rb + 1], mwr[u][2 * rb + 1]), da2);
+                                acc[rb][nf][0] = ffma2(as2, m01, acc[rb][nf][0]);
+                                acc[rb][nf][1] = ffma2(as2, m23, acc[rb][nf][1]);
+                            }
                         }
                     }
                 }
@@ -606,7 +637,7 @@ __device__ __forceinline__ void tile_rows_dp4a(const uint8_t *tile, int i, int j
         T[3] = __byte_perm(y01, y23, 0x7632);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            if constexpr (TYPE == QMM_Q4_0) {
+            if constexpr (TileFmt<TYPE>::kNibbleInt) {
                 R[r][0] = T[r] & 0x0F0F0F0Fu;             // even columns 2cp_c
                 R[r][1] = (T[r] >> 4) & 0x0F0F0F0Fu;      // odd columns 2cp_c + 1
             } else {
@@ -623,17 +654,19 @@ __device__ __forceinline__ void tile_rows_dp4a(const uint8_t *tile, int i, int j
 }
 
 // Staged activation record of (token, block, quarter j): the 8 int8 v of columns 8j..8j+7 as two
-// int8x4 words in the order of tile_rows_dp4a, the dp4a start value, and fp32(d_a).
+// int8x4 words in the order of tile_rows_dp4a, the dp4a start value (Q4_1: the sum of the 8 values,
+// for the min term), and fp32(d_a).
 __device__ __forceinline__ uint4 dp4a_record(int type, uint2 v, int j, float da) {
     unsigned long long V = (unsigned long long)v.x | ((unsigned long long)v.y << 32);
     if (j) V = (V >> (16 * j)) | (V << (64 - 16 * j));       // column pair c <- local pair (c + j) & 3
     const uint32_t lo = (uint32_t)V, hi = (uint32_t)(V >> 32);
     uint4 rec;
     int corr = 0;
-    if (type == QMM_Q4_0) {
+    if (type == QMM_Q4_0 || type == QMM_Q4_1) {
         rec.x = __byte_perm(lo, hi, 0x6420);      // even columns
         rec.y = __byte_perm(lo, hi, 0x7531);      // odd columns
-        corr = -8 * __dp4a((int)v.x, 0x01010101, __dp4a((int)v.y, 0x01010101, 0));
+        const int asum = __dp4a((int)v.x, 0x01010101, __dp4a((int)v.y, 0x01010101, 0));
+        corr = (type == QMM_Q4_0) ? -8 * asum : asum;   // Q4_0: chain start; Q4_1: sum for the min term
     } else {
         rec.x = lo;
         rec.y = hi;
@@ -757,17 +790,33 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
                     float dws[4];
                     row_scales<TYPE>(tile + SOFF, 4 * i, dws);                  // rows 4i .. 4i+3
                     const unsigned long long dw01 = pack2(dws[0], dws[1]), dw23 = pack2(dws[2], dws[3]);
+                    unsigned long long mw01 = 0ull, mw23 = 0ull;
+                    if constexpr (TileFmt<TYPE>::kAffine) {
+                        float mws[4];
+                        row_mins<TYPE>(tile + SOFF, 4 * i, mws);
+                        mw01 = pack2(mws[0], mws[1]);
+                        mw23 = pack2(mws[2], mws[3]);
+                    }
 #pragma unroll
                     for (int t = 0; t < MT; ++t) {
                         if (t >= p.M) break;
                         const uint4 a = act_s[(t * nkc + jt) * 4 + j];
                         int S[4];
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) S[r] = __dp4a((int)R[r][0], (int)a.x, __dp4a((int)R[r][1], (int)a.y, (int)a.z));
+                        const int c0 = TileFmt<TYPE>::kAffine ? 0 : (int)a.z;
+                        for (int r = 0; r < 4; ++r) S[r] = __dp4a((int)R[r][0], (int)a.x, __dp4a((int)R[r][1], (int)a.y, c0));
                         const float da = __uint_as_float(a.w);
                         const unsigned long long da2 = pack2(da, da);
                         acc[t][0] = ffma2(pack2((float)S[0], (float)S[1]), fmul2(dw01, da2), acc[t][0]);
                         acc[t][1] = ffma2(pack2((float)S[2], (float)S[3]), fmul2(dw23, da2), acc[t][1]);
+                        if constexpr (TileFmt<TYPE>::kAffine) {
+                            // + m_w * d_a * (sum of this lane's 8 activations); the 4 quarters add up to
+                            // the block's sum
+                            const float as = (float)(int)a.z;
+                            const unsigned long long as2 = pack2(as, as);
+                            acc[t][0] = ffma2(as2, fmul2(mw01, da2), acc[t][0]);
+                            acc[t][1] = ffma2(as2, fmul2(mw23, da2), acc[t][1]);
+                        }
                     }
                 }
             }
@@ -954,6 +1003,7 @@ cudaError_t run_groups(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, c
             case QMM_Q4_0: e = run<QMM_Q4_0, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
             case QMM_IQ4_NL: e = run<QMM_IQ4_NL, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
             case QMM_MXFP4: e = run<QMM_MXFP4, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
+            case QMM_Q4_1: e = run<QMM_Q4_1, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
             default: e = run<QMM_Q8_0, FUSED>(tiled, K, N, g, mm, yy, ldy, s); break;
         }
         if (e != cudaSuccess) return e;

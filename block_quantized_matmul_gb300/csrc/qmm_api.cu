@@ -13,9 +13,12 @@ using namespace qmm;
 
 namespace {
 
-bool valid_type(qmm_type t) { return t == QMM_Q4_0 || t == QMM_Q8_0 || t == QMM_IQ4_NL || t == QMM_MXFP4; }
-// Flat blocks of 18 or 34 bytes are read as halfwords; MXFP4's 17-byte blocks byte by byte.
-uintptr_t flat_align(qmm_type t) { return t == QMM_MXFP4 ? 1 : 2; }
+bool valid_type(qmm_type t) {
+    return t == QMM_Q4_0 || t == QMM_Q8_0 || t == QMM_IQ4_NL || t == QMM_MXFP4 || t == QMM_Q4_1;
+}
+// Flat blocks of 18 or 34 bytes are read as halfwords, Q4_1's 20-byte blocks start with a 4-byte
+// (d, m) pair read as one word, and MXFP4's 17-byte blocks are read byte by byte.
+uintptr_t flat_align(qmm_type t) { return t == QMM_MXFP4 ? 1 : (t == QMM_Q4_1 ? 4 : 2); }
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool valid_kn(int64_t K, int64_t N) { return K > 0 && (K % 32) == 0 && N > 0; }
 cudaStream_t cs(qmm_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }

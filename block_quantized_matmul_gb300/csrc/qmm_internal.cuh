@@ -20,17 +20,28 @@ constexpr int kBlock4Bytes = 18;      // flat GGML block: fp16 d + 16 nibble byt
 constexpr int kBlock8Bytes = 34;      // flat GGML block: fp16 d + 32 int8
 constexpr int kTileMxBytes = 544;     // MXFP4 tile: 512 nibble bytes + 32 E8M0 exponent bytes
 constexpr int kBlockMxBytes = 17;     // flat MXFP4 block: E8M0 e + 16 nibble bytes
+constexpr int kTile41Bytes = 640;     // Q4_1 tile: 512 nibble bytes + 32 fp16 (d, m) pairs
+constexpr int kBlock41Bytes = 20;     // flat Q4_1 block: fp16 d + fp16 m + 16 nibble bytes
 
-inline int tile_bytes(qmm_type t) { return t == QMM_Q8_0 ? kTile8Bytes : (t == QMM_MXFP4 ? kTileMxBytes : kTile4Bytes); }
-inline int block_bytes(qmm_type t) { return t == QMM_Q8_0 ? kBlock8Bytes : (t == QMM_MXFP4 ? kBlockMxBytes : kBlock4Bytes); }
+inline int tile_bytes(qmm_type t) {
+    return t == QMM_Q8_0 ? kTile8Bytes : (t == QMM_MXFP4 ? kTileMxBytes : (t == QMM_Q4_1 ? kTile41Bytes : kTile4Bytes));
+}
+inline int block_bytes(qmm_type t) {
+    return t == QMM_Q8_0 ? kBlock8Bytes : (t == QMM_MXFP4 ? kBlockMxBytes : (t == QMM_Q4_1 ? kBlock41Bytes : kBlock4Bytes));
+}
 
 // Per-type constants for the kernels.
 template <int TYPE>
 struct TileFmt {
-    static constexpr int kBytes = TYPE == QMM_Q8_0 ? kTile8Bytes : (TYPE == QMM_MXFP4 ? kTileMxBytes : kTile4Bytes);
-    static constexpr int kScaleOff = TYPE == QMM_Q8_0 ? kScale8Off : kScale4Off;   // MXFP4: 512 too
+    static constexpr int kBytes = TYPE == QMM_Q8_0    ? kTile8Bytes
+                                  : TYPE == QMM_MXFP4 ? kTileMxBytes
+                                  : TYPE == QMM_Q4_1  ? kTile41Bytes
+                                                      : kTile4Bytes;
+    static constexpr int kScaleOff = TYPE == QMM_Q8_0 ? kScale8Off : kScale4Off;   // MXFP4, Q4_1: 512 too
     static constexpr bool kLut = TYPE == QMM_IQ4_NL || TYPE == QMM_MXFP4;         // codes go through a table
     static constexpr bool kE8M0 = TYPE == QMM_MXFP4;                              // one exponent byte per row
+    static constexpr bool kAffine = TYPE == QMM_Q4_1;                             // (d, m) per row: d*q + m
+    static constexpr bool kNibbleInt = TYPE == QMM_Q4_0 || TYPE == QMM_Q4_1;      // integer nibble codes
 };
 
 // The built-in IQ4_NL table (16 int8 levels, ascending): 16-level Lloyd-Max quantizer of a unit

@@ -109,6 +109,37 @@ __global__ void __launch_bounds__(128) quantize_weight_kernel(int type, const fl
             for (int j = 0; j < 16; ++j) blk[1 + j] = (uint8_t)((codes[j] & 15) | ((codes[j + 16] & 15) << 4));
             continue;
         }
+        if (type == QMM_Q4_1) {
+            // d = (max - min)/15, q = min(15, trunc((x - min)*(1/d) + 0.5)), m = min
+            float mn = xs[0], mx = xs[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) {
+                mn = xs[j] < mn ? xs[j] : mn;
+                mx = xs[j] > mx ? xs[j] : mx;
+            }
+            const float d = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+            const float id = inv_or_zero(d);
+            int codes[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float v = __fadd_rn(__fmul_rn(__fsub_rn(xs[j], mn), id), 0.5f);
+                int c;
+                if (!(v >= 0.0f)) c = 0;                 // NaN
+                else if (v >= 15.0f) c = 15;
+                else c = __float2int_rz(v);
+                codes[j] = c;
+            }
+            uint16_t *out = reinterpret_cast<uint16_t *>(flat + i * kBlock41Bytes);   // 4-byte aligned
+            out[0] = __half_as_ushort(__float2half_rn(d));
+            out[1] = __half_as_ushort(__float2half_rn(mn));
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const uint32_t b0 = (uint32_t)(codes[j] & 15) | ((uint32_t)(codes[j + 16] & 15) << 4);
+                const uint32_t b1 = (uint32_t)(codes[j + 1] & 15) | ((uint32_t)(codes[j + 17] & 15) << 4);
+                out[2 + j / 2] = (uint16_t)(b0 | (b1 << 8));
+            }
+            continue;
+        }
         const int bb = (type == QMM_Q8_0) ? kBlock8Bytes : kBlock4Bytes;
         uint16_t *out = reinterpret_cast<uint16_t *>(flat + i * bb);   // 2-byte aligned
         int codes[32];

@@ -15,7 +15,9 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
                                                      int64_t n_tiles, uint8_t *__restrict__ tiled) {
     constexpr bool k8 = (TYPE == QMM_Q8_0);
     constexpr bool mx = (TYPE == QMM_MXFP4);            // 17-byte blocks: byte access only
-    constexpr int bb = k8 ? kBlock8Bytes : (mx ? kBlockMxBytes : kBlock4Bytes);
+    constexpr bool q41 = (TYPE == QMM_Q4_1);            // 20-byte blocks: (d, m) then the nibbles
+    constexpr int bb = k8 ? kBlock8Bytes : (mx ? kBlockMxBytes : (q41 ? kBlock41Bytes : kBlock4Bytes));
+    constexpr int head = mx ? 1 : (q41 ? 4 : 2);        // bytes before the quants
     constexpr int ts = TileFmt<TYPE>::kBytes;
     constexpr int soff = TileFmt<TYPE>::kScaleOff;
     const int64_t total = n_tiles * 32;
@@ -34,6 +36,7 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
                 for (int cp = 0; cp < 16; ++cp) t[cp * 32 + r] = 0;
             }
             if (mx) t[soff + r] = 0;
+            else if (q41) *reinterpret_cast<uint32_t *>(t + soff + 4 * r) = 0u;
             else *reinterpret_cast<uint16_t *>(t + soff + 2 * r) = 0;
             continue;
         }
@@ -47,7 +50,7 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
             uint32_t qs[8];                             // 16 nibble bytes as 8 halfwords
 #pragma unroll
             for (int h = 0; h < 8; ++h)
-                qs[h] = mx ? ((uint32_t)blk[1 + 2 * h] | ((uint32_t)blk[2 + 2 * h] << 8)) : ld_u16(blk + 2 + 2 * h);
+                qs[h] = mx ? ((uint32_t)blk[1 + 2 * h] | ((uint32_t)blk[2 + 2 * h] << 8)) : ld_u16(blk + head + 2 * h);
 #pragma unroll
             for (int cp = 0; cp < 16; ++cp) {
                 // element e: byte e&15 of the block, low nibble for e < 16, high nibble otherwise
@@ -60,6 +63,7 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
             }
         }
         if (mx) t[soff + r] = blk[0];                   // the row's E8M0 exponent
+        else if (q41) *reinterpret_cast<uint32_t *>(t + soff + 4 * r) = *reinterpret_cast<const uint32_t *>(blk);   // d, m
         else *reinterpret_cast<uint16_t *>(t + soff + 2 * r) = (uint16_t)ld_u16(blk);
     }
     // The decode matmul streams tiles before it waits for the kernel before it on the stream, so the
@@ -72,7 +76,8 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t *__restrict__
                                                      uint8_t *__restrict__ flat) {
     constexpr bool k8 = (TYPE == QMM_Q8_0);
     constexpr bool mx = (TYPE == QMM_MXFP4);
-    constexpr int bb = k8 ? kBlock8Bytes : (mx ? kBlockMxBytes : kBlock4Bytes);
+    constexpr bool q41 = (TYPE == QMM_Q4_1);
+    constexpr int bb = k8 ? kBlock8Bytes : (mx ? kBlockMxBytes : (q41 ? kBlock41Bytes : kBlock4Bytes));
     constexpr int ts = TileFmt<TYPE>::kBytes;
     constexpr int soff = TileFmt<TYPE>::kScaleOff;
     const int64_t total = N * n_k_tiles;
@@ -94,7 +99,12 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t *__restrict__
             continue;
         }
         uint16_t *blk = reinterpret_cast<uint16_t *>(flat + i * bb);
-        blk[0] = (uint16_t)ld_u16(t + soff + 2 * r);
+        if (q41) {
+            *reinterpret_cast<uint32_t *>(blk) = *reinterpret_cast<const uint32_t *>(t + soff + 4 * r);   // d, m
+            blk += 1;                                   // the quants follow 4 bytes in, as for 2 below
+        } else {
+            blk[0] = (uint16_t)ld_u16(t + soff + 2 * r);
+        }
         if (k8) {
 #pragma unroll
             for (int cp = 0; cp < 16; ++cp) blk[1 + cp] = (uint16_t)ld_u16(t + cp * 64 + 2 * r);
@@ -134,6 +144,7 @@ cudaError_t launch_repack(qmm_type t, const uint8_t *flat, int64_t K, int64_t N,
         case QMM_Q4_0: repack_kernel<QMM_Q4_0><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
         case QMM_IQ4_NL: repack_kernel<QMM_IQ4_NL><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
         case QMM_MXFP4: repack_kernel<QMM_MXFP4><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
+        case QMM_Q4_1: repack_kernel<QMM_Q4_1><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
         default: repack_kernel<QMM_Q8_0><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
     }
     return cudaGetLastError();
@@ -147,6 +158,7 @@ cudaError_t launch_unpack(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N
         case QMM_Q4_0: unpack_kernel<QMM_Q4_0><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
         case QMM_IQ4_NL: unpack_kernel<QMM_IQ4_NL><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
         case QMM_MXFP4: unpack_kernel<QMM_MXFP4><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
+        case QMM_Q4_1: unpack_kernel<QMM_Q4_1><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
         default: unpack_kernel<QMM_Q8_0><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
     }
     return cudaGetLastError();

@@ -52,8 +52,10 @@ typedef enum {
 
 /* Weight formats ("Block-32 Quantized Formats").  MXFP4 tiles (544 B) hold OCP FP4 (E2M1) codes in
  * the Q4_0 nibble layout and one E8M0 exponent byte per row at byte 512 + row; a weight is the FP4
- * value of its code times the power-of-two fp16 scale with bits clamp(e - 112, 0, 30) << 10. */
-typedef enum { QMM_Q4_0 = 0, QMM_Q8_0 = 1, QMM_IQ4_NL = 2, QMM_MXFP4 = 3 } qmm_type;
+ * value of its code times the power-of-two fp16 scale with bits clamp(e - 112, 0, 30) << 10.
+ * Q4_1 tiles (640 B) keep the Q4_0 nibble layout and one FP16 pair (d, m) per row at bytes
+ * 512 + 4*row; a weight is d*q + m (q = 0..15). */
+typedef enum { QMM_Q4_0 = 0, QMM_Q8_0 = 1, QMM_IQ4_NL = 2, QMM_MXFP4 = 3, QMM_Q4_1 = 4 } qmm_type;
 
 /* Which kernel qmm_matmul_path runs: AUTO picks the decode matvec for M <= qmm_decode_max_m()
  * and the tensor-core GEMM otherwise. */
@@ -64,11 +66,12 @@ QMM_API const char *qmm_status_str(qmm_status st);
 
 /* Bytes of one flat GGML block of 32 weights: 18 (Q4_0, IQ4_NL: fp16 d + 16 nibble bytes, element
  * j in the low nibble of byte j, element j+16 in its high nibble), 34 (Q8_0: fp16 d + 32 int8) or
- * 17 (MXFP4: the E8M0 exponent byte + 16 nibble bytes in the same order).  0 for an unknown type. */
+ * 17 (MXFP4: the E8M0 exponent byte + 16 nibble bytes in the same order) or 20 (Q4_1: fp16 d, fp16 m
+ * + 16 nibble bytes).  0 for an unknown type. */
 QMM_API size_t qmm_block_size(qmm_type t);
 
-/* Bytes of one tile ("Block-32 Quantized Formats"): 576 (Q4_0, IQ4_NL), 1088 (Q8_0) or 544 (MXFP4);
- * 0 if unknown. */
+/* Bytes of one tile ("Block-32 Quantized Formats"): 576 (Q4_0, IQ4_NL), 1088 (Q8_0), 544 (MXFP4) or
+ * 640 (Q4_1); 0 if unknown. */
 QMM_API size_t qmm_tile_size(qmm_type t);
 
 /* Bytes of the tiled weight [K, N] ("Tile Dimensions and Grid Layout"):
@@ -89,14 +92,15 @@ QMM_API int64_t qmm_decode_max_m(void);
 /*
  * qmm_quantize_weight -- fp32 weight rows -> flat GGML blocks (model-load helper, not the hot path).
  *   w_dev      fp32, N rows of K values, row n at w_dev + n*ldw; 16-byte aligned, ldw % 4 == 0.
- *   w_flat_dev output, qmm_flat_size(t, K, N) bytes, row-major blocks; 2-byte aligned (any address
- *              for MXFP4).
+ *   w_flat_dev output, qmm_flat_size(t, K, N) bytes, row-major blocks; 2-byte aligned (4-byte for
+ *              Q4_1, any address for MXFP4).
  * Rules per 32-element block (x = the block, m = its signed element of largest magnitude, first on
  * ties): Q8_0 d = max|x|/127, q = round-half-away(x/d) (computed as x * (1/d));  Q4_0 d = m/-8,
  * q = min(15, trunc(x*(1/d) + 8.5));  IQ4_NL d = m/table[0], q = the table index whose level
  * fp16(d)*table[q] is nearest to x (lowest index on ties).  d is stored rounded to fp16.
  * MXFP4: e = floor(log2 max|x|) - 2 + 127 (0 for an all-zero block, at most 254), then the code whose
  * level s * fp4(code) is nearest to x (lowest code on ties), s the dequantizing fp16 scale.
+ * Q4_1: d = (max - min)/15, q = min(15, trunc((x - min)*(1/d) + 0.5)), m = min; d and m as fp16.
  * Errors: INVALID_ARG (N <= 0, K <= 0, K % 32, ldw < K, NULL), UNSUPPORTED (type), MISALIGNED.
  */
 QMM_API qmm_status qmm_quantize_weight(qmm_type t, const float *w_dev, int64_t N, int64_t K, int64_t ldw,
@@ -105,7 +109,8 @@ QMM_API qmm_status qmm_quantize_weight(qmm_type t, const float *w_dev, int64_t N
 /*
  * qmm_repack -- flat GGML rows -> tiles ("Tiled Weight Formats"; the pages repack at model load,
  * in set_tensor() or rt-repack).
- *   w_flat_dev  N rows of K/32 blocks (qmm_flat_size bytes); 2-byte aligned (any address for MXFP4).
+ *   w_flat_dev  N rows of K/32 blocks (qmm_flat_size bytes); 2-byte aligned (4-byte for Q4_1, any
+ *               address for MXFP4).
  *   w_tiled_dev output, qmm_tiled_size bytes; 16-byte aligned.  Rows past N in the last column tile
  *               are written as zero bytes (scale 0, quants 0).  The buffers must not overlap.
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED.  Bit-exact, lossless.

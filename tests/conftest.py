@@ -18,3 +18,19 @@ def orc():
 
     oracle.build()
     return oracle
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean(request):
+    """After every GPU test: no kernel of the library gave up a bounded wait (QMM_ERR_TIMEOUT)."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+
+    if not torch.cuda.is_available():
+        return
+    import block_quantized_matmul_gb300 as qmm
+
+    torch.cuda.synchronize()
+    assert qmm.qmm_device_status() == 0, "a kernel timed out a pipeline wait during this test"

@@ -4,7 +4,7 @@ from __future__ import annotations
 
 import numpy as np
 
-TYPES = ["q4_0", "q8_0", "iq4_nl", "mxfp4"]
+TYPES = ["q4_0", "q8_0", "iq4_nl", "mxfp4", "q4_1"]
 
 
 def torch_mod():

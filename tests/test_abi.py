@@ -55,6 +55,9 @@ def test_sizes(L):
     assert qmm.tile_size("mxfp4") == 544 and qmm.block_size("mxfp4") == 17
     assert qmm.tiled_size("mxfp4", 4096, 14336) == 448 * 128 * 544
     assert qmm.flat_size("mxfp4", 64, 33) == 33 * 2 * 17
+    # Q4_1: 640-byte tiles of 32 rows x 20-byte blocks
+    assert qmm.tile_size("q4_1") == 640 and qmm.block_size("q4_1") == 20
+    assert qmm.tiled_size("q4_1", 4096, 4096) == 128 * 128 * 640
 
 
 def test_mxfp4_flat_blocks_need_no_alignment(L):
@@ -89,7 +92,7 @@ P = 1 << 20          # a fake, 16-byte aligned, non-null address (never derefere
     ((0, P, 64, 64, None, P, 1, P, 64, None), INVALID),  # NULL a_q
     ((0, P, 64, 64, P, None, 1, P, 64, None), INVALID),  # NULL a_d
     ((0, P, 64, 64, P, P, 1, None, 64, None), INVALID),  # NULL y
-    ((5, P, 64, 64, P, P, 1, P, 64, None), UNSUPPORTED),  # unknown type
+    ((99, P, 64, 64, P, P, 1, P, 64, None), UNSUPPORTED),  # unknown type
     ((0, P + 8, 64, 64, P, P, 1, P, 64, None), MISALIGNED),
     ((0, P, 64, 64, P + 4, P, 1, P, 64, None), MISALIGNED),
     ((0, P, 64, 64, P, P + 2, 1, P, 64, None), MISALIGNED),
@@ -116,7 +119,7 @@ def test_quantize_act_argument_errors(L):
 def test_repack_and_quantize_weight_argument_errors(L):
     assert L.qmm_repack(0, P, 48, 64, P, None) == INVALID
     assert L.qmm_repack(0, None, 64, 64, P, None) == INVALID
-    assert L.qmm_repack(6, P, 64, 64, P, None) == UNSUPPORTED
+    assert L.qmm_repack(99, P, 64, 64, P, None) == UNSUPPORTED
     assert L.qmm_repack(0, P + 1, 64, 64, P, None) == MISALIGNED
     assert L.qmm_repack(0, P, 64, 64, P + 8, None) == MISALIGNED
     assert L.qmm_unpack(1, P + 8, 64, 64, P, None) == MISALIGNED
@@ -124,7 +127,7 @@ def test_repack_and_quantize_weight_argument_errors(L):
     assert L.qmm_quantize_weight(0, P, 64, 64, 60, P, None) == INVALID      # ldw < K
     assert L.qmm_quantize_weight(0, P, 64, 64, 66, P, None) == MISALIGNED   # ldw % 4
     assert L.qmm_quantize_weight(0, P + 4, 64, 64, 64, P, None) == MISALIGNED
-    assert L.qmm_quantize_weight(9, P, 64, 64, 64, P, None) == UNSUPPORTED
+    assert L.qmm_quantize_weight(99, P, 64, 64, 64, P, None) == UNSUPPORTED
 
 
 def test_binding_raises_on_error(L):
@@ -152,7 +155,7 @@ def test_matmul_f32_argument_errors(L):
     assert f(0, None, 64, 64, P, 64, 1, P, 64, None) == INVALID  # NULL weight
     assert f(0, P, 64, 64, None, 64, 1, P, 64, None) == INVALID  # NULL x
     assert f(0, P, 64, 64, P, 64, 1, None, 64, None) == INVALID  # NULL y
-    assert f(4, P, 64, 64, P, 64, 1, P, 64, None) == UNSUPPORTED
+    assert f(99, P, 64, 64, P, 64, 1, P, 64, None) == UNSUPPORTED
     assert f(0, P + 8, 64, 64, P, 64, 1, P, 64, None) == MISALIGNED
     assert f(0, P, 64, 64, P + 2, 64, 1, P, 64, None) == MISALIGNED
     assert f(0, P, 64, 64, P, 64, 1, P + 1, 64, None) == MISALIGNED

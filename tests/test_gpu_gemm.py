@@ -108,7 +108,8 @@ def test_gemm_is_deterministic(torch):
     assert torch.equal(y1, y2)
 
 
-FULL = [("q4_0", 4096, 14336, 512), ("q8_0", 4096, 128256, 128), ("mxfp4", 4096, 14336, 512)]
+FULL = [("q4_0", 4096, 14336, 512), ("q8_0", 4096, 128256, 128), ("mxfp4", 4096, 14336, 512),
+        ("q4_1", 4096, 14336, 512)]
 
 
 @pytest.mark.parametrize("type_,K,N,M", FULL, ids=lambda v: str(v))

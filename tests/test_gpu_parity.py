@@ -150,7 +150,7 @@ def test_matvec_is_deterministic(torch, orc):
 # Full-size workloads: the whole output on the GPU, a sample of it in the oracle (every column tile
 # at least once, plus both ends), launched exactly as the benchmark launches them.
 FULL = [("q4_0", 4096, 4096, 1), ("q8_0", 4096, 14336, 1), ("iq4_nl", 4096, 4096, 8), ("q8_0", 4096, 128256, 1),
-        ("mxfp4", 4096, 14336, 1)]
+        ("mxfp4", 4096, 14336, 1), ("q4_1", 4096, 14336, 1)]
 
 
 @pytest.mark.parametrize("type_,K,N,M", FULL, ids=lambda v: str(v))

@@ -87,7 +87,7 @@ def test_shard_ranges():
     assert (last.ct0, last.ct1, last.n0, last.n_local) == (2, 3, 64, 6)
     with pytest.raises(ValueError):
         shard.shard("q4_0", 48, 10, 0, 1)
-    for t in ("q4_0", "q8_0", "iq4_nl", "mxfp4"):
+    for t in ("q4_0", "q8_0", "iq4_nl", "mxfp4", "q4_1"):
         assert shard.tile_bytes(t) == orc_tile_bytes(t)
 
 
