@@ -18,7 +18,7 @@ __all__ = [
     "Q4_0", "Q8_0", "IQ4_NL", "MXFP4", "Q4_1", "TYPES", "QmmError", "lib", "library_path",
     "block_size", "tile_size", "tiled_size", "flat_size", "iq4nl_table", "decode_max_m",
     "qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
-    "qmm_matmul_path", "qmm_matmul_f32", "qmm_device_status", "PATH_AUTO", "PATH_MATVEC", "PATH_GEMM",
+    "qmm_matmul_path", "qmm_matmul_f32", "qmm_matmul_flat", "qmm_device_status", "PATH_AUTO", "PATH_MATVEC", "PATH_GEMM",
     "matmul_workspace_size", "qmm_matmul_ws", "qmm_matmul_noalloc", "matmul_noalloc_max_workspace",
 ]
 
@@ -66,6 +66,7 @@ def lib():
         L.qmm_matmul.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp]
         L.qmm_matmul_f32.argtypes = [i32, vp, i64, i64, vp, i64, i64, vp, i64, vp]
         L.qmm_matmul_path.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, i32, vp]
+        L.qmm_matmul_flat.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp]
         L.qmm_device_status.argtypes = [vp]
         L.qmm_matmul_workspace_size.argtypes = [i64, i64]
         L.qmm_matmul_workspace_size.restype = sz
@@ -74,7 +75,8 @@ def lib():
         L.qmm_matmul_noalloc_max_workspace.argtypes = []
         L.qmm_matmul_noalloc_max_workspace.restype = sz
         for fn in ("qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
-                   "qmm_matmul_path", "qmm_device_status", "qmm_matmul_ws", "qmm_matmul_noalloc", "qmm_matmul_f32"):
+                   "qmm_matmul_path", "qmm_device_status", "qmm_matmul_ws", "qmm_matmul_noalloc", "qmm_matmul_f32",
+                   "qmm_matmul_flat"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -162,6 +164,11 @@ def qmm_matmul(type_, w_tiled, K: int, N: int, a_q, a_d, M: int, y, ldy: int, st
 def qmm_matmul_f32(type_, w_tiled, K: int, N: int, x, ldx: int, M: int, y, ldy: int, stream=None) -> None:
     _check("qmm_matmul_f32", lib().qmm_matmul_f32(_t(type_), _ptr(w_tiled), K, N, _ptr(x), ldx, M, _ptr(y), ldy,
                                                   _stream(stream)))
+
+
+def qmm_matmul_flat(type_, w_flat, K: int, N: int, a_q, a_d, M: int, y, ldy: int, stream=None) -> None:
+    _check("qmm_matmul_flat", lib().qmm_matmul_flat(_t(type_), _ptr(w_flat), K, N, _ptr(a_q), _ptr(a_d), M, _ptr(y),
+                                                    ldy, _stream(stream)))
 
 
 def qmm_matmul_path(type_, w_tiled, K: int, N: int, a_q, a_d, M: int, y, ldy: int, path: int,

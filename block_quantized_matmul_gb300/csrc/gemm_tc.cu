@@ -708,6 +708,8 @@ __global__ void __launch_bounds__(256) prepare_act_kernel(const int8_t *__restri
     }
 }
 
+}  // namespace
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -739,6 +741,8 @@ cudaError_t make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ba
                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+namespace {
 
 // 3-D tensor map of the tiled weight viewed as [n_col_tiles][n_k_tiles][tile bytes / 8] of 8-byte
 // words: one box = the 4 column tiles x 2 K tiles of a block pair (column tiles past the end read

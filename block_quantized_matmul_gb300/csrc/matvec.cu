@@ -113,6 +113,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// 2-D tensor copy of one box of `map` at element coordinates (x, y) into shared memory.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
 // Producer warp: streams the K tiles [kt0, kt0 + nkc) of every column tile this CTA owns into the
 // ring, one stage of TPS consecutive tiles per 1-D bulk copy, and returns once the copies in
 // flight have landed.
@@ -802,8 +809,8 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
                         if (t >= p.M) break;
                         const uint4 a = act_s[(t * nkc + jt) * 4 + j];
                         int S[4];
-#pragma unroll
                         const int c0 = TileFmt<TYPE>::kAffine ? 0 : (int)a.z;
+#pragma unroll
                         for (int r = 0; r < 4; ++r) S[r] = __dp4a((int)R[r][0], (int)a.x, __dp4a((int)R[r][1], (int)a.y, c0));
                         const float da = __uint_as_float(a.w);
                         const unsigned long long da2 = pack2(da, da);
@@ -983,6 +990,355 @@ cudaError_t run(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a, int
 #undef QMM_MV_ARGS
 }
 
+// ================= flat (untiled) rows: decode straight from the GGML blocks =================
+// The pages keep every supported type usable from its flat row-major GGML layout as well as from the
+// tiles.  Here a chunk is 32 consecutive weight rows; a stage holds those rows x kFlatKB blocks, brought
+// in by one 2-D tensor copy (the flat weight seen as rows of 8-byte words; a row must be a whole
+// number of 16-byte units).  Warp w of the 16 consumer warps takes rows w and w + 16 of the chunk and
+// lane b block b of the stage: it loads the block's bytes as aligned words (blocks are 17..34 bytes,
+// so most are unaligned), extracts the head and the codes with funnel shifts, turns the codes into 8
+// int8x4 words and takes dp4a against the staged activations, whose byte order matches those words
+// (natural order for Q4_0 / Q4_1 / Q8_0; for the table types the order of the table lookup, see
+// stage_flat).  Row sums: a fixed butterfly over the 32 lanes at the end of the chunk.
+constexpr int kFlatKB = 32;            // blocks per row and stage
+constexpr int kFlatCW = 16;            // consumer warps
+constexpr int kFlatMT = 4;             // tokens per launch
+
+template <int TYPE>
+struct FlatFmt {
+    static constexpr int kBlock = TYPE == QMM_Q8_0    ? kBlock8Bytes
+                                  : TYPE == QMM_MXFP4 ? kBlockMxBytes
+                                  : TYPE == QMM_Q4_1  ? kBlock41Bytes
+                                                      : kBlock4Bytes;
+    static constexpr int kHead = TYPE == QMM_MXFP4 ? 1 : (TYPE == QMM_Q4_1 ? 4 : 2);
+    // Block words u[i] (bytes 4i..4i+3 of the block) that the code words touch: the last code word
+    // starts at byte kBlock - 4 and spans u[(kBlock - 4) / 4] and, unless it is word aligned, the next.
+    static constexpr int kU = (kBlock - 4) / 4 + ((kBlock - 4) % 4 ? 1 : 0) + 1;
+};
+
+struct FlatParams {
+    const int8_t *a_q;
+    const uint16_t *a_d;
+    float *y;
+    int64_t K, nkt, N, ldy, n_chunks;
+    int M, stages, kt0, nkc, accumulate;
+    Lut16 lut;
+};
+
+struct FlatLayout {
+    int ring, bars, act, aux, total;
+};
+template <int TYPE, int MT>
+__host__ __device__ inline FlatLayout flat_layout(int nkc, int stages) {
+    FlatLayout L;
+    int off = 0;
+    L.ring = off;  off += stages * 32 * kFlatKB * FlatFmt<TYPE>::kBlock;
+    off += 16;                                                // word reads of the last block run past the ring
+    L.bars = off;  off += 2 * stages * 8 + 16;
+    off = (off + 15) & ~15;
+    L.act = off;   off += MT * nkc * 32;                      // [MT][nkc] 32 int8 in the decode order
+    L.aux = off;   off += MT * nkc * 8;                       // [MT][nkc] {fp32 d_a, int corr or sum}
+    L.total = off;
+    return L;
+}
+
+// The 8 int8x4 words of one flat block (blk_off = its byte offset from a 16-byte aligned base) in the
+// staged activation order, and its scale (and Q4_1 min).  The block is read as aligned words, shifted
+// into block-relative words u[] by one funnel shift each (blocks of 17, 18 or 34 bytes start at any
+// byte offset), then code word k at byte kHead + 4k is a fixed funnel shift of two u[].
+template <int TYPE>
+__device__ __forceinline__ void flat_block_words(const uint8_t *base, int blk_off, uint32_t (&W)[8], float &dw, float &mw,
+                                                 const uint32_t (&tb)[4]) {
+    constexpr int BB = FlatFmt<TYPE>::kBlock, H = FlatFmt<TYPE>::kHead, NU = FlatFmt<TYPE>::kU;
+    uint32_t u[NU];
+    if constexpr (BB % 4 == 0) {
+        const uint32_t *w32 = reinterpret_cast<const uint32_t *>(base + blk_off);
+#pragma unroll
+        for (int i = 0; i < NU; ++i) u[i] = w32[i];
+    } else {
+        const uint32_t *w32 = reinterpret_cast<const uint32_t *>(base + (blk_off & ~3));
+        const uint32_t sh = 8u * (uint32_t)(blk_off & 3);
+        uint32_t w[NU + 1];
+#pragma unroll
+        for (int i = 0; i <= NU; ++i) w[i] = w32[i];
+#pragma unroll
+        for (int i = 0; i < NU; ++i) u[i] = __funnelshift_r(w[i], w[i + 1], sh);
+    }
+    // code word at block byte H + 4k
+    auto at = [&](int k) -> uint32_t {
+        constexpr int s = 8 * (H & 3);
+        const int q = (H >> 2) + k;
+        if constexpr (s == 0) return u[q];
+        else return __funnelshift_r(u[q], u[q + 1], s);
+    };
+    mw = 0.0f;
+    if constexpr (TYPE == QMM_MXFP4) {
+        dw = mx_half_scale(u[0] & 0xFFu);
+    } else {
+        dw = __low2float(bits_h2(u[0]));
+        if constexpr (TYPE == QMM_Q4_1) mw = __high2float(bits_h2(u[0]));
+    }
+    if constexpr (TYPE == QMM_Q8_0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) W[k] = at(k);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t qk = at(k);                      // quant bytes 4k..4k+3: elements 4k.. (low), 16+4k.. (high)
+            if constexpr (TileFmt<TYPE>::kNibbleInt) {
+                W[k] = qk & 0x0F0F0F0Fu;
+                W[4 + k] = (qk >> 4) & 0x0F0F0F0Fu;
+            } else {
+                // table values in nibble order lo(b0), hi(b0), lo(b1), hi(b1) | lo(b2), hi(b2), lo(b3), hi(b3)
+                const uint32_t m = qk & 0x77777777u;
+                const uint32_t sel0 = ((qk >> 1) & 0x4444u) | 0x3210u;
+                const uint32_t sel1 = ((qk >> 17) & 0x4444u) | 0x3210u;
+                const uint32_t m1 = m >> 16;
+                W[2 * k] = __byte_perm(__byte_perm(tb[0], tb[1], m), __byte_perm(tb[2], tb[3], m), sel0);
+                W[2 * k + 1] = __byte_perm(__byte_perm(tb[0], tb[1], m1), __byte_perm(tb[2], tb[3], m1), sel1);
+            }
+        }
+    }
+}
+
+// Stage the 32 activations of one (token, block) in the order of flat_block_words, plus d_a and the
+// Q4_0 start value -8 * sum(a) (Q4_1: the sum itself, for the min term).
+template <int TYPE>
+__device__ __forceinline__ void stage_flat(const int8_t *a32, float da, uint32_t *dst_words, uint2 *dst_aux) {
+    const uint4 v0 = *reinterpret_cast<const uint4 *>(a32), v1 = *reinterpret_cast<const uint4 *>(a32 + 16);
+    const uint32_t a[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};   // natural order
+    if constexpr (TileFmt<TYPE>::kLut) {
+        // table lookup order: for k = 0..3, [a(4k), a(4k+16), a(4k+1), a(4k+17)], [a(4k+2), a(4k+18), a(4k+3), a(4k+19)]
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            dst_words[2 * k] = __byte_perm(a[k], a[4 + k], 0x5140);
+            dst_words[2 * k + 1] = __byte_perm(a[k], a[4 + k], 0x7362);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst_words[k] = a[k];
+    }
+    int asum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) asum = __dp4a((int)a[k], 0x01010101, asum);
+    const int aux = TYPE == QMM_Q4_0 ? -8 * asum : (TYPE == QMM_Q4_1 ? asum : 0);
+    *dst_aux = make_uint2(__float_as_uint(da), (uint32_t)aux);
+}
+
+// MT = token capacity (1, 2 or 4); p.M <= MT tokens are live.
+template <int TYPE, int MT>
+__global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
+    matvec_flat_kernel(const FlatParams p, const __grid_constant__ CUtensorMap w_map) {
+    constexpr int BB = FlatFmt<TYPE>::kBlock;
+    constexpr int kRowStage = kFlatKB * BB;                     // bytes of one row in a stage
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+    const FlatLayout L = flat_layout<TYPE, MT>(p.nkc, p.stages);
+    uint8_t *ring = smem + L.ring;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
+    uint64_t *empty = full + p.stages;
+    volatile int *abort = reinterpret_cast<volatile int *>(empty + p.stages);
+    uint32_t *act_w = reinterpret_cast<uint32_t *>(smem + L.act);
+    uint2 *act_x = reinterpret_cast<uint2 *>(smem + L.aux);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int stages = p.stages, nkc = p.nkc;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), kFlatCW);
+        }
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    if (warp == 0) {
+        // ---- producer: per chunk and stage, one 2-D tensor copy of 32 rows x kFlatKB blocks (rows past
+        // N and blocks past the row end arrive as zeros and are never used) ----
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t ch = blockIdx.x; ch < p.n_chunks && ok; ch += gridDim.x) {
+            for (int kb0 = 0; kb0 < nkc; kb0 += kFlatKB, ++it) {
+                const int s = (int)(it % (uint32_t)stages);
+                const uint32_t ph = (it / (uint32_t)stages) & 1u;
+                if (!__all_sync(0xffffffffu, wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort))) { ok = false; break; }
+                if (lane == 0) {
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(fb, (uint32_t)(32 * kRowStage));
+                    tma_load_2d(smem_u32(ring + s * 32 * kRowStage), &w_map, (p.kt0 + kb0) * BB / 8, (int)(ch * 32), fb);
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0 && it > 0) {
+            const uint32_t last = it - 1;
+            for (uint32_t k = 0; k < (uint32_t)stages && k <= last; ++k) {
+                const uint32_t i = last - k;
+                wait_drain(smem_u32(&full[i % stages]), (i / stages) & 1u);
+            }
+        }
+        return;
+    }
+
+    const int cw = warp - 1, ctid = threadIdx.x - 32;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int e = ctid; e < MT * nkc; e += kFlatCW * 32) {
+        const int tok = e / nkc, jt = e - tok * nkc;
+        if (tok < p.M) {
+            const int64_t kt = p.kt0 + jt;
+            const float da = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
+            stage_flat<TYPE>(p.a_q + (int64_t)tok * p.K + kt * 32, da, act_w + (size_t)e * 8, act_x + e);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) act_w[(size_t)e * 8 + k] = 0u;
+            act_x[e] = make_uint2(0u, 0u);
+        }
+    }
+    uint32_t tb[4] = {0u, 0u, 0u, 0u};
+    if constexpr (TileFmt<TYPE>::kLut) {
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+#pragma unroll
+            for (int b = 0; b < 4; ++b) tb[w] |= ((uint32_t)(p.lut.v[4 * w + b] & 0xFF)) << (8 * b);
+    }
+    consumer_sync<kFlatCW>();
+
+    uint32_t it = 0;
+    bool ok = true;
+    for (int64_t ch = blockIdx.x; ch < p.n_chunks; ch += gridDim.x) {
+        float acc[2][MT];
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[r][t] = 0.0f;
+        for (int kb0 = 0; kb0 < nkc; kb0 += kFlatKB, ++it) {
+            const int s = (int)(it % (uint32_t)stages);
+            const uint32_t ph = (it / (uint32_t)stages) & 1u;
+            if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
+            const int jt = kb0 + lane;                         // this lane's block
+            if (ok && jt < nkc) {
+                const uint8_t *st = ring + s * 32 * kRowStage;
+                uint4 aw[MT][2];
+                uint2 ax[MT];
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(act_w + ((size_t)t * nkc + jt) * 8);
+                    aw[t][0] = src[0];
+                    aw[t][1] = src[1];
+                    ax[t] = act_x[t * nkc + jt];
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int row = cw + 16 * r;
+                    uint32_t W[8];
+                    float dw, mw;
+                    flat_block_words<TYPE>(st, row * kRowStage + lane * BB, W, dw, mw, tb);
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) {
+                        if (t >= p.M) break;
+                        const int c0 = TYPE == QMM_Q4_0 ? (int)ax[t].y : 0;
+                        int S = __dp4a((int)W[0], (int)aw[t][0].x, c0);
+                        S = __dp4a((int)W[1], (int)aw[t][0].y, S);
+                        S = __dp4a((int)W[2], (int)aw[t][0].z, S);
+                        S = __dp4a((int)W[3], (int)aw[t][0].w, S);
+                        S = __dp4a((int)W[4], (int)aw[t][1].x, S);
+                        S = __dp4a((int)W[5], (int)aw[t][1].y, S);
+                        S = __dp4a((int)W[6], (int)aw[t][1].z, S);
+                        S = __dp4a((int)W[7], (int)aw[t][1].w, S);
+                        const float da = __uint_as_float(ax[t].x);
+                        acc[r][t] = fmaf((float)S, __fmul_rn(dw, da), acc[r][t]);
+                        if constexpr (TYPE == QMM_Q4_1) acc[r][t] = fmaf((float)(int)ax[t].y, __fmul_rn(mw, da), acc[r][t]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        }
+        // ---- row sums over the lanes (fixed butterfly), then y ----
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                float v = acc[r][t];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                const int64_t n = ch * 32 + cw + 16 * r;
+                if (ok && lane == 0 && t < p.M && n < p.N) {
+                    float *dst = p.y + (int64_t)t * p.ldy + n;
+                    *dst = p.accumulate ? (*dst + v) : v;
+                }
+            }
+    }
+}
+
+template <int TYPE, int MT>
+cudaError_t run_flat(const uint8_t *flat, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
+                     int64_t ldy, cudaStream_t s) {
+    constexpr int BB = FlatFmt<TYPE>::kBlock;
+    const int64_t nkt = K / 32;
+    int64_t nkc = kActBudget / (kFlatMT * 40);                  // staged bytes per (token, block): 32 + 8
+                                                                // (the same K passes for every MT)
+    nkc = nkc / kFlatKB * kFlatKB;
+    if (nkc > nkt) nkc = nkt;
+    const int fixed = flat_layout<TYPE, MT>((int)nkc, 0).total;
+    const int stage_bytes = 32 * kFlatKB * BB + 16;
+    int st = (kSmemLimit - 1024 - fixed - 128) / stage_bytes;
+    st = st > 8 ? 8 : (st < 2 ? 2 : st);
+    const size_t smem = (size_t)flat_layout<TYPE, MT>((int)nkc, st).total + 128;
+    auto kern = matvec_flat_kernel<TYPE, MT>;
+    static int attr_done[4] = {0, 0, 0, 0};
+    cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
+    if (e != cudaSuccess) return e;
+    const int64_t n_chunks = (N + 31) / 32;
+    int64_t grid = num_sms();
+    if (grid > n_chunks) grid = n_chunks;
+    // The flat weight as N rows of row_bytes / 8 eight-byte words; one box = 32 rows x kFlatKB blocks.
+    alignas(64) CUtensorMap w_map;
+    e = make_map_2d(&w_map, CU_TENSOR_MAP_DATA_TYPE_UINT64, flat, (uint64_t)(nkt * BB / 8), (uint64_t)N,
+                    (uint64_t)(nkt * BB), (uint32_t)(kFlatKB * BB / 8), 32u, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess) return e;
+    for (int64_t kt0 = 0; kt0 < nkt; kt0 += nkc) {
+        FlatParams p;
+        p.a_q = a_q;
+        p.a_d = a_d;
+        p.y = y;
+        p.K = K;
+        p.nkt = nkt;
+        p.N = N;
+        p.ldy = ldy;
+        p.n_chunks = n_chunks;
+        p.M = M;
+        p.stages = st;
+        p.kt0 = (int)kt0;
+        p.nkc = (int)((nkt - kt0) < nkc ? (nkt - kt0) : nkc);
+        p.accumulate = kt0 > 0;
+        p.lut = lut_for((qmm_type)TYPE);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid, 1, 1);
+        cfg.blockDim = dim3(32 * (1 + kFlatCW), 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, p, w_map);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+template <int TYPE>
+cudaError_t run_flat_mt(const uint8_t *flat, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d, int M, float *y,
+                        int64_t ldy, cudaStream_t s) {
+    if (M == 1) return run_flat<TYPE, 1>(flat, K, N, a_q, a_d, M, y, ldy, s);
+    if (M == 2) return run_flat<TYPE, 2>(flat, K, N, a_q, a_d, M, y, ldy, s);
+    return run_flat<TYPE, 4>(flat, K, N, a_q, a_d, M, y, ldy, s);
+}
+
 // Groups of at most kDecodeMaxM rows, one launch sequence each.
 template <bool FUSED>
 cudaError_t run_groups(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a, int64_t M, float *y,
@@ -1023,6 +1379,27 @@ cudaError_t launch_matvec_fused(qmm_type t, const uint8_t *tiled, int64_t K, int
                                 int64_t M, float *y, int64_t ldy, cudaStream_t s) {
     const ActSrc a = {nullptr, nullptr, x, ldx};
     return run_groups<true>(t, tiled, K, N, a, M, y, ldy, s);
+}
+
+cudaError_t launch_matvec_flat(qmm_type t, const uint8_t *flat, int64_t K, int64_t N, const int8_t *a_q,
+                               const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s) {
+    const int64_t nkt = K / 32;
+    for (int64_t m0 = 0; m0 < M; m0 += kFlatMT) {
+        const int mm = (int)((M - m0) < kFlatMT ? (M - m0) : kFlatMT);
+        const int8_t *aq = a_q + m0 * K;
+        const uint16_t *ad = a_d + m0 * nkt;
+        float *yy = y + m0 * ldy;
+        cudaError_t e;
+        switch (t) {
+            case QMM_Q4_0: e = run_flat_mt<QMM_Q4_0>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
+            case QMM_IQ4_NL: e = run_flat_mt<QMM_IQ4_NL>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
+            case QMM_MXFP4: e = run_flat_mt<QMM_MXFP4>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
+            case QMM_Q4_1: e = run_flat_mt<QMM_Q4_1>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
+            default: e = run_flat_mt<QMM_Q8_0>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t read_and_clear_matvec_status(unsigned *out, cudaStream_t s) {

@@ -138,6 +138,14 @@ qmm_status qmm_matmul_f32(qmm_type t, const void *w_tiled, int64_t K, int64_t N,
     return from_cuda(launch_matvec_fused(t, static_cast<const uint8_t *>(w_tiled), K, N, x, ldx, M, y, ldy, cs(stream)));
 }
 
+qmm_status qmm_matmul_flat(qmm_type t, const void *w_flat, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
+                           int64_t M, float *y, int64_t ldy, qmm_stream_t stream) {
+    qmm_status st = check_matmul(t, w_flat, K, N, a_q, a_d, M, y, ldy);
+    if (st != QMM_OK) return st;
+    if (((K / 32) * block_bytes(t)) % 16 != 0) return QMM_ERR_UNSUPPORTED;   // rows are copied as 16-byte units
+    return from_cuda(launch_matvec_flat(t, static_cast<const uint8_t *>(w_flat), K, N, a_q, a_d, M, y, ldy, cs(stream)));
+}
+
 size_t qmm_matmul_workspace_size(int64_t M, int64_t K) {
     if (M <= 0 || K <= 0 || (K % 32) != 0 || M > kMaxDim || K > kMaxDim) return 0;
     return gemm_workspace_bytes(M, K);

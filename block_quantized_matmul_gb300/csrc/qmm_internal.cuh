@@ -1,6 +1,7 @@
 // qmm_internal.cuh -- declarations shared by the libqmm translation units (product code only).
 #pragma once
 
+#include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched through the runtime)
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -114,6 +115,12 @@ cudaError_t launch_unpack(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N
                           cudaStream_t s);
 cudaError_t launch_matvec(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                           const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
+// 2-D tensor map: rows of `inner` elements (row stride `row_bytes`), box {box_inner, box_rows}.
+cudaError_t make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw);
+// Decode matmul straight from flat GGML rows (K % 512 == 0, flat 16-byte aligned).
+cudaError_t launch_matvec_flat(qmm_type t, const uint8_t *flat, int64_t K, int64_t N, const int8_t *a_q,
+                               const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
 cudaError_t launch_matvec_fused(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
                                 int64_t M, float *y, int64_t ldy, cudaStream_t s);
 cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,

@@ -142,7 +142,8 @@ QMM_API qmm_status qmm_quantize_act(const float *x_dev, int64_t M, int64_t K, in
  * qmm_matmul -- Y = A * W^T over tiled weights:
  *   Y[m, n] = sum_b fp32(d_w[n, b]) * fp32(d_a[m, b]) * S_b[m, n],
  *   S_b[m, n] = sum_{j<32} w_int[n, 32b+j] * a_q[m, 32b+j]  (exact integer block dot products),
- *   w_int = q-8 (Q4_0), q (Q8_0), table[q] (IQ4_NL).
+ *   w_int = q-8 (Q4_0), q (Q8_0), table[q] (IQ4_NL), 2*fp4(q) with d_w = half the E8M0 scale
+ *   (MXFP4); Q4_1 adds fp32(m_w[n, b]) * fp32(d_a[m, b]) * sum_j a_q[m, 32b+j] with w_int = q.
  *   w_tiled_dev  qmm_tiled_size bytes from qmm_repack; 16-byte aligned.
  *   a_q_dev, a_d_dev  as written by qmm_quantize_act for M rows and the same K.
  *   y_dev  fp32 output, y[m*ldy + n] for n < N (other columns untouched); 4-byte aligned.
@@ -179,6 +180,26 @@ QMM_API qmm_status qmm_matmul(qmm_type t, const void *w_tiled_dev, int64_t K, in
  */
 QMM_API qmm_status qmm_matmul_f32(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N, const float *x_dev,
                                   int64_t ldx, int64_t M, float *y_dev, int64_t ldy, qmm_stream_t stream);
+
+/*
+ * qmm_matmul_flat -- the product of qmm_matmul taken straight from flat GGML rows, without tiles.
+ * "Hexagon backend developer details", "Op and Kernel Development Guidelines", section "supports_op
+ * Independence from Buffer and Repack State": tensors that are not repacked stay flat, so every
+ * supported type must work both tiled and flat.
+ *   w_flat_dev  N rows of K/32 blocks (qmm_flat_size bytes, the layout qmm_quantize_weight writes);
+ *               16-byte aligned, and a row must be a whole number of 16-byte units:
+ *               (K/32) * qmm_block_size(t) % 16 == 0 (true for every type when K % 512 == 0).
+ *   a_q_dev, a_d_dev, y_dev  as for qmm_matmul.
+ * The same block products and the same error bound as qmm_matmul (the summation order differs, so
+ * results agree within that bound, not bit for bit).  A decode kernel: rows of A are processed in
+ * groups of 4, each group streaming the whole weight once; for prefill shapes repack and use
+ * qmm_matmul.  Launch overlap as for qmm_matmul.
+ * Errors: INVALID_ARG (sizes, ldy < N, NULL), UNSUPPORTED (type, or a row length that is not a
+ * multiple of 16 bytes), MISALIGNED, CUDA.
+ */
+QMM_API qmm_status qmm_matmul_flat(qmm_type t, const void *w_flat_dev, int64_t K, int64_t N,
+                                   const int8_t *a_q_dev, const uint16_t *a_d_dev, int64_t M, float *y_dev,
+                                   int64_t ldy, qmm_stream_t stream);
 
 /* qmm_matmul_path -- qmm_matmul with the kernel chosen by the caller.  QMM_PATH_MATVEC accepts any
  * M (rows are processed in groups of qmm_decode_max_m()); QMM_PATH_GEMM any M >= 1. */

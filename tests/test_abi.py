@@ -159,3 +159,18 @@ def test_matmul_f32_argument_errors(L):
     assert f(0, P + 8, 64, 64, P, 64, 1, P, 64, None) == MISALIGNED
     assert f(0, P, 64, 64, P + 2, 64, 1, P, 64, None) == MISALIGNED
     assert f(0, P, 64, 64, P, 64, 1, P + 1, 64, None) == MISALIGNED
+
+
+def test_matmul_flat_argument_errors(L):
+    f = L.qmm_matmul_flat
+    assert f(0, P, 48, 64, P, P, 1, P, 64, None) == INVALID       # K % 32
+    assert f(0, P, 512, 64, P, P, 0, P, 64, None) == INVALID      # M = 0
+    assert f(0, P, 512, 64, P, P, 1, P, 63, None) == INVALID      # ldy < N
+    assert f(0, None, 512, 64, P, P, 1, P, 64, None) == INVALID   # NULL weight
+    assert f(99, P, 512, 64, P, P, 1, P, 64, None) == UNSUPPORTED
+    assert f(0, P + 8, 512, 64, P, P, 1, P, 64, None) == MISALIGNED
+    # a flat row must be a whole number of 16-byte units: 2 Q4_0 blocks = 36 B, 4 Q8_0 blocks = 136 B,
+    # 8 MXFP4 blocks = 136 B
+    assert f(0, P, 64, 64, P, P, 1, P, 64, None) == UNSUPPORTED
+    assert f(1, P, 128, 64, P, P, 1, P, 64, None) == UNSUPPORTED
+    assert f(3, P, 256, 64, P, P, 1, P, 64, None) == UNSUPPORTED
