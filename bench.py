@@ -40,12 +40,16 @@ OTHERS = [("q4_0", 4096, 4096, 1), ("iq4_nl", 4096, 4096, 8), ("q8_0", 4096, 128
           # MXFP4 tiles (the next format of the pages' tile family), decode and prefill shapes
           ("mxfp4", 4096, 14336, 1), ("mxfp4", 4096, 14336, 512),
           # Q4_1 tiles (d and m per row)
-          ("q4_1", 4096, 14336, 1), ("q4_1", 4096, 14336, 512)]
+          ("q4_1", 4096, 14336, 1), ("q4_1", 4096, 14336, 512),
+          # flat (untiled) GGML rows, decode
+          ("q4_0", 4096, 14336, 1, "flat"), ("q8_0", 4096, 14336, 1, "flat"), ("mxfp4", 4096, 14336, 1, "flat")]
 METRIC = "tiled Q4_0/Q8_0 matvec weight GB/s (% HBM peak); prefill int8 GEMM TOPS"
 
 
-def workload_name(type_, K, N, M):
+def workload_name(type_, K, N, M, layout="tiled"):
     kind = "prefill_gemm" if M > 16 else ("matvec" if M == 1 else "matmul")
+    if layout == "flat":
+        kind = "flat_" + kind
     return f"{type_}_{kind}_K{K}_N{N}_M{M}"
 
 
@@ -146,10 +150,12 @@ def recorded_traffic(workload):
 # GPU arm
 # ---------------------------------------------------------------------------------------------
 class Workload:
-    def __init__(self, torch, qmm, type_, K, N, M, seed=0, copies=None):
+    def __init__(self, torch, qmm, type_, K, N, M, layout="tiled", seed=0, copies=None):
         self.torch, self.qmm = torch, qmm
         self.type_, self.K, self.N, self.M = type_, K, N, M
-        self.tiled_bytes = qmm.tiled_size(type_, K, N)
+        # flat: the decode matmul reads the GGML rows as they are (qmm_matmul_flat), no repack
+        self.flat_layout = layout == "flat"
+        self.tiled_bytes = qmm.flat_size(type_, K, N) if self.flat_layout else qmm.tiled_size(type_, K, N)
         g = torch.Generator(device="cuda")
         g.manual_seed(seed)
         # weights ~ N(0, 0.02^2), quantized and repacked once on the GPU (model-load path)
@@ -165,7 +171,10 @@ class Workload:
         self.tiled = []
         for _ in range(self.copies):
             t = torch.empty(self.tiled_bytes, dtype=torch.uint8, device="cuda")
-            qmm.qmm_repack(type_, flat, K, N, t)
+            if self.flat_layout:
+                t.copy_(flat)
+            else:
+                qmm.qmm_repack(type_, flat, K, N, t)
             self.tiled.append(t)
         del flat
         # activations ~ N(0,1), 1 % outliers x20 for the prefill workload
@@ -184,7 +193,7 @@ class Workload:
         self.ws_ptr = (self.ws.data_ptr() + (-self.ws.data_ptr()) % 256) if self.ws_bytes else None
         # decode shapes up to 4 tokens run the fused kernel (qmm_matmul_f32); from 5 tokens on the two
         # calls are faster (the fused kernel quantizes all M rows in every CTA)
-        self.fused = M <= 4
+        self.fused = M <= 4 and not self.flat_layout
         torch.cuda.synchronize()
 
     def step(self, i, stream):
@@ -208,7 +217,10 @@ class Workload:
             self.matmul_only(i, stream)
 
     def matmul_only(self, i, stream):
-        if self.ws_bytes:
+        if self.flat_layout:
+            self.qmm.qmm_matmul_flat(self.type_, self.tiled[i % self.copies], self.K, self.N, self.a_q, self.a_d,
+                                     self.M, self.y, self.N, stream=stream)
+        elif self.ws_bytes:
             self.qmm.qmm_matmul_ws(self.type_, self.tiled[i % self.copies], self.K, self.N, self.a_q, self.a_d, self.M,
                                    self.y, self.N, self.ws_ptr, self.ws_bytes, stream=stream)
         else:
@@ -225,9 +237,12 @@ class Workload:
         """Kernels of this library launched by one step: the decode kernel once per 16-row group and K
         pass (K is split only beyond its 64 KB activation staging budget), plus the activation
         quantizer unless it is fused; or quantize + activation prepare + GEMM."""
+        nkt = self.K // 32
+        if self.flat_layout:       # groups of 4 rows, K passes of at most 384 blocks
+            return 1 + -(-self.M // 4) * -(-nkt // min(nkt, 384))
         if self.M > 16:
             return 3
-        n, nkt = (0 if self.fused else 1), self.K // 32
+        n = 0 if self.fused else 1
         for m0 in range(0, self.M, 16):
             mm = min(16, self.M - m0)
             mt = mm if mm > 4 else (mm if mm <= 2 else 4)
@@ -391,6 +406,7 @@ def run_gpu(args):
             del og
             okms = kernel_time(torch, o, min(n, 200), stream)
             ent = {"workload": workload_name(*cfg), "ms_per_step": round(oms, 5), "kernel_us": round(okms * 1e3, 3),
+                   "launches_per_step": o.launches_per_step(),
                    "weight_GBps": round(o.tiled_bytes / (oms * 1e-3) / 1e9, 1)}
             kbytes = o.algorithmic_bytes() / (okms * 1e-3) / 1e9
             ent["roofline_hbm"] = {"achieved": round(kbytes, 1), "peak": hbm_peak, "unit": "GB/s",
