@@ -7,8 +7,8 @@ it, and it shares no code with the product: the arithmetic lives in ``oracle/ora
 ``oracle.build()``; this module only marshals numpy arrays through ctypes.
 
 What it follows ("Hexagon backend developer details", "Tiled Weight Formats"): the tile grid of
-"Tile Dimensions and Grid Layout" and the Q4_0 / Q8_0 / IQ4_NL / MXFP4 / Q4_1 tile byte layouts of
-"Block-32 Quantized Formats".  The readings taken where the pages are silent are listed in ``oracle.c``.
+"Tile Dimensions and Grid Layout", the Q4_0 / Q8_0 / IQ4_NL / MXFP4 / Q4_1 tile byte layouts of
+"Block-32 Quantized Formats" and the Q4_K tile of "K-Quants Formats".  The readings taken where the pages are silent are listed in ``oracle.c``.
 """
 from __future__ import annotations
 
@@ -19,8 +19,8 @@ import threading
 
 import numpy as np
 
-Q4_0, Q8_0, IQ4_NL, MXFP4, Q4_1 = 0, 1, 2, 3, 4
-TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL, "mxfp4": MXFP4, "q4_1": Q4_1}
+Q4_0, Q8_0, IQ4_NL, MXFP4, Q4_1, Q4_K = 0, 1, 2, 3, 4, 5
+TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL, "mxfp4": MXFP4, "q4_1": Q4_1, "q4_k": Q4_K}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -55,6 +55,8 @@ def _load():
             for fn in ("orc_block_bytes", "orc_tile_bytes"):
                 getattr(lib, fn).argtypes = [i32]
                 getattr(lib, fn).restype = i64
+            lib.orc_row_bytes.argtypes = [i32, i64]
+            lib.orc_row_bytes.restype = i64
             lib.orc_tile_index.argtypes = [i64, i64, i64]
             lib.orc_tile_index.restype = i64
             lib.orc_tiled_bytes.argtypes = [i32, i64, i64]
@@ -115,6 +117,15 @@ def block_bytes(type_) -> int:
     return int(_load().orc_block_bytes(_t(type_)))
 
 
+def row_bytes(type_, K: int) -> int:
+    """Bytes of one flat row of K weights (K/32 blocks, or K/256 Q4_K super-blocks)."""
+    return int(_load().orc_row_bytes(_t(type_), K))
+
+
+def _check_k(type_, K: int) -> None:
+    assert K % 32 == 0 and (_t(type_) != Q4_K or K % 256 == 0), "K must be a multiple of the block length"
+
+
 def tile_bytes(type_) -> int:
     return int(_load().orc_tile_bytes(_t(type_)))
 
@@ -137,11 +148,11 @@ def quantize_block_q8_0(x: np.ndarray):
 
 
 def quantize_rows(type_, w: np.ndarray, lut=None) -> np.ndarray:
-    """fp32 [N, K] -> flat GGML blocks, uint8 [N, K/32 * block_bytes]."""
+    """fp32 [N, K] -> flat GGML blocks, uint8 [N, row_bytes(K)]."""
     w = np.ascontiguousarray(w, dtype=np.float32)
     N, K = w.shape
-    assert K % 32 == 0
-    out = np.zeros((N, K // 32 * block_bytes(type_)), np.uint8)
+    _check_k(type_, K)
+    out = np.zeros((N, row_bytes(type_, K)), np.uint8)
     lt = _lut(lut)
     _load().orc_quantize_rows(_t(type_), _p(w), N, K, _p(lt), _p(out))
     return out
@@ -149,7 +160,8 @@ def quantize_rows(type_, w: np.ndarray, lut=None) -> np.ndarray:
 
 def dequantize_flat(type_, flat: np.ndarray, N: int, K: int, lut=None) -> np.ndarray:
     flat = np.ascontiguousarray(flat, dtype=np.uint8)
-    assert flat.size == N * (K // 32) * block_bytes(type_)
+    _check_k(type_, K)
+    assert flat.size == N * row_bytes(type_, K)
     out = np.zeros((N, K), np.float64)
     lt = _lut(lut)
     _load().orc_dequantize_flat(_t(type_), _p(flat), N, K, _p(lt), _p(out))
@@ -158,13 +170,18 @@ def dequantize_flat(type_, flat: np.ndarray, N: int, K: int, lut=None) -> np.nda
 
 def repack(type_, flat: np.ndarray, K: int, N: int) -> np.ndarray:
     flat = np.ascontiguousarray(flat, dtype=np.uint8)
-    assert flat.size == N * (K // 32) * block_bytes(type_)
+    _check_k(type_, K)
+    assert flat.size == N * row_bytes(type_, K)
     out = np.zeros(tiled_bytes(type_, K, N), np.uint8)
     _load().orc_repack(_t(type_), _p(flat), K, N, _p(out))
     return out
 
 
 def unpack(type_, tiled: np.ndarray, K: int, N: int) -> np.ndarray:
+    """Tiles -> flat rows for the block-32 types (a Q4_K tile holds rounded products of the
+    super-block's fields, which cannot be split back)."""
+    if _t(type_) == Q4_K:
+        raise ValueError("Q4_K tiles cannot be unpacked")
     tiled = np.ascontiguousarray(tiled, dtype=np.uint8)
     assert tiled.size == tiled_bytes(type_, K, N)
     out = np.zeros((N, K // 32 * block_bytes(type_)), np.uint8)

@@ -40,6 +40,17 @@
  *     fp16 scale, which is the same product.  Quantizer (test data): e = floor(log2 amax) - 2 + 127
  *     (0 for an all-zero block, clamped to 0..254), then the nearest FP4 level under the dequantizing
  *     scale, lowest code on ties.
+ *   - Q4_K ("K-Quants Formats": the Q4_1 tile, each 256-k super-block split along K into 8 tiles of 32
+ *     k, the row pair being (d * sc, -dmin * m) as FP16).  The flat super-block is GGML's block_q4_K,
+ *     which the pages do not print: {fp16 d; fp16 dmin; u8 scales[12]; u8 qs[128]} (144 B per 256
+ *     weights).  Sub-block j (0..7) has a 6-bit scale sc_j and min m_j packed in scales[]: for j < 4
+ *     the low 6 bits of scales[j] and scales[j+4]; for j >= 4 the low and high nibble of scales[j+4]
+ *     plus, as bits 4..5, the top two bits of scales[j-4] and scales[j].  Weight i of sub-block j is
+ *     nibble (j & 1) of qs[32*(j/2) + i], worth d*sc_j*q - dmin*m_j.  The tile row pair is
+ *     fp16(f32(d)*sc_j) and fp16(-(f32(dmin)*m_j)) (exact fp32 products, rounded to nearest even).
+ *     Quantizer (test data): per sub-block mn = min(0, min x), range = max x - mn, scale = range/15,
+ *     min = -mn; d = max scale/63, dmin = max min/63 (fp16); sc_j, m_j = trunc(v*(63/max) + 0.5)
+ *     clamped to 63; then q = min(15, trunc((x + f32(dmin)*m_j) * (1/(f32(d)*sc_j)) + 0.5)).
  *   - Matmul: Y[m,n] = sum_b f64(d_w[n,b]) * f64(d_a[m,b]) * S_b[m,n], where S_b is the exact integer
  *     dot product of the block's integer weights (q-8, q, lut[q]) and activation quants.  The oracle
  *     also returns B[m,n] = sum_b sum_j |d_w*w_int * d_a*q_a|, the scale of the error bound.
@@ -51,7 +62,10 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORC_Q4_0 = 0, ORC_Q8_0 = 1, ORC_IQ4_NL = 2, ORC_MXFP4 = 3, ORC_Q4_1 = 4 };
+enum { ORC_Q4_0 = 0, ORC_Q8_0 = 1, ORC_IQ4_NL = 2, ORC_MXFP4 = 3, ORC_Q4_1 = 4, ORC_Q4_K = 5 };
+
+/* Types whose tile holds a (d, m) pair per row: weight = d*q + m. */
+static int affine_tile(int type) { return type == ORC_Q4_1 || type == ORC_Q4_K; }
 
 /* OCP Microscaling FP4 (E2M1): code = sign<<3 | exponent<<1 | mantissa; value = 0.5 * mantissa for
  * exponent 0, else 2^(exponent-1) * (1 + mantissa/2).  Twice the value, as an integer. */
@@ -144,7 +158,15 @@ int64_t orc_block_bytes(int type)
     if (type == ORC_Q8_0) return 34;                        /* fp16 d + 32 int8 */
     if (type == ORC_MXFP4) return 17;                       /* E8M0 e + 16 bytes of nibbles */
     if (type == ORC_Q4_1) return 20;                        /* fp16 d + fp16 m + 16 bytes of nibbles */
+    if (type == ORC_Q4_K) return 144;                       /* one super-block of 256 weights */
     return 0;
+}
+
+/* Bytes of one flat row of K weights. */
+int64_t orc_row_bytes(int type, int64_t K)
+{
+    if (type == ORC_Q4_K) return K / 256 * 144;
+    return K / 32 * orc_block_bytes(type);
 }
 
 int64_t orc_tile_bytes(int type)
@@ -152,7 +174,7 @@ int64_t orc_tile_bytes(int type)
     if (type == ORC_Q4_0 || type == ORC_IQ4_NL) return 576;  /* 512 quant bytes + 32 fp16 scales */
     if (type == ORC_Q8_0) return 1088;                       /* 1024 quant bytes + 32 fp16 scales */
     if (type == ORC_MXFP4) return 544;                       /* 512 quant bytes + 32 E8M0 exponents */
-    if (type == ORC_Q4_1) return 640;                        /* 512 quant bytes + 32 fp16 (d, m) pairs */
+    if (type == ORC_Q4_1 || type == ORC_Q4_K) return 640;    /* 512 quant bytes + 32 fp16 (d, m) pairs */
     return 0;
 }
 
@@ -191,14 +213,14 @@ static void flat_set_code(int type, uint8_t *blk, int j, int code)
     else qs[j - 16] = (uint8_t)((qs[j - 16] & 0x0F) | ((code & 0x0F) << 4));
 }
 
-/* Integer weight value of a code: Q4_0 q-8, Q8_0 q, IQ4_NL lut[q] (BASELINE dequant rules; IQ4_NL
- * per "Block-32 Quantized Formats": index looked up in the 16-entry table, times the row scale). */
+/* Integer weight value of a code: Q4_0 q-8, Q8_0 q, IQ4_NL lut[q] (IQ4_NL per "Block-32 Quantized
+ * Formats": the index is looked up in the 16-entry table, then scaled by the row scale). */
 static int weight_int(int type, int code, const int8_t *lut)
 {
     if (type == ORC_Q4_0) return code - 8;
     if (type == ORC_Q8_0) return code;
     if (type == ORC_MXFP4) return e2m1_twice(code & 15);
-    if (type == ORC_Q4_1) return code;
+    if (affine_tile(type)) return code;
     return (int)lut[code & 15];
 }
 
@@ -207,7 +229,7 @@ static int weight_int(int type, int code, const int8_t *lut)
 /* The additive min of a block (Q4_1 only; 0 otherwise). */
 static double block_min(int type, const uint8_t *scale_bytes)
 {
-    if (type == ORC_Q4_1) return (double)orc_f16_to_f32(load_u16(scale_bytes + 2));
+    if (affine_tile(type)) return (double)orc_f16_to_f32(load_u16(scale_bytes + 2));
     return 0.0;
 }
 
@@ -337,10 +359,85 @@ static void quantize_block_mxfp4(const float *x, uint8_t *codes, uint8_t *e_out)
     }
 }
 
+/* Q4_K super-block access.  scales[] packing of the 6-bit (sc, m) of sub-block j, see the header. */
+static void q4k_scale_min(const uint8_t *scales, int j, int *sc, int *m)
+{
+    if (j < 4) {
+        *sc = scales[j] & 63;
+        *m = scales[j + 4] & 63;
+    } else {
+        *sc = (scales[j + 4] & 0x0F) | ((scales[j - 4] >> 6) << 4);
+        *m = (scales[j + 4] >> 4) | ((scales[j] >> 6) << 4);
+    }
+}
+
+static int q4k_code(const uint8_t *sb, int j, int i) { return (sb[16 + 32 * (j / 2) + i] >> (4 * (j & 1))) & 15; }
+
+static int clamp63(float v)   /* trunc(v) for v >= 0, clamped to 0..63 (0 for NaN) */
+{
+    if (!(v >= 0.0f)) return 0;
+    if (v >= 63.0f) return 63;
+    return (int)v;
+}
+
+static void quantize_superblock_q4_k(const float *x, uint8_t *sb)
+{
+    float scale[8], mins[8], max_scale = 0.0f, max_min = 0.0f;
+    for (int j = 0; j < 8; ++j) {
+        const float *xj = x + 32 * j;
+        float mn = 0.0f, mx = xj[0];
+        for (int i = 0; i < 32; ++i) {
+            if (xj[i] < mn) mn = xj[i];
+            if (xj[i] > mx) mx = xj[i];
+        }
+        float range = mx - mn;
+        if (!(range > 0.0f)) range = 0.0f;
+        scale[j] = range / 15.0f;
+        mins[j] = 0.0f - mn;
+        if (scale[j] > max_scale) max_scale = scale[j];
+        if (mins[j] > max_min) max_min = mins[j];
+    }
+    const float isc = max_scale > 0.0f ? 63.0f / max_scale : 0.0f;
+    const float imn = max_min > 0.0f ? 63.0f / max_min : 0.0f;
+    const uint16_t d16 = orc_f32_to_f16(max_scale / 63.0f), dmin16 = orc_f32_to_f16(max_min / 63.0f);
+    int sc[8], m[8];
+    for (int j = 0; j < 8; ++j) {
+        sc[j] = clamp63(scale[j] * isc + 0.5f);
+        m[j] = clamp63(mins[j] * imn + 0.5f);
+    }
+    memset(sb, 0, 144);
+    store_u16(sb, d16);
+    store_u16(sb + 2, dmin16);
+    for (int i = 0; i < 4; ++i) {
+        sb[4 + i] = (uint8_t)((sc[i] & 63) | ((sc[i + 4] >> 4) << 6));
+        sb[8 + i] = (uint8_t)((m[i] & 63) | ((m[i + 4] >> 4) << 6));
+        sb[12 + i] = (uint8_t)((sc[i + 4] & 15) | ((m[i + 4] & 15) << 4));
+    }
+    const float d = orc_f16_to_f32(d16), dmin = orc_f16_to_f32(dmin16);
+    for (int j = 0; j < 8; ++j) {
+        const float D = d * (float)sc[j], M = dmin * (float)m[j];   /* exact products */
+        const float id = D != 0.0f ? 1.0f / D : 0.0f;
+        for (int i = 0; i < 32; ++i) {
+            float v = (x[32 * j + i] + M) * id + 0.5f;
+            int c;
+            if (!(v >= 0.0f)) c = 0;
+            else if (v >= 15.0f) c = 15;
+            else c = (int)v;
+            sb[16 + 32 * (j / 2) + i] |= (uint8_t)(c << (4 * (j & 1)));
+        }
+    }
+}
+
 /* Quantize N rows of K floats (row n at w + n*K) into flat GGML blocks, row after row. */
 void orc_quantize_rows(int type, const float *w, int64_t N, int64_t K, const int8_t *lut, uint8_t *flat)
 {
     int64_t nb = K / 32, bb = orc_block_bytes(type);
+    if (type == ORC_Q4_K) {
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t b = 0; b < K / 256; ++b)
+                quantize_superblock_q4_k(w + n * K + b * 256, flat + n * orc_row_bytes(type, K) + b * 144);
+        return;
+    }
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t b = 0; b < nb; ++b) {
             const float *x = w + n * K + b * 32;
@@ -378,6 +475,20 @@ void orc_quantize_rows(int type, const float *w, int64_t N, int64_t K, const int
 void orc_dequantize_flat(int type, const uint8_t *flat, int64_t N, int64_t K, const int8_t *lut, double *out)
 {
     int64_t nb = K / 32, bb = orc_block_bytes(type);
+    if (type == ORC_Q4_K) {   /* d*sc_j*q - dmin*m_j in fp64 */
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t b = 0; b < K / 256; ++b) {
+                const uint8_t *sb = flat + n * orc_row_bytes(type, K) + b * 144;
+                double d = orc_f16_to_f32(load_u16(sb)), dmin = orc_f16_to_f32(load_u16(sb + 2));
+                for (int j = 0; j < 8; ++j) {
+                    int sc, m;
+                    q4k_scale_min(sb + 4, j, &sc, &m);
+                    for (int i = 0; i < 32; ++i)
+                        out[n * K + b * 256 + 32 * j + i] = d * sc * q4k_code(sb, j, i) - dmin * m;
+                }
+            }
+        return;
+    }
     for (int64_t n = 0; n < N; ++n)
         for (int64_t b = 0; b < nb; ++b) {
             const uint8_t *blk = flat + (n * nb + b) * bb;
@@ -403,6 +514,17 @@ void orc_repack(int type, const uint8_t *flat, int64_t K, int64_t N, uint8_t *ti
             for (int r = 0; r < 32; ++r) {
                 int64_t n = ct * 32 + r;
                 if (n >= N) continue;
+                if (type == ORC_Q4_K) {   /* tile kt = sub-block kt % 8 of super-block kt / 8 */
+                    const uint8_t *sb = flat + n * orc_row_bytes(type, K) + (kt / 8) * 144;
+                    int j = (int)(kt % 8), sc, m;
+                    q4k_scale_min(sb + 4, j, &sc, &m);
+                    for (int cp = 0; cp < 16; ++cp)
+                        tile[cp * 32 + r] = (uint8_t)(q4k_code(sb, j, 2 * cp) | (q4k_code(sb, j, 2 * cp + 1) << 4));
+                    float d = orc_f16_to_f32(load_u16(sb)), dmin = orc_f16_to_f32(load_u16(sb + 2));
+                    store_u16(tile + scale_off + 4 * r, orc_f32_to_f16(d * (float)sc));
+                    store_u16(tile + scale_off + 4 * r + 2, orc_f32_to_f16(-(dmin * (float)m)));
+                    continue;
+                }
                 const uint8_t *blk = flat + (n * n_k_tiles + kt) * bb;
                 for (int cp = 0; cp < 16; ++cp) {
                     int c0 = flat_code(type, blk, 2 * cp);
@@ -426,8 +548,10 @@ void orc_repack(int type, const uint8_t *flat, int64_t K, int64_t N, uint8_t *ti
         }
 }
 
+/* Inverse of orc_repack for the block-32 types (Q4_K's tile products cannot be split back). */
 void orc_unpack(int type, const uint8_t *tiled, int64_t K, int64_t N, uint8_t *flat)
 {
+    if (type == ORC_Q4_K) return;
     int64_t n_k_tiles = K / 32;
     int64_t ts = orc_tile_bytes(type), bb = orc_block_bytes(type);
     int64_t scale_off = (type == ORC_Q8_0) ? 1024 : 512;
@@ -481,12 +605,12 @@ static double tiled_scale(int type, const uint8_t *tiled, int64_t n_k_tiles, int
     int r = (int)(n % 32);
     const uint8_t *tile = tiled + orc_tile_index(ct, kt, n_k_tiles) * orc_tile_bytes(type);
     int64_t scale_off = (type == ORC_Q8_0) ? 1024 : 512;
-    return block_scale(type, tile + scale_off + (type == ORC_MXFP4 ? r : (type == ORC_Q4_1 ? 4 * r : 2 * r)));
+    return block_scale(type, tile + scale_off + (type == ORC_MXFP4 ? r : (affine_tile(type) ? 4 * r : 2 * r)));
 }
 
 static double tiled_min(int type, const uint8_t *tiled, int64_t n_k_tiles, int64_t n, int64_t kt)
 {
-    if (type != ORC_Q4_1) return 0.0;
+    if (!affine_tile(type)) return 0.0;
     const uint8_t *tile = tiled + orc_tile_index(n / 32, kt, n_k_tiles) * orc_tile_bytes(type);
     return block_min(type, tile + 512 + 4 * (n % 32));
 }
@@ -531,7 +655,7 @@ static void one_output(int type, const uint8_t *tiled, int64_t K, const int8_t *
         }
         /* sum_j (dw*w_j + mw) * da * a_j = da * (dw * S_b + mw * sum_j a_j) */
         acc += dw * da * (double)s + mw * da * (double)asum;
-        bacc += (type == ORC_Q4_1) ? fabs(da) * babs : fabs(dw * da) * (double)sabs;
+        bacc += affine_tile(type) ? fabs(da) * babs : fabs(dw * da) * (double)sabs;
     }
     *y = acc;
     *bound = bacc;

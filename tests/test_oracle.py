@@ -446,3 +446,108 @@ def test_q4_1_quantizer_hits_the_block_extremes(orc):
             assert d == np.float16((np.float32(x.max()) - np.float32(x.min())) / np.float32(15))
             codes = [(blk[4 + j] & 15) if j < 16 else (blk[4 + j - 16] >> 4) for j in range(32)]
             assert codes[int(np.argmin(x))] == 0 and codes[int(np.argmax(x))] == 15
+
+
+# ---------------------------------------------------------------------------------------------
+# Q4_K ("K-Quants Formats"): super-blocks of 256, tiles = the Q4_1 tile with (d*sc, -dmin*m)
+# ---------------------------------------------------------------------------------------------
+def _q4k_fixture():
+    spec = {"sm": [], "w": [], "pair": [], "tb": []}
+    sb = np.zeros(144, np.uint8)
+    for line in open(os.path.join(GOLDEN, "q4_k_superblock.txt")):
+        line = line.split("#")[0].split()
+        if not line:
+            continue
+        key, vals = line[0], line[1:]
+        if key == "d":
+            sb[0:2] = np.array([int(vals[0], 16)], np.uint16).view(np.uint8)
+        elif key == "dmin":
+            sb[2:4] = np.array([int(vals[0], 16)], np.uint16).view(np.uint8)
+        elif key == "scales":
+            sb[4:16] = [int(v, 16) for v in vals]
+        else:
+            spec[key].append([int(v, 0) if key != "w" else float(v) for v in vals])
+    sb[16:] = [(7 * b + 3) % 256 for b in range(128)]
+    return sb, spec
+
+
+def _tile_weights_q4_k(tiled, K, N):
+    """Dequantize Q4_K tiles with numpy, from the tile layout alone: code = nibble of byte
+    cp*32 + r, weight = fp16 d' * code + fp16 m' (the pair at 512 + 4r)."""
+    nkt = K // 32
+    W = np.zeros((N, K))
+    for n in range(N):
+        ct, r = divmod(n, 32)
+        for kt in range(nkt):
+            t = tiled[(ct * nkt + kt) * 640:(ct * nkt + kt + 1) * 640]
+            d, m = t[512 + 4 * r:516 + 4 * r].view(np.float16).astype(np.float64)
+            for c in range(32):
+                b = int(t[(c // 2) * 32 + r])
+                W[n, kt * 32 + c] = d * ((b >> 4) if c & 1 else (b & 15)) + m
+    return W
+
+
+def test_q4_k_hand_worked_superblock(orc):
+    sb, spec = _q4k_fixture()
+    W = orc.dequantize_flat("q4_k", sb, 1, 256)[0]
+    for j, i, w in spec["w"]:
+        assert W[32 * int(j) + int(i)] == w, (j, i)
+    tiled = orc.repack("q4_k", sb, 256, 1)
+    for kt, dbits, mbits in spec["pair"]:
+        t = tiled[kt * 640:(kt + 1) * 640]
+        assert int(t[512]) | (int(t[513]) << 8) == dbits and int(t[514]) | (int(t[515]) << 8) == mbits
+    for kt, byte, val in spec["tb"]:
+        assert tiled[kt * 640 + byte] == val
+    # (sc, m) of every sub-block: with d = 1 and dmin = 0.5 the tile pair is (sc, -m/2) exactly
+    for j, sc, m in spec["sm"]:
+        d, mm = tiled[j * 640 + 512:j * 640 + 516].view(np.float16).astype(np.float64)
+        assert d == sc and mm == -0.5 * m
+    # padding rows of the tile and rows past N are zero
+    assert not tiled[0 * 640 + 1:0 * 640 + 32].any()
+    with pytest.raises(ValueError):
+        orc.unpack("q4_k", tiled, 256, 1)
+
+
+@pytest.mark.parametrize("K,N,M", [(256, 1, 1), (512, 33, 3), (768, 64, 2)])
+def test_q4_k_tile_product(orc, K, N, M):
+    """The tiled product equals fp64 brute force over the numpy-decoded tiles, and each tile weight is
+    the flat super-block weight up to the fp16 rounding of d*sc and dmin*m (2^-11 relative each)."""
+    w = synth.weights(N, K, seed=K + 3 * N)
+    x = synth.activations(M, K, seed=M + 11, outliers=True)
+    flat = orc.quantize_rows("q4_k", w)
+    tiled = orc.repack("q4_k", flat, K, N)
+    Wt = _tile_weights_q4_k(tiled, K, N)
+    Wf = orc.dequantize_flat("q4_k", flat, N, K)
+    mprime = np.repeat(np.abs(np.stack([tiled[(n // 32 * (K // 32) + kt) * 640 + 514 + 4 * (n % 32):][:2].view(np.float16)[0]
+                                        for n in range(N) for kt in range(K // 32)]).astype(np.float64).reshape(N, K // 32)), 32, axis=1)
+    assert np.all(np.abs(Wt - Wf) <= 2.0 ** -11 * (np.abs(Wf) + 2.001 * mprime) + 1e-30)
+    a_q, a_d = orc.quantize_act(x)
+    y, bound = orc.matmul("q4_k", tiled, K, N, a_q, a_d)
+    A = a_q.astype(np.float64) * np.repeat(a_d.view(np.float16).astype(np.float64), 32, axis=1)
+    assert np.allclose(y, A @ Wt.T, rtol=1e-12, atol=1e-15)
+    assert np.allclose(bound, np.abs(A) @ np.abs(Wt).T, rtol=1e-12, atol=1e-15)
+    y41, _ = orc.matmul("q4_1", tiled, K, N, a_q, a_d)     # the same tile read as Q4_1
+    assert np.array_equal(y, y41)
+
+
+def test_q4_k_quantizer_error_bound(orc):
+    """|x - dequant| <= max(D/2, 15 |scale - D| + |min - M|) per sub-block, with the scale and min
+    errors bounded by the 6-bit rounding against d = max scale / 63 and dmin = max min / 63."""
+    K, N = 512, 24
+    w = synth.weights(N, K, seed=31)
+    w[3, :256] = 0.0                                  # an all-zero super-block
+    w[5, 256:] = np.abs(w[5, 256:])                   # a super-block with no negative element
+    flat = orc.quantize_rows("q4_k", w)
+    Wf = orc.dequantize_flat("q4_k", flat, N, K)
+    for n in range(N):
+        for s in range(K // 256):
+            x = w[n, 256 * s:256 * (s + 1)].astype(np.float64).reshape(8, 32)
+            mn = np.minimum(0.0, x.min(axis=1))
+            scale = (x.max(axis=1) - mn) / 15
+            d, dmin = scale.max() / 63, (-mn).max() / 63
+            e_scale = (0.5 + 63 * 2.0 ** -11) * d + 1e-12
+            e_min = (0.5 + 63 * 2.0 ** -11) * dmin + 1e-12
+            err = np.abs(x - Wf[n, 256 * s:256 * (s + 1)].reshape(8, 32)).max(axis=1)
+            lim = np.maximum((scale + e_scale) / 2, 15 * e_scale + e_min) * (1 + 1e-5) + 1e-9
+            assert np.all(err <= lim), (n, s, err, lim)
+    assert not Wf[3, :256].any()
