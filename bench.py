@@ -41,6 +41,8 @@ OTHERS = [("q4_0", 4096, 4096, 1), ("iq4_nl", 4096, 4096, 8), ("q8_0", 4096, 128
           ("mxfp4", 4096, 14336, 1), ("mxfp4", 4096, 14336, 512),
           # Q4_1 tiles (d and m per row)
           ("q4_1", 4096, 14336, 1), ("q4_1", 4096, 14336, 512),
+          # Q4_K super-blocks (read through the Q4_1 tile)
+          ("q4_k", 4096, 14336, 1),
           # flat (untiled) GGML rows, decode
           ("q4_0", 4096, 14336, 1, "flat"), ("q8_0", 4096, 14336, 1, "flat"), ("mxfp4", 4096, 14336, 1, "flat")]
 METRIC = "tiled Q4_0/Q8_0 matvec weight GB/s (% HBM peak); prefill int8 GEMM TOPS"

@@ -15,15 +15,15 @@ import ctypes
 import os
 
 __all__ = [
-    "Q4_0", "Q8_0", "IQ4_NL", "MXFP4", "Q4_1", "TYPES", "QmmError", "lib", "library_path",
+    "Q4_0", "Q8_0", "IQ4_NL", "MXFP4", "Q4_1", "Q4_K", "TYPES", "QmmError", "lib", "library_path",
     "block_size", "tile_size", "tiled_size", "flat_size", "iq4nl_table", "decode_max_m",
     "qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
     "qmm_matmul_path", "qmm_matmul_f32", "qmm_matmul_flat", "qmm_device_status", "PATH_AUTO", "PATH_MATVEC", "PATH_GEMM",
     "matmul_workspace_size", "qmm_matmul_ws", "qmm_matmul_noalloc", "matmul_noalloc_max_workspace",
 ]
 
-Q4_0, Q8_0, IQ4_NL, MXFP4, Q4_1 = 0, 1, 2, 3, 4
-TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL, "mxfp4": MXFP4, "q4_1": Q4_1}
+Q4_0, Q8_0, IQ4_NL, MXFP4, Q4_1, Q4_K = 0, 1, 2, 3, 4, 5
+TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL, "mxfp4": MXFP4, "q4_1": Q4_1, "q4_k": Q4_K}
 PATH_AUTO, PATH_MATVEC, PATH_GEMM = 0, 1, 2
 _STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "QMM_ERR_MISALIGNED",
            4: "QMM_ERR_CUDA", 5: "QMM_ERR_TIMEOUT"}

@@ -1006,9 +1006,11 @@ constexpr int kFlatMT = 4;             // tokens per launch
 
 template <int TYPE>
 struct FlatFmt {
+    // bytes per 32 weights (Q4_K: an eighth of a 144-byte super-block)
     static constexpr int kBlock = TYPE == QMM_Q8_0    ? kBlock8Bytes
                                   : TYPE == QMM_MXFP4 ? kBlockMxBytes
                                   : TYPE == QMM_Q4_1  ? kBlock41Bytes
+                                  : TYPE == QMM_Q4_K  ? kQ4KBytesPer32
                                                       : kBlock4Bytes;
     static constexpr int kHead = TYPE == QMM_MXFP4 ? 1 : (TYPE == QMM_Q4_1 ? 4 : 2);
     // Block words u[i] (bytes 4i..4i+3 of the block) that the code words touch: the last code word
@@ -1101,6 +1103,27 @@ __device__ __forceinline__ void flat_block_words(const uint8_t *base, int blk_of
     }
 }
 
+// Q4_K: sub-block j (0..7) of the super-block at `sb` (4-byte aligned): its 8 code words in natural
+// order, and the row pair of its tile, fp16(d*sc_j) and fp16(-dmin*m_j), so that the flat product
+// is the tiled one.
+__device__ __forceinline__ void flat_q4k_words(const uint8_t *sb_bytes, int j, uint32_t (&W)[8], float &dw, float &mw) {
+    const uint32_t *sb = reinterpret_cast<const uint32_t *>(sb_bytes);
+    const int jj = j & 3;
+    const uint32_t head = sb[0];
+    const uint32_t b0 = (sb[1] >> (8 * jj)) & 0xFF, b1 = (sb[2] >> (8 * jj)) & 0xFF, b2 = (sb[3] >> (8 * jj)) & 0xFF;
+    const uint32_t sc = j < 4 ? (b0 & 63) : ((b2 & 15) | ((b0 >> 6) << 4));
+    const uint32_t m = j < 4 ? (b1 & 63) : ((b2 >> 4) | ((b1 >> 6) << 4));
+    const float d = __low2float(bits_h2(head)), dmin = __high2float(bits_h2(head));
+    dw = __half2float(__float2half_rn(__fmul_rn(d, (float)sc)));
+    mw = __half2float(__float2half_rn(-__fmul_rn(dmin, (float)m)));
+    const uint4 *qs = reinterpret_cast<const uint4 *>(sb + 4 + 8 * (j >> 1));   // 16-byte aligned
+    const uint4 q0 = qs[0], q1 = qs[1];
+    const int sh = 4 * (j & 1);
+    const uint32_t q[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) W[k] = (q[k] >> sh) & 0x0F0F0F0Fu;
+}
+
 // Stage the 32 activations of one (token, block) in the order of flat_block_words, plus d_a and the
 // Q4_0 start value -8 * sum(a) (Q4_1: the sum itself, for the min term).
 template <int TYPE>
@@ -1121,7 +1144,7 @@ __device__ __forceinline__ void stage_flat(const int8_t *a32, float da, uint32_t
     int asum = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) asum = __dp4a((int)a[k], 0x01010101, asum);
-    const int aux = TYPE == QMM_Q4_0 ? -8 * asum : (TYPE == QMM_Q4_1 ? asum : 0);
+    const int aux = TYPE == QMM_Q4_0 ? -8 * asum : (TileFmt<TYPE>::kAffine ? asum : 0);
     *dst_aux = make_uint2(__float_as_uint(da), (uint32_t)aux);
 }
 
@@ -1234,7 +1257,10 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
                     const int row = cw + 16 * r;
                     uint32_t W[8];
                     float dw, mw;
-                    flat_block_words<TYPE>(st, row * kRowStage + lane * BB, W, dw, mw, tb);
+                    if constexpr (TYPE == QMM_Q4_K)
+                        flat_q4k_words(st + row * kRowStage + (lane >> 3) * kSuperQ4KBytes, lane & 7, W, dw, mw);
+                    else
+                        flat_block_words<TYPE>(st, row * kRowStage + lane * BB, W, dw, mw, tb);
 #pragma unroll
                     for (int t = 0; t < MT; ++t) {
                         if (t >= p.M) break;
@@ -1249,7 +1275,8 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
                         S = __dp4a((int)W[7], (int)aw[t][1].w, S);
                         const float da = __uint_as_float(ax[t].x);
                         acc[r][t] = fmaf((float)S, __fmul_rn(dw, da), acc[r][t]);
-                        if constexpr (TYPE == QMM_Q4_1) acc[r][t] = fmaf((float)(int)ax[t].y, __fmul_rn(mw, da), acc[r][t]);
+                        if constexpr (TileFmt<TYPE>::kAffine)
+                            acc[r][t] = fmaf((float)(int)ax[t].y, __fmul_rn(mw, da), acc[r][t]);
                     }
                 }
             }
@@ -1395,6 +1422,7 @@ cudaError_t launch_matvec_flat(qmm_type t, const uint8_t *flat, int64_t K, int64
             case QMM_IQ4_NL: e = run_flat_mt<QMM_IQ4_NL>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
             case QMM_MXFP4: e = run_flat_mt<QMM_MXFP4>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
             case QMM_Q4_1: e = run_flat_mt<QMM_Q4_1>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
+            case QMM_Q4_K: e = run_flat_mt<QMM_Q4_K>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
             default: e = run_flat_mt<QMM_Q8_0>(flat, K, N, aq, ad, mm, yy, ldy, s); break;
         }
         if (e != cudaSuccess) return e;

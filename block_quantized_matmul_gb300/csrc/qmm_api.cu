@@ -14,13 +14,17 @@ using namespace qmm;
 namespace {
 
 bool valid_type(qmm_type t) {
-    return t == QMM_Q4_0 || t == QMM_Q8_0 || t == QMM_IQ4_NL || t == QMM_MXFP4 || t == QMM_Q4_1;
+    return t == QMM_Q4_0 || t == QMM_Q8_0 || t == QMM_IQ4_NL || t == QMM_MXFP4 || t == QMM_Q4_1 || t == QMM_Q4_K;
 }
 // Flat blocks of 18 or 34 bytes are read as halfwords, Q4_1's 20-byte blocks start with a 4-byte
-// (d, m) pair read as one word, and MXFP4's 17-byte blocks are read byte by byte.
-uintptr_t flat_align(qmm_type t) { return t == QMM_MXFP4 ? 1 : (t == QMM_Q4_1 ? 4 : 2); }
+// (d, m) pair read as one word, Q4_K's 144-byte super-blocks are read as words, and MXFP4's
+// 17-byte blocks are read byte by byte.
+uintptr_t flat_align(qmm_type t) { return t == QMM_MXFP4 ? 1 : ((t == QMM_Q4_1 || t == QMM_Q4_K) ? 4 : 2); }
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool valid_kn(int64_t K, int64_t N) { return K > 0 && (K % 32) == 0 && N > 0; }
+// K must also be a whole number of the type's flat blocks (256 for Q4_K, whose tiles come from
+// super-blocks).
+bool valid_tkn(qmm_type t, int64_t K, int64_t N) { return valid_kn(K, N) && (K % block_len(t)) == 0; }
 cudaStream_t cs(qmm_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
@@ -30,7 +34,7 @@ constexpr int64_t kMaxDim = (int64_t)1 << 31;
 qmm_status check_matmul(qmm_type t, const void *w, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
                         int64_t M, float *y, int64_t ldy) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
-    if (!valid_kn(K, N) || M <= 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim || ldy < N) return QMM_ERR_INVALID_ARG;
+    if (!valid_tkn(t, K, N) || M <= 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim || ldy < N) return QMM_ERR_INVALID_ARG;
     if (!w || !a_q || !a_d || !y) return QMM_ERR_INVALID_ARG;
     if (!aligned(w, 16) || !aligned(a_q, 16) || !aligned(a_d, 4) || !aligned(y, 4)) return QMM_ERR_MISALIGNED;
     return QMM_OK;
@@ -57,13 +61,13 @@ size_t qmm_block_size(qmm_type t) { return valid_type(t) ? (size_t)block_bytes(t
 size_t qmm_tile_size(qmm_type t) { return valid_type(t) ? (size_t)tile_bytes(t) : 0; }
 
 size_t qmm_tiled_size(qmm_type t, int64_t K, int64_t N) {
-    if (!valid_type(t) || !valid_kn(K, N) || K > kMaxDim || N > kMaxDim) return 0;
+    if (!valid_type(t) || !valid_tkn(t, K, N) || K > kMaxDim || N > kMaxDim) return 0;
     return (size_t)((N + 31) / 32) * (size_t)(K / 32) * (size_t)tile_bytes(t);
 }
 
 size_t qmm_flat_size(qmm_type t, int64_t K, int64_t N) {
-    if (!valid_type(t) || !valid_kn(K, N) || K > kMaxDim || N > kMaxDim) return 0;
-    return (size_t)N * (size_t)(K / 32) * (size_t)block_bytes(t);
+    if (!valid_type(t) || !valid_tkn(t, K, N) || K > kMaxDim || N > kMaxDim) return 0;
+    return (size_t)N * (size_t)(K / 32) * (size_t)bytes_per_32(t);
 }
 
 void qmm_iq4nl_table(int8_t out[16]) {
@@ -76,21 +80,21 @@ int64_t qmm_decode_max_m(void) { return kDecodeMaxM; }
 qmm_status qmm_quantize_weight(qmm_type t, const float *w, int64_t N, int64_t K, int64_t ldw, void *w_flat,
                                qmm_stream_t stream) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
-    if (!valid_kn(K, N) || K > kMaxDim || N > kMaxDim || ldw < K || !w || !w_flat) return QMM_ERR_INVALID_ARG;
+    if (!valid_tkn(t, K, N) || K > kMaxDim || N > kMaxDim || ldw < K || !w || !w_flat) return QMM_ERR_INVALID_ARG;
     if (!aligned(w, 16) || (ldw % 4) != 0 || !aligned(w_flat, flat_align(t))) return QMM_ERR_MISALIGNED;
     return from_cuda(launch_quantize_weight(t, w, N, K, ldw, static_cast<uint8_t *>(w_flat), cs(stream)));
 }
 
 qmm_status qmm_repack(qmm_type t, const void *w_flat, int64_t K, int64_t N, void *w_tiled, qmm_stream_t stream) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
-    if (!valid_kn(K, N) || K > kMaxDim || N > kMaxDim || !w_flat || !w_tiled) return QMM_ERR_INVALID_ARG;
+    if (!valid_tkn(t, K, N) || K > kMaxDim || N > kMaxDim || !w_flat || !w_tiled) return QMM_ERR_INVALID_ARG;
     if (!aligned(w_flat, flat_align(t)) || !aligned(w_tiled, 16)) return QMM_ERR_MISALIGNED;
     return from_cuda(launch_repack(t, static_cast<const uint8_t *>(w_flat), K, N, static_cast<uint8_t *>(w_tiled),
                                    cs(stream)));
 }
 
 qmm_status qmm_unpack(qmm_type t, const void *w_tiled, int64_t K, int64_t N, void *w_flat, qmm_stream_t stream) {
-    if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
+    if (!valid_type(t) || t == QMM_Q4_K) return QMM_ERR_UNSUPPORTED;   // Q4_K tiles hold rounded products
     if (!valid_kn(K, N) || K > kMaxDim || N > kMaxDim || !w_flat || !w_tiled) return QMM_ERR_INVALID_ARG;
     if (!aligned(w_flat, flat_align(t)) || !aligned(w_tiled, 16)) return QMM_ERR_MISALIGNED;
     return from_cuda(launch_unpack(t, static_cast<const uint8_t *>(w_tiled), K, N, static_cast<uint8_t *>(w_flat),
@@ -112,6 +116,7 @@ qmm_status qmm_matmul_path(qmm_type t, const void *w_tiled, int64_t K, int64_t N
     if (st != QMM_OK) return st;
     if (path != QMM_PATH_AUTO && path != QMM_PATH_MATVEC && path != QMM_PATH_GEMM) return QMM_ERR_UNSUPPORTED;
     const uint8_t *w = static_cast<const uint8_t *>(w_tiled);
+    t = tile_type(t);
     if (path == QMM_PATH_AUTO) path = (M <= kDecodeMaxM) ? QMM_PATH_MATVEC : QMM_PATH_GEMM;
     cudaError_t e;
     if (path == QMM_PATH_MATVEC) {
@@ -131,18 +136,18 @@ qmm_status qmm_matmul(qmm_type t, const void *w_tiled, int64_t K, int64_t N, con
 qmm_status qmm_matmul_f32(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
                           int64_t M, float *y, int64_t ldy, qmm_stream_t stream) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
-    if (!valid_kn(K, N) || M <= 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim || ldx < K || ldx > kMaxDim || ldy < N)
+    if (!valid_tkn(t, K, N) || M <= 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim || ldx < K || ldx > kMaxDim || ldy < N)
         return QMM_ERR_INVALID_ARG;
     if (!w_tiled || !x || !y) return QMM_ERR_INVALID_ARG;
     if (!aligned(w_tiled, 16) || !aligned(x, 4) || !aligned(y, 4)) return QMM_ERR_MISALIGNED;
-    return from_cuda(launch_matvec_fused(t, static_cast<const uint8_t *>(w_tiled), K, N, x, ldx, M, y, ldy, cs(stream)));
+    return from_cuda(launch_matvec_fused(tile_type(t), static_cast<const uint8_t *>(w_tiled), K, N, x, ldx, M, y, ldy, cs(stream)));
 }
 
 qmm_status qmm_matmul_flat(qmm_type t, const void *w_flat, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
                            int64_t M, float *y, int64_t ldy, qmm_stream_t stream) {
     qmm_status st = check_matmul(t, w_flat, K, N, a_q, a_d, M, y, ldy);
     if (st != QMM_OK) return st;
-    if (((K / 32) * block_bytes(t)) % 16 != 0) return QMM_ERR_UNSUPPORTED;   // rows are copied as 16-byte units
+    if (((K / 32) * bytes_per_32(t)) % 16 != 0) return QMM_ERR_UNSUPPORTED;   // rows are copied as 16-byte units
     return from_cuda(launch_matvec_flat(t, static_cast<const uint8_t *>(w_flat), K, N, a_q, a_d, M, y, ldy, cs(stream)));
 }
 
@@ -157,6 +162,7 @@ qmm_status qmm_matmul_ws(qmm_type t, const void *w_tiled, int64_t K, int64_t N, 
     qmm_status st = check_matmul(t, w_tiled, K, N, a_q, a_d, M, y, ldy);
     if (st != QMM_OK) return st;
     const uint8_t *w = static_cast<const uint8_t *>(w_tiled);
+    t = tile_type(t);
     if (M <= kDecodeMaxM) return from_cuda(launch_matvec(t, w, K, N, a_q, a_d, M, y, ldy, cs(stream)));
     if (!workspace || workspace_bytes < gemm_workspace_bytes(M, K)) return QMM_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return QMM_ERR_MISALIGNED;
@@ -168,6 +174,7 @@ qmm_status qmm_matmul_noalloc(qmm_type t, const void *w_tiled, int64_t K, int64_
     qmm_status st = check_matmul(t, w_tiled, K, N, a_q, a_d, M, y, ldy);
     if (st != QMM_OK) return st;
     const uint8_t *w = static_cast<const uint8_t *>(w_tiled);
+    t = tile_type(t);
     if (M <= kDecodeMaxM) return from_cuda(launch_matvec(t, w, K, N, a_q, a_d, M, y, ldy, cs(stream)));
     if (gemm_workspace_bytes(M, K) > kNoAllocScratchBytes) return QMM_ERR_INVALID_ARG;
     void *scratch = nullptr;

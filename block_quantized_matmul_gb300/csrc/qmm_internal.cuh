@@ -23,26 +23,38 @@ constexpr int kTileMxBytes = 544;     // MXFP4 tile: 512 nibble bytes + 32 E8M0 
 constexpr int kBlockMxBytes = 17;     // flat MXFP4 block: E8M0 e + 16 nibble bytes
 constexpr int kTile41Bytes = 640;     // Q4_1 tile: 512 nibble bytes + 32 fp16 (d, m) pairs
 constexpr int kBlock41Bytes = 20;     // flat Q4_1 block: fp16 d + fp16 m + 16 nibble bytes
+constexpr int kSuperQ4KBytes = 144;   // flat Q4_K super-block of 256: fp16 d, fp16 dmin, 12 scale bytes, 128 nibble bytes
+constexpr int kQ4KBytesPer32 = 18;    // the same, per 32 weights
 
 inline int tile_bytes(qmm_type t) {
-    return t == QMM_Q8_0 ? kTile8Bytes : (t == QMM_MXFP4 ? kTileMxBytes : (t == QMM_Q4_1 ? kTile41Bytes : kTile4Bytes));
+    return t == QMM_Q8_0 ? kTile8Bytes
+                         : (t == QMM_MXFP4 ? kTileMxBytes : ((t == QMM_Q4_1 || t == QMM_Q4_K) ? kTile41Bytes : kTile4Bytes));
 }
+// Bytes of one flat GGML block (Q4_K: one super-block of 256 weights).
 inline int block_bytes(qmm_type t) {
-    return t == QMM_Q8_0 ? kBlock8Bytes : (t == QMM_MXFP4 ? kBlockMxBytes : (t == QMM_Q4_1 ? kBlock41Bytes : kBlock4Bytes));
+    return t == QMM_Q8_0 ? kBlock8Bytes
+                         : (t == QMM_MXFP4 ? kBlockMxBytes
+                                           : (t == QMM_Q4_1 ? kBlock41Bytes : (t == QMM_Q4_K ? kSuperQ4KBytes : kBlock4Bytes)));
 }
+// Flat bytes per 32 weights (every type's row is K/32 times this).
+inline int bytes_per_32(qmm_type t) { return t == QMM_Q4_K ? kQ4KBytesPer32 : block_bytes(t); }
+// Elements per flat block.
+inline int block_len(qmm_type t) { return t == QMM_Q4_K ? 256 : 32; }
+// The tile a type is stored in for the tiled kernels: a Q4_K tile is a Q4_1 tile.
+inline qmm_type tile_type(qmm_type t) { return t == QMM_Q4_K ? QMM_Q4_1 : t; }
 
 // Per-type constants for the kernels.
 template <int TYPE>
 struct TileFmt {
-    static constexpr int kBytes = TYPE == QMM_Q8_0    ? kTile8Bytes
-                                  : TYPE == QMM_MXFP4 ? kTileMxBytes
-                                  : TYPE == QMM_Q4_1  ? kTile41Bytes
-                                                      : kTile4Bytes;
+    static constexpr int kBytes = TYPE == QMM_Q8_0                        ? kTile8Bytes
+                                  : TYPE == QMM_MXFP4                     ? kTileMxBytes
+                                  : (TYPE == QMM_Q4_1 || TYPE == QMM_Q4_K) ? kTile41Bytes
+                                                                          : kTile4Bytes;
     static constexpr int kScaleOff = TYPE == QMM_Q8_0 ? kScale8Off : kScale4Off;   // MXFP4, Q4_1: 512 too
     static constexpr bool kLut = TYPE == QMM_IQ4_NL || TYPE == QMM_MXFP4;         // codes go through a table
     static constexpr bool kE8M0 = TYPE == QMM_MXFP4;                              // one exponent byte per row
-    static constexpr bool kAffine = TYPE == QMM_Q4_1;                             // (d, m) per row: d*q + m
-    static constexpr bool kNibbleInt = TYPE == QMM_Q4_0 || TYPE == QMM_Q4_1;      // integer nibble codes
+    static constexpr bool kAffine = TYPE == QMM_Q4_1 || TYPE == QMM_Q4_K;         // (d, m) per row: d*q + m
+    static constexpr bool kNibbleInt = TYPE == QMM_Q4_0 || kAffine;               // integer nibble codes
 };
 
 // The built-in IQ4_NL table (16 int8 levels, ascending): 16-level Lloyd-Max quantizer of a unit
@@ -118,7 +130,7 @@ cudaError_t launch_matvec(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N
 // 2-D tensor map: rows of `inner` elements (row stride `row_bytes`), box {box_inner, box_rows}.
 cudaError_t make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw);
-// Decode matmul straight from flat GGML rows (K % 512 == 0, flat 16-byte aligned).
+// Decode matmul straight from flat GGML rows (row bytes a multiple of 16, flat 16-byte aligned).
 cudaError_t launch_matvec_flat(qmm_type t, const uint8_t *flat, int64_t K, int64_t N, const int8_t *a_q,
                                const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
 cudaError_t launch_matvec_fused(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const float *x, int64_t ldx,

@@ -197,6 +197,78 @@ __global__ void __launch_bounds__(128) quantize_weight_kernel(int type, const fl
     }
 }
 
+// Q4_K super-blocks (the rule stated with qmm_quantize_weight): one warp per 256 weights, lane l
+// holding element l of each of the 8 sub-blocks.  Sub-block minima and maxima come from warp
+// reductions (min and max do not depend on the order; the range is taken as +0 when it is not
+// positive, so the sign of a zero maximum cannot matter); everything after that is the same fp32
+// arithmetic in every lane, in the order of the rule.
+__global__ void __launch_bounds__(128) quantize_q4k_kernel(const float *__restrict__ w, int64_t N, int64_t K, int64_t ldw,
+                                                           uint8_t *__restrict__ flat) {
+    const int64_t nsb = K / 256, total = N * nsb;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < total; i += nwarps) {
+        const int64_t n = i / nsb, sbi = i - n * nsb;
+        const float *x = w + n * ldw + sbi * 256;
+        uint8_t *sb = flat + i * kSuperQ4KBytes;            // row n, super-block sbi
+        float xv[8], scale[8], mins[8];
+        float max_scale = 0.0f, max_min = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            xv[j] = x[32 * j + lane];
+            float mn = xv[j] < 0.0f ? xv[j] : 0.0f, mx = xv[j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float a = __shfl_xor_sync(0xffffffffu, mn, o), b = __shfl_xor_sync(0xffffffffu, mx, o);
+                mn = a < mn ? a : mn;
+                mx = b > mx ? b : mx;
+            }
+            float range = __fsub_rn(mx, mn);
+            if (!(range > 0.0f)) range = 0.0f;
+            scale[j] = __fdiv_rn(range, 15.0f);
+            mins[j] = __fsub_rn(0.0f, mn);
+            if (scale[j] > max_scale) max_scale = scale[j];
+            if (mins[j] > max_min) max_min = mins[j];
+        }
+        const float isc = max_scale > 0.0f ? __fdiv_rn(63.0f, max_scale) : 0.0f;
+        const float imn = max_min > 0.0f ? __fdiv_rn(63.0f, max_min) : 0.0f;
+        const __half d16 = __float2half_rn(__fdiv_rn(max_scale, 63.0f));
+        const __half dmin16 = __float2half_rn(__fdiv_rn(max_min, 63.0f));
+        int sc[8], m[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float vs = __fadd_rn(__fmul_rn(scale[j], isc), 0.5f), vm = __fadd_rn(__fmul_rn(mins[j], imn), 0.5f);
+            sc[j] = !(vs >= 0.0f) ? 0 : (vs >= 63.0f ? 63 : __float2int_rz(vs));
+            m[j] = !(vm >= 0.0f) ? 0 : (vm >= 63.0f ? 63 : __float2int_rz(vm));
+        }
+        const float d = __half2float(d16), dmin = __half2float(dmin16);
+        int codes[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float D = __fmul_rn(d, (float)sc[j]), Mj = __fmul_rn(dmin, (float)m[j]);
+            const float v = __fadd_rn(__fmul_rn(__fadd_rn(xv[j], Mj), inv_or_zero(D)), 0.5f);
+            codes[j] = !(v >= 0.0f) ? 0 : (v >= 15.0f ? 15 : __float2int_rz(v));
+        }
+        // quant byte 32g + l: sub-block 2g in the low nibble, 2g + 1 in the high nibble
+#pragma unroll
+        for (int g = 0; g < 4; ++g) sb[16 + 32 * g + lane] = (uint8_t)(codes[2 * g] | (codes[2 * g + 1] << 4));
+        if (lane == 0) {
+            uint32_t s0 = 0, s1 = 0, s2 = 0;                 // scale bytes 0..3, 4..7, 8..11
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                s0 |= (uint32_t)((sc[q] & 63) | ((sc[q + 4] >> 4) << 6)) << (8 * q);
+                s1 |= (uint32_t)((m[q] & 63) | ((m[q + 4] >> 4) << 6)) << (8 * q);
+                s2 |= (uint32_t)((sc[q + 4] & 15) | ((m[q + 4] & 15) << 4)) << (8 * q);
+            }
+            uint32_t *h = reinterpret_cast<uint32_t *>(sb);   // 4-byte aligned
+            h[0] = (uint32_t)__half_as_ushort(d16) | ((uint32_t)__half_as_ushort(dmin16) << 16);
+            h[1] = s0;
+            h[2] = s1;
+            h[3] = s2;
+        }
+    }
+}
+
 int grid_for(int64_t work, int threads) {
     int64_t g = (work + threads - 1) / threads;
     if (g > 152 * 32) g = 152 * 32;
@@ -231,6 +303,10 @@ cudaError_t launch_quantize_act(const float *x, int64_t M, int64_t K, int64_t ld
 cudaError_t launch_quantize_weight(qmm_type t, const float *w, int64_t N, int64_t K, int64_t ldw, uint8_t *flat,
                                    cudaStream_t s) {
     const int threads = 128;
+    if (t == QMM_Q4_K) {
+        quantize_q4k_kernel<<<grid_for(N * (K / 256) * 32, threads), threads, 0, s>>>(w, N, K, ldw, flat);
+        return cudaGetLastError();
+    }
     const int grid = grid_for(N * (K / 32), threads);
     quantize_weight_kernel<<<grid, threads, 0, s>>>((int)t, w, N, K, ldw, flat, lut_for(t));
     return cudaGetLastError();

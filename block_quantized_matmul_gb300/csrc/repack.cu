@@ -71,6 +71,48 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
     __threadfence();
 }
 
+// Q4_K super-blocks -> Q4_1-layout tiles ("K-Quants Formats"): tile kt of row n holds sub-block
+// j = kt % 8 of super-block kt / 8, its codes in the Q4_0 nibble layout and the row pair
+// (fp16(d*sc_j), fp16(-dmin*m_j)).  One thread per (tile, tile row), as above.
+__global__ void __launch_bounds__(256) repack_q4k_kernel(const uint8_t *__restrict__ flat, int64_t n_k_tiles, int64_t N,
+                                                         int64_t n_tiles, uint8_t *__restrict__ tiled) {
+    const int64_t total = n_tiles * 32;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tile = i >> 5;
+        const int r = (int)(i & 31);
+        const int64_t ct = tile / n_k_tiles, kt = tile - ct * n_k_tiles;
+        const int64_t n = ct * 32 + r;
+        uint8_t *t = tiled + tile * kTile41Bytes;
+        if (n >= N) {
+#pragma unroll
+            for (int cp = 0; cp < 16; ++cp) t[cp * 32 + r] = 0;
+            *reinterpret_cast<uint32_t *>(t + kScale4Off + 4 * r) = 0u;
+            continue;
+        }
+        // the row is n_k_tiles * 18 bytes; super-block kt / 8 starts 144 * (kt / 8) bytes in
+        const uint32_t *sb = reinterpret_cast<const uint32_t *>(flat + (n * n_k_tiles + (kt & ~7)) * kQ4KBytesPer32);
+        const int j = (int)(kt & 7), jj = j & 3;
+        const uint32_t head = sb[0];
+        const uint32_t b0 = (sb[1] >> (8 * jj)) & 0xFF, b1 = (sb[2] >> (8 * jj)) & 0xFF, b2 = (sb[3] >> (8 * jj)) & 0xFF;
+        const uint32_t sc = j < 4 ? (b0 & 63) : ((b2 & 15) | ((b0 >> 6) << 4));
+        const uint32_t m = j < 4 ? (b1 & 63) : ((b2 >> 4) | ((b1 >> 6) << 4));
+        const uint32_t *qs = sb + 4 + 8 * (j >> 1);            // 32 bytes, nibble j & 1
+        const int sh = 4 * (j & 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t c = (qs[k] >> sh) & 0x0F0F0F0Fu;    // elements 4k..4k+3, one per byte
+            t[(2 * k) * 32 + r] = (uint8_t)((c & 15) | ((c >> 4) & 0xF0));
+            t[(2 * k + 1) * 32 + r] = (uint8_t)(((c >> 16) & 15) | ((c >> 20) & 0xF0));
+        }
+        const float d = __half2float(__ushort_as_half((unsigned short)(head & 0xFFFF)));
+        const float dmin = __half2float(__ushort_as_half((unsigned short)(head >> 16)));
+        const uint32_t dp = __half_as_ushort(__float2half_rn(__fmul_rn(d, (float)sc)));
+        const uint32_t mp = __half_as_ushort(__float2half_rn(-__fmul_rn(dmin, (float)m)));
+        *reinterpret_cast<uint32_t *>(t + kScale4Off + 4 * r) = dp | (mp << 16);
+    }
+    __threadfence();
+}
+
 template <int TYPE>
 __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t *__restrict__ tiled, int64_t n_k_tiles, int64_t N,
                                                      uint8_t *__restrict__ flat) {
@@ -145,6 +187,7 @@ cudaError_t launch_repack(qmm_type t, const uint8_t *flat, int64_t K, int64_t N,
         case QMM_IQ4_NL: repack_kernel<QMM_IQ4_NL><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
         case QMM_MXFP4: repack_kernel<QMM_MXFP4><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
         case QMM_Q4_1: repack_kernel<QMM_Q4_1><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
+        case QMM_Q4_K: repack_q4k_kernel<<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
         default: repack_kernel<QMM_Q8_0><<<grid, threads, 0, s>>>(flat, nkt, N, n_tiles, tiled); break;
     }
     return cudaGetLastError();
@@ -159,6 +202,7 @@ cudaError_t launch_unpack(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N
         case QMM_IQ4_NL: unpack_kernel<QMM_IQ4_NL><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
         case QMM_MXFP4: unpack_kernel<QMM_MXFP4><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
         case QMM_Q4_1: unpack_kernel<QMM_Q4_1><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
+        case QMM_Q4_K: return cudaErrorNotSupported;           // tiles hold rounded products
         default: unpack_kernel<QMM_Q8_0><<<grid, threads, 0, s>>>(tiled, nkt, N, flat); break;
     }
     return cudaGetLastError();

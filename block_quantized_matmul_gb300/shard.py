@@ -23,7 +23,7 @@ class Shard:
     byte_len: int       # bytes of this rank's tiles
 
 
-TILE_BYTES = {"q4_0": 576, "iq4_nl": 576, "q8_0": 1088, "mxfp4": 544, "q4_1": 640}
+TILE_BYTES = {"q4_0": 576, "iq4_nl": 576, "q8_0": 1088, "mxfp4": 544, "q4_1": 640, "q4_k": 640}
 
 
 def tile_bytes(type_: str) -> int:

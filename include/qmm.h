@@ -54,8 +54,14 @@ typedef enum {
  * the Q4_0 nibble layout and one E8M0 exponent byte per row at byte 512 + row; a weight is the FP4
  * value of its code times the power-of-two fp16 scale with bits clamp(e - 112, 0, 30) << 10.
  * Q4_1 tiles (640 B) keep the Q4_0 nibble layout and one FP16 pair (d, m) per row at bytes
- * 512 + 4*row; a weight is d*q + m (q = 0..15). */
-typedef enum { QMM_Q4_0 = 0, QMM_Q8_0 = 1, QMM_IQ4_NL = 2, QMM_MXFP4 = 3, QMM_Q4_1 = 4 } qmm_type;
+ * 512 + 4*row; a weight is d*q + m (q = 0..15).
+ * Q4_K ("K-Quants Formats"): flat rows are GGML super-blocks of 256 weights (144 B: fp16 d, fp16 dmin,
+ * 12 bytes packing a 6-bit scale sc_j and min m_j for each sub-block j of 32, then 128 nibble bytes;
+ * weight i of sub-block j is nibble (j & 1) of byte 32*(j/2) + i, worth d*sc_j*q - dmin*m_j).  Each
+ * super-block becomes 8 tiles of 32 k in the Q4_1 tile layout with the row pair
+ * (fp16(d*sc_j), fp16(-dmin*m_j)), so every tiled call reads a Q4_K weight exactly as a Q4_1 one.
+ * For Q4_K, K must be a multiple of 256 in every call. */
+typedef enum { QMM_Q4_0 = 0, QMM_Q8_0 = 1, QMM_IQ4_NL = 2, QMM_MXFP4 = 3, QMM_Q4_1 = 4, QMM_Q4_K = 5 } qmm_type;
 
 /* Which kernel qmm_matmul_path runs: AUTO picks the decode matvec for M <= qmm_decode_max_m()
  * and the tensor-core GEMM otherwise. */
@@ -67,18 +73,19 @@ QMM_API const char *qmm_status_str(qmm_status st);
 /* Bytes of one flat GGML block of 32 weights: 18 (Q4_0, IQ4_NL: fp16 d + 16 nibble bytes, element
  * j in the low nibble of byte j, element j+16 in its high nibble), 34 (Q8_0: fp16 d + 32 int8) or
  * 17 (MXFP4: the E8M0 exponent byte + 16 nibble bytes in the same order) or 20 (Q4_1: fp16 d, fp16 m
- * + 16 nibble bytes).  0 for an unknown type. */
+ * + 16 nibble bytes); for Q4_K the 144-byte super-block of 256 weights.  0 for an unknown type. */
 QMM_API size_t qmm_block_size(qmm_type t);
 
 /* Bytes of one tile ("Block-32 Quantized Formats"): 576 (Q4_0, IQ4_NL), 1088 (Q8_0), 544 (MXFP4) or
- * 640 (Q4_1); 0 if unknown. */
+ * 640 (Q4_1, Q4_K); 0 if unknown. */
 QMM_API size_t qmm_tile_size(qmm_type t);
 
 /* Bytes of the tiled weight [K, N] ("Tile Dimensions and Grid Layout"):
  * n_col_tiles * n_k_tiles * tile_size.  0 if K <= 0, K % 32 != 0, N <= 0 or the type is unknown. */
 QMM_API size_t qmm_tiled_size(qmm_type t, int64_t K, int64_t N);
 
-/* Bytes of the flat weight: N rows of K/32 GGML blocks.  0 on the same invalid inputs. */
+/* Bytes of the flat weight: N rows of K/32 GGML blocks (K/256 super-blocks for Q4_K).  0 on the
+ * same invalid inputs, and for Q4_K when K % 256 != 0. */
 QMM_API size_t qmm_flat_size(qmm_type t, int64_t K, int64_t N);
 
 /* The 16-entry IQ4_NL table the kernels use (int8 values, ascending).  The pages name the table
@@ -93,7 +100,7 @@ QMM_API int64_t qmm_decode_max_m(void);
  * qmm_quantize_weight -- fp32 weight rows -> flat GGML blocks (model-load helper, not the hot path).
  *   w_dev      fp32, N rows of K values, row n at w_dev + n*ldw; 16-byte aligned, ldw % 4 == 0.
  *   w_flat_dev output, qmm_flat_size(t, K, N) bytes, row-major blocks; 2-byte aligned (4-byte for
- *              Q4_1, any address for MXFP4).
+ *              Q4_1 and Q4_K, any address for MXFP4).
  * Rules per 32-element block (x = the block, m = its signed element of largest magnitude, first on
  * ties): Q8_0 d = max|x|/127, q = round-half-away(x/d) (computed as x * (1/d));  Q4_0 d = m/-8,
  * q = min(15, trunc(x*(1/d) + 8.5));  IQ4_NL d = m/table[0], q = the table index whose level
@@ -101,7 +108,11 @@ QMM_API int64_t qmm_decode_max_m(void);
  * MXFP4: e = floor(log2 max|x|) - 2 + 127 (0 for an all-zero block, at most 254), then the code whose
  * level s * fp4(code) is nearest to x (lowest code on ties), s the dequantizing fp16 scale.
  * Q4_1: d = (max - min)/15, q = min(15, trunc((x - min)*(1/d) + 0.5)), m = min; d and m as fp16.
- * Errors: INVALID_ARG (N <= 0, K <= 0, K % 32, ldw < K, NULL), UNSUPPORTED (type), MISALIGNED.
+ * Q4_K, per super-block: for each sub-block mn = min(0, min x), scale = (max x - mn)/15, min = -mn;
+ * d = max scale/63, dmin = max min/63 (fp16); sc, m = min(63, trunc(v*(63/max) + 0.5)); then
+ * q = min(15, trunc((x + dmin*m) * (1/(d*sc)) + 0.5)) (0 when d*sc = 0).
+ * Errors: INVALID_ARG (N <= 0, K <= 0, K % 32 (K % 256 for Q4_K), ldw < K, NULL), UNSUPPORTED
+ * (type), MISALIGNED.
  */
 QMM_API qmm_status qmm_quantize_weight(qmm_type t, const float *w_dev, int64_t N, int64_t K, int64_t ldw,
                                void *w_flat_dev, qmm_stream_t stream);
@@ -109,17 +120,20 @@ QMM_API qmm_status qmm_quantize_weight(qmm_type t, const float *w_dev, int64_t N
 /*
  * qmm_repack -- flat GGML rows -> tiles ("Tiled Weight Formats"; the pages repack at model load,
  * in set_tensor() or rt-repack).
- *   w_flat_dev  N rows of K/32 blocks (qmm_flat_size bytes); 2-byte aligned (4-byte for Q4_1, any
- *               address for MXFP4).
+ *   w_flat_dev  N rows of K/32 blocks (qmm_flat_size bytes); 2-byte aligned (4-byte for Q4_1 and
+ *               Q4_K, any address for MXFP4).
  *   w_tiled_dev output, qmm_tiled_size bytes; 16-byte aligned.  Rows past N in the last column tile
  *               are written as zero bytes (scale 0, quants 0).  The buffers must not overlap.
- * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED.  Bit-exact, lossless.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED.  Bit-exact, lossless, except for Q4_K, whose tile
+ * pairs are d*sc and -dmin*m rounded to fp16 (exact fp32 products, round to nearest even; d and dmin
+ * must be finite).
  */
 QMM_API qmm_status qmm_repack(qmm_type t, const void *w_flat_dev, int64_t K, int64_t N, void *w_tiled_dev,
                       qmm_stream_t stream);
 
 /* qmm_unpack -- inverse of qmm_repack (tiles -> flat rows); used to check a tiled buffer. Same
- * arguments and alignment rules with the roles of the two buffers swapped. */
+ * arguments and alignment rules with the roles of the two buffers swapped.  UNSUPPORTED for Q4_K
+ * (its tiles cannot be split back into a super-block). */
 QMM_API qmm_status qmm_unpack(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N, void *w_flat_dev,
                       qmm_stream_t stream);
 

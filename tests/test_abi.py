@@ -174,3 +174,17 @@ def test_matmul_flat_argument_errors(L):
     assert f(0, P, 64, 64, P, P, 1, P, 64, None) == UNSUPPORTED
     assert f(1, P, 128, 64, P, P, 1, P, 64, None) == UNSUPPORTED
     assert f(3, P, 256, 64, P, P, 1, P, 64, None) == UNSUPPORTED
+
+
+def test_q4_k_sizes_and_argument_errors(L):
+    assert qmm.block_size("q4_k") == 144 and qmm.tile_size("q4_k") == 640
+    assert qmm.flat_size("q4_k", 4096, 10) == 10 * 16 * 144
+    assert qmm.tiled_size("q4_k", 4096, 10) == 128 * 640
+    assert qmm.flat_size("q4_k", 288, 10) == 0 and qmm.tiled_size("q4_k", 288, 10) == 0   # K % 256
+    assert L.qmm_quantize_weight(5, P, 4, 288, 288, P, None) == INVALID
+    assert L.qmm_repack(5, P, 288, 4, P, None) == INVALID
+    assert L.qmm_repack(5, P + 2, 256, 4, P, None) == MISALIGNED          # super-blocks are read as words
+    assert L.qmm_unpack(5, P, 256, 4, P, None) == UNSUPPORTED             # tiles hold rounded products
+    assert L.qmm_matmul(5, P, 288, 64, P, P, 1, P, 64, None) == INVALID
+    assert L.qmm_matmul_f32(5, P, 288, 64, P, 288, 1, P, 64, None) == INVALID
+    assert L.qmm_matmul_flat(5, P, 288, 64, P, P, 1, P, 64, None) == INVALID
