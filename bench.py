@@ -120,18 +120,25 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def kernel_source_hash():
-    """Hash of the kernel sources with comments and blank lines removed (a comment edit does not
-    change the kernels the recorded counters were taken on)."""
+KERNEL_FILES = {"matvec": ("matvec.cu", "qmm_internal.cuh"), "gemm": ("gemm_tc.cu", "qmm_internal.cuh")}
+
+
+def kernel_kind(workload):
+    return "gemm" if "prefill_gemm" in workload else "matvec"
+
+
+def kernel_source_hash(kind="matvec"):
+    """Hash of the sources a kernel family is compiled from, with comments and blank lines removed
+    (a comment edit, or an edit of another kernel's file, does not change the kernels the recorded
+    counters were taken on)."""
     import re
 
     h = hashlib.sha256()
-    for name in sorted(os.listdir(os.path.join(ROOT, "block_quantized_matmul_gb300", "csrc"))):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(ROOT, "block_quantized_matmul_gb300", "csrc", name)) as f:
-                text = re.sub(r"//[^\n]*", "", f.read())
-            code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
-            h.update(name.encode() + b"\0" + code.encode())
+    for name in KERNEL_FILES[kind]:
+        with open(os.path.join(ROOT, "block_quantized_matmul_gb300", "csrc", name)) as f:
+            text = re.sub(r"//[^\n]*", "", f.read())
+        code = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 
@@ -141,16 +148,13 @@ def recorded_traffic(workload):
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
         ent = rec.get(workload)
-        if ent and ent.get("source_hash") == kernel_source_hash():
+        if ent and ent.get("source_hash") == kernel_source_hash(kernel_kind(workload)):
             return ent.get("dram_bytes_per_launch")
     except Exception:
         pass
     return None
 
 
-# ---------------------------------------------------------------------------------------------
-# GPU arm
-# ---------------------------------------------------------------------------------------------
 class Workload:
     def __init__(self, torch, qmm, type_, K, N, M, layout="tiled", seed=0, copies=None):
         self.torch, self.qmm = torch, qmm
