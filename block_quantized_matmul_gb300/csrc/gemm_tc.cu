@@ -191,7 +191,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Waits for this thread's tcgen05.ld; also written as the last writer of the 16 registers a tcgen05.ld filled, so that no use of them
+// can be scheduled before the load has completed.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
 
 __device__ __forceinline__ unsigned long long pack2f(float a, float b) {
     unsigned long long v;
@@ -620,7 +628,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                 float4 da[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) da[e] = da4[4 * cc + e];
-                tmem_wait_ld();
+                tmem_wait_ld(sv);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const unsigned long long t0 = fmul2(pack2u(sv[4 * e], sv[4 * e + 1]), pack2f(da[e].x, da[e].y));
