@@ -49,7 +49,6 @@ constexpr int kConvWarp0 = 2, kNumConvWarps = 4;
 constexpr int kRescaleWarp0 = 6, kNumRescaleWarps = 8;
 constexpr int kBProducerWarp = kRescaleWarp0 + kNumRescaleWarps;    // warp 14
 constexpr int kThreads = (kBProducerWarp + 1) * 32;
-constexpr int kOpBytes = BM * 64;          // 128 rows x 64 bytes: one K block (SW64) or the scale columns
 constexpr int kOp2Bytes = BM * 128;        // 128 rows x 128 bytes: a block pair (SW128)
 constexpr int kLutCopies = 16;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
@@ -131,12 +130,6 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     }
 }
 
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 // 2-D tensor copy: box {32 bytes of K, 128 token rows} of the int8 activations; rows past M are
 // zero-filled by the TMA unit.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
@@ -157,14 +150,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.p
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Shared-memory matrix descriptor: K-major operand, rows of 64 bytes, 64-byte swizzle,
-// 8-row groups 512 bytes apart (SBO), descriptor version 1 (sm_100 family).
-__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
-}
-
-// Same for rows of 128 bytes with the 128-byte swizzle (8-row groups 1024 bytes apart).
+// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes with the 128-byte swizzle,
+// 8-row groups 1024 bytes apart (SBO), descriptor version 1 (sm_100 family).
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
@@ -216,27 +203,11 @@ __device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsign
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-__device__ __forceinline__ void unpack2f(unsigned long long v, float &a, float &b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ unsigned long long ffma2p(unsigned long long a, unsigned long long b, unsigned long long c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
 // (y0, y1) += t * s, elementwise
 __device__ __forceinline__ void ffma2_acc(float &y0, float &y1, unsigned long long t, unsigned long long s) {
     unsigned long long yv;
     asm("mov.b64 %0, {%1, %2};" : "=l"(yv) : "f"(y0), "f"(y1));
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(yv) : "l"(t), "l"(s));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(y0), "=f"(y1) : "l"(yv));
-}
-__device__ __forceinline__ void ffma2(float &y0, float &y1, uint32_t s0, uint32_t s1, uint32_t p0, uint32_t p1) {
-    unsigned long long yv, sv, pv;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(yv) : "f"(y0), "f"(y1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(sv) : "r"(s0), "r"(s1));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(pv) : "r"(p0), "r"(p1));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(yv) : "l"(sv), "l"(pv));
     asm("mov.b64 {%0, %1}, %2;" : "=f"(y0), "=f"(y1) : "l"(yv));
 }
 
@@ -269,12 +240,6 @@ __device__ __forceinline__ uint32_t q4_byte_to_h2(uint32_t w) {
 // (chunk index XOR the row's low 3 bits; 8-row groups of 1024 bytes).
 __device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
     return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-// Byte offset of (row, 16-byte chunk) in a 128 x 64-byte K-major operand with the 64-byte swizzle
-// (chunk index XOR bits 1..2 of the row; 8-row groups of 512 bytes).
-__device__ __forceinline__ uint32_t sw64_off(int row, int chunk) {
-    return (uint32_t)((row >> 3) * 512 + (row & 7) * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
 // ---------------------------------------------------------------------------------------------
