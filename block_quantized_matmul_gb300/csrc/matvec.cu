@@ -397,6 +397,14 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     const int ctid = threadIdx.x - 32;        // 0..255
     const int g = lane >> 2, t = lane & 3;
 
+    // The byte -> half2 table depends on the parameters only: built before the wait.
+    if constexpr (TileFmt<TYPE>::kLut) {
+        for (int i = ctid; i < 256 * kLutCopies; i += kConsumerWarps * 32) {
+            const int b = i / kLutCopies;
+            lut_s[i] = h2_bits(__halves2half2(__int2half_rn(p.lut.v[b & 15]), __int2half_rn(p.lut.v[b >> 4])));
+        }
+    }
+
     // The weights never depend on the kernel launched just before on the stream, so the producer
     // starts streaming at once; the activations may, so the consumers wait for that grid first
     // (a no-op unless this grid was launched as its programmatic dependent).
@@ -404,45 +412,58 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
 
     // ---- stage activations once: per (token, block) 16 half2 in fragment order, plus the
     //      per-block scale and the exact bias of the biased weight decode ----
-    if constexpr (TileFmt<TYPE>::kLut) {
-        for (int i = ctid; i < 256 * kLutCopies; i += kConsumerWarps * 32) {
-            const int b = i / kLutCopies;
-            lut_s[i] = h2_bits(__halves2half2(__int2half_rn(p.lut.v[b & 15]), __int2half_rn(p.lut.v[b >> 4])));
-        }
-    }
     if constexpr (!FUSED) {
-        for (int i = ctid; i < TOK * nkc; i += kConsumerWarps * 32) {
-            const int j = i / TOK, tok = i - j * TOK;
-            float d = 0.0f, corr = 0.0f, asum = 0.0f;
-            if (tok < p.M) {
-                const int64_t kt = p.kt0 + j;
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.a_q + (int64_t)tok * p.K + kt * 32);
-                const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-                const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                int sum_even = 0, sum_odd = 0;
-                uint32_t hp[16];                 // half2 of column pair cp, in cp order
+        // two (token, block) entries per thread and pass, both loaded before either is converted
+        constexpr int kStep = kConsumerWarps * 32;
+        for (int i0 = ctid; i0 < TOK * nkc; i0 += 2 * kStep) {
+            uint4 ld[2][2];
+            uint16_t dbits[2] = {0, 0};
 #pragma unroll
-                for (int wi = 0; wi < 8; ++wi) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int a0 = (int)(int8_t)((wv[wi] >> (16 * h)) & 0xFF);
-                        const int a1 = (int)(int8_t)((wv[wi] >> (16 * h + 8)) & 0xFF);
-                        sum_even += a0;
-                        sum_odd += a1;
-                        hp[2 * wi + h] = act_pair<TYPE>(a0, a1);
-                    }
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * kStep, j = i / TOK, tok = i - j * TOK;
+                ld[u][0] = ld[u][1] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < TOK * nkc && tok < p.M) {
+                    const int64_t kt = p.kt0 + j;
+                    const uint4 *src = reinterpret_cast<const uint4 *>(p.a_q + (int64_t)tok * p.K + kt * 32);
+                    ld[u][0] = __ldg(src);
+                    ld[u][1] = __ldg(src + 1);
+                    dbits[u] = p.a_d[(int64_t)tok * p.nkt + kt];
                 }
-                // fragment order: position 4t + q holds column pair t + 4q
-                uint4 *dst = act_s + tok * tok_stride + j * 4;
-#pragma unroll
-                for (int tt = 0; tt < 4; ++tt) dst[tt] = make_uint4(hp[tt], hp[tt + 4], hp[tt + 8], hp[tt + 12]);
-                d = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
-                corr = act_bias<TYPE>(sum_even, sum_odd);
-                asum = (float)(sum_even + sum_odd);
             }
-            da_s[j * TOK + tok] = d;
-            corr_s[j * TOK + tok] = corr;
-            if constexpr (TileFmt<TYPE>::kAffine) asum_s[j * TOK + tok] = asum;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int i = i0 + u * kStep;
+                if (i >= TOK * nkc) break;
+                const int j = i / TOK, tok = i - j * TOK;
+                float d = 0.0f, corr = 0.0f, asum = 0.0f;
+                if (tok < p.M) {
+                    const uint4 v0 = ld[u][0], v1 = ld[u][1];
+                    const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    int sum_even = 0, sum_odd = 0;
+                    uint32_t hp[16];                 // half2 of column pair cp, in cp order
+#pragma unroll
+                    for (int wi = 0; wi < 8; ++wi) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int a0 = (int)(int8_t)((wv[wi] >> (16 * h)) & 0xFF);
+                            const int a1 = (int)(int8_t)((wv[wi] >> (16 * h + 8)) & 0xFF);
+                            sum_even += a0;
+                            sum_odd += a1;
+                            hp[2 * wi + h] = act_pair<TYPE>(a0, a1);
+                        }
+                    }
+                    // fragment order: position 4t + q holds column pair t + 4q
+                    uint4 *dst = act_s + tok * tok_stride + j * 4;
+#pragma unroll
+                    for (int tt = 0; tt < 4; ++tt) dst[tt] = make_uint4(hp[tt], hp[tt + 4], hp[tt + 8], hp[tt + 12]);
+                    d = __half2float(__ushort_as_half(dbits[u]));
+                    corr = act_bias<TYPE>(sum_even, sum_odd);
+                    asum = (float)(sum_even + sum_odd);
+                }
+                da_s[j * TOK + tok] = d;
+                corr_s[j * TOK + tok] = corr;
+                if constexpr (TileFmt<TYPE>::kAffine) asum_s[j * TOK + tok] = asum;
+            }
         }
     } else {
         // 4 lanes per (block, token), 8 columns each; lane q holds column pairs 4q..4q+3, which go to
