@@ -20,6 +20,7 @@ __all__ = [
     "qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
     "qmm_matmul_path", "qmm_matmul_f32", "qmm_matmul_flat", "qmm_device_status", "PATH_AUTO", "PATH_MATVEC", "PATH_GEMM",
     "matmul_workspace_size", "qmm_matmul_ws", "qmm_matmul_noalloc", "matmul_noalloc_max_workspace",
+    "qmm_selftest_timeout",
 ]
 
 Q4_0, Q8_0, IQ4_NL, MXFP4, Q4_1, Q4_K = 0, 1, 2, 3, 4, 5
@@ -68,6 +69,7 @@ def lib():
         L.qmm_matmul_path.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, i32, vp]
         L.qmm_matmul_flat.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp]
         L.qmm_device_status.argtypes = [vp]
+        L.qmm_selftest_timeout.argtypes = [i32, ctypes.c_uint64, vp, vp]
         L.qmm_matmul_workspace_size.argtypes = [i64, i64]
         L.qmm_matmul_workspace_size.restype = sz
         L.qmm_matmul_ws.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp, sz, vp]
@@ -76,7 +78,7 @@ def lib():
         L.qmm_matmul_noalloc_max_workspace.restype = sz
         for fn in ("qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
                    "qmm_matmul_path", "qmm_device_status", "qmm_matmul_ws", "qmm_matmul_noalloc", "qmm_matmul_f32",
-                   "qmm_matmul_flat"):
+                   "qmm_matmul_flat", "qmm_selftest_timeout"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -201,3 +203,9 @@ def matmul_noalloc_max_workspace() -> int:
 def qmm_device_status(stream=None) -> int:
     """Synchronize the stream, then return and clear the device status (0 = ok, 5 = timeout)."""
     return int(lib().qmm_device_status(_stream(stream)))
+
+
+def qmm_selftest_timeout(unit: int, limit_ns: int, flags, stream=None) -> None:
+    """Test hook: one CTA whose bounded waits run out on purpose (unit 0: decode kernels' helper,
+    1: the GEMM's); afterwards qmm_device_status() reports the timeout (see include/qmm.h)."""
+    _check("qmm_selftest_timeout", lib().qmm_selftest_timeout(int(unit), int(limit_ns), _ptr(flags), _stream(stream)))

@@ -84,13 +84,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Bounded wait.  Gives up (returning false) when `abort` is raised by another warp or after
 // kWaitLimitNs, in which case it raises `abort` and the device status word itself.  The fast path
 // (phase already complete) is inline; the timer is read only every 64 polls of the slow path.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort) {
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+                                       unsigned long long limit_ns = kWaitLimitNs) {
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
                 *abort = 1;
                 atomicOr(&g_mv_status, 1u);
                 return false;
@@ -98,9 +99,29 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
         }
     }
 }
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
+                                             unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, abort);
+    return wait_slow(bar, parity, abort, limit_ns);
+}
+
+// Runs the bounded wait out on purpose (the failure-detection test): warp 0 waits, with limit_ns,
+// for a barrier phase that nothing completes; warp 1 waits for the same phase with the normal limit
+// and must give up once warp 0 has raised the abort flag.  out[w] = 1 if warp w's wait returned
+// true (neither should); the device status word is set as by any timed-out pipeline wait.
+__global__ void __launch_bounds__(64) selftest_wait_kernel(unsigned long long limit_ns, int *out) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    volatile int *abort = &abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    const bool ok = wait_bounded(smem_u32(&bar), 0u, abort, warp == 0 ? limit_ns : kWaitLimitNs);
+    if ((threadIdx.x & 31) == 0) out[warp] = ok ? 1 : 0;
 }
 __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
@@ -1449,6 +1470,11 @@ cudaError_t launch_matvec_flat(qmm_type t, const uint8_t *flat, int64_t K, int64
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_selftest_wait_mv(unsigned long long limit_ns, int *out, cudaStream_t s) {
+    selftest_wait_kernel<<<1, 64, 0, s>>>(limit_ns, out);
+    return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_matvec_status(unsigned *out, cudaStream_t s) {

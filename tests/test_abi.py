@@ -188,3 +188,13 @@ def test_q4_k_sizes_and_argument_errors(L):
     assert L.qmm_matmul(5, P, 288, 64, P, P, 1, P, 64, None) == INVALID
     assert L.qmm_matmul_f32(5, P, 288, 64, P, 288, 1, P, 64, None) == INVALID
     assert L.qmm_matmul_flat(5, P, 288, 64, P, P, 1, P, 64, None) == INVALID
+
+
+def test_selftest_timeout_argument_errors(L):
+    f = L.qmm_selftest_timeout
+    assert f(2, 100_000_000, P, None) == INVALID              # unit
+    assert f(-1, 100_000_000, P, None) == INVALID
+    assert f(0, 999_999, P, None) == INVALID                  # below 1 ms
+    assert f(1, 2_000_000_001, P, None) == INVALID            # above 2 s
+    assert f(0, 100_000_000, None, None) == INVALID
+    assert f(0, 100_000_000, P + 2, None) == MISALIGNED
