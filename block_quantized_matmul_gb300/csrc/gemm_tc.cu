@@ -209,29 +209,6 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
                  : "memory");
 }
 
-__device__ __forceinline__ unsigned long long pack2f(float a, float b) {
-    unsigned long long v;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(a), "f"(b));
-    return v;
-}
-__device__ __forceinline__ unsigned long long pack2u(uint32_t a, uint32_t b) {
-    unsigned long long v;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(a), "r"(b));
-    return v;
-}
-__device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsigned long long b) {
-    unsigned long long d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-// (y0, y1) += t * s, elementwise
-__device__ __forceinline__ void ffma2_acc(float &y0, float &y1, unsigned long long t, unsigned long long s) {
-    unsigned long long yv;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(yv) : "f"(y0), "f"(y1));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(yv) : "l"(t), "l"(s));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(y0), "=f"(y1) : "l"(yv));
-}
-
 // ---------------------------------------------------------------------------------------------
 // fp16 helpers (exact integer values)
 // ---------------------------------------------------------------------------------------------
@@ -590,9 +567,9 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
         const int qd = warp & 3;                     // TMEM lane quadrant this warp may access
         const int half = rw >> 2;                    // token columns 64*half .. 64*half+63
         const int row = 32 * qd + lane;              // weight row within the tile (= TMEM lane)
-        float y[64];
+        float2 y2[32];                               // token columns (2i, 2i + 1)
 #pragma unroll
-        for (int i = 0; i < 64; ++i) y[i] = 0.0f;
+        for (int i = 0; i < 32; ++i) y2[i] = make_float2(0.0f, 0.0f);
         bool ok = true;
         int ts = 0, os = 0;
         uint32_t tph = 0, oph = 0;
@@ -604,7 +581,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
             tc_fence_after();
             const float *sc = reinterpret_cast<const float *>(op_s + os * P::kOpStage + P::kOffScale);
             const float dw = sc[j * 128 + row];
-            const unsigned long long dw2 = pack2f(dw, dw);
+            const float2 dw2 = make_float2(dw, dw);
             const float4 *da4 = reinterpret_cast<const float4 *>(sc + 256 + j * 128 + 64 * half);
             const uint32_t t_s = tmem_base + ((uint32_t)(32 * qd) << 16) + (uint32_t)(ts * BN + 64 * half);
 #pragma unroll
@@ -617,20 +594,22 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                 tmem_wait_ld(sv);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const unsigned long long t0 = fmul2(pack2u(sv[4 * e], sv[4 * e + 1]), pack2f(da[e].x, da[e].y));
-                    const unsigned long long t1 = fmul2(pack2u(sv[4 * e + 2], sv[4 * e + 3]), pack2f(da[e].z, da[e].w));
-                    ffma2_acc(y[16 * cc + 4 * e], y[16 * cc + 4 * e + 1], t0, dw2);
-                    ffma2_acc(y[16 * cc + 4 * e + 2], y[16 * cc + 4 * e + 3], t1, dw2);
+                    const float2 t0 = __fmul2_rn(make_float2(__uint_as_float(sv[4 * e]), __uint_as_float(sv[4 * e + 1])),
+                                                 make_float2(da[e].x, da[e].y));
+                    const float2 t1 = __fmul2_rn(make_float2(__uint_as_float(sv[4 * e + 2]), __uint_as_float(sv[4 * e + 3])),
+                                                 make_float2(da[e].z, da[e].w));
+                    y2[8 * cc + 2 * e] = __ffma2_rn(t0, dw2, y2[8 * cc + 2 * e]);
+                    y2[8 * cc + 2 * e + 1] = __ffma2_rn(t1, dw2, y2[8 * cc + 2 * e + 1]);
                 }
                 if constexpr (P::kAff) {
                     // + m_w * (d_a * sum(a_q)) of the block, per token column
                     const float4 *ca4 = reinterpret_cast<const float4 *>(sc + 768 + j * 128 + 64 * half);
-                    const unsigned long long mw2 = pack2f(sc[512 + j * 128 + row], sc[512 + j * 128 + row]);
+                    const float2 mw2 = make_float2(sc[512 + j * 128 + row], sc[512 + j * 128 + row]);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float4 ca = ca4[4 * cc + e];
-                        ffma2_acc(y[16 * cc + 4 * e], y[16 * cc + 4 * e + 1], pack2f(ca.x, ca.y), mw2);
-                        ffma2_acc(y[16 * cc + 4 * e + 2], y[16 * cc + 4 * e + 3], pack2f(ca.z, ca.w), mw2);
+                        y2[8 * cc + 2 * e] = __ffma2_rn(make_float2(ca.x, ca.y), mw2, y2[8 * cc + 2 * e]);
+                        y2[8 * cc + 2 * e + 1] = __ffma2_rn(make_float2(ca.z, ca.w), mw2, y2[8 * cc + 2 * e + 1]);
                     }
                 }
             }
@@ -649,7 +628,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
                     const int64_t m = m0 + 64 * half + i;
-                    if (m < p.M) p.y[m * p.ldy + n] = y[i];
+                    if (m < p.M) p.y[m * p.ldy + n] = (i & 1) ? y2[i >> 1].y : y2[i >> 1].x;
                 }
             }
         }

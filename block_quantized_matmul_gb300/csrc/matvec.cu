@@ -244,29 +244,14 @@ __device__ __forceinline__ void row_scales(const uint8_t *scales, int r0, float 
     }
 }
 
-__device__ __forceinline__ unsigned long long pack2(float a, float b) {
-    unsigned long long v;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(a), "f"(b));
-    return v;
+__device__ __forceinline__ float2 pack2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ void unpack2(float2 v, float &a, float &b) {
+    a = v.x;
+    b = v.y;
 }
-__device__ __forceinline__ void unpack2(unsigned long long v, float &a, float &b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
-    unsigned long long d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsigned long long b) {
-    unsigned long long d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
@@ -530,11 +515,11 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     uint32_t it = 0;
     bool ok = true;
     for (int64_t ct = blockIdx.x; ct < p.n_col_tiles; ct += gridDim.x) {
-        unsigned long long acc[2][NF][2];     // [rb][nf][row pair half]: (tok 2t, 2t+1) of rows 4g+2rb(+1)
+        float2 acc[2][NF][2];     // [rb][nf][row pair half]: (tok 2t, 2t+1) of rows 4g+2rb(+1)
 #pragma unroll
         for (int rb = 0; rb < 2; ++rb)
 #pragma unroll
-            for (int nf = 0; nf < NF; ++nf) acc[rb][nf][0] = acc[rb][nf][1] = 0ull;
+            for (int nf = 0; nf < NF; ++nf) acc[rb][nf][0] = acc[rb][nf][1] = make_float2(0.0f, 0.0f);
 
         for (int j0 = 0; j0 < nkc; j0 += kTilesPerStage, ++it) {
             const int s = (int)(it % (uint32_t)stages);
@@ -568,9 +553,9 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                         if (tok < p.M) b = act_s[tok * tok_stride + j * 4 + t];
                         const float2 da = *reinterpret_cast<const float2 *>(da_s + j * TOK + 8 * nf + 2 * t);
                         const float2 cr = *reinterpret_cast<const float2 *>(corr_s + j * TOK + 8 * nf + 2 * t);
-                        const unsigned long long ncorr = pack2(-cr.x, -cr.y);
-                        const unsigned long long da2 = pack2(da.x, da.y);
-                        unsigned long long as2 = 0ull;
+                        const float2 ncorr = pack2(-cr.x, -cr.y);
+                        const float2 da2 = pack2(da.x, da.y);
+                        float2 as2 = make_float2(0.0f, 0.0f);
                         if constexpr (TileFmt<TYPE>::kAffine) {
                             const float2 as = *reinterpret_cast<const float2 *>(asum_s + j * TOK + 8 * nf + 2 * t);
                             as2 = pack2(as.x, as.y);
@@ -581,16 +566,16 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                             mma16816(c, H[u][0][2 * rb], H[u][0][2 * rb + 1], H[u][1][2 * rb], H[u][1][2 * rb + 1], b.x, b.y);
                             mma16816(c, H[u][2][2 * rb], H[u][2][2 * rb + 1], H[u][3][2 * rb], H[u][3][2 * rb + 1], b.z, b.w);
                             // c0,c1: row 4g+2rb, tokens 2t,2t+1;  c2,c3: row 4g+2rb+1
-                            const unsigned long long s01 = fadd2(pack2(c[0], c[1]), ncorr);
-                            const unsigned long long s23 = fadd2(pack2(c[2], c[3]), ncorr);
-                            const unsigned long long p01 = fmul2(pack2(dwr[u][2 * rb], dwr[u][2 * rb]), da2);
-                            const unsigned long long p23 = fmul2(pack2(dwr[u][2 * rb + 1], dwr[u][2 * rb + 1]), da2);
+                            const float2 s01 = fadd2(pack2(c[0], c[1]), ncorr);
+                            const float2 s23 = fadd2(pack2(c[2], c[3]), ncorr);
+                            const float2 p01 = fmul2(pack2(dwr[u][2 * rb], dwr[u][2 * rb]), da2);
+                            const float2 p23 = fmul2(pack2(dwr[u][2 * rb + 1], dwr[u][2 * rb + 1]), da2);
                             acc[rb][nf][0] = ffma2(s01, p01, acc[rb][nf][0]);
                             acc[rb][nf][1] = ffma2(s23, p23, acc[rb][nf][1]);
                             if constexpr (TileFmt<TYPE>::kAffine) {
                                 // + m_w * d_a * sum(a_q) of the block, per row and token
-                                const unsigned long long m01 = fmul2(pack2(mwr[u][2 * rb], mwr[u][2 * rb]), da2);
-                                const unsigned long long m23 = fmul2(pack2(mwr[u][2 * rb + 1], mwr[u][2 * rb + 1]), da2);
+                                const float2 m01 = fmul2(pack2(mwr[u][2 * rb], mwr[u][2 * rb]), da2);
+                                const float2 m23 = fmul2(pack2(mwr[u][2 * rb + 1], mwr[u][2 * rb + 1]), da2);
                                 acc[rb][nf][0] = ffma2(as2, m01, acc[rb][nf][0]);
                                 acc[rb][nf][1] = ffma2(as2, m23, acc[rb][nf][1]);
                             }
@@ -820,9 +805,9 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
     uint32_t it = 0;
     bool ok = true;
     for (int64_t ct = blockIdx.x; ct < p.n_col_tiles; ct += gridDim.x) {
-        unsigned long long acc[MT][2];           // per token: rows (4i, 4i+1), (4i+2, 4i+3)
+        float2 acc[MT][2];           // per token: rows (4i, 4i+1), (4i+2, 4i+3)
 #pragma unroll
-        for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = 0ull;
+        for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = make_float2(0.0f, 0.0f);
 
         for (int j0 = 0; j0 < nkc; j0 += kTilesPerStage, ++it) {
             const int s = (int)(it % (uint32_t)stages);
@@ -838,8 +823,8 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
                     tile_rows_dp4a<TYPE>(tile, i, j, R, tb);
                     float dws[4];
                     row_scales<TYPE>(tile + SOFF, 4 * i, dws);                  // rows 4i .. 4i+3
-                    const unsigned long long dw01 = pack2(dws[0], dws[1]), dw23 = pack2(dws[2], dws[3]);
-                    unsigned long long mw01 = 0ull, mw23 = 0ull;
+                    const float2 dw01 = pack2(dws[0], dws[1]), dw23 = pack2(dws[2], dws[3]);
+                    float2 mw01 = make_float2(0.0f, 0.0f), mw23 = make_float2(0.0f, 0.0f);
                     if constexpr (TileFmt<TYPE>::kAffine) {
                         float mws[4];
                         row_mins<TYPE>(tile + SOFF, 4 * i, mws);
@@ -855,14 +840,14 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
 #pragma unroll
                         for (int r = 0; r < 4; ++r) S[r] = __dp4a((int)R[r][0], (int)a.x, __dp4a((int)R[r][1], (int)a.y, c0));
                         const float da = __uint_as_float(a.w);
-                        const unsigned long long da2 = pack2(da, da);
+                        const float2 da2 = pack2(da, da);
                         acc[t][0] = ffma2(pack2((float)S[0], (float)S[1]), fmul2(dw01, da2), acc[t][0]);
                         acc[t][1] = ffma2(pack2((float)S[2], (float)S[3]), fmul2(dw23, da2), acc[t][1]);
                         if constexpr (TileFmt<TYPE>::kAffine) {
                             // + m_w * d_a * (sum of this lane's 8 activations); the 4 quarters add up to
                             // the block's sum
                             const float as = (float)(int)a.z;
-                            const unsigned long long as2 = pack2(as, as);
+                            const float2 as2 = pack2(as, as);
                             acc[t][0] = ffma2(as2, fmul2(mw01, da2), acc[t][0]);
                             acc[t][1] = ffma2(as2, fmul2(mw23, da2), acc[t][1]);
                         }
