@@ -2,16 +2,18 @@
 """Benchmark of the tiled block-32 quantized matmul hot path on GB300.
 
 Headline workload: Q8_0 tiled matvec, K=4096, N=14336, batch 1 (an FFN up-projection shape).
-One step = one pass of the hot path over one batch: dynamic Q8_0 quantization of the activation
-(qmm_quantize_act) followed by the matmul over the tiled weight (qmm_matmul, decode kernel) and its
-fp32 output.  The weight is repacked once beforehand, as at model load.
+One step = one pass of the hot path over one batch: dynamic Q8_0 quantization of the activation,
+the matmul over the tiled weight and its fp32 output.  Decode shapes (up to 4 rows) run the step as
+one kernel with the quantization fused in (qmm_matmul_f32); the two-call form (qmm_quantize_act +
+qmm_matmul) is reported beside it; prefill shapes run qmm_quantize_act + the tensor-core GEMM.  The
+weight is repacked once beforehand, as at model load.
 
   value   weight-tile bytes per step / device time per step (GB/s), inputs resident in HBM;
           K consecutive steps captured in one CUDA graph and timed with CUDA events on the launching
           stream, rotating through enough weight copies that the working set exceeds the 129 MB L2
           (no step hits a weight left in L2 by the previous one).
   e2e     the same metric through the C ABI with host buffers: each step copies its activation
-          from pinned host memory, runs both calls and reads the output back.
+          from pinned host memory, runs the step's call and reads the output back (eager launches).
   roofline  the decode matvec alone: algorithmic bytes (weight tiles + activation quants and
           scales + fp32 output) per launch / mean launch time (a graph of back-to-back launches
           timed with CUDA events), against the measured HBM copy bandwidth.
