@@ -932,6 +932,7 @@ template <typename Kern>
 cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const Lut16 &lut, const uint8_t *tiled, int64_t K,
                           int64_t N, const ActSrc &a, int M, float *y, int64_t ldy, cudaStream_t s) {
     const int64_t nkt = K / 32, nct = (N + 31) / 32;
+    if (pl.smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;   // a ring of two stages must fit
     int64_t grid = (int64_t)num_sms() * pl.ctas_per_sm;
     if (grid > nct) grid = nct;
     for (int64_t kt0 = 0; kt0 < nkt; kt0 += pl.nkc) {
