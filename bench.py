@@ -57,6 +57,28 @@ def workload_name(type_, K, N, M, layout="tiled"):
     return f"{type_}_{kind}_K{K}_N{N}_M{M}"
 
 
+def int8_library_tops(torch, n=8192, reps=5):
+    """Reference point for the int8 tensor rate on this GPU: torch._int_mm (the vendor library's int8
+    GEMM) on n x n x n, timed with CUDA events.  Context only; the prefill GEMM's roofline is the
+    measured bf16 peak (there is no int8 tcgen05 on sm_103a)."""
+    try:
+        a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device="cuda")
+        b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device="cuda")
+        torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            torch._int_mm(a, b)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        return {"tops": round(2.0 * n ** 3 / (ms * 1e-3) / 1e12, 1), "shape": f"{n}^3", "via": "torch._int_mm"}
+    except Exception as exc:  # an int8 GEMM the library does not offer on this GPU
+        return {"tops": None, "error": str(exc)[:120]}
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -448,6 +470,7 @@ def run_gpu(args):
         "clocks": clk.summary(),
         "device_status": status,
         "other_configs": others,
+        "int8_library_reference": None if args.headline_only else int8_library_tops(torch),
     }
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(HEADLINE, budget_s=args.cpu_seconds) if not args.no_cpu else None
