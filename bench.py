@@ -144,7 +144,8 @@ class ClockSampler:
         return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
 
 
-KERNEL_FILES = {"matvec": ("matvec.cu", "qmm_internal.cuh"), "gemm": ("gemm_tc.cu", "qmm_internal.cuh")}
+KERNEL_FILES = {"matvec": ("matvec.cu", "qmm_internal.cuh", "pipeline.cuh"),
+                "gemm": ("gemm_tc.cu", "qmm_internal.cuh", "pipeline.cuh")}
 
 
 def kernel_kind(workload):

@@ -33,6 +33,7 @@
 
 #include <mutex>
 
+#include "pipeline.cuh"
 #include "qmm_internal.cuh"
 
 namespace qmm {
@@ -51,7 +52,8 @@ constexpr int kBProducerWarp = kRescaleWarp0 + kNumRescaleWarps;    // warp 14
 constexpr int kThreads = (kBProducerWarp + 1) * 32;
 constexpr int kOp2Bytes = BM * 128;        // 128 rows x 128 bytes: a block pair (SW128)
 constexpr int kLutCopies = 16;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+
+using namespace pipe;
 
 struct GemmParams {
     const uint8_t *tiled;
@@ -63,58 +65,10 @@ struct GemmParams {
     Lut16 lut;
 };
 
-// ---------------------------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait.  Gives up (returning false) when `abort` is raised by another warp or after
-// kWaitLimitNs, in which case it raises `abort` and the device status word itself.  The fast path
-// (phase already complete) is inline; the timer is read only every 64 polls of the slow path.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
-                                       unsigned long long limit_ns = kWaitLimitNs) {
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > limit_ns) {
-                *abort = 1;
-                atomicOr(&g_device_status, 1u);
-                return false;
-            }
-        }
-    }
-}
+// Bounded wait (pipeline.cuh) reporting to this file's status word.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
                                              unsigned long long limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, abort, limit_ns);
+    return wait_bounded_on(bar, parity, abort, &g_device_status, limit_ns);
 }
 
 // Runs the bounded wait out on purpose (the failure-detection test): warp 0 waits, with limit_ns,
@@ -141,23 +95,6 @@ __global__ void __launch_bounds__(64) selftest_wait_kernel(unsigned long long li
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort) {
     const bool ok = wait_bounded(bar, parity, abort);
     return __all_sync(0xffffffffu, ok);
-}
-
-// Wait used while draining after an abort: no abort check, shorter limit, never raises.
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > kWaitLimitNs / 4) return;
-    }
-}
-
-// 2-D tensor copy: box {32 bytes of K, 128 token rows} of the int8 activations; rows past M are
-// zero-filled by the TMA unit.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar) {

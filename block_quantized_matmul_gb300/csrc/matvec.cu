@@ -23,6 +23,7 @@
 //     (the activation quantizer), and only the activation staging waits for it.
 //   * No atomics and no scratch memory: each column tile is reduced across the warps in a fixed
 //     order; if the staged activations would not fit, K is processed in passes that add into y.
+#include "pipeline.cuh"
 #include "qmm_internal.cuh"
 
 namespace qmm {
@@ -37,7 +38,7 @@ constexpr int kDp4aMaxM = 4;                            // tokens up to which th
 constexpr int kLutCopies = 16;
 constexpr int kActBudget = 64 * 1024;                   // bytes of staged activations per CTA
 constexpr int kSmemLimit = 227 * 1024;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+using namespace pipe;
 
 struct MvParams {
     const uint8_t *tiled;
@@ -57,52 +58,10 @@ struct MvParams {
 
 __device__ unsigned g_mv_status = 0;   // set when a bounded wait gave up (reported with the GEMM's word)
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait.  Gives up (returning false) when `abort` is raised by another warp or after
-// kWaitLimitNs, in which case it raises `abort` and the device status word itself.  The fast path
-// (phase already complete) is inline; the timer is read only every 64 polls of the slow path.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
-                                       unsigned long long limit_ns = kWaitLimitNs) {
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer() - t0 > limit_ns) {
-                *abort = 1;
-                atomicOr(&g_mv_status, 1u);
-                return false;
-            }
-        }
-    }
-}
+// Bounded wait (pipeline.cuh) reporting to this file's status word.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
                                              unsigned long long limit_ns = kWaitLimitNs) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, abort, limit_ns);
+    return wait_bounded_on(bar, parity, abort, &g_mv_status, limit_ns);
 }
 
 // Runs the bounded wait out on purpose (the failure-detection test): warp 0 waits, with limit_ns,
@@ -122,24 +81,6 @@ __global__ void __launch_bounds__(64) selftest_wait_kernel(unsigned long long li
     const int warp = threadIdx.x >> 5;
     const bool ok = wait_bounded(smem_u32(&bar), 0u, abort, warp == 0 ? limit_ns : kWaitLimitNs);
     if ((threadIdx.x & 31) == 0) out[warp] = ok ? 1 : 0;
-}
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > kWaitLimitNs / 4) return;
-    }
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-// 2-D tensor copy of one box of `map` at element coordinates (x, y) into shared memory.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
 }
 // Producer warp: streams the K tiles [kt0, kt0 + nkc) of every column tile this CTA owns into the
 // ring, one stage of TPS consecutive tiles per 1-D bulk copy, and returns once the copies in
