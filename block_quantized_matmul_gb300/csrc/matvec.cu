@@ -855,14 +855,15 @@ int chunk_tiles(int64_t nkt, int64_t bytes_per_tile) {
     return (int)nkc;
 }
 
+// SM count of the device current at the first call (thread-safe static initialization).
 int num_sms() {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 152;
-    }
+    static const int sms = []() {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0)
+            n = 152;
+        return n;
+    }();
     return sms;
 }
 
