@@ -51,7 +51,7 @@ constexpr int kRescaleWarp0 = 6, kNumRescaleWarps = 8;
 constexpr int kBProducerWarp = kRescaleWarp0 + kNumRescaleWarps;    // warp 14
 constexpr int kThreads = (kBProducerWarp + 1) * 32;
 constexpr int kOp2Bytes = BM * 128;        // 128 rows x 128 bytes: a block pair (SW128)
-constexpr int kLutCopies = 16;
+constexpr int kLutCopies = 32;          // byte-indexed table copies (one per lane: no bank conflicts)
 
 using namespace pipe;
 

@@ -35,7 +35,7 @@ constexpr int kTilesPerWarp = 2;                        // independent tiles per
 template <int TYPE>
 constexpr int kDp4aTilesPerWarp = TYPE == QMM_Q8_0 ? 2 : 4;
 constexpr int kDp4aMaxM = 4;                            // tokens up to which the int8 dot-product path runs
-constexpr int kLutCopies = 16;
+constexpr int kLutCopies = 32;                          // byte-indexed table copies (one per lane: no bank conflicts)
 constexpr int kActBudget = 64 * 1024;                   // bytes of staged activations per CTA
 constexpr int kSmemLimit = 227 * 1024;
 using namespace pipe;
