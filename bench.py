@@ -12,8 +12,9 @@ weight is repacked once beforehand, as at model load.
           K consecutive steps captured in one CUDA graph and timed with CUDA events on the launching
           stream, rotating through enough weight copies that the working set exceeds the 129 MB L2
           (no step hits a weight left in L2 by the previous one).
-  e2e     the same metric through the C ABI with host buffers: each step copies its activation
-          from pinned host memory, runs the step's call and reads the output back (eager launches).
+  e2e     the same metric through the C ABI with host buffers (eager launches): each step hands the
+          call its pinned host activation and output buffers, which the kernel reads and writes over
+          NVLink-C2C; the variant with explicit copies to and from device buffers is reported beside.
   roofline  the decode matvec alone: algorithmic bytes (weight tiles + activation quants and
           scales + fp32 output) per launch / mean launch time (a graph of back-to-back launches
           timed with CUDA events), against the measured HBM copy bandwidth.
@@ -400,24 +401,38 @@ def run_gpu(args):
                 "unit": "GB/s", "step": "qmm_quantize_act + qmm_matmul (two kernels)"}
     wl_launches = wl.launches_per_step()
 
-    # end to end through the C ABI with host buffers
+    # end to end through the C ABI with host buffers (pinned), eager launches.  The call is given the
+    # host buffers themselves: the kernel reads x from and writes y to host memory over NVLink-C2C.
+    # The same step with an explicit host-to-device copy, the call on device buffers and a
+    # device-to-host copy is reported beside it.
     x_host = torch.empty((wl.n_act, M, K), dtype=torch.float32).pin_memory()
     x_host.copy_(wl.x.cpu())
     y_host = torch.empty((M, N), dtype=torch.float32).pin_memory()
     x_dev = torch.empty((M, K), dtype=torch.float32, device="cuda")
 
     def e2e_step(i, s):
+        qmm.qmm_matmul_f32(type_, wl.tiled[i % wl.copies], K, N, x_host[i % wl.n_act], K, M, y_host, N, stream=s)
+
+    def e2e_copy_step(i, s):
         x_dev.copy_(x_host[i % wl.n_act], non_blocking=True)
         qmm.qmm_matmul_f32(type_, wl.tiled[i % wl.copies], K, N, x_dev, K, M, wl.y, N, stream=s)
         y_host.copy_(wl.y, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            e2e_step(i, stream)
-        torch.cuda.synchronize()
-        e2e_ms = time_steps(torch, e2e_step, args.steps, stream)
+    def e2e_time(fn):
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                fn(i, stream)
+            torch.cuda.synchronize()
+            return time_steps(torch, fn, args.steps, stream)
+
+    e2e_ms, e2e_copy_ms = e2e_time(e2e_step), e2e_time(e2e_copy_step)
     e2e = {"value": round(wl.tiled_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-           "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(e2e_ms, 5)}
+           "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(e2e_ms, 5),
+           "transfer": "host buffers passed to the call; the kernel reads x and writes y over NVLink-C2C",
+           "with_copies": {"value": round(wl.tiled_bytes * world / (e2e_copy_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                           "ms_per_step": round(e2e_copy_ms, 5),
+                           "transfer": "cudaMemcpyAsync host-to-device, the call on device buffers, "
+                                       "cudaMemcpyAsync device-to-host"}}
 
     # ---------------- other workloads ----------------
     others = []

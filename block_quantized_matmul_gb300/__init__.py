@@ -89,13 +89,14 @@ def _t(type_) -> int:
 
 
 def _ptr(x) -> int | None:
-    """Device pointer of a CUDA tensor (or a raw integer address)."""
+    """Address of a CUDA tensor or of a page-locked (pinned) host tensor, which the GPU reads and
+    writes directly (or a raw integer address)."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
-    if not x.is_cuda:
-        raise ValueError("libqmm takes CUDA tensors only")
+    if not x.is_cuda and not x.is_pinned():
+        raise ValueError("libqmm takes CUDA tensors or pinned host tensors only")
     return x.data_ptr()
 
 

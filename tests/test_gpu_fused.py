@@ -110,3 +110,25 @@ def test_fused_full_size_sampled(torch, orc, type_, K, N, M):
     ys, bs = orc.matmul_at(type_, tiled_ref, K, q_ref, d_ref, ms, ns)
     assert_within_bound(y[ms, ns], ys, bs, f"fused {type_} {K}x{N} M={M}")
     assert np.isfinite(y).all()
+
+
+@pytest.mark.parametrize("type_", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("M", [1, 4, 9])
+def test_fused_with_host_buffers(torch, orc, type_, M):
+    """x and y in page-locked host memory, handed to the call as they are: the kernel reads and
+    writes them over the host link; the result equals the device-buffer call bit for bit."""
+    import block_quantized_matmul_gb300 as qmm
+
+    K, N = 1024, 300
+    w = synth.weights(N, K, seed=41)
+    x = synth.activations(M, K, seed=42)
+    _, tiled = gpu_prepare_weight(type_, w)
+    y_dev = gpu_matmul_f32(type_, tiled, K, N, x)
+    x_host = torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    y_host = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+    qmm.qmm_matmul_f32(type_, tiled, K, N, x_host, K, M, y_host, N)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, y_dev.cpu())
+    q_ref, d_ref = orc.quantize_act(x)
+    y_ref, bound = orc.matmul(type_, orc.repack(type_, orc.quantize_rows(type_, w), K, N), K, N, q_ref, d_ref)
+    assert_within_bound(y_host.numpy(), y_ref, bound, f"host buffers {type_} M={M}")
