@@ -13,11 +13,10 @@
  *     into a 16-entry non-linear table.
  *
  * Conventions for every call below:
- *   - Pointers named *_dev are addresses the GPU can access: device memory, or page-locked host
- *     memory mapped into the device's address space (cudaHostAlloc / cudaHostRegister; on GB300 the
- *     kernels then read and write it over the coherent NVLink-C2C link, with no separate copy).  The
- *     caller owns every buffer and the stream.  The library allocates no device memory and keeps no
- *     per-call state.
+ *   - Pointers named *_dev are addresses the GPU accesses directly: device memory, except where a
+ *     call says otherwise (qmm_matmul_f32 also takes x and y in page-locked host memory, which on
+ *     GB300 its kernel reads and writes over the coherent NVLink-C2C link).  The caller owns every
+ *     buffer and the stream.  The library allocates no device memory and keeps no per-call state.
  *   - Calls that take a stream only validate their arguments on the host and enqueue work on that
  *     stream; they return before the GPU has run.  `stream` is a cudaStream_t (NULL = legacy
  *     default stream).  Calls on different streams with distinct outputs may run concurrently.
@@ -193,7 +192,8 @@ QMM_API qmm_status qmm_matmul(qmm_type t, const void *w_tiled_dev, int64_t K, in
  * of qmm_decode_max_m() rows, far slower than quantize + the tensor-core GEMM.  Nothing is
  * written but y; no workspace.  Launch overlap as for qmm_matmul (x is read only after the
  * preceding kernel has completed).
- * x and y may live in page-locked host memory: a decode step then moves its 4*M*K input bytes and
+ * x and y may also live in page-locked host memory mapped for the device (cudaHostAlloc, or
+ * cudaHostRegister with cudaHostRegisterMapped): a decode step then moves its 4*M*K input bytes and
  * 4*M*N output bytes over NVLink-C2C inside the kernel, which on GB300 is faster end to end than a
  * host-to-device copy, the kernel and a device-to-host copy in sequence (same results, bit for bit).
  * Errors: INVALID_ARG (sizes, ldx < K, ldy < N, NULL), UNSUPPORTED, MISALIGNED, CUDA.
