@@ -1,13 +1,26 @@
 """block_quantized_matmul_gb300 -- Python binding of libqmm (include/qmm.h).
 
-Matrix multiply over block-32 quantized weights (Q4_0, Q8_0, IQ4_NL) stored in the 32-row tiled
-layout of "Hexagon backend developer details" ("Tiled Weight Formats"), with activations
-dynamically quantized to Q8_0 blocks, on one GB300 (sm_103a).
+Matrix multiply over block-32 quantized weights (Q4_0, Q8_0, IQ4_NL; also MXFP4, Q4_1 and the
+Q4_K super-blocks) stored in the 32-row tiled layout of "Hexagon backend developer details" ("Tiled
+Weight Formats") or in flat GGML rows, with activations dynamically quantized to Q8_0 blocks, on
+one GB300 (sm_103a).
 
 This module only marshals arguments: every function takes torch CUDA tensors (PyTorch provides the
-device memory and the stream), passes raw device pointers and sizes through ctypes, and raises
-QmmError on any status other than QMM_OK.  All computation runs in the CUDA kernels of libqmm.so;
-there is no CPU fallback, and importing the binding fails loudly if the library is missing.
+device memory and the stream; the fused decode call also takes pinned host tensors for x and y),
+passes raw addresses and sizes through ctypes, and raises QmmError on any status other than QMM_OK.
+All computation runs in the CUDA kernels of libqmm.so; there is no CPU fallback, and the first call
+fails loudly if the library is missing.
+
+A decode step over a weight w (fp32 [N, K] on the GPU):
+
+    flat = torch.empty(flat_size("q4_0", K, N), dtype=torch.uint8, device="cuda")
+    tiled = torch.empty(tiled_size("q4_0", K, N), dtype=torch.uint8, device="cuda")
+    qmm_quantize_weight("q4_0", w, N, K, K, flat)        # load time
+    qmm_repack("q4_0", flat, K, N, tiled)               # load time
+    qmm_matmul_f32("q4_0", tiled, K, N, x, K, M, y, N)   # y[M, N] = Q8_0(x[M, K]) @ W^T
+
+Prefill shapes: qmm_quantize_act, then qmm_matmul_ws with a workspace of matmul_workspace_size(M, K)
+bytes (or qmm_matmul, which needs none).
 """
 from __future__ import annotations
 
