@@ -200,6 +200,26 @@ def quantize_act(x: np.ndarray):
     return a_q, a_d
 
 
+def act_to_blocks(a_q: np.ndarray, a_d: np.ndarray) -> np.ndarray:
+    """The activation arrays as GGML Q8_0 blocks: per row, K/32 blocks of {fp16 d; int8 qs[32]} (34 B).
+    A byte rearrangement only; the library keeps the two arrays separate for aligned vector loads."""
+    a_q = np.ascontiguousarray(a_q, dtype=np.int8)
+    a_d = np.ascontiguousarray(a_d, dtype=np.uint16)
+    M, K = a_q.shape
+    out = np.zeros((M, K // 32, 34), np.uint8)
+    out[:, :, 0:2] = a_d.astype("<u2").view(np.uint8).reshape(M, K // 32, 2)
+    out[:, :, 2:] = a_q.view(np.uint8).reshape(M, K // 32, 32)
+    return out.reshape(M, K // 32 * 34)
+
+
+def blocks_to_act(blocks: np.ndarray, M: int, K: int):
+    """Inverse of act_to_blocks: (a_q int8 [M, K], a_d uint16 [M, K/32])."""
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(M, K // 32, 34)
+    a_d = np.ascontiguousarray(b[:, :, 0:2]).view("<u2").reshape(M, K // 32).astype(np.uint16)
+    a_q = np.ascontiguousarray(b[:, :, 2:]).view(np.int8).reshape(M, K)
+    return a_q, a_d
+
+
 def matmul(type_, tiled: np.ndarray, K: int, N: int, a_q: np.ndarray, a_d: np.ndarray, lut=None):
     """Full output: (Y fp64 [M, N], B fp64 [M, N])."""
     tiled = np.ascontiguousarray(tiled, dtype=np.uint8)

@@ -551,3 +551,16 @@ def test_q4_k_quantizer_error_bound(orc):
             lim = np.maximum((scale + e_scale) / 2, 15 * e_scale + e_min) * (1 + 1e-5) + 1e-9
             assert np.all(err <= lim), (n, s, err, lim)
     assert not Wf[3, :256].any()
+
+
+def test_activation_arrays_are_ggml_q8_0_blocks(orc):
+    """a_q / a_d hold the same values as GGML Q8_0 blocks: packed as {d, qs[32]} they equal, byte for
+    byte, the Q8_0 quantization of the same rows through the flat-block writer (a separate code path
+    that applies the same rule), and unpack back unchanged."""
+    x = synth.activations(5, 256, seed=77, outliers=True)
+    x[1, :32] = 0.0
+    a_q, a_d = orc.quantize_act(x)
+    blocks = orc.act_to_blocks(a_q, a_d)
+    assert np.array_equal(blocks, orc.quantize_rows("q8_0", x))
+    q2, d2 = orc.blocks_to_act(blocks, 5, 256)
+    assert np.array_equal(q2, a_q) and np.array_equal(d2, a_d)
