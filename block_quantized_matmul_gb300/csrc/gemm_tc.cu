@@ -8,7 +8,9 @@
 //     exact integer (|w| <= 127, |a| <= 127) and contracted with tcgen05.mma.kind::f16; every partial
 //     sum of a 32-element block is an integer below 2^24, so the fp32 accumulator in TMEM is exact.
 //   * Each block's sums S_b go to their own TMEM slot; the CUDA cores then apply the two scales,
-//     y += (S_b * d_a) * d_w, with packed mul.rn.f32x2 / fma.rn.f32x2 in registers.
+//     y += (S_b * d_a) * d_w, with packed f32x2 multiplies and FMAs in registers (affine tiles, Q4_1
+//     and Q4_K: + m_w * (d_a * sum_j a_q), one more FMA).  w_int is q-8 (Q4_0), q (Q8_0, Q4_1),
+//     table[q] (IQ4_NL) or twice the FP4 value (MXFP4, with half the E8M0 scale).
 //
 // Tile: 128 weight rows (4 column tiles, the UMMA M dimension) x 128 tokens (UMMA N), all of K.
 // The pipeline moves K in pairs of 32-wide blocks; TMEM holds S of four single blocks (4 x 128

@@ -1,24 +1,33 @@
-// matvec.cu -- decode-shaped matmul (M <= 16 activation rows per pass) over 32-row weight tiles.
+// matvec.cu -- decode-shaped matmul (M <= 16 activation rows per pass) over 32-row weight tiles, and
+// over flat GGML rows.
 //
 // What it computes ("Hexagon backend developer details", "Tiled Weight Formats"):
 //   Y[m, n] = sum_b fp32(d_w[n,b]) * fp32(d_a[m,b]) * S_b[m,n],  S_b = sum_j w_int[n,32b+j] * a_q[m,32b+j]
-// with w_int = q-8 (Q4_0), q (Q8_0), table[q] (IQ4_NL) read from the tile layouts of "Block-32
-// Quantized Formats".  The pages' decode kernel is an HVX 32x1 / 32x2 vector dot product fed by a
-// DDR -> DMA -> VTCM multi-buffered pipeline ("DDR -> DMA -> VTCM Execution Pipeline"); this is the
-// GB300 counterpart of both.
+// with w_int = q-8 (Q4_0), q (Q8_0), table[q] (IQ4_NL), twice the FP4 value (MXFP4, with half the
+// E8M0 scale) read from the tile layouts of "Block-32 Quantized Formats"; the affine tiles (Q4_1, and
+// Q4_K through the same tile) add d_a * m_w * sum_j a_q per block.  The pages' decode kernel is an
+// HVX 32x1 / 32x2 vector dot product fed by a DDR -> DMA -> VTCM multi-buffered pipeline ("DDR -> DMA
+// -> VTCM Execution Pipeline"); this file is the GB300 counterpart of both.
 //
 // GB300 design:
-//   * Persistent CTAs (one wide or two narrow per SM) each own a set of column tiles.  The K tiles of a column
-//     tile are contiguous in memory (tile_idx = ct*n_k_tiles + kt), so one producer warp streams them
-//     with 1-D cp.async.bulk copies of one stage (2 tiles per consumer warp) into a deep ring (mbarrier
-//     complete_tx / consumer release) -- the pipelined multi-buffering of the pages, with the TMA
-//     engine as the DMA queue.
-//   * 8 or 16 consumer warps take two tiles each of every stage (two independent chains per warp).  Quants become fp16 holding exact integers
-//     (biased: 1024+q or 1152+q, see decode_*), activations are staged once per CTA as fp16 in the
-//     mma fragment order, and mma.sync.m16n8k16 (fp32 accumulate) yields block sums that are exact
-//     integers; subtracting the exact per-(token, block) bias gives S_b.  fp16 mma.sync runs at ~4x
-//     the int8 mma.sync rate on sm_103a, where int8 tcgen05 does not exist.
-//   * Per block the fp32 result is rescaled by d_w*d_a with packed f32x2 arithmetic and accumulated.
+//   * Persistent CTAs (one wide or two narrow per SM) each own a set of column tiles.  The K tiles of
+//     a column tile are contiguous in memory (tile_idx = ct*n_k_tiles + kt), so one producer warp
+//     streams them with 1-D cp.async.bulk copies of one stage into a deep ring (mbarrier complete_tx /
+//     consumer release) -- the pipelined multi-buffering of the pages, with the TMA engine as the DMA
+//     queue.
+//   * Up to 4 activation rows (matvec_dp4a_kernel): each lane takes 4 rows x 8 columns of a tile,
+//     byte-transposes them into int8x4 words (nibble masks, or a 16-entry table held in registers
+//     for IQ4_NL / MXFP4) and takes dp4a against int8 activations staged once per CTA.
+//   * 5 to 16 rows (matvec_kernel): quants become fp16 holding exact integers (biased: 1024+q or
+//     1152+q, see decode_*), activations are staged once per CTA as fp16 in the mma fragment order,
+//     and mma.sync.m16n8k16 (fp32 accumulate) yields block sums that are exact integers; subtracting
+//     the exact per-(token, block) bias gives S_b.  fp16 mma.sync runs at ~4x the int8 mma.sync rate
+//     on sm_103a, where int8 tcgen05 does not exist.
+//   * Per block the result is rescaled by d_w*d_a with packed f32x2 arithmetic and accumulated.
+//   * The fused variants (qmm_matmul_f32) quantize the fp32 activation rows into shared memory
+//     themselves, by the rule of qmm_quantize_act, while the first weight stages stream in.
+//   * Flat GGML rows (matvec_flat_kernel, qmm_matmul_flat): 2-D tensor copies of 32 rows x 32 blocks,
+//     one block per lane, dp4a.
 //   * Launched as a programmatic dependent: weight streaming overlaps the end of the preceding grid
 //     (the activation quantizer), and only the activation staging waits for it.
 //   * No atomics and no scratch memory: each column tile is reduced across the warps in a fixed
