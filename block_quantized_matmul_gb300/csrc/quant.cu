@@ -4,6 +4,9 @@
 // q = round-half-away(x*id) clamped to [-127,127] (NaN product -> 0), stored scale fp16(d).
 // Every operation is an IEEE-rounded fp32 intrinsic (__fdiv_rn, __frcp_rn-free 1/d via __fdiv_rn,
 // __fmul_rn, __fadd_rn), so nvcc cannot contract or reassociate them.
+// Weight rules (test data and load time; stated with qmm_quantize_weight in qmm.h): Q4_0, Q8_0,
+// IQ4_NL, MXFP4 and Q4_1 per 32-element block (one thread per block), Q4_K per 256-element
+// super-block (one warp per super-block).
 #include "qmm_internal.cuh"
 
 namespace qmm {

@@ -3,6 +3,9 @@
 //
 // Thread mapping: one thread per (tile, tile row).  A warp covers the 32 rows of one tile, so each
 // per-column-pair store of the warp is one contiguous run (32 bytes for 4-bit tiles, 64 for Q8_0).
+// Q4_K super-blocks ("K-Quants Formats") are split into the 8 Q4_1-layout tiles of their 32-wide
+// sub-blocks, the row pair becoming (fp16(d*sc), fp16(-dmin*m)); that direction only (the products
+// cannot be split back).
 #include "qmm_internal.cuh"
 
 namespace qmm {
