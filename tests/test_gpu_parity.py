@@ -201,3 +201,24 @@ def test_column_shards_match_the_full_product(torch, orc, type_, M):
             qmm.qmm_matmul(type_, tiled[sh.byte_offset:], K, sh.n_local, a_q, a_d, M, y[:, sh.n0:], N)
     torch.cuda.synchronize()
     assert torch.equal(y, full)
+
+
+def test_quantize_act_golden_cases(torch):
+    """The hand-worked blocks of tests/golden/act_quant_cases.txt through the GPU quantizer, against
+    the worked-out codes and scales directly."""
+    import block_quantized_matmul_gb300 as qmm
+    from tests.test_oracle import _read_act_cases
+
+    cases = _read_act_cases()
+    x = np.stack([c[1] for c in cases])
+    M = x.shape[0]
+    xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    a_q = torch.full((M, 32), 99, dtype=torch.int8, device="cuda")
+    a_d = torch.full((M, 1), 0x7E00, dtype=torch.int16, device="cuda")
+    qmm.qmm_quantize_act(xd, M, 32, 32, a_q, a_d)
+    torch.cuda.synchronize()
+    q = a_q.cpu().numpy()
+    d = a_d.cpu().numpy().view(np.uint16)[:, 0]
+    for i, (name, _, q_exp, d_exp) in enumerate(cases):
+        assert np.array_equal(q[i], q_exp), name
+        assert d[i] == d_exp, name
