@@ -214,6 +214,18 @@ def test_q4_0_hand_case(orc):
     assert all(c == 8 for c in codes[4:])
 
 
+def test_q4_0_tie_takes_the_first_extreme(orc):
+    """|0.5| = |-0.5|: the first element sets the sign, d = 0.5/-8 = -0.0625 (1/d = -16), so 0.5 maps
+    to trunc(-8 + 8.5) = 0, -0.5 to min(15, trunc(16.5)) = 15 and 0 to 8 (worked by hand)."""
+    x = np.zeros((1, 32), np.float32)
+    x[0, :2] = [0.5, -0.5]
+    flat = orc.quantize_rows("q4_0", x)
+    d = np.array([int(flat[0, 0]) | (int(flat[0, 1]) << 8)], np.uint16).view(np.float16)[0]
+    assert d == np.float16(-0.0625)
+    codes = [(flat[0, 2 + j] & 15) if j < 16 else (flat[0, 2 + j - 16] >> 4) for j in range(32)]
+    assert codes[:3] == [0, 15, 8]
+
+
 @pytest.mark.parametrize("type_", TYPES)
 def test_weight_quantizer_error_bound(orc, type_):
     w = synth.weights(64, 256)
@@ -564,3 +576,21 @@ def test_activation_arrays_are_ggml_q8_0_blocks(orc):
     assert np.array_equal(blocks, orc.quantize_rows("q8_0", x))
     q2, d2 = orc.blocks_to_act(blocks, 5, 256)
     assert np.array_equal(q2, a_q) and np.array_equal(d2, a_d)
+
+
+def test_q4_k_quantizer_hand_case(orc):
+    """Sub-block 0 spans [0, 15] (scale 1), sub-block 1 spans [0, 7.5] (scale 0.5), the rest are zero,
+    nothing is negative.  By hand: d = fp16(1/63) = 0x2410, dmin = 0; sc_0 = trunc(1*63 + 0.5) = 63,
+    sc_1 = trunc(0.5*63 + 0.5) = 32 (31 if the 6-bit scales were truncated instead of rounded);
+    f32(d) = 1.015625/64, so 15 and 7.5 both land on code 15 and the zeros on code 0."""
+    x = np.zeros((1, 256), np.float32)
+    x[0, 1] = 15.0
+    x[0, 33] = 7.5
+    sb = orc.quantize_rows("q4_k", x)[0]
+    assert int(sb[0]) | (int(sb[1]) << 8) == 0x2410
+    assert int(sb[2]) | (int(sb[3]) << 8) == 0
+    assert sb[4] & 63 == 63 and sb[5] & 63 == 32
+    assert not (sb[6:8] & 63).any() and not (sb[8:12] & 63).any()
+    codes = [(sb[16 + 32 * (j // 2) + i] >> (4 * (j & 1))) & 15 for j in range(2) for i in range(32)]
+    assert codes[1] == 15 and codes[33] == 15
+    assert sum(codes) == 30
