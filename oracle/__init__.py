@@ -23,8 +23,10 @@ Q4_0, Q8_0, IQ4_NL, MXFP4, Q4_1, Q4_K = 0, 1, 2, 3, 4, 5
 TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL, "mxfp4": MXFP4, "q4_1": Q4_1, "q4_k": Q4_K}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "oracle.c")
-_LIB = os.path.join(_HERE, "liboracle.so")
+# QMM_ORACLE_SRC points the module at another copy of the C source (the pin-strength test builds
+# copies with one planted mistake each); the library is then built next to that copy.
+_SRC = os.environ.get("QMM_ORACLE_SRC") or os.path.join(_HERE, "oracle.c")
+_LIB = os.path.splitext(_SRC)[0] + ".so" if os.environ.get("QMM_ORACLE_SRC") else os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
