@@ -159,7 +159,8 @@ QMM_API qmm_status qmm_quantize_act(const float *x_dev, int64_t M, int64_t K, in
  *   Y[m, n] = sum_b fp32(d_w[n, b]) * fp32(d_a[m, b]) * S_b[m, n],
  *   S_b[m, n] = sum_{j<32} w_int[n, 32b+j] * a_q[m, 32b+j]  (exact integer block dot products),
  *   w_int = q-8 (Q4_0), q (Q8_0), table[q] (IQ4_NL), 2*fp4(q) with d_w = half the E8M0 scale
- *   (MXFP4); Q4_1 adds fp32(m_w[n, b]) * fp32(d_a[m, b]) * sum_j a_q[m, 32b+j] with w_int = q.
+ *   (MXFP4); Q4_1 adds fp32(m_w[n, b]) * fp32(d_a[m, b]) * sum_j a_q[m, 32b+j] with w_int = q, and
+ *   so does Q4_K, whose tile pair (d, m) is (d*sc, -dmin*m) of the super-block.
  *   w_tiled_dev  qmm_tiled_size bytes from qmm_repack; 16-byte aligned.
  *   a_q_dev, a_d_dev  as written by qmm_quantize_act for M rows and the same K.
  *   y_dev  fp32 output, y[m*ldy + n] for n < N (other columns untouched); 4-byte aligned.
