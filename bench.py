@@ -146,7 +146,7 @@ class ClockSampler:
 
 
 KERNEL_FILES = {"matvec": ("matvec.cu", "qmm_internal.cuh", "pipeline.cuh"),
-                "gemm": ("gemm_tc.cu", "qmm_internal.cuh", "pipeline.cuh")}
+                "gemm": ("gemm_fold.cu", "gemm_tc.cu", "tc_common.cuh", "qmm_internal.cuh", "pipeline.cuh")}
 
 
 def kernel_kind(workload):
@@ -460,10 +460,13 @@ def run_gpu(args):
             if cfg[3] > 16:
                 tf = o.flops() / (okms * 1e-3) / 1e12
                 ent["TFLOPs"] = round(tf, 1)
+                folded = cfg[0] in ("q4_0", "q8_0", "iq4_nl")
+                note = ("folded-scale GEMM: block scales inside exact hi + lo fp16 operands, three fp16 tcgen05 "
+                        "MMAs per K step (the tensor pipe executes 3x the algorithmic flops)" if folded else
+                        "fp16 tcgen05 MMA on exact integer operands, per-block fp32 rescale")
                 ent["roofline_tensor"] = {"achieved": round(tf, 1), "peak": bf16_peak, "unit": "TFLOP/s",
                                           "frac": round(tf / bf16_peak, 4),
-                                          "note": "fp16 tcgen05 MMA on exact integer operands (no int8 tcgen05 "
-                                                  "on sm_103a); peak = measured bf16 burst"}
+                                          "note": note + " (no int8 tcgen05 on sm_103a); peak = measured bf16 burst"}
             others.append(ent)
             del o
             torch.cuda.empty_cache()

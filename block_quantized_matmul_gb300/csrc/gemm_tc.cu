@@ -37,6 +37,7 @@
 
 #include "pipeline.cuh"
 #include "qmm_internal.cuh"
+#include "tc_common.cuh"
 
 namespace qmm {
 
@@ -56,6 +57,7 @@ constexpr int kOp2Bytes = BM * 128;        // 128 rows x 128 bytes: a block pair
 constexpr int kLutCopies = 32;          // byte-indexed table copies (one per lane: no bank conflicts)
 
 using namespace pipe;
+using namespace tc;
 
 struct GemmParams {
     const uint8_t *tiled;
@@ -99,84 +101,11 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major operand, rows of 128 bytes with the 128-byte swizzle,
-// 8-row groups 1024 bytes apart (SBO), descriptor version 1 (sm_100 family).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, both K-major, M = 128, N = BN.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdesc = idesc_f16(BM, BN);
 
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-// Waits for this thread's tcgen05.ld; also written as the last writer of the 16 registers a tcgen05.ld filled, so that no use of them
-// can be scheduled before the load has completed.
-__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-                 :
-                 : "memory");
-}
-
-// ---------------------------------------------------------------------------------------------
-// fp16 helpers (exact integer values)
-// ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
-__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
-
-// int8 pairs of a word (bytes 0,1 and 2,3) -> two half2, exact.
-__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const uint32_t x = w ^ 0x80808080u;
-    const __half2 bias = __halves2half2(__float2half_rn(1152.0f), __float2half_rn(1152.0f));
-    lo = h2_bits(__hsub2(bits_h2(__byte_perm(x, 0x64646464u, 0x4140u)), bias));
-    hi = h2_bits(__hsub2(bits_h2(__byte_perm(x, 0x64646464u, 0x4342u)), bias));
-}
-
-// 4-bit nibble byte (lo = even column, hi = odd column) at byte position I -> half2(lo-OFF, hi-OFF)
-// (OFF = 8 for Q4_0, 0 for Q4_1), exact.
-template <int I, int OFF = 8>
-__device__ __forceinline__ uint32_t q4_byte_to_h2(uint32_t w) {
-    const uint32_t y = __byte_perm(w, 0u, 0x4040u | (I << 8) | I);
-    uint32_t h;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(y), "r"(0x00F0000Fu), "r"(0x64006400u));
-    return h2_bits(__hfma2(bits_h2(h), __halves2half2(__float2half_rn(1.0f), __float2half_rn(0.0625f)),
-                           __halves2half2(__float2half_rn(-1024.0f - OFF), __float2half_rn(-64.0f - OFF))));
-}
-
-// Byte offset of (row, 16-byte chunk) in a 128 x 128-byte K-major operand with the 128-byte swizzle
-// (chunk index XOR the row's low 3 bits; 8-row groups of 1024 bytes).
-__device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
-    return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+    mma_f16_ss(d_tmem, adesc, bdesc, kIdesc, accumulate);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -653,8 +582,6 @@ cudaError_t make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *ba
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-namespace {
-
 // 3-D tensor map of the tiled weight viewed as [n_col_tiles][n_k_tiles][tile bytes / 8] of 8-byte
 // words: one box = the 4 column tiles x 2 K tiles of a block pair (column tiles past the end read
 // as zeros).
@@ -670,6 +597,8 @@ cudaError_t make_weight_map(CUtensorMap *map, const uint8_t *tiled, int tile_byt
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+namespace {
 
 template <int TYPE, int ACT>
 cudaError_t launch_typed(const GemmParams &p, const CUtensorMap &act_map, const CUtensorMap &da_map, const CUtensorMap &ca_map,
@@ -731,28 +660,16 @@ cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, 
     return dispatch<kActInt8>(t, p, am, dm, am, s);
 }
 
-// Workspace: fp16 a_q [M][K] | fp16 a_d transposed [K/32][M_pad] | fp32 d_a * sum(a_q) transposed
-// [K/32][M_pad] (used by Q4_1), each region 256-byte aligned.
-namespace {
-size_t ws_dT_off(int64_t M, int64_t K) { return ((size_t)M * (size_t)K * 2 + 255) / 256 * 256; }
-size_t ws_cA_off(int64_t M, int64_t K) {
-    const int64_t m_pad = (M + 7) / 8 * 8;
-    return ws_dT_off(M, K) + ((size_t)(K / 32) * (size_t)m_pad * 2 + 255) / 256 * 256;
-}
-}  // namespace
-
-size_t gemm_workspace_bytes(int64_t M, int64_t K) {
-    const int64_t m_pad = (M + 7) / 8 * 8;
-    return ws_cA_off(M, K) + (size_t)(K / 32) * (size_t)m_pad * 4 + 256;
-}
+size_t gemm_workspace_bytes(int64_t M, int64_t K) { return gemm_ws_layout(M, K).total; }
 
 cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                            const uint16_t *a_d, int64_t M, float *y, int64_t ldy, void *ws, cudaStream_t s) {
     if ((M + BN - 1) / BN > 65535) return cudaErrorInvalidValue;
     const int64_t nkt = K / 32, m_pad = (M + 7) / 8 * 8;
-    __half *a_h = static_cast<__half *>(ws);
-    uint16_t *a_dT = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + ws_dT_off(M, K));
-    float *cA = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + ws_cA_off(M, K));
+    const GemmWsLayout L = gemm_ws_layout(M, K);
+    __half *a_h = reinterpret_cast<__half *>(static_cast<uint8_t *>(ws) + L.hi);
+    uint16_t *a_dT = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + L.dT);
+    float *cA = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + L.cA);
     const bool need_ca = t == QMM_Q4_1;
     {
         const int64_t work = M * K / 4 > nkt * m_pad ? M * K / 4 : nkt * m_pad;

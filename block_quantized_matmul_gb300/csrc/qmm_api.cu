@@ -28,6 +28,14 @@ bool valid_tkn(qmm_type t, int64_t K, int64_t N) { return valid_kn(K, N) && (K %
 cudaStream_t cs(qmm_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
+// Prefill product with a workspace: the folded-scale GEMM for the tile types it covers, the
+// exact-integer GEMM with a prepared token operand for the others (t is already a tile type).
+cudaError_t launch_prefill_ws(qmm_type t, const uint8_t *w, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
+                              int64_t M, float *y, int64_t ldy, void *ws, cudaStream_t s) {
+    if (gemm_fold_supports(t)) return launch_gemm_fold(t, w, K, N, a_q, a_d, M, y, ldy, ws, s);
+    return launch_gemm_ws(t, w, K, N, a_q, a_d, M, y, ldy, ws, s);
+}
+
 // Sizes are capped so every byte offset fits comfortably in int64 arithmetic on both sides.
 constexpr int64_t kMaxDim = (int64_t)1 << 31;
 
@@ -166,7 +174,7 @@ qmm_status qmm_matmul_ws(qmm_type t, const void *w_tiled, int64_t K, int64_t N, 
     if (M <= kDecodeMaxM) return from_cuda(launch_matvec(t, w, K, N, a_q, a_d, M, y, ldy, cs(stream)));
     if (!workspace || workspace_bytes < gemm_workspace_bytes(M, K)) return QMM_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return QMM_ERR_MISALIGNED;
-    return from_cuda(launch_gemm_ws(t, w, K, N, a_q, a_d, M, y, ldy, workspace, cs(stream)));
+    return from_cuda(launch_prefill_ws(t, w, K, N, a_q, a_d, M, y, ldy, workspace, cs(stream)));
 }
 
 qmm_status qmm_matmul_noalloc(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const int8_t *a_q,
@@ -179,7 +187,7 @@ qmm_status qmm_matmul_noalloc(qmm_type t, const void *w_tiled, int64_t K, int64_
     if (gemm_workspace_bytes(M, K) > kNoAllocScratchBytes) return QMM_ERR_INVALID_ARG;
     void *scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return QMM_ERR_CUDA;
-    return from_cuda(launch_gemm_ws(t, w, K, N, a_q, a_d, M, y, ldy, scratch, cs(stream)));
+    return from_cuda(launch_prefill_ws(t, w, K, N, a_q, a_d, M, y, ldy, scratch, cs(stream)));
 }
 
 size_t qmm_matmul_noalloc_max_workspace(void) { return kNoAllocScratchBytes; }
@@ -193,11 +201,12 @@ qmm_status qmm_selftest_timeout(int unit, uint64_t limit_ns, int *flags_dev, qmm
 }
 
 qmm_status qmm_device_status(qmm_stream_t stream) {
-    unsigned v = 0, w = 0;
+    unsigned v = 0, w = 0, f = 0;
     cudaError_t e = read_and_clear_device_status(&v, cs(stream));
     if (e == cudaSuccess) e = read_and_clear_matvec_status(&w, cs(stream));
+    if (e == cudaSuccess) e = read_and_clear_fold_status(&f, cs(stream));
     if (e != cudaSuccess) return QMM_ERR_CUDA;
-    return (v | w) ? QMM_ERR_TIMEOUT : QMM_OK;
+    return (v | w | f) ? QMM_ERR_TIMEOUT : QMM_OK;
 }
 
 }  // extern "C"

@@ -130,6 +130,9 @@ cudaError_t launch_matvec(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N
 // 2-D tensor map: rows of `inner` elements (row stride `row_bytes`), box {box_inner, box_rows}.
 cudaError_t make_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner, uint64_t rows,
                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw);
+// 3-D tensor map of the tiled weight as [n_col_tiles][n_k_tiles][tile bytes / 8] 8-byte words, one box
+// = 4 column tiles x 2 K tiles (column tiles past the end read as zeros).
+cudaError_t make_weight_map(CUtensorMap *map, const uint8_t *tiled, int tile_bytes, int64_t nkt, int64_t nct);
 // Decode matmul straight from flat GGML rows (row bytes a multiple of 16, flat 16-byte aligned).
 cudaError_t launch_matvec_flat(qmm_type t, const uint8_t *flat, int64_t K, int64_t N, const int8_t *a_q,
                                const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
@@ -140,9 +143,34 @@ cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, 
 cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                            const uint16_t *a_d, int64_t M, float *y, int64_t ldy, void *ws, cudaStream_t s);
 size_t gemm_workspace_bytes(int64_t M, int64_t K);
+// The folded-scale GEMM (block scales inside exact hi + lo fp16 operands): Q4_0, Q8_0, IQ4_NL tiles.
+bool gemm_fold_supports(qmm_type t);
+cudaError_t launch_gemm_fold(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
+                             const uint16_t *a_d, int64_t M, float *y, int64_t ldy, void *ws, cudaStream_t s);
+cudaError_t read_and_clear_fold_status(unsigned *out, cudaStream_t s);
+
+// Workspace of the tensor-core GEMMs, each region 256-byte aligned.  The exact-integer kernel uses
+// hi (fp16 copies of the int8 quants), dT (block scales transposed, [K/32][M_pad] fp16) and cA
+// (Q4_1: d_a * sum(a_q), [K/32][M_pad] fp32); the folded-scale kernel uses hi and lo (the two fp16
+// terms of d_a * a_q, [M][K] each) and ts (per token row, the power of two it was scaled by).
+struct GemmWsLayout {
+    size_t hi, lo, dT, cA, ts, total;
+};
+inline size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+inline GemmWsLayout gemm_ws_layout(int64_t M, int64_t K) {
+    const size_t m_pad = (size_t)((M + 7) / 8 * 8), nkt = (size_t)(K / 32), mk2 = (size_t)M * (size_t)K * 2;
+    GemmWsLayout L;
+    L.hi = 0;
+    L.lo = round256(mk2);
+    L.dT = L.lo + round256(mk2);
+    L.cA = L.dT + round256(nkt * m_pad * 2);
+    L.ts = L.cA + round256(nkt * m_pad * 4);
+    L.total = L.ts + round256((size_t)M * 4);
+    return L;
+}
 
 // Fixed device scratch used by qmm_matmul_noalloc (bytes, per device).
-constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
 constexpr int kMaxDevices = 64;
 cudaError_t noalloc_scratch(void **out);
 cudaError_t read_and_clear_device_status(unsigned *out, cudaStream_t s);   // tensor-core GEMM

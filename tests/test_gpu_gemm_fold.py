@@ -1,0 +1,100 @@
+"""GPU parity of the folded-scale tensor-core GEMM against the CPU oracle.
+
+qmm_matmul_ws (and qmm_matmul_noalloc) run Q4_0, Q8_0 and IQ4_NL prefill shapes on the kernel that
+folds the block scales into exact hi + lo fp16 operands and accumulates 128-wide K chunks in fp32 on
+the tensor cores.  Bound: |gpu - oracle| <= 1e-5 * sum_k |w_k x_k| + 1e-6 per element.  Beyond the
+shapes of test_gpu_gemm.py these cases aim at what is particular to that kernel:
+  * long K with a partial last chunk and an odd number of blocks (K = 4192: 131 blocks);
+  * all-positive operands, where every rounding of the fp32 accumulation pushes the same way;
+  * token rows and weight rows large enough to take the power-of-two range shift, including rows
+    whose blocks differ in magnitude by 10^6;
+  * operands at the other end of fp16's range (tiny block scales, subnormal lo terms).
+"""
+import numpy as np
+import pytest
+
+from block_quantized_matmul_gb300 import synth
+from tests.gpu_util import assert_within_bound, gpu_matmul_ws, gpu_prepare_weight, gpu_quantize_act, torch_mod
+
+pytestmark = pytest.mark.gpu
+FOLD_TYPES = ["q4_0", "q8_0", "iq4_nl"]
+
+
+@pytest.fixture(scope="module")
+def torch():
+    t = torch_mod()
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_quantized_matmul_gb300 import build
+
+    build.build()
+    return t
+
+
+def _run(orc, type_, w, x, what, ldy=None):
+    import block_quantized_matmul_gb300 as qmm
+
+    N, K = w.shape
+    M = x.shape[0]
+    tiled_ref = orc.repack(type_, orc.quantize_rows(type_, w), K, N)
+    q_ref, d_ref = orc.quantize_act(x)
+    y_ref, bound = orc.matmul(type_, tiled_ref, K, N, q_ref, d_ref)
+    _, tiled_d = gpu_prepare_weight(type_, w)
+    a_q, a_d = gpu_quantize_act(x)
+    assert np.array_equal(tiled_d.cpu().numpy(), tiled_ref)
+    assert np.array_equal(a_q.cpu().numpy(), q_ref)
+    y = gpu_matmul_ws(type_, tiled_d, K, N, a_q, a_d, M, ldy=ldy).cpu().numpy()
+    assert qmm.qmm_device_status() == 0
+    assert_within_bound(y[:, :N], y_ref, bound, f"fold {type_} {what} N={N} K={K} M={M}")
+    return y
+
+
+@pytest.mark.parametrize("type_", FOLD_TYPES)
+@pytest.mark.parametrize("N,K,M", [(256, 4192, 150), (96, 8192, 40), (4100, 64, 257)])
+def test_fold_shapes(torch, orc, type_, N, K, M):
+    w = synth.weights(N, K, seed=N + K)
+    x = synth.activations(M, K, seed=M + K, outliers=True)
+    _run(orc, type_, w, x, "shape")
+
+
+@pytest.mark.parametrize("type_", FOLD_TYPES)
+def test_fold_all_positive(torch, orc, type_):
+    w = np.abs(synth.weights(160, 4096, seed=41))
+    x = np.abs(synth.activations(130, 4096, seed=42))
+    _run(orc, type_, w, x, "all positive")
+
+
+@pytest.mark.parametrize("type_", FOLD_TYPES)
+def test_fold_token_range_shift(torch, orc, type_):
+    x = synth.activations(140, 1024, seed=43, outliers=True)
+    # (block maxima stay below 127 * 65504, where the Q8_0 rule's fp16 scale itself would overflow)
+    x[3] *= np.float32(5e4)                 # 127 * d_a far beyond 2^15: shifted row
+    x[77, :512] *= np.float32(2e4)          # half a row large, half ordinary: one shift for both
+    x[90] *= np.float32(1e-6)               # tiny scales (subnormal lo terms), no shift
+    w = synth.weights(200, 1024, seed=44)
+    _run(orc, type_, w, x, "token range")
+
+
+@pytest.mark.parametrize("type_", FOLD_TYPES)
+def test_fold_weight_range_shift(torch, orc, type_):
+    w = synth.weights(200, 1024, seed=45)
+    w[5] *= np.float32(1e6)                 # |d_w| * max|w_int| beyond 2^15: shifted row
+    w[40, :256] *= np.float32(1e6)          # one row with large and ordinary blocks
+    w[130] *= np.float32(1e-3)              # tiny block scales
+    x = synth.activations(150, 1024, seed=46)
+    _run(orc, type_, w, x, "weight range")
+
+
+def test_fold_matches_exact_kernel(torch, orc):
+    # the folded-scale and exact-integer kernels compute the same sum: both within the bound and
+    # close to each other
+    from tests.gpu_util import gpu_matmul
+
+    w = synth.weights(384, 2048, seed=47)
+    x = synth.activations(200, 2048, seed=48, outliers=True)
+    _, tiled = gpu_prepare_weight("q4_0", w)
+    a_q, a_d = gpu_quantize_act(x)
+    y_exact = gpu_matmul("q4_0", tiled, 2048, 384, a_q, a_d, 200, path=2).cpu().numpy()
+    y_fold = gpu_matmul_ws("q4_0", tiled, 2048, 384, a_q, a_d, 200).cpu().numpy()
+    scale = np.abs(y_exact).max()
+    assert np.abs(y_exact - y_fold).max() <= 1e-5 * scale
