@@ -232,16 +232,31 @@ QMM_API qmm_status qmm_matmul_path(qmm_type t, const void *w_tiled_dev, int64_t 
 QMM_API size_t qmm_matmul_workspace_size(int64_t M, int64_t K);
 
 /*
- * qmm_matmul_ws -- qmm_matmul with caller-provided scratch memory for the tensor-core path.
+ * qmm_matmul_ws -- the product of qmm_matmul, with caller-provided scratch memory for the tensor-core
+ * path ("Hexagon backend developer details", "Tiled Weight Formats"; the pages' prefill path
+ * dequantizes tiles to FP16 and contracts them on the matrix unit).
  *   workspace_dev  >= qmm_matmul_workspace_size(M, K) bytes, 256-byte aligned, owned by the caller;
  *                  its contents on entry do not matter and are overwritten.  Calls that overlap on the
  *                  GPU must use different workspaces.
- * For M > qmm_decode_max_m() the activation quants are first rewritten into the workspace as fp16
- * holding the same integers (plus a transposed copy of the block scales), which the GEMM then loads
- * with TMA directly in its operand layout; each token tile is converted once instead of once per
- * weight tile.  Results equal qmm_matmul's within the stated bound.  For smaller M the workspace is
- * not touched.  Errors: those of qmm_matmul, plus INVALID_ARG (workspace missing or too small) and
- * MISALIGNED (workspace not 256-byte aligned).
+ * For M > qmm_decode_max_m() a first kernel prepares the token operand in the workspace, and the GEMM
+ * loads it with TMA straight into its operand layout (each token tile prepared once, not once per
+ * weight tile):
+ *   - Q4_0, Q8_0, IQ4_NL tiles: the folded-scale GEMM.  Every dequantized value d*q (an fp16 scale
+ *     times an integer code of at most 8 bits) is split exactly into two fp16 terms hi + lo, for
+ *     the activations in the workspace and for the weights inside the kernel.  The sum is
+ *     Y = sum_k (a_hi w_hi + a_hi w_lo + a_lo w_hi) on the tensor cores, in fp32, over 128-wide K
+ *     chunks added in fp32.  The dropped a_lo w_lo is below 2^-22 |a w|; rounding stays below about
+ *     5e-6 * sum_k |w_k * x_k|, inside the bound of qmm_matmul, with a different summation order.
+ *     A token row whose largest |d_a| * 127 (or a weight row whose largest |d_w| * max|w_int|)
+ *     reaches 2^15 is scaled by a power of two and its outputs unscaled; that is exact unless the
+ *     row's block scales span more than 2^24.
+ *   - MXFP4, Q4_1, Q4_K tiles: the exact-integer GEMM of qmm_matmul, with the quants copied to fp16
+ *     and the block scales transposed in the workspace (results identical to qmm_matmul's).
+ * For smaller M the workspace is not touched and the decode kernel runs.  Launch overlap: the
+ * preparation kernel and the GEMM are programmatic dependent launches; the preparation waits for
+ * the kernel before it on the stream before it reads a_q / a_d or writes the workspace.
+ * Errors: those of qmm_matmul, plus INVALID_ARG (workspace missing or too small) and MISALIGNED
+ * (workspace not 256-byte aligned).
  */
 QMM_API qmm_status qmm_matmul_ws(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N,
                                  const int8_t *a_q_dev, const uint16_t *a_d_dev, int64_t M, float *y_dev,
@@ -257,9 +272,11 @@ QMM_API qmm_status qmm_matmul_ws(qmm_type t, const void *w_tiled_dev, int64_t K,
  * up front, or sections that must not enter the CUDA allocator at all.  This call takes the same
  * inputs and outputs as qmm_matmul and allocates nothing: for M > qmm_decode_max_m() the
  * tensor-core path's workspace is a fixed scratch array of qmm_matmul_noalloc_max_workspace() bytes
- * (8 MiB) that the library holds on every GPU that loads it, until the process exits.
+ * (16 MiB) that the library holds on every GPU that loads it, until the process exits.  The kernels
+ * and results are those of qmm_matmul_ws.
  *   - Sizes: if qmm_matmul_workspace_size(M, K) exceeds that limit the call returns
- *     QMM_ERR_INVALID_ARG without launching anything (e.g. M*K up to about 4M elements fits).
+ *     QMM_ERR_INVALID_ARG without launching anything (the workspace is about 4.2 bytes per
+ *     activation element: M = 960 tokens at K = 4096 fit, 1024 do not).
  *   - The first call with M > qmm_decode_max_m() on a device looks up the scratch array's device
  *     address with that device current and caches it; make that first call before any stream capture.
  *   - The scratch array is shared by all calls and keeps the last call's contents; nothing in it
