@@ -446,9 +446,12 @@ gemm_fold_kernel(const FoldParams p, const __grid_constant__ CUtensorMap w_map, 
     }
 }
 
-// Token operand of the folded GEMM, one warp per token row m: the row's shift s (so that
-// 127 * max_b |d_a| * 2^-s < 2^15), tscale[m] = 2^s, and for every k the exact split of
-// d_a[m, k/32] * 2^-s * a_q[m, k] into a_hi[m, k] + a_lo[m, k] (fp16).
+// Token operand of the folded GEMM, one warp per 512-element segment of a token row m (lane c takes
+// elements 16c..16c+15 of the segment): the row's shift s (so that 127 * max_b |d_a| * 2^-s < 2^15;
+// every warp of the row finds the same s), tscale[m] = 2^s (written by the row's first segment), and
+// for each element the exact split of d_a[m, k/32] * 2^-s * a_q[m, k] into a_hi[m, k] + a_lo[m, k]
+// (fp16).  All of a lane's loads are issued before its arithmetic.
+constexpr int kPrepSeg = 512;
 __global__ void __launch_bounds__(256) prepare_fold_act_kernel(const int8_t *__restrict__ a_q, const uint16_t *__restrict__ a_d,
                                                                int64_t M, int64_t K, __half *__restrict__ a_hi,
                                                                __half *__restrict__ a_lo, float *__restrict__ tscale) {
@@ -457,55 +460,43 @@ __global__ void __launch_bounds__(256) prepare_fold_act_kernel(const int8_t *__r
     // and weight streaming; the GEMM waits for this grid before it reads the prepared tokens.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int64_t nkt = K / 32;
+    const int64_t nkt = K / 32, nseg = (K + kPrepSeg - 1) / kPrepSeg;
     const int lane = threadIdx.x & 31;
-    const int64_t step = (int64_t)gridDim.x * 8;
-    for (int64_t m = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); m < M; m += step) {
+    const int64_t warps = (int64_t)gridDim.x * 8;
+    for (int64_t wi = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); wi < M * nseg; wi += warps) {
+        const int64_t m = wi / nseg, seg = wi - m * nseg;
         const uint16_t *dr = a_d + m * nkt;
+        const int64_t c = seg * (kPrepSeg / 16) + lane;        // 16-element chunk of the row
+        const bool has = c < K / 16;
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        uint16_t dq = 0;
+        if (has) {
+            q = __ldg(reinterpret_cast<const uint4 *>(a_q + m * K + 16 * c));
+            dq = dr[c >> 1];
+        }
         float dmax = 0.0f;
 #pragma unroll 4
         for (int64_t kt = lane; kt < nkt; kt += 32) dmax = fmaxf(dmax, fabsf(__half2float(__ushort_as_half(dr[kt]))));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
         const int s = range_shift(dmax * 127.0f);
-        const float down = exp2i(-s);
-        if (lane == 0) tscale[m] = exp2i(s);
-        const int8_t *qr = a_q + m * K;
-        __half *hr = a_hi + m * K, *lr = a_lo + m * K;
-        const int64_t nc = K / 16;                     // 16-element chunks of the row
-        // four chunks per lane at a time, all loads issued before any arithmetic
-        for (int64_t c0 = lane; c0 < nc; c0 += 4 * 32) {
-            uint4 q[4];
-            uint16_t dq[4];
+        if (seg == 0 && lane == 0) tscale[m] = exp2i(s);
+        if (!has) continue;
+        __half d = __ushort_as_half(dq);
+        if (s != 0) d = __float2half_rn(__half2float(d) * exp2i(-s));
+        const __half2 d2 = __half2half2(d);
+        uint32_t v[8], h[8], l[8];
+        i8x4_to_h2x2(q.x, v[0], v[1]);
+        i8x4_to_h2x2(q.y, v[2], v[3]);
+        i8x4_to_h2x2(q.z, v[4], v[5]);
+        i8x4_to_h2x2(q.w, v[6], v[7]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t c = c0 + 32 * u;
-                if (c < nc) {
-                    q[u] = __ldg(reinterpret_cast<const uint4 *>(qr + 16 * c));
-                    dq[u] = dr[c >> 1];
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int64_t c = c0 + 32 * u;
-                if (c >= nc) break;
-                __half d = __ushort_as_half(dq[u]);
-                if (s != 0) d = __float2half_rn(__half2float(d) * down);
-                const __half2 d2 = __half2half2(d);
-                uint32_t v[8], h[8], l[8];
-                i8x4_to_h2x2(q[u].x, v[0], v[1]);
-                i8x4_to_h2x2(q[u].y, v[2], v[3]);
-                i8x4_to_h2x2(q[u].z, v[4], v[5]);
-                i8x4_to_h2x2(q[u].w, v[6], v[7]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) split2(v[e], d2, h[e], l[e]);
-                uint4 *ho = reinterpret_cast<uint4 *>(hr + 16 * c), *lo = reinterpret_cast<uint4 *>(lr + 16 * c);
-                ho[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                ho[1] = make_uint4(h[4], h[5], h[6], h[7]);
-                lo[0] = make_uint4(l[0], l[1], l[2], l[3]);
-                lo[1] = make_uint4(l[4], l[5], l[6], l[7]);
-            }
-        }
+        for (int e = 0; e < 8; ++e) split2(v[e], d2, h[e], l[e]);
+        uint4 *ho = reinterpret_cast<uint4 *>(a_hi + m * K + 16 * c), *lo = reinterpret_cast<uint4 *>(a_lo + m * K + 16 * c);
+        ho[0] = make_uint4(h[0], h[1], h[2], h[3]);
+        ho[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        lo[0] = make_uint4(l[0], l[1], l[2], l[3]);
+        lo[1] = make_uint4(l[4], l[5], l[6], l[7]);
     }
 }
 
@@ -549,7 +540,8 @@ cudaError_t launch_gemm_fold(qmm_type t, const uint8_t *tiled, int64_t K, int64_
     __half *a_lo = reinterpret_cast<__half *>(base + L.lo);
     float *tscale = reinterpret_cast<float *>(base + L.ts);
     {
-        int64_t grid = (M + 7) / 8;
+        const int64_t warps = M * ((K + kPrepSeg - 1) / kPrepSeg);
+        int64_t grid = (warps + 7) / 8;
         if (grid > 152 * 8) grid = 152 * 8;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid, 1, 1);

@@ -98,3 +98,43 @@ def test_fold_matches_exact_kernel(torch, orc):
     y_fold = gpu_matmul_ws("q4_0", tiled, 2048, 384, a_q, a_d, 200).cpu().numpy()
     scale = np.abs(y_exact).max()
     assert np.abs(y_exact - y_fold).max() <= 1e-5 * scale
+
+
+@pytest.mark.parametrize("scale", [1.0, 5e4])
+def test_fold_token_split_is_exact(torch, scale):
+    # White-box check of the token preparation: after qmm_matmul_ws the workspace holds, per
+    # activation element, two fp16 numbers hi, lo with hi = fp16(v) (nearest) and hi + lo == v
+    # exactly, v = d_a * q_a * 2^-s, where 2^s (stored per token row) is 1 unless the row's range
+    # needs the shift.  Region offsets follow GemmWsLayout in qmm_internal.cuh.
+    import block_quantized_matmul_gb300 as qmm
+
+    M, K, N = 200, 1024, 128
+    x = synth.activations(M, K, seed=51, outliers=True)
+    x[7] *= np.float32(scale)
+    w = synth.weights(N, K, seed=52)
+    _, tiled = gpu_prepare_weight("q4_0", w)
+    a_q, a_d = gpu_quantize_act(x)
+    nbytes = qmm.matmul_workspace_size(M, K)
+    ws = torch.full((nbytes + 256,), 0x5A, dtype=torch.uint8, device="cuda")
+    off = (-ws.data_ptr()) % 256
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    qmm.qmm_matmul_ws("q4_0", tiled, K, N, a_q, a_d, M, y, N, ws.data_ptr() + off, nbytes)
+    torch.cuda.synchronize()
+    buf = ws[off:off + nbytes].cpu().numpy()
+
+    def r256(v):
+        return (v + 255) // 256 * 256
+
+    nkt, m_pad, mk2 = K // 32, (M + 7) // 8 * 8, M * K * 2
+    lo_off = r256(mk2)
+    ts_off = lo_off + r256(mk2) + r256(nkt * m_pad * 2) + r256(nkt * m_pad * 4)
+    hi = buf[:mk2].view(np.float16).reshape(M, K)
+    lo = buf[lo_off:lo_off + mk2].view(np.float16).reshape(M, K)
+    ts = buf[ts_off:ts_off + 4 * M].view(np.float32).astype(np.float64)
+    q = a_q.cpu().numpy().astype(np.float64)
+    d = np.repeat(a_d.cpu().numpy().view(np.float16).astype(np.float64), 32, axis=1)
+    v = d * q / ts[:, None]                                   # exact in float64
+    assert np.array_equal(hi, v.astype(np.float16))           # nearest fp16
+    assert np.array_equal(hi.astype(np.float64) + lo.astype(np.float64), v)
+    shifted = np.nonzero(ts != 1.0)[0].tolist()
+    assert shifted == ([7] if scale > 1 else [])
