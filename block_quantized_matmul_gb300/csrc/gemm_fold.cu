@@ -97,6 +97,25 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, ok);
 }
 
+// Runs this file's bounded wait out on purpose (the failure-detection test): warp 0 waits, with
+// limit_ns, for a barrier phase that nothing completes; warp 1 waits for the same phase with the
+// normal limit and must give up once warp 0 has raised the abort flag.  out[w] = 1 if warp w's wait
+// returned true (neither should); the status word is set as by any timed-out wait of this kernel.
+__global__ void __launch_bounds__(64) selftest_wait_fold_kernel(unsigned long long limit_ns, int *out) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    volatile int *abort = &abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        *abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5;
+    const bool ok = wait_bounded_on(smem_u32(&bar), 0u, abort, &g_fold_status, warp == 0 ? limit_ns : kWaitLimitNs);
+    if ((threadIdx.x & 31) == 0) out[warp] = ok ? 1 : 0;
+}
+
 // 2^k as an exact fp32 (k within the normal exponent range).
 __device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }
 
@@ -577,6 +596,11 @@ cudaError_t launch_gemm_fold(qmm_type t, const uint8_t *tiled, int64_t K, int64_
         case QMM_Q8_0: return launch_fold_typed<QMM_Q8_0>(p, ah, al, s);
         default: return launch_fold_typed<QMM_IQ4_NL>(p, ah, al, s);
     }
+}
+
+cudaError_t launch_selftest_wait_fold(unsigned long long limit_ns, int *out, cudaStream_t s) {
+    selftest_wait_fold_kernel<<<1, 64, 0, s>>>(limit_ns, out);
+    return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_fold_status(unsigned *out, cudaStream_t s) {

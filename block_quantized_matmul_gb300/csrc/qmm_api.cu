@@ -193,11 +193,12 @@ qmm_status qmm_matmul_noalloc(qmm_type t, const void *w_tiled, int64_t K, int64_
 size_t qmm_matmul_noalloc_max_workspace(void) { return kNoAllocScratchBytes; }
 
 qmm_status qmm_selftest_timeout(int unit, uint64_t limit_ns, int *flags_dev, qmm_stream_t stream) {
-    if ((unit != 0 && unit != 1) || limit_ns < 1000000ull || limit_ns > 2000000000ull || !flags_dev)
+    if (unit < 0 || unit > 2 || limit_ns < 1000000ull || limit_ns > 2000000000ull || !flags_dev)
         return QMM_ERR_INVALID_ARG;
     if (!aligned(flags_dev, 4)) return QMM_ERR_MISALIGNED;
-    return from_cuda(unit == 0 ? launch_selftest_wait_mv(limit_ns, flags_dev, cs(stream))
-                               : launch_selftest_wait_gemm(limit_ns, flags_dev, cs(stream)));
+    return from_cuda(unit == 0   ? launch_selftest_wait_mv(limit_ns, flags_dev, cs(stream))
+                     : unit == 1 ? launch_selftest_wait_gemm(limit_ns, flags_dev, cs(stream))
+                                 : launch_selftest_wait_fold(limit_ns, flags_dev, cs(stream)));
 }
 
 qmm_status qmm_device_status(qmm_stream_t stream) {

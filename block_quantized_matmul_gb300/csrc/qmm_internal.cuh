@@ -178,6 +178,7 @@ cudaError_t read_and_clear_matvec_status(unsigned *out, cudaStream_t s);   // de
 // One CTA whose bounded waits run out on purpose (decode kernels' and GEMM's wait helpers).
 cudaError_t launch_selftest_wait_mv(unsigned long long limit_ns, int *out, cudaStream_t s);
 cudaError_t launch_selftest_wait_gemm(unsigned long long limit_ns, int *out, cudaStream_t s);
+cudaError_t launch_selftest_wait_fold(unsigned long long limit_ns, int *out, cudaStream_t s);
 
 // Raises a kernel's dynamic shared-memory limit once per device (the attribute is per device and
 // per function, and setting it on every call costs host time on the launch path).

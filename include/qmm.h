@@ -302,12 +302,13 @@ QMM_API qmm_status qmm_device_status(qmm_stream_t stream);
 /*
  * qmm_selftest_timeout -- test hook for the failure detection above; not part of the hot path.
  * Launches one CTA that uses the pipelined kernels' own bounded-wait helper (unit 0: the decode
- * kernels', unit 1: the GEMM's) on a barrier phase that nothing completes: one warp waits with a
+ * kernels', unit 1: the exact-integer GEMM's, unit 2: the folded-scale GEMM's, each with its own
+ * device status word) on a barrier phase that nothing completes: one warp waits with a
  * limit of limit_ns, a second with the normal 2 s limit and must give up as soon as the first has
  * raised the CTA's abort flag.  flags_dev[0..1] (int32, device) receive 1 for a wait that returned
  * success (neither should), 0 otherwise.  Afterwards qmm_device_status() reports QMM_ERR_TIMEOUT,
  * and the context stays usable: nothing faults, traps or hangs.
- * Errors: INVALID_ARG (unit not 0 or 1, limit_ns outside [1 ms, 2 s], NULL), MISALIGNED, CUDA.
+ * Errors: INVALID_ARG (unit not 0, 1 or 2, limit_ns outside [1 ms, 2 s], NULL), MISALIGNED, CUDA.
  */
 QMM_API qmm_status qmm_selftest_timeout(int unit, uint64_t limit_ns, int *flags_dev, qmm_stream_t stream);
 

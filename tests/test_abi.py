@@ -192,7 +192,7 @@ def test_q4_k_sizes_and_argument_errors(L):
 
 def test_selftest_timeout_argument_errors(L):
     f = L.qmm_selftest_timeout
-    assert f(2, 100_000_000, P, None) == INVALID              # unit
+    assert f(3, 100_000_000, P, None) == INVALID              # unit
     assert f(-1, 100_000_000, P, None) == INVALID
     assert f(0, 999_999, P, None) == INVALID                  # below 1 ms
     assert f(1, 2_000_000_001, P, None) == INVALID            # above 2 s

@@ -11,7 +11,8 @@ import numpy as np
 import pytest
 
 from block_quantized_matmul_gb300 import synth
-from tests.gpu_util import assert_within_bound, gpu_matmul, gpu_prepare_weight, gpu_quantize_act, torch_mod
+from tests.gpu_util import (assert_within_bound, gpu_matmul, gpu_matmul_ws, gpu_prepare_weight, gpu_quantize_act,
+                            torch_mod)
 
 pytestmark = pytest.mark.gpu
 TIMEOUT = 5
@@ -28,7 +29,7 @@ def torch():
     return t
 
 
-@pytest.mark.parametrize("unit", [0, 1], ids=["decode_wait", "gemm_wait"])
+@pytest.mark.parametrize("unit", [0, 1, 2], ids=["decode_wait", "gemm_wait", "fold_gemm_wait"])
 def test_wait_runs_out_and_is_reported(torch, orc, unit):
     import block_quantized_matmul_gb300 as qmm
 
@@ -51,6 +52,9 @@ def test_wait_runs_out_and_is_reported(torch, orc, unit):
     y_ref, bound = orc.matmul("q4_0", orc.repack("q4_0", orc.quantize_rows("q4_0", w), K, N), K, N, q_ref, d_ref)
     _, tiled = gpu_prepare_weight("q4_0", w)
     a_q, a_d = gpu_quantize_act(x)
-    y = gpu_matmul("q4_0", tiled, K, N, a_q, a_d, M, path=0).cpu().numpy()
+    if unit == 2:      # the folded-scale GEMM runs on the workspace path
+        y = gpu_matmul_ws("q4_0", tiled, K, N, a_q, a_d, M).cpu().numpy()
+    else:
+        y = gpu_matmul("q4_0", tiled, K, N, a_q, a_d, M, path=0).cpu().numpy()
     assert_within_bound(y, y_ref, bound, "after the timeout")
     assert qmm.qmm_device_status() == 0
