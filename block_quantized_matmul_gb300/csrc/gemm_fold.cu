@@ -12,13 +12,15 @@
 //     lo = fma(d, q, -hi) (the fma is exact because v - hi is representable);
 //   * Y = sum a_hi w_hi + a_hi w_lo + a_lo w_hi: three fp16 MMAs per K step; the dropped a_lo w_lo is
 //     below 2^-22 |a w|;
-//   * the fp32 accumulator in tensor memory takes kChunk = 4 blocks (128 K) at a time, and the CUDA
-//     cores add the chunk sums in fp32.  With at most one fp32 rounding per MMA step (24 steps per
-//     chunk) and one per chunk sum, the error stays below 5e-6 of sum_k |a w|.
+//   * the fp32 accumulator in tensor memory takes a chunk of kChunkPairs = 2 block pairs (128 K) at a
+//     time, and the CUDA cores add the chunk sums in fp32.  With at most one fp32 rounding per MMA
+//     step (24 steps per chunk) and one per chunk sum, the error stays below 5e-6 of sum_k |a w|.
 // Compared with the exact-integer kernel (gemm_tc.cu), the tensor cores do three times the MACs but
 // the per-block fp32 rescale of every output (two CUDA-core operations per output and block, which
 // made that kernel issue-bound) is gone: what is left for the CUDA cores is the weight split (once
-// per weight element and token tile) and one fp32 add per output and chunk.
+// per weight element and token tile) and one fp32 add per output and chunk.  The token operand is
+// split once per call by prepare_fold_act_kernel into the caller's workspace (a_hi, a_lo, and the
+// per-row power of two); the GEMM is its programmatic dependent and overlaps it with its set-up.
 //
 // Ranges.  hi must stay finite.  A weight row whose largest |d_w| * max|w_int| reaches 2^15 (and a
 // token row whose largest |d_a| * 127 does) is scaled by a power of two 2^-t before the split, and its
