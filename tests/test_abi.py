@@ -146,6 +146,18 @@ def test_matmul_ws_argument_errors(L):
     assert L.qmm_matmul_ws(0, P, 48, 64, P, P, 64, P, 64, P, need, None) == INVALID
 
 
+def test_workspace_sizes_as_documented(L):
+    # the folded-scale GEMM's token operand is two fp16 terms per element (4 B), plus the block-scale
+    # and per-row regions of the exact-integer GEMM: about 4.2 B per activation element
+    for M, K in [(17, 32), (300, 1024), (512, 4096)]:
+        need = L.qmm_matmul_workspace_size(M, K)
+        assert 4 * M * K <= need <= 4.3 * M * K + 4096, (M, K, need)
+    # the no-allocation scratch: 16 MiB, which holds M = 960 tokens at K = 4096 but not 1024
+    limit = L.qmm_matmul_noalloc_max_workspace()
+    assert limit == 16 << 20
+    assert L.qmm_matmul_workspace_size(960, 4096) <= limit < L.qmm_matmul_workspace_size(1024, 4096)
+
+
 def test_matmul_f32_argument_errors(L):
     f = L.qmm_matmul_f32
     assert f(0, P, 48, 64, P, 64, 1, P, 64, None) == INVALID     # K % 32
