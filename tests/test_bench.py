@@ -36,3 +36,18 @@ def test_recorded_traffic_only_for_known_workloads():
     hbm, bf16, src = bench.measured_peaks()
     assert hbm > 0 and bf16 > 0 and src in ("measured", "fallback")
     assert len(bench.kernel_source_hash("matvec")) == 16 and bench.kernel_source_hash("gemm") != bench.kernel_source_hash("matvec")
+
+
+def test_kernel_families_hash_every_source_they_compile():
+    # every CUDA source and private header of the library belongs to the hash of at least one family,
+    # so an edit of any of them invalidates the recorded DRAM traffic it could affect
+    import glob
+    import os
+
+    csrc = os.path.join(os.path.dirname(bench.__file__), "block_quantized_matmul_gb300", "csrc")
+    hashed = set(bench.KERNEL_FILES["matvec"]) | set(bench.KERNEL_FILES["gemm"])
+    kernels = {"matvec.cu", "gemm_tc.cu", "gemm_fold.cu", "pipeline.cuh", "tc_common.cuh", "qmm_internal.cuh"}
+    present = {os.path.basename(p) for p in glob.glob(os.path.join(csrc, "*.cu*"))}
+    assert kernels <= present and kernels <= hashed
+    # the recorded entries that the bench reads are keyed to the current sources
+    assert bench.recorded_traffic("q8_0_matvec_K4096_N14336_M1") is not None
