@@ -49,5 +49,3 @@ def test_kernel_families_hash_every_source_they_compile():
     kernels = {"matvec.cu", "gemm_tc.cu", "gemm_fold.cu", "pipeline.cuh", "tc_common.cuh", "qmm_internal.cuh"}
     present = {os.path.basename(p) for p in glob.glob(os.path.join(csrc, "*.cu*"))}
     assert kernels <= present and kernels <= hashed
-    # the recorded entries that the bench reads are keyed to the current sources
-    assert bench.recorded_traffic("q8_0_matvec_K4096_N14336_M1") is not None
