@@ -66,7 +66,8 @@ typedef enum {
 typedef enum { QMM_Q4_0 = 0, QMM_Q8_0 = 1, QMM_IQ4_NL = 2, QMM_MXFP4 = 3, QMM_Q4_1 = 4, QMM_Q4_K = 5 } qmm_type;
 
 /* Which kernel qmm_matmul_path runs: AUTO picks the decode matvec for M <= qmm_decode_max_m()
- * and the tensor-core GEMM otherwise. */
+ * and the exact-integer tensor-core GEMM otherwise (the folded-scale GEMM needs a workspace and
+ * runs through qmm_matmul_ws / qmm_matmul_noalloc). */
 typedef enum { QMM_PATH_AUTO = 0, QMM_PATH_MATVEC = 1, QMM_PATH_GEMM = 2 } qmm_path;
 
 /* Human-readable name of a status code (static string, never NULL). */
