@@ -57,9 +57,11 @@ struct TileFmt {
     static constexpr bool kNibbleInt = TYPE == QMM_Q4_0 || kAffine;               // integer nibble codes
 };
 
-// The built-in IQ4_NL table (16 int8 levels, ascending): 16-level Lloyd-Max quantizer of a unit
-// normal, scaled so the outer levels are -127 and +127, rounded to integers.
-constexpr int8_t kIq4nlTable[16] = {-127, -96, -75, -58, -44, -31, -18, -6, 6, 18, 31, 44, 58, 75, 96, 127};
+// The built-in IQ4_NL table (16 int8 levels, ascending): the levels of GGML's published IQ4_NL
+// format, so that IQ4_NL weights quantized elsewhere (GGUF files) decode to their own values.  The
+// pages name the table (iq4_nl_to_fp16_lut) without printing it.  Every level is an integer in
+// [-127, 113], so every block sum stays an exact integer.
+constexpr int8_t kIq4nlTable[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
 
 // Table passed by value to kernels (host-side precomputed parameters, no device-global state).
 struct Lut16 {
@@ -198,5 +200,11 @@ inline cudaError_t ensure_smem_limit(Kern kern, size_t bytes, int (&done_mask)[4
 
 // Largest M handled by one decode-matvec launch (two 8-token mma fragments).
 constexpr int kDecodeMaxM = 16;
+
+// Blocks of 32 that the exact-integer GEMM sums per output in a register before adding the partial
+// into y, and the largest K any product call accepts: the fp32 accumulation error of every kernel
+// stays below 1e-5 * sum_k |w_k x_k| up to this K (131072 = 4096 blocks).
+constexpr int kGemmChunkBlocks = 128;
+constexpr int64_t kMaxMatmulK = (int64_t)1 << 17;
 
 }  // namespace qmm

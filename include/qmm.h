@@ -92,8 +92,9 @@ QMM_API size_t qmm_tiled_size(qmm_type t, int64_t K, int64_t N);
 QMM_API size_t qmm_flat_size(qmm_type t, int64_t K, int64_t N);
 
 /* The 16-entry IQ4_NL table the kernels use (int8 values, ascending).  The pages name the table
- * (iq4_nl_to_fp16_lut) without printing it; the built-in one is the 16-level Lloyd-Max quantizer of
- * a unit normal scaled to +-127.  Writes 16 bytes to `out`. */
+ * (iq4_nl_to_fp16_lut) without printing it; the built-in one holds the 16 levels of GGML's
+ * published IQ4_NL format {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113},
+ * so IQ4_NL weights from GGUF files decode to their own values.  Writes 16 bytes to `out`. */
 QMM_API void qmm_iq4nl_table(int8_t out[16]);
 
 /* Largest activation row count M that QMM_PATH_AUTO sends to the decode matvec. */

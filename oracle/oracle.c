@@ -18,7 +18,7 @@
  *     keeps the Q4_0 nibble layout and stores the FP16 pair (d, m) of a row at 512+4*row and
  *     514+4*row.
  *
- * Readings where the pages are silent (each listed in the design notes):
+ * Readings where the pages are silent:
  *   - Flat (untiled) rows are GGML blocks: Q4_0 / IQ4_NL = {fp16 d; u8 qs[16]} (18 B), element j in
  *     the low nibble of qs[j] and element j+16 in its high nibble; Q8_0 = {fp16 d; i8 qs[32]} (34 B).
  *   - Rows past N in the last column tile are zero bytes (d = 0, quants 0).
@@ -29,7 +29,8 @@
  *     Q8_0 uses the activation rule;
  *     IQ4_NL takes d = m/lut[0], d16 = fp16(d), and for each x the index i minimising
  *     |x - f32(d16)*lut[i]| (lowest index on ties).
- *   - The IQ4_NL table itself is not printed on the pages; callers pass the table in.
+ *   - The IQ4_NL table itself is not printed on the pages; the built-in one holds the 16 levels of
+ *     GGML's published IQ4_NL format, and callers may pass another table in.
  *   - Q4_1: "m (min)" read as the GGML affine rule, weight = d*q + m; flat block {fp16 d; fp16 m;
  *     u8 qs[16]} (20 B, nibble order as Q4_0).  So a block adds d_a * m_w * sum_j a_q[j] to the
  *     product.  Quantizer (test data): min and max of the block, d = (max - min)/15, id = d ? 1/d : 0,
@@ -86,10 +87,11 @@ uint16_t orc_e8m0_to_f16_bits(int e)
     return (uint16_t)(f << 10);
 }
 
-/* The oracle's own copy of the 16-entry IQ4_NL table.  The pages name the table but print no values;
- * this stand-in is the 16-level Lloyd-Max quantizer of a unit normal, scaled so that its outermost
- * levels are -127 and +127 and rounded to integers (ascending order, lut[0] most negative). */
-const int8_t orc_iq4nl_table[16] = {-127, -96, -75, -58, -44, -31, -18, -6, 6, 18, 31, 44, 58, 75, 96, 127};
+/* The oracle's own copy of the 16-entry IQ4_NL table.  The pages name the table
+ * (iq4_nl_to_fp16_lut) but print no values.  These are the 16 levels of GGML's published IQ4_NL
+ * format (its non-linear value table), so that IQ4_NL weights from GGUF files decode to their own
+ * values; ascending, lut[0] = -127 the most negative, and not symmetric (the top level is 113). */
+const int8_t orc_iq4nl_table[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
 
 /* ------------------------------------------------------------------------------------------------
  * IEEE 754 binary16 <-> binary32, written from the format definition (1 sign bit, 5 exponent bits

@@ -253,10 +253,13 @@ def test_weight_quantizer_error_bound(orc, type_):
         err = np.abs(dq - blocks)
         assert np.all(err <= np.maximum(scale, amax - 6 * scale) + 1e-12)
     else:
+        # d = m / lut[0] puts the block's extreme m exactly on lut[0] (d > 0 for a negative m, d < 0 for
+        # a positive one).  Inside the levels the error is at most half the widest gap; past the other
+        # end of the (asymmetric) table, x can reach |m| while the last level is |d| * |lut[15]|.
         lut = orc.iq4nl_table().astype(np.float64)
-        gaps = np.diff(lut).max()
         step = amax / 127
-        assert np.all(np.abs(dq - blocks) <= step * (gaps / 2 + 127 * 2.0 ** -11) + 1e-12)
+        reach = max(np.diff(lut).max() / 2, 127 - abs(lut[-1]))
+        assert np.all(np.abs(dq - blocks) <= step * (reach + 127 * 2.0 ** -11) + 1e-12)
 
 
 def test_iq4_nl_picks_nearest_entry(orc):
@@ -277,20 +280,15 @@ def test_iq4_nl_picks_nearest_entry(orc):
                 assert c == int(np.argmax(errs == errs.min()))     # lowest index among ties
 
 
-def test_iq4_nl_table_is_the_lloyd_max_stand_in(orc):
-    # The pages print no table values; the stand-in is the 16-level Lloyd-Max quantizer of N(0,1),
-    # scaled to +-127 and rounded.  Recompute it from the centroid conditions.
-    scipy_stats = pytest.importorskip("scipy.stats")
-    norm = scipy_stats.norm
-    levels = np.linspace(-2.5, 2.5, 16)
-    for _ in range(5000):
-        edges = np.concatenate([[-np.inf], (levels[1:] + levels[:-1]) / 2, [np.inf]])
-        new = (norm.pdf(edges[:-1]) - norm.pdf(edges[1:])) / (norm.cdf(edges[1:]) - norm.cdf(edges[:-1]))
-        if np.max(np.abs(new - levels)) < 1e-14:
-            break
-        levels = new
-    table = np.round(levels * 127 / levels[-1]).astype(np.int8)
-    assert np.array_equal(orc.iq4nl_table(), table)
+def test_iq4_nl_table_is_ggmls_published_table(orc):
+    # The pages name the table (iq4_nl_to_fp16_lut) but print no values.  The oracle holds the 16
+    # levels of GGML's published IQ4_NL format, written out here from that format's definition.
+    ggml_iq4_nl = [-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113]
+    table = orc.iq4nl_table()
+    assert table.dtype == np.int8 and table.shape == (16,)
+    assert table.tolist() == ggml_iq4_nl
+    # what the kernels rely on: ascending, lut[0] the most negative level, every |level| <= 127
+    assert np.all(np.diff(table.astype(int)) > 0) and table[0] == -127 and np.abs(table.astype(int)).max() == 127
 
 
 # ---------------------------------------------------------------------------------------------
