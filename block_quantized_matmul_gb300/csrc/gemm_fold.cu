@@ -59,7 +59,8 @@ namespace qmm {
 
 namespace {
 
-__device__ unsigned g_fold_status = 0;     // non-zero once a bounded wait gave up
+__device__ unsigned g_fold_status = 0;     // bit 0: a bounded wait gave up; bit 1: an operand row not exact
+constexpr unsigned kFoldStatusRange = 2u;
 
 constexpr int FM = 128;                    // weight rows per CTA (UMMA M)
 constexpr int FN = 128;                    // tokens per CTA (UMMA N)
@@ -85,7 +86,9 @@ struct FoldParams {
     const float *tscale;                   // per token: 2^s, the power of two its row was scaled by
     float *y;
     int64_t N, M, ldy, n_col_tiles;
-    int nkt;
+    int nkt;            // K blocks of the whole row (stride of the weight tiles)
+    int kt0, nkc;       // K blocks of this pass: [kt0, kt0 + nkc)
+    int accumulate;     // 0: y = result, 1: y += result (passes after the first)
     Lut16 lut;
 };
 
@@ -148,10 +151,10 @@ __device__ __forceinline__ int weight_row_shift(const FoldParams &p, unsigned *r
     constexpr float kWMax = TYPE == QMM_Q4_0 ? 8.0f : 128.0f;   // largest |w_int| (IQ4_NL's table: 127)
     const int row = 32 * qd + lane;
     const int64_t ct = ct0 + qd;
-    const int nkt = p.nkt;
+    const int nkt = p.nkc;
     bool signalled = false;
     if (ct < p.n_col_tiles) {
-        const uint8_t *sp = p.tiled + (size_t)ct * (size_t)nkt * TS + TileFmt<TYPE>::kScaleOff + 2 * lane;
+        const uint8_t *sp = p.tiled + ((size_t)ct * (size_t)p.nkt + (size_t)p.kt0) * TS + TileFmt<TYPE>::kScaleOff + 2 * lane;
         float dmax = 0.0f;
         for (int k0 = part; k0 < nkt; k0 += 2 * 64) {
             unsigned short v[64];
@@ -229,7 +232,8 @@ gemm_fold_kernel(const FoldParams p, const __grid_constant__ CUtensorMap w_map, 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t ct0 = (int64_t)blockIdx.x * 4;
     const int64_t m0 = (int64_t)blockIdx.y * FN;
-    const int nkt = p.nkt;
+    const int nkt = p.nkc;                    // blocks of this pass
+    const int kt0 = p.kt0;
     const int npairs = (nkt + 1) >> 1;
     const int nchunks = (npairs + kChunkPairs - 1) / kChunkPairs;
 
@@ -275,7 +279,7 @@ gemm_fold_kernel(const FoldParams p, const __grid_constant__ CUtensorMap w_map, 
                 if (!wait_bounded(smem_u32(&w_empty[s]), (uint32_t)(((pr / WS) & 1) ^ 1), abort)) break;
                 const uint32_t fb = smem_u32(&w_full[s]);
                 mbar_arrive_expect_tx(fb, (uint32_t)P::kWTiles);
-                tma_load_3d(smem_u32(w_s + s * P::kWStageBytes), &w_map, 0, 2 * pr, (int)ct0, fb);
+                tma_load_3d(smem_u32(w_s + s * P::kWStageBytes), &w_map, 0, kt0 + 2 * pr, (int)ct0, fb);
                 issued = pr + 1;
             }
             for (int i = (issued > WS ? issued - WS : 0); i < issued; ++i)
@@ -297,8 +301,8 @@ gemm_fold_kernel(const FoldParams p, const __grid_constant__ CUtensorMap w_map, 
                 const uint32_t fb = smem_u32(&b_full[s]);
                 const uint32_t dst = smem_u32(b_s + s * kBStageBytes);
                 mbar_arrive_expect_tx(fb, (uint32_t)kBStageBytes);
-                tma_load_2d(dst, &ah_map, 64 * pr, (int)m0, fb);
-                tma_load_2d(dst + kTokBytes, &al_map, 64 * pr, (int)m0, fb);
+                tma_load_2d(dst, &ah_map, 32 * kt0 + 64 * pr, (int)m0, fb);
+                tma_load_2d(dst + kTokBytes, &al_map, 32 * kt0 + 64 * pr, (int)m0, fb);
                 issued = pr + 1;
             }
             for (int i = (issued > kPairSlots ? issued - kPairSlots : 0); i < issued; ++i)
@@ -395,7 +399,12 @@ gemm_fold_kernel(const FoldParams p, const __grid_constant__ CUtensorMap w_map, 
             if (kt < nkt) {
                 const uint8_t *tile = w_s + (pr % WS) * P::kWStageBytes + (qd * 2 + h) * TS;
                 __half d = __ushort_as_half(*reinterpret_cast<const uint16_t *>(tile + SOFF + 2 * lane));
-                if (t != 0) d = __float2half_rn(__half2float(d) * down);
+                if (t != 0) {
+                    const float d0 = __half2float(d);
+                    d = __float2half_rn(d0 * down);
+                    // a scale that does not survive the shift exactly: this call's result is not exact
+                    if (__half2float(d) * exp2i(t) != d0) atomicOr(&g_fold_status, kFoldStatusRange);
+                }
                 const __half2 d2 = __half2half2(d);
 #pragma unroll
                 for (int cp = 0; cp < 16; ++cp) {
@@ -447,12 +456,20 @@ gemm_fold_kernel(const FoldParams p, const __grid_constant__ CUtensorMap w_map, 
             const int64_t n = ct0 * 32 + row;
             const float rs = exp2i(t);
             if (n < p.N) {
+                if (!p.accumulate) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const int64_t m = m0 + 64 * h + i;
-                    if (m < p.M) {
+                    for (int i = 0; i < 64; ++i) {
+                        const int64_t m = m0 + 64 * h + i;
                         const float v = (i & 1) ? y2[i >> 1].y : y2[i >> 1].x;
-                        p.y[m * p.ldy + n] = v * rs * __ldg(p.tscale + m);
+                        if (m < p.M) p.y[m * p.ldy + n] = v * rs * __ldg(p.tscale + m);
+                    }
+                } else {
+                    // a later K pass adds its partial sums into y
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const int64_t m = m0 + 64 * h + i;
+                        const float v = (i & 1) ? y2[i >> 1].y : y2[i >> 1].x;
+                        if (m < p.M) p.y[m * p.ldy + n] = __fadd_rn(p.y[m * p.ldy + n], v * rs * __ldg(p.tscale + m));
                     }
                 }
             }
@@ -473,6 +490,17 @@ gemm_fold_kernel(const FoldParams p, const __grid_constant__ CUtensorMap w_map, 
 // for each element the exact split of d_a[m, k/32] * 2^-s * a_q[m, k] into a_hi[m, k] + a_lo[m, k]
 // (fp16).  All of a lane's loads are issued before its arithmetic.
 constexpr int kPrepSeg = 512;
+
+// Every block scale of a row shifted by 2^-s must survive the shift exactly; if one does not, the call
+// is reported (QMM_ERR_RANGE).  Called by one warp per shifted row (rare, so kept out of line).
+inline __device__ __noinline__ void check_shifted_row(const uint16_t *dr, int64_t nkt, int s, int lane) {
+    bool exact = true;
+    for (int64_t kt = lane; kt < nkt; kt += 32) {
+        const float d0 = __half2float(__ushort_as_half(dr[kt]));
+        exact = exact && __half2float(__float2half_rn(d0 * exp2i(-s))) * exp2i(s) == d0;
+    }
+    if (!__all_sync(0xffffffffu, exact) && lane == 0) atomicOr(&g_fold_status, kFoldStatusRange);
+}
 __global__ void __launch_bounds__(256) prepare_fold_act_kernel(const int8_t *__restrict__ a_q, const uint16_t *__restrict__ a_d,
                                                                int64_t M, int64_t K, __half *__restrict__ a_hi,
                                                                __half *__restrict__ a_lo, float *__restrict__ tscale) {
@@ -502,6 +530,7 @@ __global__ void __launch_bounds__(256) prepare_fold_act_kernel(const int8_t *__r
         for (int o = 16; o > 0; o >>= 1) dmax = fmaxf(dmax, __shfl_xor_sync(0xffffffffu, dmax, o));
         const int s = range_shift(dmax * 127.0f);
         if (seg == 0 && lane == 0) tscale[m] = exp2i(s);
+        if (s != 0 && seg == 0) check_shifted_row(dr, nkt, s, lane);
         if (!has) continue;
         __half d = __ushort_as_half(dq);
         if (s != 0) d = __float2half_rn(__half2float(d) * exp2i(-s));
@@ -544,7 +573,16 @@ cudaError_t launch_fold_typed(const FoldParams &p, const CUtensorMap &ah, const 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p, w_map, ah, al);
+    // K in passes of at most kGemmChunkBlocks blocks, each adding into y in order (the error bound)
+    for (int kt0 = 0; kt0 < p.nkt; kt0 += kGemmChunkBlocks) {
+        FoldParams q = p;
+        q.kt0 = kt0;
+        q.nkc = p.nkt - kt0 < kGemmChunkBlocks ? p.nkt - kt0 : kGemmChunkBlocks;
+        q.accumulate = kt0 > 0;
+        e = cudaLaunchKernelEx(&cfg, kern, q, w_map, ah, al);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -592,6 +630,9 @@ cudaError_t launch_gemm_fold(qmm_type t, const uint8_t *tiled, int64_t K, int64_
     p.ldy = ldy;
     p.n_col_tiles = (N + 31) / 32;
     p.nkt = (int)(K / 32);
+    p.kt0 = 0;
+    p.nkc = p.nkt;
+    p.accumulate = 0;
     p.lut = lut_for(t);
     switch (t) {
         case QMM_Q4_0: return launch_fold_typed<QMM_Q4_0>(p, ah, al, s);

@@ -29,6 +29,10 @@
 // Two token-operand variants: int8 quants converted in the kernel (no scratch memory), or a prepared
 // fp16 copy in a caller workspace (every token tile is then converted once instead of once per
 // weight tile).
+// Long K: one launch covers at most kGemmChunkBlocks blocks (K = 4096); longer rows run in passes, each
+// adding its partial sums into y in order.  Error: two roundings per block (S_b * d_a, then the FMA)
+// along a pass and one per pass add, at most (kGemmChunkBlocks + 2 + n_passes) * 2^-24 *
+// sum_k |w_k x_k|: 7.9e-6 at K = 4096, 9.7e-6 at the largest accepted K (131072).
 // Every mbarrier wait is bounded in time; on expiry the kernel records QMM_ERR_TIMEOUT in a device
 // status word, lets its copies and MMAs in flight land, frees TMEM and returns.
 #include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched through the runtime)
@@ -66,6 +70,8 @@ struct GemmParams {
     float *y;
     int64_t K, nkt, N, M, ldy;
     int64_t n_col_tiles;
+    int kt0, nkc;       // K blocks of this pass: [kt0, kt0 + nkc)
+    int accumulate;     // 0: y = result, 1: y += result (passes after the first)
     Lut16 lut;
 };
 
@@ -193,8 +199,9 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
     const int64_t m0 = (int64_t)blockIdx.y * BN;
     const int n_tiles = (int)((p.n_col_tiles - ct0) < 4 ? (p.n_col_tiles - ct0) : 4);
     const int n_tok = (int)((p.M - m0) < BN ? (p.M - m0) : BN);
-    const int64_t nkt = p.nkt;
-    const int nkt32 = (int)p.nkt;
+    const int64_t nkt = p.nkt;                  // row stride of a_d (all K blocks)
+    const int nkt32 = p.nkc;                     // blocks of this pass
+    const int kt0 = p.kt0;
     const int npairs = (nkt32 + 1) >> 1;
 
     // ---- set-up: barriers, IQ4_NL table, TMEM ----
@@ -240,12 +247,12 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                 const uint32_t fb = smem_u32(&w_full[s]);
                 const uint32_t dst = smem_u32(w_s + s * P::kWStageBytes);
                 mbar_arrive_expect_tx(fb, (uint32_t)(P::kWTiles + P::kWTok));
-                tma_load_3d(dst, &w_map, 0, 2 * pr, (int)ct0, fb);
+                tma_load_3d(dst, &w_map, 0, kt0 + 2 * pr, (int)ct0, fb);
                 if constexpr (P::kPrep) {
-                    tma_load_2d(dst + P::kWTiles, &da_map, (int)m0, 2 * pr, fb);
-                    if constexpr (P::kAff) tma_load_2d(dst + P::kWTiles + 2 * BN * 2, &ca_map, (int)m0, 2 * pr, fb);
+                    tma_load_2d(dst + P::kWTiles, &da_map, (int)m0, kt0 + 2 * pr, fb);
+                    if constexpr (P::kAff) tma_load_2d(dst + P::kWTiles + 2 * BN * 2, &ca_map, (int)m0, kt0 + 2 * pr, fb);
                 } else {
-                    tma_load_2d(dst + P::kWTiles, &act_map, 64 * pr, (int)m0, fb);
+                    tma_load_2d(dst + P::kWTiles, &act_map, 32 * kt0 + 64 * pr, (int)m0, fb);
                 }
             }
             __syncwarp();
@@ -265,7 +272,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                 if (lane == 0) {
                     const uint32_t fb = smem_u32(&b_full[s]);
                     mbar_arrive_expect_tx(fb, (uint32_t)kOp2Bytes);
-                    tma_load_2d(smem_u32(b_s + s * kOp2Bytes), &act_map, 64 * pr, (int)m0, fb);
+                    tma_load_2d(smem_u32(b_s + s * kOp2Bytes), &act_map, 32 * kt0 + 64 * pr, (int)m0, fb);
                 }
                 __syncwarp();
                 issued = pr + 1;
@@ -324,8 +331,8 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
         if (!P::kPrep) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                da_cur[u] = (tok_ok && u < nkt32) ? p.a_d[(m0 + c) * nkt + u] : (uint16_t)0;
-                da_nxt[u] = (tok_ok && 8 + u < nkt32) ? p.a_d[(m0 + c) * nkt + 8 + u] : (uint16_t)0;
+                da_cur[u] = (tok_ok && u < nkt32) ? p.a_d[(m0 + c) * nkt + kt0 + u] : (uint16_t)0;
+                da_nxt[u] = (tok_ok && 8 + u < nkt32) ? p.a_d[(m0 + c) * nkt + kt0 + 8 + u] : (uint16_t)0;
             }
         }
         bool ok = true;
@@ -424,7 +431,7 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                 for (int u = 0; u < 8; ++u) {
                     da_cur[u] = da_nxt[u];
                     const int kn = 2 * pg + 16 + u;
-                    da_nxt[u] = (tok_ok && kn < nkt32) ? p.a_d[(m0 + c) * nkt + kn] : (uint16_t)0;
+                    da_nxt[u] = (tok_ok && kn < nkt32) ? p.a_d[(m0 + c) * nkt + kt0 + kn] : (uint16_t)0;
                 }
             }
         }
@@ -493,10 +500,19 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
         if (ok) {
             const int64_t n = (ct0 * 32) + row;
             if (n < p.N) {
+                if (!p.accumulate) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const int64_t m = m0 + 64 * half + i;
-                    if (m < p.M) p.y[m * p.ldy + n] = (i & 1) ? y2[i >> 1].y : y2[i >> 1].x;
+                    for (int i = 0; i < 64; ++i) {
+                        const int64_t m = m0 + 64 * half + i;
+                        if (m < p.M) p.y[m * p.ldy + n] = (i & 1) ? y2[i >> 1].y : y2[i >> 1].x;
+                    }
+                } else {
+                    // a later K pass adds its partial sums into y
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const int64_t m = m0 + 64 * half + i;
+                        if (m < p.M) p.y[m * p.ldy + n] = __fadd_rn(p.y[m * p.ldy + n], (i & 1) ? y2[i >> 1].y : y2[i >> 1].x);
+                    }
                 }
             }
         }
@@ -613,8 +629,17 @@ cudaError_t launch_typed(const GemmParams &p, const CUtensorMap &act_map, const 
     e = make_weight_map(&w_map, p.tiled, P::TS, p.nkt, p.n_col_tiles);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((p.n_col_tiles + 3) / 4), (unsigned)((p.M + BN - 1) / BN), 1);
-    kern<<<grid, kThreads, P::kSmem, s>>>(p, w_map, act_map, da_map, ca_map);
-    return cudaGetLastError();
+    // K in passes of at most kGemmChunkBlocks blocks, each adding into y in order (the error bound)
+    for (int kt0 = 0; kt0 < (int)p.nkt; kt0 += kGemmChunkBlocks) {
+        GemmParams q = p;
+        q.kt0 = kt0;
+        q.nkc = (int)p.nkt - kt0 < kGemmChunkBlocks ? (int)p.nkt - kt0 : kGemmChunkBlocks;
+        q.accumulate = kt0 > 0;
+        kern<<<grid, kThreads, P::kSmem, s>>>(q, w_map, act_map, da_map, ca_map);
+        const cudaError_t le = cudaGetLastError();
+        if (le != cudaSuccess) return le;
+    }
+    return cudaSuccess;
 }
 
 template <int ACT>
@@ -642,6 +667,9 @@ GemmParams make_params(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, c
     p.M = M;
     p.ldy = ldy;
     p.n_col_tiles = (N + 31) / 32;
+    p.kt0 = 0;
+    p.nkc = (int)p.nkt;
+    p.accumulate = 0;
     p.lut = lut_for(t);
     return p;
 }

@@ -28,8 +28,9 @@ bool valid_tkn(qmm_type t, int64_t K, int64_t N) { return valid_kn(K, N) && (K %
 cudaStream_t cs(qmm_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 qmm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA; }
 
-// Prefill product with a workspace: the folded-scale GEMM for the tile types it covers, the
-// exact-integer GEMM with a prepared token operand for the others (t is already a tile type).
+// Prefill product with a workspace: the GEMM with the token scales folded into the tensor-core operand
+// for the tile types it covers, the exact-integer GEMM with a prepared token operand for the affine
+// tiles (t is already a tile type).
 cudaError_t launch_prefill_ws(qmm_type t, const uint8_t *w, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
                               int64_t M, float *y, int64_t ldy, void *ws, cudaStream_t s) {
     if (gemm_fold_supports(t)) return launch_gemm_fold(t, w, K, N, a_q, a_d, M, y, ldy, ws, s);
@@ -42,7 +43,7 @@ constexpr int64_t kMaxDim = (int64_t)1 << 31;
 qmm_status check_matmul(qmm_type t, const void *w, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,
                         int64_t M, float *y, int64_t ldy) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
-    if (!valid_tkn(t, K, N) || M <= 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim || ldy < N) return QMM_ERR_INVALID_ARG;
+    if (!valid_tkn(t, K, N) || M <= 0 || K > kMaxMatmulK || N > kMaxDim || M > kMaxDim || ldy < N) return QMM_ERR_INVALID_ARG;
     if (!w || !a_q || !a_d || !y) return QMM_ERR_INVALID_ARG;
     if (!aligned(w, 16) || !aligned(a_q, 16) || !aligned(a_d, 4) || !aligned(y, 4)) return QMM_ERR_MISALIGNED;
     return QMM_OK;
@@ -60,6 +61,7 @@ const char *qmm_status_str(qmm_status st) {
         case QMM_ERR_MISALIGNED: return "misaligned pointer or stride";
         case QMM_ERR_CUDA: return "CUDA error";
         case QMM_ERR_TIMEOUT: return "device pipeline wait timed out";
+        case QMM_ERR_RANGE: return "operand row not exactly representable in the folded-scale GEMM";
     }
     return "unknown status";
 }
@@ -144,7 +146,7 @@ qmm_status qmm_matmul(qmm_type t, const void *w_tiled, int64_t K, int64_t N, con
 qmm_status qmm_matmul_f32(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
                           int64_t M, float *y, int64_t ldy, qmm_stream_t stream) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
-    if (!valid_tkn(t, K, N) || M <= 0 || K > kMaxDim || N > kMaxDim || M > kMaxDim || ldx < K || ldx > kMaxDim || ldy < N)
+    if (!valid_tkn(t, K, N) || M <= 0 || K > kMaxMatmulK || N > kMaxDim || M > kMaxDim || ldx < K || ldx > kMaxDim || ldy < N)
         return QMM_ERR_INVALID_ARG;
     if (!w_tiled || !x || !y) return QMM_ERR_INVALID_ARG;
     if (!aligned(w_tiled, 16) || !aligned(x, 4) || !aligned(y, 4)) return QMM_ERR_MISALIGNED;
@@ -207,7 +209,8 @@ qmm_status qmm_device_status(qmm_stream_t stream) {
     if (e == cudaSuccess) e = read_and_clear_matvec_status(&w, cs(stream));
     if (e == cudaSuccess) e = read_and_clear_fold_status(&f, cs(stream));
     if (e != cudaSuccess) return QMM_ERR_CUDA;
-    return (v | w | f) ? QMM_ERR_TIMEOUT : QMM_OK;
+    if (v | w | (f & 1u)) return QMM_ERR_TIMEOUT;
+    return (f & 2u) ? QMM_ERR_RANGE : QMM_OK;
 }
 
 }  // extern "C"

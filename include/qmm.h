@@ -49,7 +49,9 @@ typedef enum {
     QMM_ERR_UNSUPPORTED = 2,   /* type or path not implemented */
     QMM_ERR_MISALIGNED = 3,    /* a pointer or stride violates the stated alignment */
     QMM_ERR_CUDA = 4,          /* the CUDA runtime reported an error at launch */
-    QMM_ERR_TIMEOUT = 5        /* a kernel gave up waiting on its own pipeline (see qmm_device_status) */
+    QMM_ERR_TIMEOUT = 5,       /* a kernel gave up waiting on its own pipeline (see qmm_device_status) */
+    QMM_ERR_RANGE = 6          /* the folded-scale GEMM met an operand row it cannot represent exactly
+                                  (see qmm_matmul_ws and qmm_device_status) */
 } qmm_status;
 
 /* Weight formats ("Block-32 Quantized Formats").  MXFP4 tiles (544 B) hold OCP FP4 (E2M1) codes in
@@ -167,7 +169,9 @@ QMM_API qmm_status qmm_quantize_act(const float *x_dev, int64_t M, int64_t K, in
  *   a_q_dev, a_d_dev  as written by qmm_quantize_act for M rows and the same K.
  *   y_dev  fp32 output, y[m*ldy + n] for n < N (other columns untouched); 4-byte aligned.
  * Accumulation is fp32 in a fixed order (results are reproducible run to run); the error against
- * the exact value is at most about n_k_tiles * 2^-24 * sum_k |w_k * x_k| (dequantized).
+ * the exact value stays below 1e-5 * sum_k |w_k * x_k| (dequantized) for every accepted K: the
+ * tensor-core GEMM runs K in passes of at most 4096 that add into y in order.  K may be at most
+ * 131072 in every product call (qmm_matmul*, INVALID_ARG beyond).
  * Launch overlap (M <= qmm_decode_max_m()): the decode kernel is a programmatic dependent launch.
  * It may start while the kernel before it on the stream is finishing, and it starts streaming the
  * weight tiles at once; it waits for that kernel to complete before it reads a_q, a_d or y.  So
@@ -250,8 +254,12 @@ QMM_API size_t qmm_matmul_workspace_size(int64_t M, int64_t K);
  *     chunks added in fp32.  The dropped a_lo w_lo is below 2^-22 |a w|; rounding stays below about
  *     5e-6 * sum_k |w_k * x_k|, inside the bound of qmm_matmul, with a different summation order.
  *     A token row whose largest |d_a| * 127 (or a weight row whose largest |d_w| * max|w_int|)
- *     reaches 2^15 is scaled by a power of two and its outputs unscaled; that is exact unless the
- *     row's block scales span more than 2^24.
+ *     reaches 2^15 is scaled by a power of two 2^-t and its outputs by 2^t; that is exact when every
+ *     block scale of the row survives the scaling (fp16(d * 2^-t) * 2^t == d), which fails only
+ *     for rows holding values of at least 32768 whose block scales also span more than about
+ *     2^28 / 127.  Every scaled row is checked; a row that fails the check is reported as
+ *     QMM_ERR_RANGE by the next qmm_device_status() (the result of that call is then not exact).
+ *     K runs in passes of at most 4096 that add into y in order.
  *   - MXFP4, Q4_1, Q4_K tiles: the exact-integer GEMM of qmm_matmul, with the quants copied to fp16
  *     and the block scales transposed in the workspace (results identical to qmm_matmul's).
  * For smaller M the workspace is not touched and the decode kernel runs.  Launch overlap: the
@@ -296,8 +304,11 @@ QMM_API size_t qmm_matmul_noalloc_max_workspace(void);
 
 /*
  * qmm_device_status -- synchronizes `stream`, then returns and clears the library's device status
- * word for the current device: QMM_OK, or QMM_ERR_TIMEOUT when a pipelined kernel gave up on one of
- * its bounded waits (its outputs are then undefined).  QMM_ERR_CUDA if the synchronization fails.
+ * words for the current device: QMM_OK; QMM_ERR_TIMEOUT when a pipelined kernel gave up on one of
+ * its bounded waits (its outputs are then undefined); else QMM_ERR_RANGE when a qmm_matmul_ws /
+ * qmm_matmul_noalloc call since the last read met an operand row the folded-scale GEMM cannot
+ * represent exactly (that call's outputs may be off by more than the stated bound; qmm_matmul,
+ * the exact-integer GEMM, computes such data within it).  QMM_ERR_CUDA if the synchronization fails.
  */
 QMM_API qmm_status qmm_device_status(qmm_stream_t stream);
 

@@ -73,8 +73,9 @@ def test_iq4nl_table_matches_the_oracle(L, orc):
 
 
 def test_status_strings(L):
-    for st in range(6):
+    for st in range(7):
         assert L.qmm_status_str(st)
+    assert L.qmm_status_str(6) != L.qmm_status_str(99)
     assert L.qmm_status_str(99) == b"unknown status"
 
 
@@ -210,3 +211,17 @@ def test_selftest_timeout_argument_errors(L):
     assert f(1, 2_000_000_001, P, None) == INVALID            # above 2 s
     assert f(0, 100_000_000, None, None) == INVALID
     assert f(0, 100_000_000, P + 2, None) == MISALIGNED
+
+
+def test_product_calls_cap_k(L):
+    # the fp32 accumulation bound of every kernel is derived up to K = 131072 (4096 blocks); longer
+    # rows are refused before anything is launched
+    K = 131072 + 32
+    assert L.qmm_matmul(1, P, K, 64, P, P, 1, P, 64, None) == INVALID
+    assert L.qmm_matmul_path(1, P, K, 64, P, P, 300, P, 64, 2, None) == INVALID
+    assert L.qmm_matmul_ws(1, P, K, 64, P, P, 300, P, 64, P, 1 << 40, None) == INVALID
+    assert L.qmm_matmul_noalloc(1, P, K, 64, P, P, 300, P, 64, None) == INVALID
+    assert L.qmm_matmul_f32(1, P, K, 64, P, K, 1, P, 64, None) == INVALID
+    assert L.qmm_matmul_flat(1, P, K, 64, P, P, 1, P, 64, None) == INVALID
+    # the weight-side calls are not products and keep the wider limit
+    assert L.qmm_tiled_size(1, K, 64) > 0

@@ -2,12 +2,13 @@
 
 qmm_matmul_ws (and qmm_matmul_noalloc) run Q4_0, Q8_0 and IQ4_NL prefill shapes on the kernel that
 folds the block scales into exact hi + lo fp16 operands and accumulates 128-wide K chunks in fp32 on
-the tensor cores.  Bound: |gpu - oracle| <= 1e-5 * sum_k |w_k x_k| + 1e-6 per element.  Beyond the
+the tensor cores (K in passes of at most 4096 added into y).  Bound: |gpu - oracle| <= 1e-5 * sum_k |w_k x_k| + 1e-6 per element.  Beyond the
 shapes of test_gpu_gemm.py these cases aim at what is particular to that kernel:
   * long K with a partial last chunk and an odd number of blocks (K = 4192: 131 blocks);
   * all-positive operands, where every rounding of the fp32 accumulation pushes the same way;
   * token rows and weight rows large enough to take the power-of-two range shift, including rows
-    whose blocks differ in magnitude by 10^6;
+    whose blocks differ in magnitude by 10^6, and rows whose small block scales cannot survive the
+    shift (the call reports QMM_ERR_RANGE; the exact-integer path computes them);
   * operands at the other end of fp16's range (tiny block scales, subnormal lo terms).
 """
 import numpy as np
@@ -83,6 +84,58 @@ def test_fold_weight_range_shift(torch, orc, type_):
     w[130] *= np.float32(1e-3)              # tiny block scales
     x = synth.activations(150, 1024, seed=46)
     _run(orc, type_, w, x, "weight range")
+
+
+RANGE = 6          # QMM_ERR_RANGE
+
+
+def _range_case(torch, orc, type_, w, x, what):
+    """The folded-scale path reports the call (its result is then not exact); the exact-integer path
+    computes the same data within the bound."""
+    import block_quantized_matmul_gb300 as qmm
+    from tests.gpu_util import gpu_matmul
+
+    N, K = w.shape
+    M = x.shape[0]
+    tiled_ref = orc.repack(type_, orc.quantize_rows(type_, w), K, N)
+    q_ref, d_ref = orc.quantize_act(x)
+    y_ref, bound = orc.matmul(type_, tiled_ref, K, N, q_ref, d_ref)
+    _, tiled = gpu_prepare_weight(type_, w)
+    a_q, a_d = gpu_quantize_act(x)
+    assert qmm.qmm_device_status() == 0
+    gpu_matmul_ws(type_, tiled, K, N, a_q, a_d, M)
+    assert qmm.qmm_device_status() == RANGE, what
+    assert qmm.qmm_device_status() == 0                      # the read clears it
+    y = gpu_matmul(type_, tiled, K, N, a_q, a_d, M, path=2).cpu().numpy()
+    assert qmm.qmm_device_status() == 0
+    assert_within_bound(y, y_ref, bound, f"exact path, {what}")
+
+
+@pytest.mark.parametrize("type_", FOLD_TYPES)
+def test_fold_reports_token_row_it_cannot_represent(torch, orc, type_):
+    # Row 9 holds a block of 1e5 (the row takes the power-of-two shift) and blocks of about 1e-4, whose
+    # fp16 scales (subnormal) lose bits when shifted.  Weight rows 0..79 are zero under the large block,
+    # so their outputs come from the small blocks alone: lost bits there would be far above the bound.
+    K, N, M = 1024, 160, 140
+    x = synth.activations(M, K, seed=53)
+    x[9, :32] = np.float32(1e5) * np.sign(x[9, :32])
+    x[9, 32:] *= np.float32(1e-4)
+    w = synth.weights(N, K, seed=54)
+    w[:80, :32] = 0.0
+    _range_case(torch, orc, type_, w, x, "token row")
+
+
+@pytest.mark.parametrize("type_", FOLD_TYPES)
+def test_fold_reports_weight_row_it_cannot_represent(torch, orc, type_):
+    # Weight row 7: one block large enough for the row shift, the others with subnormal fp16 scales that
+    # lose bits when shifted; token rows 0..59 are zero under the large block.
+    K, N, M = 1024, 96, 130
+    w = synth.weights(N, K, seed=55)
+    w[7, :32] *= np.float32(1e6)
+    w[7, 32:] *= np.float32(7e-5)
+    x = synth.activations(M, K, seed=56)
+    x[:60, :32] = 0.0
+    _range_case(torch, orc, type_, w, x, "weight row")
 
 
 def test_fold_matches_exact_kernel(torch, orc):
