@@ -133,10 +133,11 @@ __device__ __forceinline__ void consumer_sync() {      // named barrier over the
 
 // Fused activation quantization.  The 4 lanes q = 0..3 of an aligned lane quad quantize one block
 // of 32 (columns 8q..8q+7 each) by the rule of qmm_quantize_act, sharing amax through two
-// shuffles; every lane of the warp must call this (dead lanes pass live = false).  Returns the 8
-// int8 codes (columns 8q..8q+7, in order) and sets da = fp32(fp16(d)).
-__device__ __forceinline__ uint2 quantize_quarter(const MvParams &p, bool live, int tok, int64_t kt, int q, float &da) {
-    float v[8];
+// shuffles; every lane of the warp must call quantize_loaded (dead lanes load with live = false).
+// load_quarter fetches the lane's 8 fp32 values (so that a thread can have several blocks in
+// flight before it quantizes any); quantize_loaded returns the 8 int8 codes (columns 8q..8q+7, in
+// order) and sets da = fp32(fp16(d)).
+__device__ __forceinline__ void load_quarter(const MvParams &p, bool live, int tok, int64_t kt, int q, float (&v)[8]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) v[k] = 0.0f;
     if (live) {
@@ -149,6 +150,10 @@ __device__ __forceinline__ uint2 quantize_quarter(const MvParams &p, bool live, 
             for (int k = 0; k < 8; ++k) v[k] = __ldg(src + k);
         }
     }
+}
+// The int8 codes of a quarter loaded by load_quarter (the 4 lanes of a quad hold one block's quarters
+// and take the block's amax together) and fp32(d_a).
+__device__ __forceinline__ uint2 quantize_loaded(const float (&v)[8], float &da) {
     float amax = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
@@ -163,6 +168,13 @@ __device__ __forceinline__ uint2 quantize_quarter(const MvParams &p, bool live, 
     }
     da = __half2float(__float2half_rn(d));
     return make_uint2(lo, hi);
+}
+
+// Both steps for one quarter: block kt of token tok.
+__device__ __forceinline__ uint2 quantize_quarter(const MvParams &p, bool live, int tok, int64_t kt, int q, float &da) {
+    float v[8];
+    load_quarter(p, live, tok, kt, q, v);
+    return quantize_loaded(v, da);
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
@@ -660,6 +672,46 @@ __device__ __forceinline__ uint4 dp4a_record(int type, uint2 v, int j, float da)
     return rec;
 }
 
+// One tile for lane (i, j): the int8 dot products of its rows 4i..4i+3 with the MT staged tokens
+// (act[4 t + j]: token t's record of the tile's block for this lane's column pairs), rescaled by
+// d_w * d_a and added to acc.  Tokens past the live ones have all-zero records and add nothing.
+template <int TYPE, int MT>
+__device__ __forceinline__ void dp4a_tile(const uint8_t *tile, const uint4 *act, int i, int j, const uint32_t (&tb)[4],
+                                          float2 (&acc)[MT][2]) {
+    constexpr int SOFF = TileFmt<TYPE>::kScaleOff;
+    uint32_t R[4][2];
+    tile_rows_dp4a<TYPE>(tile, i, j, R, tb);
+    float dws[4];
+    row_scales<TYPE>(tile + SOFF, 4 * i, dws);                  // rows 4i .. 4i+3
+    const float2 dw01 = pack2(dws[0], dws[1]), dw23 = pack2(dws[2], dws[3]);
+    float2 mw01 = make_float2(0.0f, 0.0f), mw23 = make_float2(0.0f, 0.0f);
+    if constexpr (TileFmt<TYPE>::kAffine) {
+        float mws[4];
+        row_mins<TYPE>(tile + SOFF, 4 * i, mws);
+        mw01 = pack2(mws[0], mws[1]);
+        mw23 = pack2(mws[2], mws[3]);
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        const uint4 a = act[4 * t + j];
+        int S[4];
+        const int c0 = TileFmt<TYPE>::kAffine ? 0 : (int)a.z;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) S[r] = __dp4a((int)R[r][0], (int)a.x, __dp4a((int)R[r][1], (int)a.y, c0));
+        const float da = __uint_as_float(a.w);
+        const float2 da2 = pack2(da, da);
+        acc[t][0] = ffma2(pack2((float)S[0], (float)S[1]), fmul2(dw01, da2), acc[t][0]);
+        acc[t][1] = ffma2(pack2((float)S[2], (float)S[3]), fmul2(dw23, da2), acc[t][1]);
+        if constexpr (TileFmt<TYPE>::kAffine) {
+            // + m_w * d_a * (sum of this lane's 8 activations); the 4 quarters add up to the block's sum
+            const float as = (float)(int)a.z;
+            const float2 as2 = pack2(as, as);
+            acc[t][0] = ffma2(as2, fmul2(mw01, da2), acc[t][0]);
+            acc[t][1] = ffma2(as2, fmul2(mw23, da2), acc[t][1]);
+        }
+    }
+}
+
 struct Dp4aLayout {
     int ring, bars, act, red, total;
 };
@@ -672,7 +724,7 @@ __host__ __device__ inline Dp4aLayout dp4a_layout(int nkc, int stages) {
     off = (off + 15) & ~15;
     L.bars = off;  off += 2 * stages * 8 + 16;
     off = (off + 15) & ~15;
-    L.act = off;   off += MT * nkc * 4 * 16;                 // [MT][nkc][4] uint4
+    L.act = off;   off += MT * nkc * 4 * 16;                 // [nkc][MT][4] uint4
     L.red = off;   off += CW * MT * 32 * 4;                  // [CW][MT][32] float
     L.total = off;
     return L;
@@ -683,7 +735,6 @@ template <int TYPE, int MT, int CW, bool FUSED, int TPW>
 __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(const MvParams p) {
     constexpr int kTilesPerStage = CW * TPW;
     constexpr int TS = TileFmt<TYPE>::kBytes;
-    constexpr int SOFF = TileFmt<TYPE>::kScaleOff;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const Dp4aLayout L = dp4a_layout<TYPE, MT, CW, TPW>(p.nkc, p.stages);
@@ -719,28 +770,48 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
 
     // the activations may come from the grid launched just before this one (see produce)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // records e = (block jt, token t, quarter q) at act_s[(jt * MT + t) * 4 + q]; each thread first
+    // issues the loads of its records (up to MT of them at a time), then builds them
+    constexpr int kStageBatch = MT;
+    const int total = MT * nkc * 4;
     if constexpr (!FUSED) {
-        for (int e = ctid; e < MT * nkc * 4; e += CW * 32) {
-            const int tok = e / (nkc * 4), rem = e - tok * nkc * 4, jt = rem >> 2, q = rem & 3;
-            uint4 rec = make_uint4(0u, 0u, 0u, 0u);
-            if (tok < p.M) {
-                const int64_t kt = p.kt0 + jt;
-                const float da = __half2float(__ushort_as_half(p.a_d[(int64_t)tok * p.nkt + kt]));
-                const uint2 v = *reinterpret_cast<const uint2 *>(p.a_q + (int64_t)tok * p.K + kt * 32 + 8 * q);
-                rec = dp4a_record(TYPE, v, q, da);
+        for (int base = ctid; base < total; base += CW * 32 * kStageBatch) {
+            uint2 v[kStageBatch];
+            uint16_t db[kStageBatch];
+#pragma unroll
+            for (int u = 0; u < kStageBatch; ++u) {
+                const int e = base + u * CW * 32, q = e & 3, tok = (e >> 2) % MT, jt = (e >> 2) / MT;
+                v[u] = make_uint2(0u, 0u);
+                db[u] = 0;
+                if (e < total && tok < p.M) {
+                    const int64_t kt = p.kt0 + jt;
+                    db[u] = p.a_d[(int64_t)tok * p.nkt + kt];
+                    v[u] = *reinterpret_cast<const uint2 *>(p.a_q + (int64_t)tok * p.K + kt * 32 + 8 * q);
+                }
             }
-            act_s[e] = rec;
+#pragma unroll
+            for (int u = 0; u < kStageBatch; ++u) {
+                const int e = base + u * CW * 32, q = e & 3, tok = (e >> 2) % MT;
+                if (e < total)
+                    act_s[e] = tok < p.M ? dp4a_record(TYPE, v[u], q, __half2float(__ushort_as_half(db[u]))) : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     } else {
-        // record e = (token, block, quarter) is made by lane quad e & ~3 (all lanes of a warp iterate together)
-        const int total = MT * nkc * 4;
-        for (int base = cw * 32; base < total; base += CW * 32) {
-            const int e = base + lane;
-            const int tok = e / (nkc * 4), rem = e - tok * nkc * 4, jt = rem >> 2, q = rem & 3;
-            const bool live = e < total && tok < p.M;
-            float da;
-            const uint2 v = quantize_quarter(p, live, tok, p.kt0 + jt, q, da);
-            if (e < total) act_s[e] = live ? dp4a_record(TYPE, v, q, da) : make_uint4(0u, 0u, 0u, 0u);
+        // a record is made by the lane quad of its 4 quarters (all lanes of a warp iterate together)
+        for (int base = cw * 32; base < total; base += CW * 32 * kStageBatch) {
+            float v[kStageBatch][8];
+#pragma unroll
+            for (int u = 0; u < kStageBatch; ++u) {
+                const int e = base + u * CW * 32 + lane, q = e & 3, tok = (e >> 2) % MT, jt = (e >> 2) / MT;
+                load_quarter(p, e < total && tok < p.M, tok, p.kt0 + jt, q, v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kStageBatch; ++u) {
+                const int e = base + u * CW * 32 + lane, q = e & 3, tok = (e >> 2) % MT;
+                float da;
+                const uint2 c = quantize_loaded(v[u], da);
+                if (e < total) act_s[e] = tok < p.M ? dp4a_record(TYPE, c, q, da) : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
     }
     uint32_t tb[4] = {0u, 0u, 0u, 0u};
@@ -764,44 +835,16 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
             const uint32_t ph = (it / (uint32_t)stages) & 1u;
             if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
             if (ok) {
+                // tiles cw, cw + CW, ... of the stage; only the last stage of a pass can be partial
+                const uint8_t *tile = ring + (s * kTilesPerStage + cw) * TS;
+                const uint4 *act = act_s + (j0 + cw) * MT * 4;
+                if (j0 + kTilesPerStage <= nkc) {
 #pragma unroll
-                for (int u = 0; u < TPW; ++u) {
-                    const int jt = j0 + cw + CW * u;
-                    if (jt >= nkc) continue;
-                    const uint8_t *tile = ring + (s * kTilesPerStage + cw + CW * u) * TS;
-                    uint32_t R[4][2];
-                    tile_rows_dp4a<TYPE>(tile, i, j, R, tb);
-                    float dws[4];
-                    row_scales<TYPE>(tile + SOFF, 4 * i, dws);                  // rows 4i .. 4i+3
-                    const float2 dw01 = pack2(dws[0], dws[1]), dw23 = pack2(dws[2], dws[3]);
-                    float2 mw01 = make_float2(0.0f, 0.0f), mw23 = make_float2(0.0f, 0.0f);
-                    if constexpr (TileFmt<TYPE>::kAffine) {
-                        float mws[4];
-                        row_mins<TYPE>(tile + SOFF, 4 * i, mws);
-                        mw01 = pack2(mws[0], mws[1]);
-                        mw23 = pack2(mws[2], mws[3]);
-                    }
+                    for (int u = 0; u < TPW; ++u) dp4a_tile<TYPE, MT>(tile + CW * u * TS, act + CW * u * MT * 4, i, j, tb, acc);
+                } else {
 #pragma unroll
-                    for (int t = 0; t < MT; ++t) {
-                        if (t >= p.M) break;
-                        const uint4 a = act_s[(t * nkc + jt) * 4 + j];
-                        int S[4];
-                        const int c0 = TileFmt<TYPE>::kAffine ? 0 : (int)a.z;
-#pragma unroll
-                        for (int r = 0; r < 4; ++r) S[r] = __dp4a((int)R[r][0], (int)a.x, __dp4a((int)R[r][1], (int)a.y, c0));
-                        const float da = __uint_as_float(a.w);
-                        const float2 da2 = pack2(da, da);
-                        acc[t][0] = ffma2(pack2((float)S[0], (float)S[1]), fmul2(dw01, da2), acc[t][0]);
-                        acc[t][1] = ffma2(pack2((float)S[2], (float)S[3]), fmul2(dw23, da2), acc[t][1]);
-                        if constexpr (TileFmt<TYPE>::kAffine) {
-                            // + m_w * d_a * (sum of this lane's 8 activations); the 4 quarters add up to
-                            // the block's sum
-                            const float as = (float)(int)a.z;
-                            const float2 as2 = pack2(as, as);
-                            acc[t][0] = ffma2(as2, fmul2(mw01, da2), acc[t][0]);
-                            acc[t][1] = ffma2(as2, fmul2(mw23, da2), acc[t][1]);
-                        }
-                    }
+                    for (int u = 0; u < TPW; ++u)
+                        if (j0 + cw + CW * u < nkc) dp4a_tile<TYPE, MT>(tile + CW * u * TS, act + CW * u * MT * 4, i, j, tb, acc);
                 }
             }
             __syncwarp();
