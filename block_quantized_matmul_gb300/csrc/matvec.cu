@@ -38,7 +38,9 @@
 namespace qmm {
 namespace {
 
-constexpr int kTilesPerWarp = 2;                        // independent tiles per warp per stage (ILP)
+// Independent tiles per warp and stage of the fp16 mma path (ILP); measured best for 8 and 16 tokens
+// alike (one tile per warp at 16 tokens, which avoids a few spilled registers, is 3-7 % slower).
+constexpr int kTilesPerWarp = 2;
 // Independent tiles per warp and stage for the int8 dot-product consumers: 4 where decoding a tile takes
 // many instructions per byte (4-bit codes, table lookups), 2 for the plain Q8_0 bytes (measured).
 template <int TYPE>
@@ -314,6 +316,64 @@ __host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
     return L;
 }
 
+// The TPW tiles cw, cw + CW, ... of one ring stage for lane (g, t): all of them decoded first, then
+// contracted with the staged tokens (act_s[act_off[nf] + 4 j]: block j of this lane's activation row
+// of token group nf) and rescaled into acc.  jt0 = the K tile of the warp's first tile;
+// FULL: every tile of the stage is live, else tiles at or past nkc are skipped.
+template <int TYPE, int NF, int CW, int TPW, bool FULL>
+__device__ __forceinline__ void mma_stage(const uint8_t *tile, int jt0, int nkc, const uint4 *act_s, const int (&act_off)[NF],
+                                          const float *da_s, const float *corr_s, const float *asum_s,
+                                          const uint32_t *lut_lane, int g, int t, float2 (&acc)[2][NF][2]) {
+    constexpr int TS = TileFmt<TYPE>::kBytes;
+    constexpr int SOFF = TileFmt<TYPE>::kScaleOff;
+    constexpr int TOK = 8 * NF;
+    uint32_t H[TPW][4][4];
+    float dwr[TPW][4];
+    float mwr[TPW][4];              // Q4_1 row mins
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
+        if (FULL || jt0 + CW * u < nkc) {
+            decode_tile<TYPE>(tile + CW * u * TS, g, t, H[u], lut_lane);
+            row_scales<TYPE>(tile + CW * u * TS + SOFF, 4 * g, dwr[u]);            // rows 4g .. 4g+3
+            if constexpr (TileFmt<TYPE>::kAffine) row_mins<TYPE>(tile + CW * u * TS + SOFF, 4 * g, mwr[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < TPW; ++u) {
+        const int j = jt0 + CW * u;
+        if (!FULL && j >= nkc) continue;
+#pragma unroll
+        for (int nf = 0; nf < NF; ++nf) {
+            const uint4 b = act_s[act_off[nf] + 4 * j];
+            const float2 da = *reinterpret_cast<const float2 *>(da_s + j * TOK + 8 * nf + 2 * t);
+            const float2 cr = *reinterpret_cast<const float2 *>(corr_s + j * TOK + 8 * nf + 2 * t);
+            const float2 ncorr = pack2(-cr.x, -cr.y);
+            float2 as2 = make_float2(0.0f, 0.0f);
+            if constexpr (TileFmt<TYPE>::kAffine) as2 = *reinterpret_cast<const float2 *>(asum_s + j * TOK + 8 * nf + 2 * t);
+#pragma unroll
+            for (int rb = 0; rb < 2; ++rb) {
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(c, H[u][0][2 * rb], H[u][0][2 * rb + 1], H[u][1][2 * rb], H[u][1][2 * rb + 1], b.x, b.y);
+                mma16816(c, H[u][2][2 * rb], H[u][2][2 * rb + 1], H[u][3][2 * rb], H[u][3][2 * rb + 1], b.z, b.w);
+                // c0,c1: row 4g+2rb, tokens 2t,2t+1;  c2,c3: row 4g+2rb+1
+                const float2 s01 = fadd2(pack2(c[0], c[1]), ncorr);
+                const float2 s23 = fadd2(pack2(c[2], c[3]), ncorr);
+                const float2 p01 = fmul2(pack2(dwr[u][2 * rb], dwr[u][2 * rb]), da);
+                const float2 p23 = fmul2(pack2(dwr[u][2 * rb + 1], dwr[u][2 * rb + 1]), da);
+                acc[rb][nf][0] = ffma2(s01, p01, acc[rb][nf][0]);
+                acc[rb][nf][1] = ffma2(s23, p23, acc[rb][nf][1]);
+                if constexpr (TileFmt<TYPE>::kAffine) {
+                    // + m_w * d_a * sum(a_q) of the block, per row and token
+                    const float2 m01 = fmul2(pack2(mwr[u][2 * rb], mwr[u][2 * rb]), da);
+                    const float2 m23 = fmul2(pack2(mwr[u][2 * rb + 1], mwr[u][2 * rb + 1]), da);
+                    acc[rb][nf][0] = ffma2(as2, m01, acc[rb][nf][0]);
+                    acc[rb][nf][1] = ffma2(as2, m23, acc[rb][nf][1]);
+                }
+            }
+        }
+    }
+}
+
 // CW consumer warps per CTA: 8 (two CTAs per SM) for grids with many column tiles, 16 (one wide CTA
 // per SM) for small ones.
 template <int TYPE, int NF, int CW, bool FUSED>
@@ -321,7 +381,6 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     constexpr int kConsumerWarps = CW;
     constexpr int kTilesPerStage = CW * kTilesPerWarp;
     constexpr int TS = TileFmt<TYPE>::kBytes;
-    constexpr int SOFF = TileFmt<TYPE>::kScaleOff;
     constexpr int TOK = 8 * NF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
@@ -474,6 +533,12 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     // After a timed-out wait a warp stops waiting and computing but keeps the loop structure, so
     // every consumer warp still reaches the same named barriers.
     const uint32_t *lut_lane = lut_s + (lane & (kLutCopies - 1));
+    // this lane's activation row per token group: token 8 nf + g, or for a token past the live ones
+    // (its output column is dropped) the last live token's row, so that every read stays in the
+    // staged rows
+    int act_off[NF];
+#pragma unroll
+    for (int nf = 0; nf < NF; ++nf) act_off[nf] = min(8 * nf + g, p.M - 1) * tok_stride + t;
     uint32_t it = 0;
     bool ok = true;
     for (int64_t ct = blockIdx.x; ct < p.n_col_tiles; ct += gridDim.x) {
@@ -488,62 +553,12 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
             const uint32_t ph = (it / (uint32_t)stages) & 1u;
             if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
             if (ok) {
-                // tiles cw and cw + 8 of this stage, decoded and contracted side by side
-                uint32_t H[kTilesPerWarp][4][4];
-                float dwr[kTilesPerWarp][4];
-                float mwr[kTilesPerWarp][4];              // Q4_1 row mins
-                bool live[kTilesPerWarp];
-#pragma unroll
-                for (int u = 0; u < kTilesPerWarp; ++u) {
-                    const int jt = j0 + cw + kConsumerWarps * u;
-                    live[u] = jt < nkc;
-                    const uint8_t *tile = ring + (s * kTilesPerStage + cw + kConsumerWarps * u) * TS;
-                    if (live[u]) {
-                        decode_tile<TYPE>(tile, g, t, H[u], lut_lane);
-                        row_scales<TYPE>(tile + SOFF, 4 * g, dwr[u]);            // rows 4g .. 4g+3
-                        if constexpr (TileFmt<TYPE>::kAffine) row_mins<TYPE>(tile + SOFF, 4 * g, mwr[u]);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kTilesPerWarp; ++u) {
-                    if (!live[u]) continue;
-                    const int j = j0 + cw + kConsumerWarps * u;
-#pragma unroll
-                    for (int nf = 0; nf < NF; ++nf) {
-                        const int tok = 8 * nf + g;
-                        uint4 b = make_uint4(0, 0, 0, 0);
-                        if (tok < p.M) b = act_s[tok * tok_stride + j * 4 + t];
-                        const float2 da = *reinterpret_cast<const float2 *>(da_s + j * TOK + 8 * nf + 2 * t);
-                        const float2 cr = *reinterpret_cast<const float2 *>(corr_s + j * TOK + 8 * nf + 2 * t);
-                        const float2 ncorr = pack2(-cr.x, -cr.y);
-                        const float2 da2 = pack2(da.x, da.y);
-                        float2 as2 = make_float2(0.0f, 0.0f);
-                        if constexpr (TileFmt<TYPE>::kAffine) {
-                            const float2 as = *reinterpret_cast<const float2 *>(asum_s + j * TOK + 8 * nf + 2 * t);
-                            as2 = pack2(as.x, as.y);
-                        }
-#pragma unroll
-                        for (int rb = 0; rb < 2; ++rb) {
-                            float c[4] = {0.f, 0.f, 0.f, 0.f};
-                            mma16816(c, H[u][0][2 * rb], H[u][0][2 * rb + 1], H[u][1][2 * rb], H[u][1][2 * rb + 1], b.x, b.y);
-                            mma16816(c, H[u][2][2 * rb], H[u][2][2 * rb + 1], H[u][3][2 * rb], H[u][3][2 * rb + 1], b.z, b.w);
-                            // c0,c1: row 4g+2rb, tokens 2t,2t+1;  c2,c3: row 4g+2rb+1
-                            const float2 s01 = fadd2(pack2(c[0], c[1]), ncorr);
-                            const float2 s23 = fadd2(pack2(c[2], c[3]), ncorr);
-                            const float2 p01 = fmul2(pack2(dwr[u][2 * rb], dwr[u][2 * rb]), da2);
-                            const float2 p23 = fmul2(pack2(dwr[u][2 * rb + 1], dwr[u][2 * rb + 1]), da2);
-                            acc[rb][nf][0] = ffma2(s01, p01, acc[rb][nf][0]);
-                            acc[rb][nf][1] = ffma2(s23, p23, acc[rb][nf][1]);
-                            if constexpr (TileFmt<TYPE>::kAffine) {
-                                // + m_w * d_a * sum(a_q) of the block, per row and token
-                                const float2 m01 = fmul2(pack2(mwr[u][2 * rb], mwr[u][2 * rb]), da2);
-                                const float2 m23 = fmul2(pack2(mwr[u][2 * rb + 1], mwr[u][2 * rb + 1]), da2);
-                                acc[rb][nf][0] = ffma2(as2, m01, acc[rb][nf][0]);
-                                acc[rb][nf][1] = ffma2(as2, m23, acc[rb][nf][1]);
-                            }
-                        }
-                    }
-                }
+                // tiles cw, cw + CW, ... of this stage; only the last stage of a pass can be partial
+                const uint8_t *tile = ring + (s * kTilesPerStage + cw) * TS;
+                if (j0 + kTilesPerStage <= nkc)
+                    mma_stage<TYPE, NF, CW, kTilesPerWarp, true>(tile, j0 + cw, nkc, act_s, act_off, da_s, corr_s, asum_s, lut_lane, g, t, acc);
+                else
+                    mma_stage<TYPE, NF, CW, kTilesPerWarp, false>(tile, j0 + cw, nkc, act_s, act_off, da_s, corr_s, asum_s, lut_lane, g, t, acc);
             }
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(smem_u32(&empty[s]));
@@ -887,7 +902,7 @@ struct Plan {
 
 // Ring depth from what is left of the CTA's share of shared memory: CW = 16 runs one wide CTA per
 // SM (all of it), CW = 8 two narrow CTAs per SM (half each).
-template <int TS, int CW, int TPW = kTilesPerWarp>
+template <int TS, int CW, int TPW>
 Plan plan_ring(int nkc, int fixed_bytes) {
     constexpr int kTilesPerStage = CW * TPW;
     Plan pl;
@@ -970,7 +985,7 @@ cudaError_t run_mma(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a,
                     cudaStream_t s) {
     constexpr int TS = TileFmt<TYPE>::kBytes;
     const int nkc = chunk_tiles(K / 32, 64 * (int64_t)M);
-    Plan pl = plan_ring<TS, CW>(nkc, mv_layout<TYPE, NF, CW>(M, nkc, 0).total);
+    Plan pl = plan_ring<TS, CW, kTilesPerWarp>(nkc, mv_layout<TYPE, NF, CW>(M, nkc, 0).total);
     pl.smem = (size_t)mv_layout<TYPE, NF, CW>(M, nkc, pl.stages).total + 128;
     auto kern = matvec_kernel<TYPE, NF, CW, FUSED>;
     static int attr_done[4] = {0, 0, 0, 0};
