@@ -19,6 +19,8 @@ weight is repacked once beforehand, as at model load.
           scales + fp32 output) per launch / mean launch time (a graph of back-to-back launches
           timed with CUDA events), against the measured HBM copy bandwidth.
   other_configs  the remaining workloads, each as its own step (prefill GEMM in TFLOP/s).
+  configs   last key of the line: the five quoted workloads -> kernel_us and roofline frac (HBM for
+          the decode shapes, both HBM and bf16 tensor peak for the prefill shapes).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -49,6 +51,11 @@ OTHERS = [("q4_0", 4096, 4096, 1), ("iq4_nl", 4096, 4096, 8), ("q8_0", 4096, 128
           # flat (untiled) GGML rows, decode
           ("q4_0", 4096, 14336, 1, "flat"), ("q8_0", 4096, 14336, 1, "flat"), ("mxfp4", 4096, 14336, 1, "flat")]
 METRIC = "tiled Q4_0/Q8_0 matvec weight GB/s (% HBM peak); prefill int8 GEMM TOPS"
+# The five workloads the metric is quoted on (lm-head at batch 1 and 128), summarized at the end of
+# the printed line: kernel time and roofline fraction of each.
+SUMMARY = [("c1", ("q4_0", 4096, 4096, 1)), ("c2", HEADLINE), ("c3", ("iq4_nl", 4096, 4096, 8)),
+           ("c4", ("q4_0", 4096, 14336, 512)), ("c5_b1", ("q8_0", 4096, 128256, 1)),
+           ("c5_b128", ("q8_0", 4096, 128256, 128))]
 
 
 def workload_name(type_, K, N, M, layout="tiled"):
@@ -495,9 +502,30 @@ def run_gpu(args):
         line["cpu_baseline"] = cpu_baseline(HEADLINE, budget_s=args.cpu_seconds) if not args.no_cpu else None
         if line["cpu_baseline"] is not None:
             line["cpu_baseline"]["all_cores"] = cpu_baseline_all_cores(HEADLINE)
+        line["configs"] = summary_configs(line)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def summary_configs(line):
+    """Compact per-workload summary of SUMMARY from the headline roofline and other_configs."""
+    by_name = {o["workload"]: o for o in line.get("other_configs") or []}
+    out = {}
+    for key, cfg in SUMMARY:
+        name = workload_name(*cfg)
+        if cfg == HEADLINE:
+            r = line["roofline"]
+            out[key] = {"workload": name, "kernel_us": r["kernel_us"], "frac": r["frac"], "of": "hbm"}
+            continue
+        o = by_name.get(name)
+        if o is None:
+            continue
+        ent = {"workload": name, "kernel_us": o["kernel_us"], "frac": o["roofline_hbm"]["frac"], "of": "hbm"}
+        if "roofline_tensor" in o:
+            ent["tensor_frac"] = o["roofline_tensor"]["frac"]
+        out[key] = ent
+    return out
 
 
 def wl_copies_note(qmm, type_, K, N):

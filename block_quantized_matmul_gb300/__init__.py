@@ -40,10 +40,11 @@ Q4_0, Q8_0, IQ4_NL, MXFP4, Q4_1, Q4_K = 0, 1, 2, 3, 4, 5
 TYPES = {"q4_0": Q4_0, "q8_0": Q8_0, "iq4_nl": IQ4_NL, "mxfp4": MXFP4, "q4_1": Q4_1, "q4_k": Q4_K}
 PATH_AUTO, PATH_MATVEC, PATH_GEMM = 0, 1, 2
 _STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED", 3: "QMM_ERR_MISALIGNED",
-           4: "QMM_ERR_CUDA", 5: "QMM_ERR_TIMEOUT", 6: "QMM_ERR_RANGE"}
+           4: "QMM_ERR_CUDA", 5: "QMM_ERR_TIMEOUT", 6: "QMM_ERR_RANGE", 7: "QMM_ERR_BOUNDS"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-library_path = os.path.join(_HERE, "libqmm.so")
+# QMM_DEBUG=1 in the environment selects the build with device bounds checks (libqmm_debug.so)
+library_path = os.path.join(_HERE, "libqmm_debug.so" if os.environ.get("QMM_DEBUG") == "1" else "libqmm.so")
 _lib = None
 
 

@@ -13,8 +13,13 @@
 //   * Y = sum a_hi w_hi + a_hi w_lo + a_lo w_hi: three fp16 MMAs per K step; the dropped a_lo w_lo is
 //     below 2^-22 |a w|;
 //   * the fp32 accumulator in tensor memory takes a chunk of kChunkPairs = 2 block pairs (128 K) at a
-//     time, and the CUDA cores add the chunk sums in fp32.  With at most one fp32 rounding per MMA
-//     step (24 steps per chunk) and one per chunk sum, the error stays below 5e-6 of sum_k |a w|.
+//     time, and the CUDA cores add the chunk sums in fp32.  A host model of this order (each MMA
+//     step's product sum exact and rounded once into the accumulator, 24 steps per chunk, one rounding
+//     per chunk sum) puts the error below 5e-6 of sum_k |a w| for K up to 4096.  That figure is a
+//     modelled estimate: the tensor cores' internal accumulation order is not documented.  The GPU
+//     parity tests on all-positive operands (the worst case for cancellation-free growth) measure it.
+//   * the host launches K in passes of at most kGemmChunkBlocks blocks (K = 4096); a pass after the first
+//     adds its result into y, which adds one fp32 rounding per pass to the bound.
 // Compared with the exact-integer kernel (gemm_tc.cu), the tensor cores do three times the MACs but
 // the per-block fp32 rescale of every output (two CUDA-core operations per output and block, which
 // made that kernel issue-bound) is gone: what is left for the CUDA cores is the weight split (once
@@ -24,8 +29,13 @@
 //
 // Ranges.  hi must stay finite.  A weight row whose largest |d_w| * max|w_int| reaches 2^15 (and a
 // token row whose largest |d_a| * 127 does) is scaled by a power of two 2^-t before the split, and its
-// outputs by 2^t after the sum.  That is exact unless a scaled-down block scale of that row falls
-// below fp16's normal range (a row whose block scales span more than 2^24).
+// outputs by 2^t after the sum.  That is exact unless a scaled-down block scale d * 2^-t of that row
+// loses bits, i.e. falls below fp16's normal range (d * 2^-t < 2^-14): with t about
+// log2(max d * qmax) - 14, a row whose block scales span more than about 2^28 / qmax (2^21 for
+// qmax = 127, 2^25 for Q4_0's 8).  Both sides check every scaled scale for that (the token rows when
+// they are prepared, the weight rows when the workers scale them) and report a row that fails as
+// QMM_ERR_RANGE through qmm_device_status, after which the caller can run the call again on the
+// exact-integer kernel (qmm_matmul_path with QMM_PATH_GEMM).
 //
 // Tile: 128 weight rows (4 column tiles, the UMMA M) x 128 tokens (UMMA N), all of K.  K moves in
 // pairs of 32-wide blocks; a chunk is two pairs.
@@ -278,8 +288,12 @@ gemm_fold_kernel(const FoldParams p, const __grid_constant__ CUtensorMap w_map, 
                 const int s = pr % WS;
                 if (!wait_bounded(smem_u32(&w_empty[s]), (uint32_t)(((pr / WS) & 1) ^ 1), abort)) break;
                 const uint32_t fb = smem_u32(&w_full[s]);
-                mbar_arrive_expect_tx(fb, (uint32_t)P::kWTiles);
-                tma_load_3d(smem_u32(w_s + s * P::kWStageBytes), &w_map, 0, kt0 + 2 * pr, (int)ct0, fb);
+                if (QMM_DCHECK(s < WS && ct0 < p.n_col_tiles && kt0 + 2 * pr < p.nkt)) {
+                    mbar_arrive_expect_tx(fb, (uint32_t)P::kWTiles);
+                    tma_load_3d(smem_u32(w_s + s * P::kWStageBytes), &w_map, 0, kt0 + 2 * pr, (int)ct0, fb);
+                } else {
+                    mbar_arrive(fb);
+                }
                 issued = pr + 1;
             }
             for (int i = (issued > WS ? issued - WS : 0); i < issued; ++i)
@@ -300,9 +314,13 @@ gemm_fold_kernel(const FoldParams p, const __grid_constant__ CUtensorMap w_map, 
                 if (!wait_bounded(smem_u32(&pair_done[s]), (uint32_t)(((pr / kPairSlots) & 1) ^ 1), abort)) break;
                 const uint32_t fb = smem_u32(&b_full[s]);
                 const uint32_t dst = smem_u32(b_s + s * kBStageBytes);
-                mbar_arrive_expect_tx(fb, (uint32_t)kBStageBytes);
-                tma_load_2d(dst, &ah_map, 32 * kt0 + 64 * pr, (int)m0, fb);
-                tma_load_2d(dst + kTokBytes, &al_map, 32 * kt0 + 64 * pr, (int)m0, fb);
+                if (QMM_DCHECK(s < kPairSlots && kt0 + 2 * pr < p.nkt && m0 < p.M)) {
+                    mbar_arrive_expect_tx(fb, (uint32_t)kBStageBytes);
+                    tma_load_2d(dst, &ah_map, 32 * kt0 + 64 * pr, (int)m0, fb);
+                    tma_load_2d(dst + kTokBytes, &al_map, 32 * kt0 + 64 * pr, (int)m0, fb);
+                } else {
+                    mbar_arrive(fb);
+                }
                 issued = pr + 1;
             }
             for (int i = (issued > kPairSlots ? issued - kPairSlots : 0); i < issued; ++i)
@@ -654,5 +672,7 @@ cudaError_t read_and_clear_fold_status(unsigned *out, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     return cudaStreamSynchronize(s);
 }
+
+QMM_DCHECK_READER(read_dcheck_fold)
 
 }  // namespace qmm

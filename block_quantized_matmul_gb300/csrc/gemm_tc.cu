@@ -37,7 +37,6 @@
 // status word, lets its copies and MMAs in flight land, frees TMEM and returns.
 #include <cuda.h>   // CUtensorMap and its enums (the encoder is fetched through the runtime)
 
-#include <mutex>
 
 #include "pipeline.cuh"
 #include "qmm_internal.cuh"
@@ -243,7 +242,9 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
         uint32_t ph = 0;
         for (int pr = 0; pr < npairs; ++pr) {
             if (!wait_warp(smem_u32(&w_empty[s]), ph ^ 1u, abort)) break;
-            if (lane == 0) {
+            if (lane == 0 && !QMM_DCHECK(s < WS && ct0 < p.n_col_tiles && kt0 + 2 * pr < nkt)) {
+                mbar_arrive(smem_u32(&w_full[s]));      // a failed check: skip the copies of this pair
+            } else if (lane == 0) {
                 const uint32_t fb = smem_u32(&w_full[s]);
                 const uint32_t dst = smem_u32(w_s + s * P::kWStageBytes);
                 mbar_arrive_expect_tx(fb, (uint32_t)(P::kWTiles + P::kWTok));
@@ -271,8 +272,12 @@ gemm_kernel(const GemmParams p, const __grid_constant__ CUtensorMap w_map, const
                 if (!wait_warp(smem_u32(&b_empty[s]), ph ^ 1u, abort)) break;
                 if (lane == 0) {
                     const uint32_t fb = smem_u32(&b_full[s]);
-                    mbar_arrive_expect_tx(fb, (uint32_t)kOp2Bytes);
-                    tma_load_2d(smem_u32(b_s + s * kOp2Bytes), &act_map, 32 * kt0 + 64 * pr, (int)m0, fb);
+                    if (QMM_DCHECK(s < BR && kt0 + 2 * pr < nkt && m0 < p.M)) {
+                        mbar_arrive_expect_tx(fb, (uint32_t)kOp2Bytes);
+                        tma_load_2d(smem_u32(b_s + s * kOp2Bytes), &act_map, 32 * kt0 + 64 * pr, (int)m0, fb);
+                    } else {
+                        mbar_arrive(fb);
+                    }
                 }
                 __syncwarp();
                 issued = pr + 1;
@@ -735,27 +740,14 @@ cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t 
 // ---------------------------------------------------------------------------------------------
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-namespace {
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices] = {};
-}  // namespace
-
-// Device address of the scratch array on the current device.  The host-side symbol is only a
-// stand-in for the device variable, so the address is looked up once per device (with that device
-// current) and cached.
+// Device address of the scratch array in the current context.  The host-side symbol is only a
+// stand-in for the device variable, and the module (with the array) is loaded again after a device
+// reset, so the address is looked up on every call rather than cached.
 cudaError_t noalloc_scratch(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void *ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_noalloc_ptr[dev] = ptr;
-    }
-    *out = g_noalloc_ptr[dev];
+    *out = ptr;
     return cudaSuccess;
 }
 
@@ -772,5 +764,7 @@ cudaError_t read_and_clear_device_status(unsigned *out, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     return cudaStreamSynchronize(s);
 }
+
+QMM_DCHECK_READER(read_dcheck_gemm)
 
 }  // namespace qmm

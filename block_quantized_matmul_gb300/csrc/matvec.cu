@@ -112,8 +112,13 @@ __device__ __forceinline__ void produce(const MvParams &p, uint8_t *ring, uint64
                 const int nt = (nkc - j0) < TPS ? (nkc - j0) : TPS;
                 const uint32_t bytes = (uint32_t)(nt * TS);
                 const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, bytes);
-                bulk_g2s(smem_u32(ring + s * TPS * TS), src + (int64_t)j0 * TS, bytes, fb);
+                // tiles [ct * nkt + kt0 + j0, + nt) of this column tile, into ring slot s
+                if (QMM_DCHECK(s < stages && ct < p.n_col_tiles && p.kt0 + j0 + nt <= p.nkt)) {
+                    mbar_arrive_expect_tx(fb, bytes);
+                    bulk_g2s(smem_u32(ring + s * TPS * TS), src + (int64_t)j0 * TS, bytes, fb);
+                } else {
+                    mbar_arrive(fb);
+                }
             }
             __syncwarp();
         }
@@ -142,7 +147,7 @@ __device__ __forceinline__ void consumer_sync() {      // named barrier over the
 __device__ __forceinline__ void load_quarter(const MvParams &p, bool live, int tok, int64_t kt, int q, float (&v)[8]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) v[k] = 0.0f;
-    if (live) {
+    if (live && QMM_DCHECK(kt < p.nkt && tok < p.M)) {
         const float *src = p.x + (int64_t)tok * p.ldx + kt * 32 + 8 * q;
         if (p.x_vec) {
             const float4 a = __ldg(reinterpret_cast<const float4 *>(src)), b = __ldg(reinterpret_cast<const float4 *>(src + 4));
@@ -449,7 +454,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
             for (int u = 0; u < 2; ++u) {
                 const int i = i0 + u * kStep, j = i / TOK, tok = i - j * TOK;
                 ld[u][0] = ld[u][1] = make_uint4(0u, 0u, 0u, 0u);
-                if (i < TOK * nkc && tok < p.M) {
+                if (i < TOK * nkc && tok < p.M && QMM_DCHECK(p.kt0 + j < p.nkt)) {
                     const int64_t kt = p.kt0 + j;
                     const uint4 *src = reinterpret_cast<const uint4 *>(p.a_q + (int64_t)tok * p.K + kt * 32);
                     ld[u][0] = __ldg(src);
@@ -552,7 +557,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
             const int s = (int)(it % (uint32_t)stages);
             const uint32_t ph = (it / (uint32_t)stages) & 1u;
             if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
-            if (ok) {
+            if (ok && QMM_DCHECK(s < stages)) {
                 // tiles cw, cw + CW, ... of this stage; only the last stage of a pass can be partial
                 const uint8_t *tile = ring + (s * kTilesPerStage + cw) * TS;
                 if (j0 + kTilesPerStage <= nkc)
@@ -798,7 +803,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
                 const int e = base + u * CW * 32, q = e & 3, tok = (e >> 2) % MT, jt = (e >> 2) / MT;
                 v[u] = make_uint2(0u, 0u);
                 db[u] = 0;
-                if (e < total && tok < p.M) {
+                if (e < total && tok < p.M && QMM_DCHECK(p.kt0 + jt < p.nkt)) {
                     const int64_t kt = p.kt0 + jt;
                     db[u] = p.a_d[(int64_t)tok * p.nkt + kt];
                     v[u] = *reinterpret_cast<const uint2 *>(p.a_q + (int64_t)tok * p.K + kt * 32 + 8 * q);
@@ -849,7 +854,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
             const int s = (int)(it % (uint32_t)stages);
             const uint32_t ph = (it / (uint32_t)stages) & 1u;
             if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
-            if (ok) {
+            if (ok && QMM_DCHECK(s < stages)) {
                 // tiles cw, cw + CW, ... of the stage; only the last stage of a pass can be partial
                 const uint8_t *tile = ring + (s * kTilesPerStage + cw) * TS;
                 const uint4 *act = act_s + (j0 + cw) * MT * 4;
@@ -1226,8 +1231,13 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
                 if (!__all_sync(0xffffffffu, wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort))) { ok = false; break; }
                 if (lane == 0) {
                     const uint32_t fb = smem_u32(&full[s]);
-                    mbar_arrive_expect_tx(fb, (uint32_t)(32 * kRowStage));
-                    tma_load_2d(smem_u32(ring + s * 32 * kRowStage), &w_map, (p.kt0 + kb0) * BB / 8, (int)(ch * 32), fb);
+                    // rows ch*32.. of blocks kt0 + kb0.. into ring slot s
+                    if (QMM_DCHECK(s < stages && ch < p.n_chunks && p.kt0 + kb0 < p.nkt)) {
+                        mbar_arrive_expect_tx(fb, (uint32_t)(32 * kRowStage));
+                        tma_load_2d(smem_u32(ring + s * 32 * kRowStage), &w_map, (p.kt0 + kb0) * BB / 8, (int)(ch * 32), fb);
+                    } else {
+                        mbar_arrive(fb);
+                    }
                 }
                 __syncwarp();
             }
@@ -1480,5 +1490,7 @@ cudaError_t read_and_clear_matvec_status(unsigned *out, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     return cudaStreamSynchronize(s);
 }
+
+QMM_DCHECK_READER(read_dcheck_matvec)
 
 }  // namespace qmm

@@ -62,6 +62,7 @@ const char *qmm_status_str(qmm_status st) {
         case QMM_ERR_CUDA: return "CUDA error";
         case QMM_ERR_TIMEOUT: return "device pipeline wait timed out";
         case QMM_ERR_RANGE: return "operand row not exactly representable in the folded-scale GEMM";
+        case QMM_ERR_BOUNDS: return "device bounds check failed (debug build)";
     }
     return "unknown status";
 }
@@ -208,7 +209,15 @@ qmm_status qmm_device_status(qmm_stream_t stream) {
     cudaError_t e = read_and_clear_device_status(&v, cs(stream));
     if (e == cudaSuccess) e = read_and_clear_matvec_status(&w, cs(stream));
     if (e == cudaSuccess) e = read_and_clear_fold_status(&f, cs(stream));
+    // the bounds-check words (always 0 unless the library was built with QMM_DEBUG)
+    unsigned d[5] = {0, 0, 0, 0, 0};
+    if (e == cudaSuccess) e = read_dcheck_matvec(&d[0], cs(stream));
+    if (e == cudaSuccess) e = read_dcheck_gemm(&d[1], cs(stream));
+    if (e == cudaSuccess) e = read_dcheck_fold(&d[2], cs(stream));
+    if (e == cudaSuccess) e = read_dcheck_quant(&d[3], cs(stream));
+    if (e == cudaSuccess) e = read_dcheck_repack(&d[4], cs(stream));
     if (e != cudaSuccess) return QMM_ERR_CUDA;
+    if (d[0] | d[1] | d[2] | d[3] | d[4]) return QMM_ERR_BOUNDS;
     if (v | w | (f & 1u)) return QMM_ERR_TIMEOUT;
     return (f & 2u) ? QMM_ERR_RANGE : QMM_OK;
 }

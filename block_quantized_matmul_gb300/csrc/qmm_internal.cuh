@@ -171,9 +171,45 @@ inline GemmWsLayout gemm_ws_layout(int64_t M, int64_t K) {
     return L;
 }
 
+// ---- device bounds checks (QMM_DEBUG builds) ----
+// QMM_DCHECK(cond) is `true` in release builds, so the compiler drops it and the branch it guards.
+// Built with -DQMM_DEBUG it evaluates cond; when cond fails it records the source line in this
+// translation unit's check word (the first failure stays) and yields false, and the caller skips the
+// access it guards -- nothing traps.  qmm_device_status() reports a recorded failure as
+// QMM_ERR_BOUNDS.  Each file with kernels defines its word's reader with QMM_DCHECK_READER(name).
+#ifdef QMM_DEBUG
+static __device__ unsigned g_dcheck_line = 0;
+__device__ __forceinline__ bool dcheck(bool ok, unsigned line) {
+    if (!ok) atomicCAS(&g_dcheck_line, 0u, line);
+    return ok;
+}
+#define QMM_DCHECK(cond) (::qmm::dcheck((cond), __LINE__))
+#define QMM_DCHECK_READER(name)                                                                       \
+    cudaError_t name(unsigned *out, cudaStream_t s) {                                                 \
+        unsigned zero = 0;                                                                            \
+        cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_dcheck_line, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, s); \
+        if (e == cudaSuccess)                                                                         \
+            e = cudaMemcpyToSymbolAsync(g_dcheck_line, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, s); \
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);                                           \
+        return e;                                                                                     \
+    }
+#else
+#define QMM_DCHECK(cond) (true)
+#define QMM_DCHECK_READER(name)                        \
+    cudaError_t name(unsigned *out, cudaStream_t) {    \
+        *out = 0;                                      \
+        return cudaSuccess;                            \
+    }
+#endif
+// The readers: the source line of the first failed check in each file since the last read, or 0.
+cudaError_t read_dcheck_matvec(unsigned *out, cudaStream_t s);
+cudaError_t read_dcheck_gemm(unsigned *out, cudaStream_t s);
+cudaError_t read_dcheck_fold(unsigned *out, cudaStream_t s);
+cudaError_t read_dcheck_quant(unsigned *out, cudaStream_t s);
+cudaError_t read_dcheck_repack(unsigned *out, cudaStream_t s);
+
 // Fixed device scratch used by qmm_matmul_noalloc (bytes, per device).
 constexpr size_t kNoAllocScratchBytes = (size_t)16 << 20;
-constexpr int kMaxDevices = 64;
 cudaError_t noalloc_scratch(void **out);
 cudaError_t read_and_clear_device_status(unsigned *out, cudaStream_t s);   // tensor-core GEMM
 cudaError_t read_and_clear_matvec_status(unsigned *out, cudaStream_t s);   // decode matvec

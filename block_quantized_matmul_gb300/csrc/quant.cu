@@ -36,7 +36,7 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
         const bool active = i < total;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         int64_t m = 0, kq = 0;
-        if (active) {
+        if (active && QMM_DCHECK(i / quads_per_row < M)) {
             m = i / quads_per_row;
             kq = (i - m * quads_per_row) * 4;
             const float *p = x + m * ldx + kq;
@@ -56,8 +56,11 @@ __global__ void __launch_bounds__(256) quantize_act_kernel(const float *__restri
             const uint32_t packed = (uint32_t)(q8_code(v.x, id) & 0xFF) | ((uint32_t)(q8_code(v.y, id) & 0xFF) << 8) |
                                     ((uint32_t)(q8_code(v.z, id) & 0xFF) << 16) |
                                     ((uint32_t)(q8_code(v.w, id) & 0xFF) << 24);
-            *reinterpret_cast<uint32_t *>(a_q + m * K + kq) = packed;
-            if ((lane & 7u) == 0) a_d[m * (K / 32) + kq / 32] = __half_as_ushort(__float2half_rn(d));
+            // block kq / 32 < K / 32 of row m < M
+            if (QMM_DCHECK(m < M && kq + 4 <= K)) {
+                *reinterpret_cast<uint32_t *>(a_q + m * K + kq) = packed;
+                if ((lane & 7u) == 0) a_d[m * (K / 32) + kq / 32] = __half_as_ushort(__float2half_rn(d));
+            }
         }
     }
 }
@@ -314,5 +317,7 @@ cudaError_t launch_quantize_weight(qmm_type t, const float *w, int64_t N, int64_
     quantize_weight_kernel<<<grid, threads, 0, s>>>((int)t, w, N, K, ldw, flat, lut_for(t));
     return cudaGetLastError();
 }
+
+QMM_DCHECK_READER(read_dcheck_quant)
 
 }  // namespace qmm

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
         const int r = (int)(i & 31);
         const int64_t ct = tile / n_k_tiles, kt = tile - ct * n_k_tiles;
         const int64_t n = ct * 32 + r;
+        // tile index < n_col_tiles * n_k_tiles, block index kt < K / 32
+        if (!QMM_DCHECK(tile < n_tiles && kt < n_k_tiles)) continue;
         uint8_t *t = tiled + tile * ts;
         if (n >= N) {                                   // padding row: all zero
             if (k8) {
@@ -130,6 +132,7 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t *__restrict__
         const int64_t n = i / n_k_tiles, kt = i - n * n_k_tiles;
         const int64_t ct = n >> 5;
         const int r = (int)(n & 31);
+        if (!QMM_DCHECK(n < N && kt < n_k_tiles)) continue;
         const uint8_t *t = tiled + (ct * n_k_tiles + kt) * ts;
         if (mx) {
             uint8_t *b8 = flat + i * bb;
@@ -210,5 +213,7 @@ cudaError_t launch_unpack(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N
     }
     return cudaGetLastError();
 }
+
+QMM_DCHECK_READER(read_dcheck_repack)
 
 }  // namespace qmm

@@ -50,8 +50,10 @@ typedef enum {
     QMM_ERR_MISALIGNED = 3,    /* a pointer or stride violates the stated alignment */
     QMM_ERR_CUDA = 4,          /* the CUDA runtime reported an error at launch */
     QMM_ERR_TIMEOUT = 5,       /* a kernel gave up waiting on its own pipeline (see qmm_device_status) */
-    QMM_ERR_RANGE = 6          /* the folded-scale GEMM met an operand row it cannot represent exactly
+    QMM_ERR_RANGE = 6,         /* the folded-scale GEMM met an operand row it cannot represent exactly
                                   (see qmm_matmul_ws and qmm_device_status) */
+    QMM_ERR_BOUNDS = 7         /* a device bounds check failed (builds with QMM_DEBUG only; see
+                                  qmm_device_status) */
 } qmm_status;
 
 /* Weight formats ("Block-32 Quantized Formats").  MXFP4 tiles (544 B) hold OCP FP4 (E2M1) codes in
@@ -287,8 +289,10 @@ QMM_API qmm_status qmm_matmul_ws(qmm_type t, const void *w_tiled_dev, int64_t K,
  *   - Sizes: if qmm_matmul_workspace_size(M, K) exceeds that limit the call returns
  *     QMM_ERR_INVALID_ARG without launching anything (the workspace is about 4.2 bytes per
  *     activation element: M = 960 tokens at K = 4096 fit, 1024 do not).
- *   - The first call with M > qmm_decode_max_m() on a device looks up the scratch array's device
- *     address with that device current and caches it; make that first call before any stream capture.
+ *   - Every call with M > qmm_decode_max_m() looks up the scratch array's device address in the
+ *     current context (a host-side lookup, no device work), so it follows a device reset that loads
+ *     the library's device code again.  The first such call in a context may load that code; make it
+ *     before any stream capture.
  *   - The scratch array is shared by all calls and keeps the last call's contents; nothing in it
  *     needs to start at zero (each call rewrites what it reads).  Calls that overlap on the GPU (on
  *     different streams, or from different threads) race on it and must be serialized by the caller.
@@ -304,7 +308,10 @@ QMM_API size_t qmm_matmul_noalloc_max_workspace(void);
 
 /*
  * qmm_device_status -- synchronizes `stream`, then returns and clears the library's device status
- * words for the current device: QMM_OK; QMM_ERR_TIMEOUT when a pipelined kernel gave up on one of
+ * words for the current device: QMM_OK; QMM_ERR_BOUNDS (only in a library built with QMM_DEBUG,
+ * whose kernels check every tile index against n_col_tiles * n_k_tiles, every block index against
+ * K / 32 and every ring slot against the ring's depth, and skip an access that fails) when such a
+ * check failed since the last read; else QMM_ERR_TIMEOUT when a pipelined kernel gave up on one of
  * its bounded waits (its outputs are then undefined); else QMM_ERR_RANGE when a qmm_matmul_ws /
  * qmm_matmul_noalloc call since the last read met an operand row the folded-scale GEMM cannot
  * represent exactly (that call's outputs may be off by more than the stated bound; qmm_matmul,

@@ -22,7 +22,9 @@ def orc():
 
 @pytest.fixture(autouse=True)
 def _device_status_clean(request):
-    """After every GPU test: no kernel of the library gave up a bounded wait (QMM_ERR_TIMEOUT)."""
+    """After every GPU test: no kernel of the library gave up a bounded wait (QMM_ERR_TIMEOUT) and, with
+    the library built with QMM_DEBUG (QMM_DEBUG=1 in the environment), no device bounds check failed
+    (QMM_ERR_BOUNDS)."""
     yield
     if request.node.get_closest_marker("gpu") is None:
         return
@@ -33,4 +35,5 @@ def _device_status_clean(request):
     import block_quantized_matmul_gb300 as qmm
 
     torch.cuda.synchronize()
-    assert qmm.qmm_device_status() == 0, "a kernel timed out a pipeline wait during this test"
+    st = qmm.qmm_device_status()
+    assert st == 0, f"device status {qmm._STATUS.get(st, st)} after this test"

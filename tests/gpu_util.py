@@ -2,6 +2,8 @@
 and through the CPU oracle, on the same seeded inputs."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 TYPES = ["q4_0", "q8_0", "iq4_nl", "mxfp4", "q4_1"]
@@ -97,3 +99,43 @@ def gpu_matmul_f32(type_, tiled, K, N, x: np.ndarray, ldx=None, ldy=None, x_offs
     qmm.qmm_matmul_f32(type_, tiled, K, N, rows, ldx, M, y, ldy)
     torch.cuda.synchronize()
     return y
+
+
+def _oracle_at_task(job):
+    """One worker's share of oracle_at_parallel: outputs of a few column tiles, re-indexed locally."""
+    import oracle as orc
+
+    type_, tiles, K, a_q, a_d, ms, ns = job
+    return orc.matmul_at(type_, tiles, K, a_q, a_d, ms, ns)
+
+
+def oracle_at_parallel(type_, tiled_ref: np.ndarray, K: int, a_q, a_d, ms, ns, workers=None):
+    """The oracle's Y[ms[i], ns[i]] and bounds, computed by a pool of processes started with spawn
+    (safe after CUDA is initialized).  Each task gets only the contiguous bytes of the column tiles it
+    needs (tile_idx = ct * n_k_tiles + kt, so a column tile is one byte range) and its points with
+    the column re-indexed into those tiles."""
+    import multiprocessing as mp
+
+    import oracle as orc
+
+    ms = np.asarray(ms, dtype=np.int64)
+    ns = np.asarray(ns, dtype=np.int64)
+    ct_bytes = (K // 32) * orc.tile_bytes(type_)
+    cts = ns // 32
+    uniq = np.unique(cts)
+    workers = workers or max(1, min(16, os.cpu_count() or 1))
+    groups = np.array_split(uniq, min(len(uniq), 4 * workers))
+    jobs, where = [], []
+    for grp in groups:
+        sel = np.nonzero(np.isin(cts, grp))[0]
+        local = np.searchsorted(grp, cts[sel])
+        tiles = np.concatenate([tiled_ref[c * ct_bytes:(c + 1) * ct_bytes] for c in grp])
+        jobs.append((type_, tiles, K, a_q, a_d, ms[sel], local * 32 + ns[sel] % 32))
+        where.append(sel)
+    y = np.empty(ms.size, np.float64)
+    b = np.empty(ms.size, np.float64)
+    with mp.get_context("spawn").Pool(workers) as pool:
+        for sel, (ys, bs) in zip(where, pool.map(_oracle_at_task, jobs)):
+            y[sel] = ys
+            b[sel] = bs
+    return y, b

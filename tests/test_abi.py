@@ -73,9 +73,9 @@ def test_iq4nl_table_matches_the_oracle(L, orc):
 
 
 def test_status_strings(L):
-    for st in range(7):
+    for st in range(8):
         assert L.qmm_status_str(st)
-    assert L.qmm_status_str(6) != L.qmm_status_str(99)
+    assert L.qmm_status_str(7) != L.qmm_status_str(99)
     assert L.qmm_status_str(99) == b"unknown status"
 
 

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 from block_quantized_matmul_gb300 import synth
-from tests.gpu_util import (TYPES, assert_within_bound, gpu_matmul, gpu_matmul_ws, gpu_prepare_weight,
+from tests.gpu_util import (TYPES, assert_within_bound, gpu_matmul, gpu_matmul_ws, gpu_prepare_weight, oracle_at_parallel,
                             gpu_quantize_act, torch_mod)
 
 pytestmark = pytest.mark.gpu
@@ -123,6 +123,8 @@ def test_gemm_is_deterministic(torch):
 
 FULL = [("q4_0", 4096, 14336, 512), ("q8_0", 4096, 128256, 128), ("mxfp4", 4096, 14336, 512),
         ("q4_1", 4096, 14336, 512)]
+# the prefill and batched lm-head workloads: checked on a dense grid (all rows x ~1024 or 4010 columns)
+DENSE = {("q4_0", 4096, 14336, 512), ("q8_0", 4096, 128256, 128)}
 
 
 @pytest.mark.parametrize("type_,K,N,M", FULL, ids=lambda v: str(v))
@@ -146,9 +148,18 @@ def test_gemm_full_size_sampled(torch, orc, type_, K, N, M):
     assert qmm.qmm_device_status() == 0
     rng = np.random.default_rng(1)
     n_ct = (N + 31) // 32
-    ns = np.concatenate([np.arange(n_ct) * 32 + rng.integers(0, 32, n_ct), [0, N - 1, N - 1]]).clip(0, N - 1)
-    ms = np.concatenate([rng.integers(0, M, n_ct), [0, M - 1, 0]])
-    ys, bs = orc.matmul_at(type_, tiled_ref, K, q_ref, d_ref, ms, ns)
+    if (type_, K, N, M) in DENSE:
+        # every token row x (one column in every column tile, random columns up to 1024 where there
+        # are fewer tiles, and both ends); the oracle runs on a spawned process pool
+        cols = np.arange(n_ct) * 32 + rng.integers(0, 32, n_ct)
+        cols = np.concatenate([cols, rng.integers(0, N, max(0, 1024 - n_ct - 2)), [0, N - 1]])
+        cols = np.unique(cols.clip(0, N - 1))
+        ms, ns = np.repeat(np.arange(M), cols.size), np.tile(cols, M)
+        ys, bs = oracle_at_parallel(type_, tiled_ref, K, q_ref, d_ref, ms, ns)
+    else:
+        ns = np.concatenate([np.arange(n_ct) * 32 + rng.integers(0, 32, n_ct), [0, N - 1, N - 1]]).clip(0, N - 1)
+        ms = np.concatenate([rng.integers(0, M, n_ct), [0, M - 1, 0]])
+        ys, bs = orc.matmul_at(type_, tiled_ref, K, q_ref, d_ref, ms, ns)
     assert_within_bound(y[ms, ns], ys, bs, f"gemm {type_} {K}x{N} M={M}")
     assert_within_bound(y_ws[ms, ns], ys, bs, f"gemm (workspace) {type_} {K}x{N} M={M}")
     assert np.isfinite(y).all() and np.isfinite(y_ws).all()

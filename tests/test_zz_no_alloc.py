@@ -4,8 +4,9 @@ Such callers (custom allocators or memory pools that must not see foreign alloca
 pre-plan all device memory, allocation-free critical sections) get the tensor-core path with its
 workspace in the library's fixed per-device scratch array.  This file is collected last on purpose.
 The test calls the C ABI (through the binding) twice in a row with different inputs -- the second
-call runs on scratch left dirty by the first -- and compares each result with the existing
-workspace entry point, qmm_matmul_ws, within the tolerance the other parity tests use.
+call runs on scratch left dirty by the first.  Each result must equal that of the existing workspace
+entry point, qmm_matmul_ws, bit for bit (the same kernels run on the same inputs), and the oracle's Y
+within the tolerance the other parity tests use.
 """
 import numpy as np
 import pytest
@@ -45,11 +46,12 @@ def test_noalloc_matches_workspace_entry_point_twice(torch, orc):
     for call, (M, seed) in enumerate([(300, 32), (130, 33)]):        # two calls in a row, different M
         x = synth.activations(M, K, seed=seed, outliers=True)
         a_q, a_d = gpu_quantize_act(x)
-        y_na = _noalloc(torch, type_, tiled, K, N, a_q, a_d, M).cpu().numpy()
-        y_ws = gpu_matmul_ws(type_, tiled, K, N, a_q, a_d, M).cpu().numpy()
+        y_na = _noalloc(torch, type_, tiled, K, N, a_q, a_d, M)
+        y_ws = gpu_matmul_ws(type_, tiled, K, N, a_q, a_d, M)
+        assert torch.equal(y_na, y_ws), f"noalloc differs from the workspace entry point, call {call}"
         q_ref, d_ref = orc.quantize_act(x)
-        _, bound = orc.matmul(type_, tiled_ref, K, N, q_ref, d_ref)
-        assert_within_bound(y_na, y_ws.astype(np.float64), bound, f"noalloc vs ws, call {call}")
+        y_ref, bound = orc.matmul(type_, tiled_ref, K, N, q_ref, d_ref)
+        assert_within_bound(y_na.cpu().numpy(), y_ref, bound, f"noalloc vs oracle, call {call}")
 
 
 def test_noalloc_decode_rows_and_size_limit(torch):
