@@ -177,13 +177,6 @@ __device__ __forceinline__ uint2 quantize_loaded(const float (&v)[8], float &da)
     return make_uint2(lo, hi);
 }
 
-// Both steps for one quarter: block kt of token tok.
-__device__ __forceinline__ uint2 quantize_quarter(const MvParams &p, bool live, int tok, int64_t kt, int q, float &da) {
-    float v[8];
-    load_quarter(p, live, tok, kt, q, v);
-    return quantize_loaded(v, da);
-}
-
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
@@ -271,18 +264,32 @@ __device__ __forceinline__ void decode_tile(const uint8_t *tile, int g, int t, u
                 H[q][3] = q4_biased<3>(w);
             } else {
 #pragma unroll
-                for (int r = 0; r < 4; ++r) H[q][r] = lut_lane[((w >> (8 * r)) & 0xFFu) * kLutCopies];
+                for (int r = 0; r < 4; ++r) H[q][r] = lut_lane[__byte_perm(w, 0u, 0x4440u | (uint32_t)r) * kLutCopies];
             }
         }
     }
 }
 
-// Staged fp16 activation pair (column 2cp, 2cp+1) for the biased decode: the odd column is divided
-// by 16 (exact) for Q4_0, whose high nibble is decoded as 16*hi.
+// Staged fp16 activation pairs (column 2cp, 2cp+1) for the biased decode, the odd column divided by 16
+// (exact) for the nibble types, whose high nibble is decoded as 16*hi; for a whole int8x4 word w
+// (columns c..c+3): lo = (c, c+1), hi = (c+2, c+3).  Byte b ^ 0x80
+// under the exponent byte 0x64 is the fp16 number 1152 + b (exact), and one fp16 subtract (or, for the
+// nibble types, an fma by (1, 1/16) minus (1152, 72)) leaves b (or b/16) exactly.
 template <int TYPE>
-__device__ __forceinline__ uint32_t act_pair(int a0, int a1) {
-    const float f1 = TileFmt<TYPE>::kNibbleInt ? (float)a1 * 0.0625f : (float)a1;
-    return h2_bits(__halves2half2(__float2half_rn((float)a0), __float2half_rn(f1)));
+__device__ __forceinline__ void act_pairs4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    const __half2 b01 = bits_h2(__byte_perm(x, 0x64646464u, 0x5140u));
+    const __half2 b23 = bits_h2(__byte_perm(x, 0x64646464u, 0x7362u));
+    if constexpr (TileFmt<TYPE>::kNibbleInt) {
+        const __half2 sc = __halves2half2(__float2half_rn(1.0f), __float2half_rn(0.0625f));
+        const __half2 off = __halves2half2(__float2half_rn(-1152.0f), __float2half_rn(-72.0f));
+        lo = h2_bits(__hfma2(b01, sc, off));
+        hi = h2_bits(__hfma2(b23, sc, off));
+    } else {
+        const __half2 off = __float2half2_rn(1152.0f);
+        lo = h2_bits(__hsub2(b01, off));
+        hi = h2_bits(__hsub2(b23, off));
+    }
 }
 // The exact bias of the biased weight decode for one (token, block).
 template <int TYPE>
@@ -429,13 +436,19 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     const int ctid = threadIdx.x - 32;        // 0..255
     const int g = lane >> 2, t = lane & 3;
 
-    // The byte -> half2 table depends on the parameters only: built before the wait.
-    if constexpr (TileFmt<TYPE>::kLut) {
-        for (int i = ctid; i < 256 * kLutCopies; i += kConsumerWarps * 32) {
-            const int b = i / kLutCopies;
-            lut_s[i] = h2_bits(__halves2half2(__int2half_rn(p.lut.v[b & 15]), __int2half_rn(p.lut.v[b >> 4])));
+    // Once the thread's first activation loads are in flight, it builds its share of the byte -> half2
+    // table (which depends on the parameters only) while they land.  Runs once per thread.
+    bool requested = false;
+    auto on_loads_issued = [&]() {
+        if (requested) return;
+        requested = true;
+        if constexpr (TileFmt<TYPE>::kLut) {
+            for (int i = ctid; i < 256 * kLutCopies; i += kConsumerWarps * 32) {
+                const int b = i / kLutCopies;
+                lut_s[i] = h2_bits(__halves2half2(__int2half_rn(p.lut.v[b & 15]), __int2half_rn(p.lut.v[b >> 4])));
+            }
         }
-    }
+    };
 
     // The weights never depend on the kernel launched just before on the stream, so the producer
     // starts streaming at once; the activations may, so the consumers wait for that grid first
@@ -445,9 +458,11 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     // ---- stage activations once: per (token, block) 16 half2 in fragment order, plus the
     //      per-block scale and the exact bias of the biased weight decode ----
     if constexpr (!FUSED) {
-        // two (token, block) entries per thread and pass, both loaded before either is converted
+        // two (token, block) entries per thread and pass, both loaded before either is converted (the
+        // loop runs warp-uniformly: every lane of a warp takes part in every pass)
         constexpr int kStep = kConsumerWarps * 32;
-        for (int i0 = ctid; i0 < TOK * nkc; i0 += 2 * kStep) {
+        for (int w0 = cw * 32; w0 < TOK * nkc; w0 += 2 * kStep) {
+            const int i0 = w0 + lane;
             uint4 ld[2][2];
             uint16_t dbits[2] = {0, 0};
 #pragma unroll
@@ -462,6 +477,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                     dbits[u] = p.a_d[(int64_t)tok * p.nkt + kt];
                 }
             }
+            on_loads_issued();
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const int i = i0 + u * kStep;
@@ -475,14 +491,9 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
                     uint32_t hp[16];                 // half2 of column pair cp, in cp order
 #pragma unroll
                     for (int wi = 0; wi < 8; ++wi) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int a0 = (int)(int8_t)((wv[wi] >> (16 * h)) & 0xFF);
-                            const int a1 = (int)(int8_t)((wv[wi] >> (16 * h + 8)) & 0xFF);
-                            sum_even += a0;
-                            sum_odd += a1;
-                            hp[2 * wi + h] = act_pair<TYPE>(a0, a1);
-                        }
+                        act_pairs4<TYPE>(wv[wi], hp[2 * wi], hp[2 * wi + 1]);
+                        sum_even = __dp4a((int)wv[wi], 0x00010001, sum_even);     // columns 4wi, 4wi + 2
+                        sum_odd = __dp4a((int)wv[wi], 0x01000100, sum_odd);       // columns 4wi + 1, 4wi + 3
                     }
                     // fragment order: position 4t + q holds column pair t + 4q
                     uint4 *dst = act_s + tok * tok_stride + j * 4;
@@ -504,19 +515,15 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
         for (int base = cw * 32; base < total; base += kConsumerWarps * 32) {
             const int e = base + lane, q = e & 3, jt = (e >> 2) / TOK, tok = (e >> 2) - jt * TOK;
             const bool live = e < total && tok < p.M;
-            float d;
-            const uint2 c = quantize_quarter(p, live, tok, p.kt0 + jt, q, d);
-            int sum_even = 0, sum_odd = 0;
+            float v[8], d;
+            load_quarter(p, live, tok, p.kt0 + jt, q, v);
+            on_loads_issued();
+            const uint2 c = quantize_loaded(v, d);
             uint32_t hp[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t w = u < 2 ? c.x : c.y;
-                const int a0 = (int)(int8_t)((w >> (16 * (u & 1))) & 0xFF);
-                const int a1 = (int)(int8_t)((w >> (16 * (u & 1) + 8)) & 0xFF);
-                sum_even += a0;
-                sum_odd += a1;
-                hp[u] = act_pair<TYPE>(a0, a1);
-            }
+            act_pairs4<TYPE>(c.x, hp[0], hp[1]);
+            act_pairs4<TYPE>(c.y, hp[2], hp[3]);
+            int sum_even = __dp4a((int)c.y, 0x00010001, __dp4a((int)c.x, 0x00010001, 0));
+            int sum_odd = __dp4a((int)c.y, 0x01000100, __dp4a((int)c.x, 0x01000100, 0));
             sum_even += __shfl_xor_sync(0xffffffffu, sum_even, 1);
             sum_odd += __shfl_xor_sync(0xffffffffu, sum_odd, 1);
             sum_even += __shfl_xor_sync(0xffffffffu, sum_even, 2);
@@ -533,6 +540,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
             }
         }
     }
+    on_loads_issued();             // threads that had no activation entries
     consumer_sync<CW>();
 
     // After a timed-out wait a warp stops waiting and computing but keeps the loop structure, so
@@ -785,7 +793,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
         return;
     }
 
-    const int cw = warp - 1, ctid = threadIdx.x - 32;
+    const int cw = warp - 1;
     const int i = lane & 7, j = lane >> 3;
 
     // the activations may come from the grid launched just before this one (see produce)
@@ -795,7 +803,8 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
     constexpr int kStageBatch = MT;
     const int total = MT * nkc * 4;
     if constexpr (!FUSED) {
-        for (int base = ctid; base < total; base += CW * 32 * kStageBatch) {
+        for (int w0 = cw * 32; w0 < total; w0 += CW * 32 * kStageBatch) {     // warp-uniform passes
+            const int base = w0 + lane;
             uint2 v[kStageBatch];
             uint16_t db[kStageBatch];
 #pragma unroll
