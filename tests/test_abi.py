@@ -225,3 +225,45 @@ def test_product_calls_cap_k(L):
     assert L.qmm_matmul_flat(1, P, K, 64, P, P, 1, P, 64, None) == INVALID
     # the weight-side calls are not products and keep the wider limit
     assert L.qmm_tiled_size(1, K, 64) > 0
+
+
+def test_debug_build_is_a_separate_library_with_the_checks_on(monkeypatch, tmp_path):
+    """build(debug=True) compiles every source with -DQMM_DEBUG into its own object folder and links
+    libqmm_debug.so; the release build passes no such flag (nothing is compiled here: nvcc is faked)."""
+    from block_quantized_matmul_gb300 import build
+
+    calls = []
+
+    class Done:
+        returncode = 0
+        stdout = stderr = ""
+
+    def fake_run(cmd, capture_output=True, text=True):
+        calls.append(cmd)
+        out = cmd[cmd.index("-o") + 1]
+        os.makedirs(os.path.dirname(out), exist_ok=True)
+        with open(out, "w") as f:
+            f.write("")
+        return Done()
+
+    monkeypatch.setattr(build.subprocess, "run", fake_run)
+    monkeypatch.setattr(build, "OBJ_DIR", str(tmp_path / "_build"))
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "libqmm.so"))
+    monkeypatch.setattr(build, "LIB_DEBUG", str(tmp_path / "libqmm_debug.so"))
+    assert build.build(force=True, debug=True) == str(tmp_path / "libqmm_debug.so")
+    compiles = [c for c in calls if "-c" in c]
+    assert compiles and all("-DQMM_DEBUG" in c for c in compiles)
+    assert all(os.path.dirname(c[c.index("-o") + 1]).endswith("_build_debug") for c in compiles)
+    calls.clear()
+    assert build.build(force=True, debug=False) == str(tmp_path / "libqmm.so")
+    assert not any("-DQMM_DEBUG" in c for c in calls)
+    # the environment switch selects the debug build by default
+    monkeypatch.setenv("QMM_DEBUG", "1")
+    calls.clear()
+    assert build.build(force=True) == str(tmp_path / "libqmm_debug.so")
+
+
+def test_bounds_status_is_documented(L):
+    assert L.qmm_status_str(7) == b"device bounds check failed (debug build)"
+    with open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qmm.h")) as f:
+        assert "QMM_ERR_BOUNDS = 7" in f.read()
