@@ -46,6 +46,12 @@ constexpr int kTilesPerWarp = 2;
 template <int TYPE>
 constexpr int kDp4aTilesPerWarp = TYPE == QMM_Q8_0 ? 2 : 4;
 constexpr int kDp4aMaxM = 4;                            // tokens up to which the int8 dot-product path runs
+// Parts per ring stage of the int8 path: each its own bulk copy and barrier, consumed by CW / parts
+// warps that take contiguous tiles, so a stage's first parts are worked on while the rest lands.  Four
+// for the 4-bit types, whose decode makes the work per byte large (Q4_0 K=N=4096: 3.64 -> 3.37 us);
+// one for Q8_0, which streams at the bandwidth limit and only pays for the extra copies (measured).
+template <int TYPE>
+constexpr int kDp4aSub = TYPE == QMM_Q8_0 ? 1 : 4;
 constexpr int kLutCopies = 32;                          // byte-indexed table copies (one per lane: no bank conflicts)
 constexpr int kActBudget = 64 * 1024;                   // bytes of staged activations per CTA
 constexpr int kSmemLimit = 227 * 1024;
@@ -94,11 +100,14 @@ __global__ void __launch_bounds__(64) selftest_wait_kernel(unsigned long long li
     if ((threadIdx.x & 31) == 0) out[warp] = ok ? 1 : 0;
 }
 // Producer warp: streams the K tiles [kt0, kt0 + nkc) of every column tile this CTA owns into the
-// ring, one stage of TPS consecutive tiles per 1-D bulk copy, and returns once the copies in
-// flight have landed.
-template <int TS, int TPS>
+// ring, one stage of TPS consecutive tiles at a time in NSUB 1-D bulk copies of TPS / NSUB tiles, each
+// completing its own barrier full[stage * NSUB + q] (so the consumers of the first part of a stage can
+// start before the rest has landed), and returns once the copies in flight have landed.
+template <int TS, int TPS, int NSUB = 1>
 __device__ __forceinline__ void produce(const MvParams &p, uint8_t *ring, uint64_t *full, uint64_t *empty,
                                         volatile int *abort, int lane) {
+    static_assert(TPS % NSUB == 0, "sub-copies split a stage evenly");
+    constexpr int kSubTiles = TPS / NSUB;
     const int stages = p.stages, nkc = p.nkc;
     uint32_t it = 0;
     bool ok = true;
@@ -110,14 +119,18 @@ __device__ __forceinline__ void produce(const MvParams &p, uint8_t *ring, uint64
             if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort)) { ok = false; break; }
             if (lane == 0) {
                 const int nt = (nkc - j0) < TPS ? (nkc - j0) : TPS;
-                const uint32_t bytes = (uint32_t)(nt * TS);
-                const uint32_t fb = smem_u32(&full[s]);
-                // tiles [ct * nkt + kt0 + j0, + nt) of this column tile, into ring slot s
-                if (QMM_DCHECK(s < stages && ct < p.n_col_tiles && p.kt0 + j0 + nt <= p.nkt)) {
-                    mbar_arrive_expect_tx(fb, bytes);
-                    bulk_g2s(smem_u32(ring + s * TPS * TS), src + (int64_t)j0 * TS, bytes, fb);
-                } else {
-                    mbar_arrive(fb);
+#pragma unroll
+                for (int q = 0; q < NSUB; ++q) {
+                    // tiles [ct * nkt + kt0 + j0 + t0, .. + t1) of this column tile, into ring slot s
+                    const int t0 = q * kSubTiles, t1 = (t0 + kSubTiles) < nt ? (t0 + kSubTiles) : nt;
+                    const uint32_t fb = smem_u32(&full[s * NSUB + q]);
+                    if (t1 > t0 && QMM_DCHECK(s < stages && ct < p.n_col_tiles && p.kt0 + j0 + t1 <= p.nkt)) {
+                        const uint32_t bytes = (uint32_t)((t1 - t0) * TS);
+                        mbar_arrive_expect_tx(fb, bytes);
+                        bulk_g2s(smem_u32(ring + (s * TPS + t0) * TS), src + (int64_t)(j0 + t0) * TS, bytes, fb);
+                    } else {
+                        mbar_arrive(fb);           // nothing of this part in a short last stage
+                    }
                 }
             }
             __syncwarp();
@@ -128,7 +141,7 @@ __device__ __forceinline__ void produce(const MvParams &p, uint8_t *ring, uint64
         const uint32_t last = it - 1;
         for (uint32_t k = 0; k < (uint32_t)stages && k <= last; ++k) {
             const uint32_t i = last - k;
-            wait_drain(smem_u32(&full[i % stages]), (i / stages) & 1u);
+            for (int q = 0; q < NSUB; ++q) wait_drain(smem_u32(&full[(i % stages) * NSUB + q]), (i / stages) & 1u);
         }
     }
 }
@@ -750,7 +763,7 @@ __host__ __device__ inline Dp4aLayout dp4a_layout(int nkc, int stages) {
     int off = 0;
     L.ring = off;  off += stages * CW * TPW * TS;
     off = (off + 15) & ~15;
-    L.bars = off;  off += 2 * stages * 8 + 16;
+    L.bars = off;  off += (kDp4aSub<TYPE> + 1) * stages * 8 + 16;   // full [stage][part], empty [stage], abort flag
     off = (off + 15) & ~15;
     L.act = off;   off += MT * nkc * 4 * 16;                 // [nkc][MT][4] uint4
     L.red = off;   off += CW * MT * 32 * 4;                  // [CW][MT][32] float
@@ -768,7 +781,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
     const Dp4aLayout L = dp4a_layout<TYPE, MT, CW, TPW>(p.nkc, p.stages);
     uint8_t *ring = smem + L.ring;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *empty = full + p.stages;
+    uint64_t *empty = full + p.stages * kDp4aSub<TYPE>;     // full: [stage][part]
     volatile int *abort = reinterpret_cast<volatile int *>(empty + p.stages);
     uint4 *act_s = reinterpret_cast<uint4 *>(smem + L.act);
     float *red_s = reinterpret_cast<float *>(smem + L.red);
@@ -777,7 +790,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
+            for (int q = 0; q < kDp4aSub<TYPE>; ++q) mbar_init(smem_u32(&full[s * kDp4aSub<TYPE> + q]), 1);
             mbar_init(smem_u32(&empty[s]), CW);
         }
         *abort = 0;
@@ -789,7 +802,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
-        produce<TS, kTilesPerStage>(p, ring, full, empty, abort, lane);
+        produce<TS, kTilesPerStage, kDp4aSub<TYPE>>(p, ring, full, empty, abort, lane);
         return;
     }
 
@@ -862,18 +875,20 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
         for (int j0 = 0; j0 < nkc; j0 += kTilesPerStage, ++it) {
             const int s = (int)(it % (uint32_t)stages);
             const uint32_t ph = (it / (uint32_t)stages) & 1u;
-            if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
+            // warp cw takes tiles cw * TPW .. cw * TPW + TPW - 1 of the stage, which arrive with part
+            // cw / (CW / kDp4aSub<TYPE>) of its copies
+            if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s * kDp4aSub<TYPE> + cw / (CW / kDp4aSub<TYPE>)]), ph, abort));
             if (ok && QMM_DCHECK(s < stages)) {
-                // tiles cw, cw + CW, ... of the stage; only the last stage of a pass can be partial
-                const uint8_t *tile = ring + (s * kTilesPerStage + cw) * TS;
-                const uint4 *act = act_s + (j0 + cw) * MT * 4;
+                // only the last stage of a pass can be partial
+                const uint8_t *tile = ring + (s * kTilesPerStage + cw * TPW) * TS;
+                const uint4 *act = act_s + (j0 + cw * TPW) * MT * 4;
                 if (j0 + kTilesPerStage <= nkc) {
 #pragma unroll
-                    for (int u = 0; u < TPW; ++u) dp4a_tile<TYPE, MT>(tile + CW * u * TS, act + CW * u * MT * 4, i, j, tb, acc);
+                    for (int u = 0; u < TPW; ++u) dp4a_tile<TYPE, MT>(tile + u * TS, act + u * MT * 4, i, j, tb, acc);
                 } else {
 #pragma unroll
                     for (int u = 0; u < TPW; ++u)
-                        if (j0 + cw + CW * u < nkc) dp4a_tile<TYPE, MT>(tile + CW * u * TS, act + CW * u * MT * 4, i, j, tb, acc);
+                        if (j0 + cw * TPW + u < nkc) dp4a_tile<TYPE, MT>(tile + u * TS, act + u * MT * 4, i, j, tb, acc);
                 }
             }
             __syncwarp();
