@@ -1069,6 +1069,9 @@ cudaError_t run(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a, int
 constexpr int kFlatKB = 32;            // blocks per row and stage
 constexpr int kFlatCW = 16;            // consumer warps
 constexpr int kFlatMT = 4;             // tokens per launch
+// Parts per stage: 8-row tensor copies, each completing its own barrier; warp w takes rows 2w and
+// 2w + 1, so the warps of a stage's first rows compute while the rest lands.
+constexpr int kFlatSub = 4;
 
 template <int TYPE>
 struct FlatFmt {
@@ -1102,7 +1105,7 @@ __host__ __device__ inline FlatLayout flat_layout(int nkc, int stages) {
     int off = 0;
     L.ring = off;  off += stages * 32 * kFlatKB * FlatFmt<TYPE>::kBlock;
     off += 16;                                                // word reads of the last block run past the ring
-    L.bars = off;  off += 2 * stages * 8 + 16;
+    L.bars = off;  off += (kFlatSub + 1) * stages * 8 + 16;  // full [stage][part], empty [stage], abort flag
     off = (off + 15) & ~15;
     L.act = off;   off += MT * nkc * 32;                      // [MT][nkc] 32 int8 in the decode order
     L.aux = off;   off += MT * nkc * 8;                       // [MT][nkc] {fp32 d_a, int corr or sum}
@@ -1225,7 +1228,7 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
     const FlatLayout L = flat_layout<TYPE, MT>(p.nkc, p.stages);
     uint8_t *ring = smem + L.ring;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *empty = full + p.stages;
+    uint64_t *empty = full + p.stages * kFlatSub;           // full: [stage][part]
     volatile int *abort = reinterpret_cast<volatile int *>(empty + p.stages);
     uint32_t *act_w = reinterpret_cast<uint32_t *>(smem + L.act);
     uint2 *act_x = reinterpret_cast<uint2 *>(smem + L.aux);
@@ -1234,7 +1237,7 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
+            for (int q = 0; q < kFlatSub; ++q) mbar_init(smem_u32(&full[s * kFlatSub + q]), 1);
             mbar_init(smem_u32(&empty[s]), kFlatCW);
         }
         *abort = 0;
@@ -1244,8 +1247,8 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
-        // ---- producer: per chunk and stage, one 2-D tensor copy of 32 rows x kFlatKB blocks (rows past
-        // N and blocks past the row end arrive as zeros and are never used) ----
+        // ---- producer: per chunk and stage, kFlatSub 2-D tensor copies of 32 / kFlatSub rows x kFlatKB
+        // blocks (rows past N and blocks past the row end arrive as zeros and are never used) ----
         uint32_t it = 0;
         bool ok = true;
         for (int64_t ch = blockIdx.x; ch < p.n_chunks && ok; ch += gridDim.x) {
@@ -1254,13 +1257,18 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
                 const uint32_t ph = (it / (uint32_t)stages) & 1u;
                 if (!__all_sync(0xffffffffu, wait_bounded(smem_u32(&empty[s]), ph ^ 1u, abort))) { ok = false; break; }
                 if (lane == 0) {
-                    const uint32_t fb = smem_u32(&full[s]);
-                    // rows ch*32.. of blocks kt0 + kb0.. into ring slot s
-                    if (QMM_DCHECK(s < stages && ch < p.n_chunks && p.kt0 + kb0 < p.nkt)) {
-                        mbar_arrive_expect_tx(fb, (uint32_t)(32 * kRowStage));
-                        tma_load_2d(smem_u32(ring + s * 32 * kRowStage), &w_map, (p.kt0 + kb0) * BB / 8, (int)(ch * 32), fb);
-                    } else {
-                        mbar_arrive(fb);
+#pragma unroll
+                    for (int q = 0; q < kFlatSub; ++q) {
+                        constexpr int kRows = 32 / kFlatSub;
+                        const uint32_t fb = smem_u32(&full[s * kFlatSub + q]);
+                        // rows ch*32 + kRows*q .. of blocks kt0 + kb0.. into part q of ring slot s
+                        if (QMM_DCHECK(s < stages && ch < p.n_chunks && p.kt0 + kb0 < p.nkt)) {
+                            mbar_arrive_expect_tx(fb, (uint32_t)(kRows * kRowStage));
+                            tma_load_2d(smem_u32(ring + (s * 32 + kRows * q) * kRowStage), &w_map, (p.kt0 + kb0) * BB / 8,
+                                        (int)(ch * 32 + kRows * q), fb);
+                        } else {
+                            mbar_arrive(fb);
+                        }
                     }
                 }
                 __syncwarp();
@@ -1270,7 +1278,7 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
             const uint32_t last = it - 1;
             for (uint32_t k = 0; k < (uint32_t)stages && k <= last; ++k) {
                 const uint32_t i = last - k;
-                wait_drain(smem_u32(&full[i % stages]), (i / stages) & 1u);
+                for (int q = 0; q < kFlatSub; ++q) wait_drain(smem_u32(&full[(i % stages) * kFlatSub + q]), (i / stages) & 1u);
             }
         }
         return;
@@ -1310,7 +1318,8 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
         for (int kb0 = 0; kb0 < nkc; kb0 += kFlatKB, ++it) {
             const int s = (int)(it % (uint32_t)stages);
             const uint32_t ph = (it / (uint32_t)stages) & 1u;
-            if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s]), ph, abort));
+            // rows 2cw, 2cw + 1 arrive with part cw / (kFlatCW / kFlatSub) of the stage
+            if (ok) ok = __all_sync(0xffffffffu, wait_bounded(smem_u32(&full[s * kFlatSub + cw / (kFlatCW / kFlatSub)]), ph, abort));
             const int jt = kb0 + lane;                         // this lane's block
             if (ok && jt < nkc) {
                 const uint8_t *st = ring + s * 32 * kRowStage;
@@ -1325,7 +1334,7 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
                 }
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const int row = cw + 16 * r;
+                    const int row = 2 * cw + r;
                     uint32_t W[8];
                     float dw, mw;
                     if constexpr (TYPE == QMM_Q4_K)
@@ -1362,7 +1371,7 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
                 float v = acc[r][t];
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                const int64_t n = ch * 32 + cw + 16 * r;
+                const int64_t n = ch * 32 + 2 * cw + r;
                 if (ok && lane == 0 && t < p.M && n < p.N) {
                     float *dst = p.y + (int64_t)t * p.ldy + n;
                     *dst = p.accumulate ? (*dst + v) : v;
@@ -1392,10 +1401,11 @@ cudaError_t run_flat(const uint8_t *flat, int64_t K, int64_t N, const int8_t *a_
     const int64_t n_chunks = (N + 31) / 32;
     int64_t grid = num_sms();
     if (grid > n_chunks) grid = n_chunks;
-    // The flat weight as N rows of row_bytes / 8 eight-byte words; one box = 32 rows x kFlatKB blocks.
+    // The flat weight as N rows of row_bytes / 8 eight-byte words; one box = 32 / kFlatSub rows x kFlatKB
+    // blocks (a stage part).
     alignas(64) CUtensorMap w_map;
     e = make_map_2d(&w_map, CU_TENSOR_MAP_DATA_TYPE_UINT64, flat, (uint64_t)(nkt * BB / 8), (uint64_t)N,
-                    (uint64_t)(nkt * BB), (uint32_t)(kFlatKB * BB / 8), 32u, CU_TENSOR_MAP_SWIZZLE_NONE);
+                    (uint64_t)(nkt * BB), (uint32_t)(kFlatKB * BB / 8), (uint32_t)(32 / kFlatSub), CU_TENSOR_MAP_SWIZZLE_NONE);
     if (e != cudaSuccess) return e;
     for (int64_t kt0 = 0; kt0 < nkt; kt0 += nkc) {
         FlatParams p;
