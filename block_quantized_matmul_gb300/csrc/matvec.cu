@@ -756,14 +756,18 @@ __device__ __forceinline__ void dp4a_tile(const uint8_t *tile, const uint4 *act,
 struct Dp4aLayout {
     int ring, bars, act, red, total;
 };
+// The barriers come first, sized for the deepest ring (kMaxRingStages), so that their place does not
+// depend on the launch parameters: thread 0 initialises them while the parameters are still being
+// fetched at kernel start.
+constexpr int kMaxRingStages = 12;
 template <int TYPE, int MT, int CW, int TPW>
 __host__ __device__ inline Dp4aLayout dp4a_layout(int nkc, int stages) {
     constexpr int TS = TileFmt<TYPE>::kBytes;
     Dp4aLayout L;
     int off = 0;
+    L.bars = off;  off += (kDp4aSub<TYPE> + 1) * kMaxRingStages * 8 + 16;   // full [stage][part], empty [stage], abort flag
+    off = (off + 127) & ~127;
     L.ring = off;  off += stages * CW * TPW * TS;
-    off = (off + 15) & ~15;
-    L.bars = off;  off += (kDp4aSub<TYPE> + 1) * stages * 8 + 16;   // full [stage][part], empty [stage], abort flag
     off = (off + 15) & ~15;
     L.act = off;   off += MT * nkc * 4 * 16;                 // [nkc][MT][4] uint4
     L.red = off;   off += CW * MT * 32 * 4;                  // [CW][MT][32] float
@@ -781,15 +785,18 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
     const Dp4aLayout L = dp4a_layout<TYPE, MT, CW, TPW>(p.nkc, p.stages);
     uint8_t *ring = smem + L.ring;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *empty = full + p.stages * kDp4aSub<TYPE>;     // full: [stage][part]
-    volatile int *abort = reinterpret_cast<volatile int *>(empty + p.stages);
+    uint64_t *empty = full + kMaxRingStages * kDp4aSub<TYPE>;     // full: [stage][part]
+    volatile int *abort = reinterpret_cast<volatile int *>(empty + kMaxRingStages);
     uint4 *act_s = reinterpret_cast<uint4 *>(smem + L.act);
     float *red_s = reinterpret_cast<float *>(smem + L.red);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stages = p.stages, nkc = p.nkc;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
+        // every stage the ring could have: no dependence on the launch parameters
+#pragma unroll
+        for (int s = 0; s < kMaxRingStages; ++s) {
+#pragma unroll
             for (int q = 0; q < kDp4aSub<TYPE>; ++q) mbar_init(smem_u32(&full[s * kDp4aSub<TYPE> + q]), 1);
             mbar_init(smem_u32(&empty[s]), CW);
         }
@@ -939,7 +946,7 @@ Plan plan_ring(int nkc, int fixed_bytes) {
     const int stage_bytes = kTilesPerStage * TS + 16;
     const int budget = (CW == 16) ? kSmemLimit : kSmemLimit / 2;
     const int st = (budget - 1024 - fixed_bytes - 128) / stage_bytes;
-    pl.stages = st > 12 ? 12 : (st < 2 ? 2 : st);
+    pl.stages = st > kMaxRingStages ? kMaxRingStages : (st < 2 ? 2 : st);
     pl.ctas_per_sm = 16 / CW;
     return pl;
 }
