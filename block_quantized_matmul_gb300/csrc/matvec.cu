@@ -54,6 +54,10 @@ template <int TYPE>
 constexpr int kDp4aSub = TYPE == QMM_Q8_0 ? 1 : 4;
 constexpr int kLutCopies = 32;                          // byte-indexed table copies (one per lane: no bank conflicts)
 constexpr int kActBudget = 64 * 1024;                   // bytes of staged activations per CTA
+// Deepest ring of the tiled decode kernels.  Their barriers come first in shared memory, laid out for
+// this many stages, so that their place does not depend on the launch parameters: thread 0
+// initialises them while the parameters are still being fetched at kernel start.
+constexpr int kMaxRingStages = 12;
 constexpr int kSmemLimit = 227 * 1024;
 using namespace pipe;
 
@@ -327,9 +331,9 @@ __host__ __device__ inline MvLayout mv_layout(int M, int nkc, int stages) {
     constexpr int kTilesPerStage = CW * kTilesPerWarp;
     MvLayout L;
     int off = 0;
+    L.bars = off;  off += 2 * kMaxRingStages * 8 + 16;       // full, empty, abort flag: a fixed place
+    off = (off + 127) & ~127;
     L.ring = off;  off += stages * kTilesPerStage * TS;
-    off = (off + 15) & ~15;
-    L.bars = off;  off += 2 * stages * 8 + 16;
     off = (off + 15) & ~15;
     L.act = off;   off += M * act_tok_stride(nkc) * 16;     // [M][stride] uint4 (16 half2 per block)
     L.da = off;    off += nkc * 8 * NF * 4;                 // [nkc][8*NF] float
@@ -412,8 +416,8 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     const MvLayout L = mv_layout<TYPE, NF, CW>(p.M, p.nkc, p.stages);
     uint8_t *ring = smem + L.ring;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *empty = full + p.stages;
-    volatile int *abort = reinterpret_cast<volatile int *>(empty + p.stages);
+    uint64_t *empty = full + kMaxRingStages;
+    volatile int *abort = reinterpret_cast<volatile int *>(empty + kMaxRingStages);
     uint4 *act_s = reinterpret_cast<uint4 *>(smem + L.act);      // [M][act_tok_stride] uint4
     const int tok_stride = act_tok_stride(p.nkc);
     float *da_s = reinterpret_cast<float *>(smem + L.da);         // [nkc][TOK]
@@ -427,7 +431,9 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_kernel(const Mv
     const int nkc = p.nkc;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
+        // every stage the ring could have: no dependence on the launch parameters
+#pragma unroll
+        for (int s = 0; s < kMaxRingStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), kConsumerWarps);
         }
@@ -756,10 +762,6 @@ __device__ __forceinline__ void dp4a_tile(const uint8_t *tile, const uint4 *act,
 struct Dp4aLayout {
     int ring, bars, act, red, total;
 };
-// The barriers come first, sized for the deepest ring (kMaxRingStages), so that their place does not
-// depend on the launch parameters: thread 0 initialises them while the parameters are still being
-// fetched at kernel start.
-constexpr int kMaxRingStages = 12;
 template <int TYPE, int MT, int CW, int TPW>
 __host__ __device__ inline Dp4aLayout dp4a_layout(int nkc, int stages) {
     constexpr int TS = TileFmt<TYPE>::kBytes;
@@ -1079,6 +1081,7 @@ constexpr int kFlatMT = 4;             // tokens per launch
 // Parts per stage: 8-row tensor copies, each completing its own barrier; warp w takes rows 2w and
 // 2w + 1, so the warps of a stage's first rows compute while the rest lands.
 constexpr int kFlatSub = 4;
+constexpr int kFlatMaxStages = 8;      // ring depth cap; the barriers are laid out for this many
 
 template <int TYPE>
 struct FlatFmt {
@@ -1110,9 +1113,10 @@ template <int TYPE, int MT>
 __host__ __device__ inline FlatLayout flat_layout(int nkc, int stages) {
     FlatLayout L;
     int off = 0;
+    L.bars = off;  off += (kFlatSub + 1) * kFlatMaxStages * 8 + 16;   // full [stage][part], empty [stage], abort flag
+    off = (off + 127) & ~127;
     L.ring = off;  off += stages * 32 * kFlatKB * FlatFmt<TYPE>::kBlock;
     off += 16;                                                // word reads of the last block run past the ring
-    L.bars = off;  off += (kFlatSub + 1) * stages * 8 + 16;  // full [stage][part], empty [stage], abort flag
     off = (off + 15) & ~15;
     L.act = off;   off += MT * nkc * 32;                      // [MT][nkc] 32 int8 in the decode order
     L.aux = off;   off += MT * nkc * 8;                       // [MT][nkc] {fp32 d_a, int corr or sum}
@@ -1235,15 +1239,18 @@ __global__ void __launch_bounds__(32 * (1 + kFlatCW), 1)
     const FlatLayout L = flat_layout<TYPE, MT>(p.nkc, p.stages);
     uint8_t *ring = smem + L.ring;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
-    uint64_t *empty = full + p.stages * kFlatSub;           // full: [stage][part]
-    volatile int *abort = reinterpret_cast<volatile int *>(empty + p.stages);
+    uint64_t *empty = full + kFlatMaxStages * kFlatSub;     // full: [stage][part]
+    volatile int *abort = reinterpret_cast<volatile int *>(empty + kFlatMaxStages);
     uint32_t *act_w = reinterpret_cast<uint32_t *>(smem + L.act);
     uint2 *act_x = reinterpret_cast<uint2 *>(smem + L.aux);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stages = p.stages, nkc = p.nkc;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
+        // every stage the ring could have: no dependence on the launch parameters
+#pragma unroll
+        for (int s = 0; s < kFlatMaxStages; ++s) {
+#pragma unroll
             for (int q = 0; q < kFlatSub; ++q) mbar_init(smem_u32(&full[s * kFlatSub + q]), 1);
             mbar_init(smem_u32(&empty[s]), kFlatCW);
         }
@@ -1399,7 +1406,7 @@ cudaError_t run_flat(const uint8_t *flat, int64_t K, int64_t N, const int8_t *a_
     const int fixed = flat_layout<TYPE, MT>((int)nkc, 0).total;
     const int stage_bytes = 32 * kFlatKB * BB + 16;
     int st = (kSmemLimit - 1024 - fixed - 128) / stage_bytes;
-    st = st > 8 ? 8 : (st < 2 ? 2 : st);
+    st = st > kFlatMaxStages ? kFlatMaxStages : (st < 2 ? 2 : st);
     const size_t smem = (size_t)flat_layout<TYPE, MT>((int)nkc, st).total + 128;
     auto kern = matvec_flat_kernel<TYPE, MT>;
     static int attr_done[4] = {0, 0, 0, 0};
