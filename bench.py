@@ -12,9 +12,10 @@ weight is repacked once beforehand, as at model load.
           K consecutive steps captured in one CUDA graph and timed with CUDA events on the launching
           stream, rotating through enough weight copies that the working set exceeds the 129 MB L2
           (no step hits a weight left in L2 by the previous one).
-  e2e     the same metric through the C ABI with host buffers (eager launches): each step hands the
-          call its pinned host activation and output buffers, which the kernel reads and writes over
-          NVLink-C2C; the variant with explicit copies to and from device buffers is reported beside.
+  e2e     the same metric through the C ABI with host buffers (eager launches): each step hands
+          qmm_matmul_f32_ws its pinned host activation and output buffers (and a device workspace made
+          once): x crosses NVLink-C2C once into the workspace, y is written over the link.  Beside it:
+          qmm_matmul_f32 without a workspace, and explicit copies to and from device buffers.
   roofline  the decode matvec alone: algorithmic bytes (weight tiles + activation quants and
           scales + fp32 output) per launch / mean launch time (a graph of back-to-back launches
           timed with CUDA events), against the measured HBM copy bandwidth.
@@ -409,15 +410,23 @@ def run_gpu(args):
     wl_launches = wl.launches_per_step()
 
     # end to end through the C ABI with host buffers (pinned), eager launches.  The call is given the
-    # host buffers themselves: the kernel reads x from and writes y to host memory over NVLink-C2C.
-    # The same step with an explicit host-to-device copy, the call on device buffers and a
-    # device-to-host copy is reported beside it.
+    # host buffers themselves and a device workspace (allocated once, as at start-up): a first kernel
+    # copies x over NVLink-C2C into the workspace, the decode kernel writes y to host memory.  Beside
+    # it: the same call without a workspace (the decode kernel reads x over the link, once per
+    # thread-block cluster), and an explicit host-to-device copy, the call on device buffers and a
+    # device-to-host copy.
     x_host = torch.empty((wl.n_act, M, K), dtype=torch.float32).pin_memory()
     x_host.copy_(wl.x.cpu())
     y_host = torch.empty((M, N), dtype=torch.float32).pin_memory()
     x_dev = torch.empty((M, K), dtype=torch.float32, device="cuda")
+    ws_bytes = qmm.matmul_f32_workspace_size(M, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
 
     def e2e_step(i, s):
+        qmm.qmm_matmul_f32_ws(type_, wl.tiled[i % wl.copies], K, N, x_host[i % wl.n_act], K, M, y_host, N, ws,
+                              ws_bytes, stream=s)
+
+    def e2e_nows_step(i, s):
         qmm.qmm_matmul_f32(type_, wl.tiled[i % wl.copies], K, N, x_host[i % wl.n_act], K, M, y_host, N, stream=s)
 
     def e2e_copy_step(i, s):
@@ -432,10 +441,15 @@ def run_gpu(args):
             torch.cuda.synchronize()
             return time_steps(torch, fn, args.steps, stream)
 
-    e2e_ms, e2e_copy_ms = e2e_time(e2e_step), e2e_time(e2e_copy_step)
+    e2e_ms, e2e_nows_ms, e2e_copy_ms = e2e_time(e2e_step), e2e_time(e2e_nows_step), e2e_time(e2e_copy_step)
     e2e = {"value": round(wl.tiled_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": M * K * 4, "d2h_bytes_per_step": M * N * 4, "ms_per_step": round(e2e_ms, 5),
-           "transfer": "host buffers passed to the call; the kernel reads x and writes y over NVLink-C2C",
+           "transfer": "qmm_matmul_f32_ws with pinned host x and y and a device workspace: one kernel copies x "
+                       "over NVLink-C2C, the decode kernel writes y over it",
+           "without_workspace": {"value": round(wl.tiled_bytes * world / (e2e_nows_ms * 1e-3) / 1e9, 1),
+                                 "unit": "GB/s", "ms_per_step": round(e2e_nows_ms, 5),
+                                 "transfer": "qmm_matmul_f32 with pinned host x and y: the decode kernel reads x "
+                                             "over NVLink-C2C once per thread-block cluster"},
            "with_copies": {"value": round(wl.tiled_bytes * world / (e2e_copy_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                            "ms_per_step": round(e2e_copy_ms, 5),
                            "transfer": "cudaMemcpyAsync host-to-device, the call on device buffers, "

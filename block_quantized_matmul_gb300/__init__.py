@@ -90,9 +90,12 @@ def lib():
         L.qmm_matmul_noalloc.argtypes = [i32, vp, i64, i64, vp, vp, i64, vp, i64, vp]
         L.qmm_matmul_noalloc_max_workspace.argtypes = []
         L.qmm_matmul_noalloc_max_workspace.restype = sz
+        L.qmm_matmul_f32_workspace_size.argtypes = [i64, i64]
+        L.qmm_matmul_f32_workspace_size.restype = sz
+        L.qmm_matmul_f32_ws.argtypes = [i32, vp, i64, i64, vp, i64, i64, vp, i64, vp, sz, vp]
         for fn in ("qmm_quantize_weight", "qmm_repack", "qmm_unpack", "qmm_quantize_act", "qmm_matmul",
                    "qmm_matmul_path", "qmm_device_status", "qmm_matmul_ws", "qmm_matmul_noalloc", "qmm_matmul_f32",
-                   "qmm_matmul_flat", "qmm_selftest_timeout"):
+                   "qmm_matmul_flat", "qmm_selftest_timeout", "qmm_matmul_f32_ws"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -111,6 +114,14 @@ def _ptr(x) -> int | None:
         return x
     if not x.is_cuda and not x.is_pinned():
         raise ValueError("libqmm takes CUDA tensors or pinned host tensors only")
+    return x.data_ptr()
+
+
+def _ptr_located(x) -> int | None:
+    """Address of a tensor for the calls that check on their own where x and y point (device or
+    page-locked host memory; pageable memory is refused by the library): no host-side query here."""
+    if x is None or isinstance(x, int):
+        return x
     return x.data_ptr()
 
 
@@ -179,8 +190,19 @@ def qmm_matmul(type_, w_tiled, K: int, N: int, a_q, a_d, M: int, y, ldy: int, st
 
 
 def qmm_matmul_f32(type_, w_tiled, K: int, N: int, x, ldx: int, M: int, y, ldy: int, stream=None) -> None:
-    _check("qmm_matmul_f32", lib().qmm_matmul_f32(_t(type_), _ptr(w_tiled), K, N, _ptr(x), ldx, M, _ptr(y), ldy,
-                                                  _stream(stream)))
+    _check("qmm_matmul_f32", lib().qmm_matmul_f32(_t(type_), _ptr(w_tiled), K, N, _ptr_located(x), ldx, M,
+                                                  _ptr_located(y), ldy, _stream(stream)))
+
+
+def matmul_f32_workspace_size(M: int, K: int) -> int:
+    return int(lib().qmm_matmul_f32_workspace_size(M, K))
+
+
+def qmm_matmul_f32_ws(type_, w_tiled, K: int, N: int, x, ldx: int, M: int, y, ldy: int, workspace,
+                      workspace_bytes: int, stream=None) -> None:
+    _check("qmm_matmul_f32_ws", lib().qmm_matmul_f32_ws(_t(type_), _ptr(w_tiled), K, N, _ptr_located(x), ldx, M,
+                                                        _ptr_located(y), ldy, _ptr(workspace), int(workspace_bytes),
+                                                        _stream(stream)))
 
 
 def qmm_matmul_flat(type_, w_flat, K: int, N: int, a_q, a_d, M: int, y, ldy: int, stream=None) -> None:

@@ -25,7 +25,10 @@
 //     on sm_103a, where int8 tcgen05 does not exist.
 //   * Per block the result is rescaled by d_w*d_a with packed f32x2 arithmetic and accumulated.
 //   * The fused variants (qmm_matmul_f32) quantize the fp32 activation rows into shared memory
-//     themselves, by the rule of qmm_quantize_act, while the first weight stages stream in.
+//     themselves, by the rule of qmm_quantize_act, while the first weight stages stream in.  With the
+//     rows in host memory (read over NVLink-C2C, whose bytes set the cost) the int8 path runs in
+//     thread-block clusters: each CTA reads and quantizes only its share of the blocks and writes the
+//     records into every CTA of its cluster through distributed shared memory.
 //   * Flat GGML rows (matvec_flat_kernel, qmm_matmul_flat): 2-D tensor copies of 32 rows x 32 blocks,
 //     one block per lane, dp4a.
 //   * Launched as a programmatic dependent: weight streaming overlaps the end of the preceding grid
@@ -778,8 +781,12 @@ __host__ __device__ inline Dp4aLayout dp4a_layout(int nkc, int stages) {
 }
 
 // MT = token capacity (1, 2 or 4); p.M <= MT tokens are live.  TPW independent tiles per warp and stage.
-template <int TYPE, int MT, int CW, bool FUSED, int TPW>
+// SHARE_X (fused only, launched in clusters): CTA r of a cluster of C quantizes the blocks jt with
+// jt % C == r and stores each record into all C CTAs' shared memory; one thread per CTA then arrives
+// on every CTA's exchange barrier, which completes once all C CTAs have published their share.
+template <int TYPE, int MT, int CW, bool FUSED, int TPW, bool SHARE_X = false>
 __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(const MvParams p) {
+    static_assert(FUSED || !SHARE_X, "the shared staging quantizes fp32 rows");
     constexpr int kTilesPerStage = CW * TPW;
     constexpr int TS = TileFmt<TYPE>::kBytes;
     extern __shared__ uint8_t smem_raw[];
@@ -789,6 +796,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.bars);
     uint64_t *empty = full + kMaxRingStages * kDp4aSub<TYPE>;     // full: [stage][part]
     volatile int *abort = reinterpret_cast<volatile int *>(empty + kMaxRingStages);
+    uint64_t *xbar = empty + kMaxRingStages + 1;          // exchange barrier (SHARE_X), after the abort flag
     uint4 *act_s = reinterpret_cast<uint4 *>(smem + L.act);
     float *red_s = reinterpret_cast<float *>(smem + L.red);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -802,16 +810,22 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
             for (int q = 0; q < kDp4aSub<TYPE>; ++q) mbar_init(smem_u32(&full[s * kDp4aSub<TYPE> + q]), 1);
             mbar_init(smem_u32(&empty[s]), CW);
         }
+        if constexpr (SHARE_X) mbar_init(smem_u32(xbar), cluster_size());
         *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // SHARE_X: every thread signals the cluster barrier once, here (this CTA's barriers exist); each
+    // waits on it before it leaves or touches another CTA's barrier, so no CTA arrives on a barrier
+    // that is not initialised yet and none exits while its cluster peers may still write to it.
+    if constexpr (SHARE_X) asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
     // A grid launched after this one as a programmatic dependent may start now: it waits for this
     // grid to complete before it reads anything this grid writes.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == 0) {
         produce<TS, kTilesPerStage, kDp4aSub<TYPE>>(p, ring, full, empty, abort, lane);
+        if constexpr (SHARE_X) asm volatile("barrier.cluster.wait;" ::: "memory");
         return;
     }
 
@@ -824,6 +838,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
     // issues the loads of its records (up to MT of them at a time), then builds them
     constexpr int kStageBatch = MT;
     const int total = MT * nkc * 4;
+    bool x_ok = true;
     if constexpr (!FUSED) {
         for (int w0 = cw * 32; w0 < total; w0 += CW * 32 * kStageBatch) {     // warp-uniform passes
             const int base = w0 + lane;
@@ -847,7 +862,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
                     act_s[e] = tok < p.M ? dp4a_record(TYPE, v[u], q, __half2float(__ushort_as_half(db[u]))) : make_uint4(0u, 0u, 0u, 0u);
             }
         }
-    } else {
+    } else if constexpr (!SHARE_X) {
         // a record is made by the lane quad of its 4 quarters (all lanes of a warp iterate together)
         for (int base = cw * 32; base < total; base += CW * 32 * kStageBatch) {
             float v[kStageBatch][8];
@@ -864,6 +879,46 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
                 if (e < total) act_s[e] = tok < p.M ? dp4a_record(TYPE, c, q, da) : make_uint4(0u, 0u, 0u, 0u);
             }
         }
+    } else {
+        // this CTA's share: blocks jt = rank + C * l; local record index el = (l * MT + tok) * 4 + q
+        const int rank = (int)cluster_rank(), csize = (int)cluster_size();
+        const int nloc = (nkc - rank + csize - 1) / csize;
+        const int total_l = MT * nloc * 4;
+        for (int base = cw * 32; base < total_l; base += CW * 32 * kStageBatch) {
+            float v[kStageBatch][8];
+#pragma unroll
+            for (int u = 0; u < kStageBatch; ++u) {
+                const int el = base + u * CW * 32 + lane, q = el & 3, tok = (el >> 2) % MT;
+                const int jt = rank + csize * ((el >> 2) / MT);
+                load_quarter(p, el < total_l && tok < p.M, tok, p.kt0 + jt, q, v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kStageBatch; ++u) {
+                const int el = base + u * CW * 32 + lane, q = el & 3, tok = (el >> 2) % MT;
+                const int jt = rank + csize * ((el >> 2) / MT);
+                float da;
+                const uint2 c = quantize_loaded(v[u], da);
+                if (el < total_l && QMM_DCHECK(jt < nkc)) {
+                    const uint4 rec = tok < p.M ? dp4a_record(TYPE, c, q, da) : make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t dst = smem_u32(&act_s[(jt * MT + tok) * 4 + q]);
+                    for (int r = 0; r < csize; ++r) st_peer_v4(peer_addr(dst, (uint32_t)r), rec);
+                }
+            }
+        }
+        // publish: this CTA's stores are done (named barrier), then one thread releases them to every
+        // CTA of the cluster; every consumer thread then acquires all C shares
+        consumer_sync<CW>();
+        asm volatile("barrier.cluster.wait;" ::: "memory");
+        if (cw == 0 && lane == 0) {
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
+            for (int r = 0; r < csize; ++r) mbar_arrive_peer(peer_addr(smem_u32(xbar), (uint32_t)r));
+        }
+        if (!wait_cluster_bounded(smem_u32(xbar), 0u, abort, &g_mv_status, kWaitLimitNs)) {
+            // a share never came: keep this CTA (and its shared memory) alive for a late writer as
+            // long as a second bounded wait allows, then skip the tiles
+            wait_drain(smem_u32(xbar), 0u);
+            x_ok = false;
+        }
     }
     uint32_t tb[4] = {0u, 0u, 0u, 0u};
     if constexpr (TileFmt<TYPE>::kLut) {
@@ -876,6 +931,7 @@ __global__ void __launch_bounds__(32 * (1 + CW), 16 / CW) matvec_dp4a_kernel(con
 
     uint32_t it = 0;
     bool ok = true;
+    if constexpr (SHARE_X) ok = __all_sync(0xffffffffu, x_ok);
     for (int64_t ct = blockIdx.x; ct < p.n_col_tiles; ct += gridDim.x) {
         float2 acc[MT][2];           // per token: rows (4i, 4i+1), (4i+2, 4i+3)
 #pragma unroll
@@ -972,16 +1028,62 @@ int num_sms() {
     return sms;
 }
 
+// CTAs of one launch: one persistent CTA per SM (two narrow ones), at most one per column tile.
+inline int64_t decode_grid(const Plan &pl, int64_t N) {
+    const int64_t nct = (N + 31) / 32;
+    const int64_t grid = (int64_t)num_sms() * pl.ctas_per_sm;
+    return grid > nct ? nct : grid;
+}
+
+// Cluster size for the shared activation staging: the largest C in {8, 4, 2} for which the grid,
+// rounded up to a multiple of C, fits in clusters that can all be resident at once
+// (cudaOccupancyMaxActiveClusters, cached per kernel and shared-memory size); 1 if none does.
+// A cluster of C CTAs reads 1/C of the host rows per CTA instead of all of them.
+constexpr int kShareSizes[3] = {8, 4, 2};
+template <typename Kern>
+int share_cluster_size(Kern kern, int threads, size_t smem, int64_t grid, uint64_t (&cache)[3]) {
+    for (int i = 0; i < 3; ++i) {
+        const int c = kShareSizes[i];
+        const int64_t g = (grid + c - 1) / c * c;
+        const uint64_t v = __atomic_load_n(&cache[i], __ATOMIC_RELAXED);
+        int n = 0;
+        if (v != 0 && (v >> 32) == (uint64_t)smem) {
+            n = (int)(v & 0xffffffffu) - 1;
+        } else {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)g, 1, 1);
+            cfg.blockDim = dim3((unsigned)threads, 1, 1);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+                n = 0;
+                (void)cudaGetLastError();        // a refused query is an answer (no clusters), not an error
+            }
+            __atomic_store_n(&cache[i], ((uint64_t)smem << 32) | (uint64_t)(uint32_t)(n + 1), __ATOMIC_RELAXED);
+        }
+        if ((int64_t)n * c >= g) return c;
+    }
+    return 1;
+}
+
 // Launch `kern` once per K pass (passes after the first add into y).  Each launch is a programmatic
 // dependent of the grid before it on the stream: it may start while that grid is still running (if
-// that grid allows it), and the kernel waits for it before reading activations or y.
+// that grid allows it), and the kernel waits for it before reading activations or y.  cs > 1: in
+// clusters of cs CTAs, the grid rounded up to a multiple of cs (CTAs past the last column tile only
+// stage their share of the activations).
 template <typename Kern>
 cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const Lut16 &lut, const uint8_t *tiled, int64_t K,
-                          int64_t N, const ActSrc &a, int M, float *y, int64_t ldy, cudaStream_t s) {
+                          int64_t N, const ActSrc &a, int M, float *y, int64_t ldy, cudaStream_t s, int cs = 1) {
     const int64_t nkt = K / 32, nct = (N + 31) / 32;
     if (pl.smem > (size_t)kSmemLimit) return cudaErrorInvalidValue;   // a ring of two stages must fit
-    int64_t grid = (int64_t)num_sms() * pl.ctas_per_sm;
-    if (grid > nct) grid = nct;
+    int64_t grid = decode_grid(pl, N);
+    if (cs > 1) grid = (grid + cs - 1) / cs * cs;
     for (int64_t kt0 = 0; kt0 < nkt; kt0 += pl.nkc) {
         MvParams p;
         p.tiled = tiled;
@@ -1007,11 +1109,15 @@ cudaError_t launch_passes(Kern kern, int threads, const Plan &pl, const Lut16 &l
         cfg.blockDim = dim3((unsigned)threads, 1, 1);
         cfg.dynamicSmemBytes = pl.smem;
         cfg.stream = s;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)cs;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = cs > 1 ? 2 : 1;
         const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
         if (e != cudaSuccess) return e;
     }
@@ -1040,6 +1146,18 @@ cudaError_t run_dp4a(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a
     const int nkc = chunk_tiles(K / 32, 64 * (int64_t)MT);
     Plan pl = plan_ring<TS, CW, TPW>(nkc, dp4a_layout<TYPE, MT, CW, TPW>(nkc, 0).total);
     pl.smem = (size_t)dp4a_layout<TYPE, MT, CW, TPW>(nkc, pl.stages).total + 128;
+    if constexpr (FUSED) {
+        if (a.x_host) {
+            // rows in host memory: one read of them per cluster instead of one per CTA
+            auto kx = matvec_dp4a_kernel<TYPE, MT, CW, true, TPW, true>;
+            static int attr_x[4] = {0, 0, 0, 0};
+            static uint64_t clusters[3] = {0, 0, 0};
+            const cudaError_t e = ensure_smem_limit(kx, kSmemLimit, attr_x);
+            if (e != cudaSuccess) return e;
+            const int cs = share_cluster_size(kx, 32 * (1 + CW), pl.smem, decode_grid(pl, N), clusters);
+            if (cs > 1) return launch_passes(kx, 32 * (1 + CW), pl, lut_for((qmm_type)TYPE), tiled, K, N, a, M, y, ldy, s, cs);
+        }
+    }
     auto kern = matvec_dp4a_kernel<TYPE, MT, CW, FUSED, TPW>;
     static int attr_done[4] = {0, 0, 0, 0};
     const cudaError_t e = ensure_smem_limit(kern, kSmemLimit, attr_done);
@@ -1493,13 +1611,13 @@ cudaError_t run_groups(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, c
 
 cudaError_t launch_matvec(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                           const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s) {
-    const ActSrc a = {a_q, a_d, nullptr, 0};
+    const ActSrc a = {a_q, a_d, nullptr, 0, 0};
     return run_groups<false>(t, tiled, K, N, a, M, y, ldy, s);
 }
 
 cudaError_t launch_matvec_fused(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
-                                int64_t M, float *y, int64_t ldy, cudaStream_t s) {
-    const ActSrc a = {nullptr, nullptr, x, ldx};
+                                int64_t M, float *y, int64_t ldy, cudaStream_t s, int x_host) {
+    const ActSrc a = {nullptr, nullptr, x, ldx, x_host};
     return run_groups<true>(t, tiled, K, N, a, M, y, ldy, s);
 }
 

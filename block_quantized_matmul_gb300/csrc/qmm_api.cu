@@ -5,8 +5,6 @@
 // Guidelines": shapes, strides, tiling and validation are settled on the host before the kernel
 // runs), every check below happens before anything is enqueued, and the kernels trust their
 // parameters.
-#include <mutex>
-
 #include "qmm_internal.cuh"
 
 using namespace qmm;
@@ -144,14 +142,75 @@ qmm_status qmm_matmul(qmm_type t, const void *w_tiled, int64_t K, int64_t N, con
     return qmm_matmul_path(t, w_tiled, K, N, a_q, a_d, M, y, ldy, QMM_PATH_AUTO, stream);
 }
 
-qmm_status qmm_matmul_f32(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
-                          int64_t M, float *y, int64_t ldy, qmm_stream_t stream) {
+static qmm_status check_matmul_f32(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
+                                   int64_t M, float *y, int64_t ldy) {
     if (!valid_type(t)) return QMM_ERR_UNSUPPORTED;
     if (!valid_tkn(t, K, N) || M <= 0 || K > kMaxMatmulK || N > kMaxDim || M > kMaxDim || ldx < K || ldx > kMaxDim || ldy < N)
         return QMM_ERR_INVALID_ARG;
     if (!w_tiled || !x || !y) return QMM_ERR_INVALID_ARG;
     if (!aligned(w_tiled, 16) || !aligned(x, 4) || !aligned(y, 4)) return QMM_ERR_MISALIGNED;
-    return from_cuda(launch_matvec_fused(tile_type(t), static_cast<const uint8_t *>(w_tiled), K, N, x, ldx, M, y, ldy, cs(stream)));
+    return QMM_OK;
+}
+
+// Where p points: 1 page-locked host memory, 0 device (or managed) memory, -1 memory the driver does
+// not know (pageable host memory, which the kernels must not touch).  One driver query
+// (cuPointerGetAttribute, looked up once through the runtime), or the runtime's attribute query if
+// the driver entry point is unavailable.
+using PointerAttrFn = CUresult (*)(void *, CUpointer_attribute, CUdeviceptr);
+static int mem_where(const void *p) {
+    static const PointerAttrFn fn = []() -> PointerAttrFn {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<PointerAttrFn>(ptr);
+        return nullptr;
+    }();
+    if (fn) {
+        unsigned type = 0;
+        if (fn(&type, CU_POINTER_ATTRIBUTE_MEMORY_TYPE, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return -1;
+        return type == CU_MEMORYTYPE_HOST ? 1 : 0;
+    }
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    if (at.type == cudaMemoryTypeHost) return 1;
+    return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) ? 0 : -1;
+}
+
+qmm_status qmm_matmul_f32(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
+                          int64_t M, float *y, int64_t ldy, qmm_stream_t stream) {
+    const qmm_status st = check_matmul_f32(t, w_tiled, K, N, x, ldx, M, y, ldy);
+    if (st != QMM_OK) return st;
+    const int wx = mem_where(x);
+    if (wx < 0 || mem_where(y) < 0) return QMM_ERR_INVALID_ARG;
+    return from_cuda(launch_matvec_fused(tile_type(t), static_cast<const uint8_t *>(w_tiled), K, N, x, ldx, M, y, ldy,
+                                         cs(stream), wx));
+}
+
+size_t qmm_matmul_f32_workspace_size(int64_t M, int64_t K) {
+    if (M <= 0 || K <= 0 || (K % 32) != 0 || M > kMaxDim || K > kMaxMatmulK) return 0;
+    return ((size_t)M * (size_t)K * 4 + 255) / 256 * 256;
+}
+
+qmm_status qmm_matmul_f32_ws(qmm_type t, const void *w_tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
+                             int64_t M, float *y, int64_t ldy, void *workspace, size_t workspace_bytes,
+                             qmm_stream_t stream) {
+    const qmm_status st = check_matmul_f32(t, w_tiled, K, N, x, ldx, M, y, ldy);
+    if (st != QMM_OK) return st;
+    if (!workspace || workspace_bytes < qmm_matmul_f32_workspace_size(M, K)) return QMM_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return QMM_ERR_MISALIGNED;
+    const uint8_t *w = static_cast<const uint8_t *>(w_tiled);
+    const int wx = mem_where(x);
+    if (wx < 0 || mem_where(y) < 0) return QMM_ERR_INVALID_ARG;
+    if (wx == 0)                                 // device rows: the workspace is not needed
+        return from_cuda(launch_matvec_fused(tile_type(t), w, K, N, x, ldx, M, y, ldy, cs(stream), 0));
+    float *rows = static_cast<float *>(workspace);
+    cudaError_t e = launch_stage_rows(x, M, K, ldx, rows, cs(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(launch_matvec_fused(tile_type(t), w, K, N, rows, K, M, y, ldy, cs(stream), 0));
 }
 
 qmm_status qmm_matmul_flat(qmm_type t, const void *w_flat, int64_t K, int64_t N, const int8_t *a_q, const uint16_t *a_d,

@@ -116,11 +116,13 @@ struct ActSrc {
     const uint16_t *a_d;
     const float *x;
     int64_t ldx;
+    int x_host;       // x lives in host memory (read over NVLink-C2C)
 };
 
 // Launchers (each returns cudaGetLastError() after enqueueing).
 cudaError_t launch_quantize_act(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *a_q,
                                 uint16_t *a_d, cudaStream_t s);
+cudaError_t launch_stage_rows(const float *x, int64_t M, int64_t K, int64_t ldx, float *dst, cudaStream_t s);
 cudaError_t launch_quantize_weight(qmm_type t, const float *w, int64_t N, int64_t K, int64_t ldw,
                                    uint8_t *flat, cudaStream_t s);
 cudaError_t launch_repack(qmm_type t, const uint8_t *flat, int64_t K, int64_t N, uint8_t *tiled,
@@ -138,8 +140,9 @@ cudaError_t make_weight_map(CUtensorMap *map, const uint8_t *tiled, int tile_byt
 // Decode matmul straight from flat GGML rows (row bytes a multiple of 16, flat 16-byte aligned).
 cudaError_t launch_matvec_flat(qmm_type t, const uint8_t *flat, int64_t K, int64_t N, const int8_t *a_q,
                                const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
+// x_host: the rows are in page-locked host memory (the int8 path then shares them across clusters).
 cudaError_t launch_matvec_fused(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const float *x, int64_t ldx,
-                                int64_t M, float *y, int64_t ldy, cudaStream_t s);
+                                int64_t M, float *y, int64_t ldy, cudaStream_t s, int x_host);
 cudaError_t launch_gemm(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,
                         const uint16_t *a_d, int64_t M, float *y, int64_t ldy, cudaStream_t s);
 cudaError_t launch_gemm_ws(qmm_type t, const uint8_t *tiled, int64_t K, int64_t N, const int8_t *a_q,

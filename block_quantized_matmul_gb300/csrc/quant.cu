@@ -282,7 +282,52 @@ int grid_for(int64_t work, int threads) {
     return (int)g;
 }
 
+// Copies M fp32 rows (row stride ldx) from page-locked host memory into the dense device buffer
+// dst [M][K]: each byte crosses NVLink-C2C once (a kernel reading host rows from every CTA pays the
+// link once per CTA).  Launched as a programmatic dependent.  It lets the dependent decode kernel
+// launch at once, so that the decode's CTAs take the SMs as the grid before this one leaves them
+// and start streaming weights (the decode waits for this grid before it reads dst or writes y);
+// then it waits for the grid before it before it reads x or writes dst.
+template <bool vec>
+__global__ void __launch_bounds__(256) stage_rows_kernel(const float *__restrict__ x, int64_t M, int64_t K, int64_t ldx,
+                                                         float *__restrict__ dst) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t quads_per_row = K / 4;
+    const int64_t total = M * quads_per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / quads_per_row, k = (i - m * quads_per_row) * 4;
+        if (!QMM_DCHECK(m < M && k + 4 <= K)) continue;
+        const float *src = x + m * ldx + k;
+        float4 v;
+        if constexpr (vec) {
+            v = *reinterpret_cast<const float4 *>(src);
+        } else {
+            v = make_float4(src[0], src[1], src[2], src[3]);
+        }
+        *reinterpret_cast<float4 *>(dst + m * K + k) = v;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_stage_rows(const float *x, int64_t M, int64_t K, int64_t ldx, float *dst, cudaStream_t s) {
+    const int threads = 256;
+    const int grid = grid_for(M * (K / 4), threads);
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) && (ldx % 4 == 0);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (vec) return cudaLaunchKernelEx(&cfg, stage_rows_kernel<true>, x, M, K, ldx, dst);
+    return cudaLaunchKernelEx(&cfg, stage_rows_kernel<false>, x, M, K, ldx, dst);
+}
 
 cudaError_t launch_quantize_act(const float *x, int64_t M, int64_t K, int64_t ldx, int8_t *a_q, uint16_t *a_d,
                                 cudaStream_t s) {

@@ -202,13 +202,47 @@ QMM_API qmm_status qmm_matmul(qmm_type t, const void *w_tiled_dev, int64_t K, in
  * written but y; no workspace.  Launch overlap as for qmm_matmul (x is read only after the
  * preceding kernel has completed).
  * x and y may also live in page-locked host memory mapped for the device (cudaHostAlloc, or
- * cudaHostRegister with cudaHostRegisterMapped): a decode step then moves its 4*M*K input bytes and
- * 4*M*N output bytes over NVLink-C2C inside the kernel, which on GB300 is faster end to end than a
- * host-to-device copy, the kernel and a device-to-host copy in sequence (same results, bit for bit).
- * Errors: INVALID_ARG (sizes, ldx < K, ldy < N, NULL), UNSUPPORTED, MISALIGNED, CUDA.
+ * cudaHostRegister with cudaHostRegisterMapped); the call checks where each points (one driver query
+ * per pointer) and refuses pageable host memory, which the GPU must not touch, with INVALID_ARG
+ * before anything is enqueued.  A decode step then reads x and writes y over
+ * NVLink-C2C inside the kernel (same results, bit for bit).  Host memory is not cached in the GPU's
+ * L2, so every CTA that reads x pays the link for it: for M <= 4 the call finds out (one driver
+ * pointer query per call) that x is in host memory and runs the decode kernel in
+ * thread-block clusters of 2 to 8 CTAs, each CTA reading 1/C of the blocks and sharing them through
+ * distributed shared memory (the cluster size is the largest whose clusters all fit on the GPU at
+ * once).  qmm_matmul_f32_ws reads x over the link only once.
+ * Errors: INVALID_ARG (sizes, ldx < K, ldy < N, NULL, x or y in pageable host memory),
+ * UNSUPPORTED, MISALIGNED, CUDA.
  */
 QMM_API qmm_status qmm_matmul_f32(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N, const float *x_dev,
                                   int64_t ldx, int64_t M, float *y_dev, int64_t ldy, qmm_stream_t stream);
+
+/* Bytes of device workspace qmm_matmul_f32_ws needs for M rows of length K: 4*M*K rounded up to
+ * 256 (0 if invalid). */
+QMM_API size_t qmm_matmul_f32_workspace_size(int64_t M, int64_t K);
+
+/*
+ * qmm_matmul_f32_ws -- qmm_matmul_f32 with a caller-provided device workspace, for activation rows
+ * in page-locked host memory.  The pages' decode path brings each operand into on-chip memory once
+ * per op ("DDR -> DMA -> VTCM Execution Pipeline"); here a first kernel copies the rows over
+ * NVLink-C2C once into the workspace (dense, row stride K), and the fused decode kernel reads them
+ * from there (its CTAs then share the copy through L2).  Same arguments and results, bit for bit,
+ * as qmm_matmul_f32, plus:
+ *   workspace_dev  >= qmm_matmul_f32_workspace_size(M, K) bytes, 256-byte aligned, owned by the
+ *                  caller; overwritten when x is in host memory, untouched otherwise.  Calls that
+ *                  overlap on the GPU must use different workspaces.
+ * The copy is a programmatic dependent launch: it lets the decode kernel launch at once (the decode
+ * kernel takes the SMs as the kernel before the call leaves them and starts streaming the weight
+ * tiles), and waits for the kernel before it on the stream before it reads x or writes the
+ * workspace; the decode kernel reads the rows and writes y only after the copy has completed.  So
+ * the launch-overlap rule of qmm_matmul applies to the kernel launched immediately before this call.
+ * x and y are located as for qmm_matmul_f32 (pageable host memory is refused).
+ * Errors: those of qmm_matmul_f32, plus INVALID_ARG (workspace missing or too small) and
+ * MISALIGNED (workspace not 256-byte aligned).
+ */
+QMM_API qmm_status qmm_matmul_f32_ws(qmm_type t, const void *w_tiled_dev, int64_t K, int64_t N, const float *x,
+                                     int64_t ldx, int64_t M, float *y, int64_t ldy, void *workspace_dev,
+                                     size_t workspace_bytes, qmm_stream_t stream);
 
 /*
  * qmm_matmul_flat -- the product of qmm_matmul taken straight from flat GGML rows, without tiles.

@@ -174,6 +174,22 @@ def test_matmul_f32_argument_errors(L):
     assert f(0, P, 64, 64, P, 64, 1, P + 1, 64, None) == MISALIGNED
 
 
+def test_matmul_f32_ws_argument_errors(L):
+    assert L.qmm_matmul_f32_workspace_size(4, 4096) == 4 * 4096 * 4
+    assert L.qmm_matmul_f32_workspace_size(3, 32) == 512          # 384 B rounded up to 256
+    assert L.qmm_matmul_f32_workspace_size(0, 64) == 0 and L.qmm_matmul_f32_workspace_size(1, 48) == 0
+    need = L.qmm_matmul_f32_workspace_size(1, 64)
+    f = L.qmm_matmul_f32_ws
+    # the arguments of qmm_matmul_f32 are checked first
+    assert f(0, P, 48, 64, P, 64, 1, P, 64, P, need, None) == INVALID
+    assert f(0, P, 64, 64, P, 63, 1, P, 64, P, need, None) == INVALID
+    assert f(0, P, 64, 64, P + 2, 64, 1, P, 64, P, need, None) == MISALIGNED
+    # then the workspace
+    assert f(0, P, 64, 64, P, 64, 1, P, 64, None, need, None) == INVALID
+    assert f(0, P, 64, 64, P, 64, 1, P, 64, P, need - 1, None) == INVALID
+    assert f(0, P, 64, 64, P, 64, 1, P, 64, P + 16, need, None) == MISALIGNED
+
+
 def test_matmul_flat_argument_errors(L):
     f = L.qmm_matmul_flat
     assert f(0, P, 48, 64, P, P, 1, P, 64, None) == INVALID       # K % 32

@@ -132,3 +132,133 @@ def test_fused_with_host_buffers(torch, orc, type_, M):
     q_ref, d_ref = orc.quantize_act(x)
     y_ref, bound = orc.matmul(type_, orc.repack(type_, orc.quantize_rows(type_, w), K, N), K, N, q_ref, d_ref)
     assert_within_bound(y_host.numpy(), y_ref, bound, f"host buffers {type_} M={M}")
+
+
+# Rows in page-locked host memory take the cluster-shared staging: each CTA of a cluster reads and
+# quantizes a share of the blocks and stores the records into every CTA of the cluster.  Shapes: a
+# grid smaller than one cluster of the largest size, a grid that is not a multiple of the cluster
+# size, the headline grid, the narrow (two CTAs per SM) grid, and K in several passes.
+HOST_SHAPES = [(300, 1024), (4096, 4096), (14336, 4096), (40000, 256), (100, 33024)]
+
+
+@pytest.mark.parametrize("type_", TYPES)
+@pytest.mark.parametrize("N,K", HOST_SHAPES)
+def test_fused_host_rows_equal_device_rows(torch, orc, type_, N, K):
+    """The same bits as the call on device rows, for 1 to 4 tokens (the int8 path), and within the
+    oracle's bound where the oracle is quick."""
+    import block_quantized_matmul_gb300 as qmm
+
+    w = synth.weights(N, K, seed=N + 3 * K)
+    _, tiled = gpu_prepare_weight(type_, w)
+    tiled_ref = orc.repack(type_, orc.quantize_rows(type_, w), K, N) if N * K <= 4_000_000 else None
+    del w
+    for M in (1, 2, 3, 4):
+        x = synth.activations(M, K, seed=5 * M + K, outliers=M == 3)
+        y_dev = gpu_matmul_f32(type_, tiled, K, N, x)
+        x_host = torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+        y_host = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+        qmm.qmm_matmul_f32(type_, tiled, K, N, x_host, K, M, y_host, N)
+        torch.cuda.synchronize()
+        assert torch.equal(y_host, y_dev.cpu()), f"host rows differ from device rows: {type_} {N}x{K} M={M}"
+        # the workspace variant: one copy of the rows over the link, then the device-row kernel
+        ws_bytes = qmm.matmul_f32_workspace_size(M, K)
+        ws = torch.full((ws_bytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
+        y_ws = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+        qmm.qmm_matmul_f32_ws(type_, tiled, K, N, x_host, K, M, y_ws, N, ws, ws_bytes)
+        torch.cuda.synchronize()
+        assert torch.equal(y_ws, y_dev.cpu()), f"workspace call differs: {type_} {N}x{K} M={M}"
+        assert torch.equal(ws[: M * K].view(M, K).cpu(), x_host), "the workspace holds the rows"
+        if tiled_ref is not None:
+            q_ref, d_ref = orc.quantize_act(x)
+            y_ref, bound = orc.matmul(type_, tiled_ref, K, N, q_ref, d_ref)
+            assert_within_bound(y_host.numpy(), y_ref, bound, f"host rows {type_} {N}x{K} M={M}")
+
+
+@pytest.mark.parametrize("type_", ["q4_0", "iq4_nl"])
+def test_fused_host_rows_strided_unaligned(torch, type_):
+    """Host rows with an odd stride that start one float past a 16-byte boundary (scalar loads)."""
+    import block_quantized_matmul_gb300 as qmm
+
+    K, N, M, ldx = 2048, 1000, 4, 2051
+    w = synth.weights(N, K, seed=77)
+    _, tiled = gpu_prepare_weight(type_, w)
+    x = synth.activations(M, K, seed=78)
+    y_dev = gpu_matmul_f32(type_, tiled, K, N, x)
+    buf = torch.full((1 + M * ldx,), float("nan"), dtype=torch.float32).pin_memory()
+    rows = buf[1:].view(M, ldx)
+    rows[:, :K] = torch.from_numpy(np.ascontiguousarray(x))
+    y_host = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+    qmm.qmm_matmul_f32(type_, tiled, K, N, rows, ldx, M, y_host, N)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, y_dev.cpu())
+    ws_bytes = qmm.matmul_f32_workspace_size(M, K)
+    ws = torch.zeros(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    y_ws = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    qmm.qmm_matmul_f32_ws(type_, tiled, K, N, rows, ldx, M, y_ws, N, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert torch.equal(y_ws, y_dev)
+
+
+@pytest.mark.parametrize("M", [1, 4, 9])
+def test_fused_ws_device_rows_leave_the_workspace_alone(torch, M):
+    """Device rows need no copy: the workspace variant runs the plain call and never writes it."""
+    import block_quantized_matmul_gb300 as qmm
+
+    K, N = 1024, 700
+    w = synth.weights(N, K, seed=91)
+    _, tiled = gpu_prepare_weight("q8_0", w)
+    x = synth.activations(M, K, seed=92)
+    y_dev = gpu_matmul_f32("q8_0", tiled, K, N, x)
+    ws_bytes = qmm.matmul_f32_workspace_size(M, K)
+    ws = torch.full((ws_bytes // 4,), 7.0, dtype=torch.float32, device="cuda")
+    y_ws = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    qmm.qmm_matmul_f32_ws("q8_0", tiled, K, N, torch.from_numpy(x).cuda(), K, M, y_ws, N, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert torch.equal(y_ws, y_dev)
+    assert bool((ws == 7.0).all())
+
+
+def test_fused_ws_host_rows_back_to_back(torch):
+    """Consecutive calls on one workspace and stream, each with new host rows: every call's copy waits
+    for the decode kernel before it, so no call reads rows of another."""
+    import block_quantized_matmul_gb300 as qmm
+
+    K, N, M, calls = 4096, 4096, 1, 24
+    w = synth.weights(N, K, seed=93)
+    _, tiled = gpu_prepare_weight("q4_0", w)
+    xs = [synth.activations(M, K, seed=100 + c) for c in range(calls)]
+    refs = [gpu_matmul_f32("q4_0", tiled, K, N, x).cpu() for x in xs]
+    ws_bytes = qmm.matmul_f32_workspace_size(M, K)
+    ws = torch.empty(ws_bytes // 4, dtype=torch.float32, device="cuda")
+    x_host = [torch.from_numpy(x).pin_memory() for x in xs]
+    y_host = [torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory() for _ in xs]
+    for c in range(calls):
+        qmm.qmm_matmul_f32_ws("q4_0", tiled, K, N, x_host[c], K, M, y_host[c], N, ws, ws_bytes)
+    torch.cuda.synchronize()
+    for c in range(calls):
+        assert torch.equal(y_host[c], refs[c]), f"call {c}"
+
+
+def test_fused_refuses_pageable_host_memory(torch):
+    """x or y in pageable host memory is refused (INVALID_ARG) before anything is enqueued."""
+    import block_quantized_matmul_gb300 as qmm
+
+    K, N, M = 256, 64, 1
+    _, tiled = gpu_prepare_weight("q8_0", synth.weights(N, K, seed=5))
+    x_page = torch.from_numpy(synth.activations(M, K, seed=6))
+    assert not x_page.is_pinned()
+    x_dev = x_page.cuda()
+    y_dev = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    y_page = torch.full((M, N), float("nan"), dtype=torch.float32)
+    ws_bytes = qmm.matmul_f32_workspace_size(M, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    calls = [lambda: qmm.qmm_matmul_f32("q8_0", tiled, K, N, x_page, K, M, y_dev, N),
+             lambda: qmm.qmm_matmul_f32("q8_0", tiled, K, N, x_dev, K, M, y_page, N),
+             lambda: qmm.qmm_matmul_f32_ws("q8_0", tiled, K, N, x_page, K, M, y_dev, N, ws, ws_bytes),
+             lambda: qmm.qmm_matmul_f32_ws("q8_0", tiled, K, N, x_dev, K, M, y_page, N, ws, ws_bytes)]
+    for call in calls:
+        with pytest.raises(qmm.QmmError) as e:
+            call()
+        assert e.value.status == 1
+    torch.cuda.synchronize()
+    assert bool(torch.isnan(y_dev).all()) and bool(torch.isnan(y_page).all())
