@@ -1037,19 +1037,19 @@ inline int64_t decode_grid(const Plan &pl, int64_t N) {
 
 // Cluster size for the shared activation staging: the largest C in {8, 4, 2} for which the grid,
 // rounded up to a multiple of C, fits in clusters that can all be resident at once
-// (cudaOccupancyMaxActiveClusters, cached per kernel and shared-memory size); 1 if none does.
-// A cluster of C CTAs reads 1/C of the host rows per CTA instead of all of them.
+// (cudaOccupancyMaxActiveClusters); 1 if none does.  A cluster of C CTAs reads 1/C of the host rows
+// per CTA instead of all of them.  The answer depends on the kernel only: its ring is sized to fill
+// its share of shared memory, which pins it to one CTA per SM (16 consumer warps) or two (8), so it
+// is cached per kernel (cache[i] = clusters + 1 once known).  A stale or refused answer costs speed, never correctness:
+// clusters that do not fit at once run one after another.
 constexpr int kShareSizes[3] = {8, 4, 2};
 template <typename Kern>
-int share_cluster_size(Kern kern, int threads, size_t smem, int64_t grid, uint64_t (&cache)[3]) {
+int share_cluster_size(Kern kern, int threads, size_t smem, int64_t grid, int (&cache)[3]) {
     for (int i = 0; i < 3; ++i) {
         const int c = kShareSizes[i];
         const int64_t g = (grid + c - 1) / c * c;
-        const uint64_t v = __atomic_load_n(&cache[i], __ATOMIC_RELAXED);
-        int n = 0;
-        if (v != 0 && (v >> 32) == (uint64_t)smem) {
-            n = (int)(v & 0xffffffffu) - 1;
-        } else {
+        int n = __atomic_load_n(&cache[i], __ATOMIC_RELAXED) - 1;
+        if (n < 0) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)g, 1, 1);
             cfg.blockDim = dim3((unsigned)threads, 1, 1);
@@ -1061,11 +1061,11 @@ int share_cluster_size(Kern kern, int threads, size_t smem, int64_t grid, uint64
             attr[0].val.clusterDim.z = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 0) {
                 n = 0;
                 (void)cudaGetLastError();        // a refused query is an answer (no clusters), not an error
             }
-            __atomic_store_n(&cache[i], ((uint64_t)smem << 32) | (uint64_t)(uint32_t)(n + 1), __ATOMIC_RELAXED);
+            __atomic_store_n(&cache[i], n + 1, __ATOMIC_RELAXED);
         }
         if ((int64_t)n * c >= g) return c;
     }
@@ -1151,7 +1151,7 @@ cudaError_t run_dp4a(const uint8_t *tiled, int64_t K, int64_t N, const ActSrc &a
             // rows in host memory: one read of them per cluster instead of one per CTA
             auto kx = matvec_dp4a_kernel<TYPE, MT, CW, true, TPW, true>;
             static int attr_x[4] = {0, 0, 0, 0};
-            static uint64_t clusters[3] = {0, 0, 0};
+            static int clusters[3] = {0, 0, 0};
             const cudaError_t e = ensure_smem_limit(kx, kSmemLimit, attr_x);
             if (e != cudaSuccess) return e;
             const int cs = share_cluster_size(kx, 32 * (1 + CW), pl.smem, decode_grid(pl, N), clusters);
