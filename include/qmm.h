@@ -204,13 +204,12 @@ QMM_API qmm_status qmm_matmul(qmm_type t, const void *w_tiled_dev, int64_t K, in
  * x and y may also live in page-locked host memory mapped for the device (cudaHostAlloc, or
  * cudaHostRegister with cudaHostRegisterMapped); the call checks where each points (one driver query
  * per pointer) and refuses pageable host memory, which the GPU must not touch, with INVALID_ARG
- * before anything is enqueued.  A decode step then reads x and writes y over
- * NVLink-C2C inside the kernel (same results, bit for bit).  Host memory is not cached in the GPU's
- * L2, so every CTA that reads x pays the link for it: for M <= 4 the call finds out (one driver
- * pointer query per call) that x is in host memory and runs the decode kernel in
- * thread-block clusters of 2 to 8 CTAs, each CTA reading 1/C of the blocks and sharing them through
- * distributed shared memory (the cluster size is the largest whose clusters all fit on the GPU at
- * once).  qmm_matmul_f32_ws reads x over the link only once.
+ * before anything is enqueued.  A decode step then reads x and writes y over NVLink-C2C inside the
+ * kernel (same results, bit for bit).  Host memory is not cached in the GPU's L2, so every CTA that
+ * reads x pays the link for it: with x in host memory and M <= 4 the decode kernel runs in
+ * thread-block clusters of C = 2 to 8 CTAs, each CTA reading 1/C of the blocks and sharing them
+ * through distributed shared memory (C is the largest whose clusters all fit on the GPU at once).
+ * qmm_matmul_f32_ws reads x over the link only once.
  * Errors: INVALID_ARG (sizes, ldx < K, ldy < N, NULL, x or y in pageable host memory),
  * UNSUPPORTED, MISALIGNED, CUDA.
  */
