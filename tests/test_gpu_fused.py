@@ -262,3 +262,27 @@ def test_fused_refuses_pageable_host_memory(torch):
         assert e.value.status == 1
     torch.cuda.synchronize()
     assert bool(torch.isnan(y_dev).all()) and bool(torch.isnan(y_page).all())
+
+
+@pytest.mark.parametrize("type_", ["q8_0", "iq4_nl"])
+@pytest.mark.parametrize("M", [9, 17])
+def test_fused_ws_host_rows_many_tokens(torch, orc, type_, M):
+    """Host rows for the fp16 mma decode (9 tokens) and for more rows than one decode launch takes (17:
+    a 16-row group, then one row): the rows are copied once, every group reads the device copy."""
+    import block_quantized_matmul_gb300 as qmm
+
+    K, N = 2048, 520
+    w = synth.weights(N, K, seed=95)
+    _, tiled = gpu_prepare_weight(type_, w)
+    x = synth.activations(M, K, seed=96)
+    y_dev = gpu_matmul_f32(type_, tiled, K, N, x)
+    x_host = torch.from_numpy(np.ascontiguousarray(x)).pin_memory()
+    y_host = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+    ws_bytes = qmm.matmul_f32_workspace_size(M, K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    qmm.qmm_matmul_f32_ws(type_, tiled, K, N, x_host, K, M, y_host, N, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host, y_dev.cpu())
+    q_ref, d_ref = orc.quantize_act(x)
+    y_ref, bound = orc.matmul(type_, orc.repack(type_, orc.quantize_rows(type_, w), K, N), K, N, q_ref, d_ref)
+    assert_within_bound(y_host.numpy(), y_ref, bound, f"workspace call, host rows {type_} M={M}")
