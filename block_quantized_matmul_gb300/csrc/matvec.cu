@@ -1040,8 +1040,8 @@ inline int64_t decode_grid(const Plan &pl, int64_t N) {
 // (cudaOccupancyMaxActiveClusters); 1 if none does.  A cluster of C CTAs reads 1/C of the host rows
 // per CTA instead of all of them.  The answer depends on the kernel only: its ring is sized to fill
 // its share of shared memory, which pins it to one CTA per SM (16 consumer warps) or two (8), so it
-// is cached per kernel (cache[i] = clusters + 1 once known).  A stale or refused answer costs speed, never correctness:
-// clusters that do not fit at once run one after another.
+// is cached per kernel (cache[i] = clusters + 1 once known).  A stale or refused answer costs
+// speed, never correctness: clusters that do not fit at once run one after another.
 constexpr int kShareSizes[3] = {8, 4, 2};
 template <typename Kern>
 int share_cluster_size(Kern kern, int threads, size_t smem, int64_t grid, int (&cache)[3]) {
