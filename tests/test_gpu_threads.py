@@ -1,8 +1,9 @@
 """Host threads calling the library at the same time, from the very first call of a fresh process.
 
 The first calls resolve one-time state (the tensor-map encoder, the SM count, per-kernel shared-memory
-limits); several threads doing that at once must all get a working path.  Each thread runs the GEMM
-and the decode kernel on its own stream and checks its result against a single-threaded run.
+limits, the cluster occupancy of the host-row decode); several threads doing that at once must all get
+a working path.  Each thread runs the GEMM, the decode kernel or the decode on pinned host rows on its
+own stream and checks its result against a single-threaded run.
 """
 import os
 import subprocess
@@ -31,7 +32,13 @@ SCRIPT = textwrap.dedent("""
 
     def run(i):
         s = torch.cuda.Stream()
-        M = 1 + (i % 2) * 63                     # decode (M = 1) and GEMM (M = 64) threads
+        if i % 3 == 2:                           # decode on pinned host rows (cluster-shared staging)
+            xh = x[:1].cpu().pin_memory()
+            yh = torch.full((1, N), float("nan"), dtype=torch.float32).pin_memory()
+            qmm.qmm_matmul_f32("q4_0", tiled, K, N, xh, K, 1, yh, N, stream=s)
+            s.synchronize()
+            return yh.clone()
+        M = 1 + (i % 3) * 63                     # decode (M = 1) and GEMM (M = 64) threads
         a_q = torch.empty((M, K), dtype=torch.int8, device="cuda")
         a_d = torch.empty((M, K // 32), dtype=torch.int16, device="cuda")
         y = torch.empty((M, N), dtype=torch.float32, device="cuda")
@@ -53,14 +60,15 @@ SCRIPT = textwrap.dedent("""
     qmm.qmm_quantize_weight("q4_0", w, N, K, K, flat)
     qmm.qmm_repack("q4_0", flat, K, N, tiled)
     torch.cuda.synchronize()
-    threads = [threading.Thread(target=work, args=(i,)) for i in range(8)]
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(9)]
     for t in threads: t.start()
     for t in threads: t.join()
     assert not errors, errors
     # the same calls once more, one thread: identical bits (both paths are deterministic)
-    ref = {0: run(0), 1: run(1)}
-    for i in range(8):
-        assert torch.equal(results[i], ref[i % 2]), i
+    ref = {k: run(k) for k in range(3)}
+    for i in range(9):
+        assert torch.equal(results[i], ref[i % 3]), i
+    assert torch.equal(ref[2], ref[0])           # host rows: the device-row bits
     assert qmm.qmm_device_status() == 0
     print("threads ok")
 """).replace("ROOT", repr(ROOT))
