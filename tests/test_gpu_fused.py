@@ -137,8 +137,9 @@ def test_fused_with_host_buffers(torch, orc, type_, M):
 # Rows in page-locked host memory take the cluster-shared staging: each CTA of a cluster reads and
 # quantizes a share of the blocks and stores the records into every CTA of the cluster.  Shapes: a
 # grid smaller than one cluster of the largest size, a grid that is not a multiple of the cluster
-# size, the headline grid, the narrow (two CTAs per SM) grid, and K in several passes.
-HOST_SHAPES = [(300, 1024), (4096, 4096), (14336, 4096), (40000, 256), (100, 33024)]
+# size, the headline grid, the narrow (two CTAs per SM) grid, K in several passes, and fewer blocks
+# than CTAs in a cluster (K = 64: most CTAs have no share to stage).
+HOST_SHAPES = [(300, 1024), (4096, 4096), (14336, 4096), (40000, 256), (100, 33024), (300, 64)]
 
 
 @pytest.mark.parametrize("type_", TYPES)
